@@ -1,0 +1,60 @@
+"""Planted mistakes in copies of the oracle must each be caught by some pin (no GPU).
+
+Each case rewrites one expression of oracle/w4a16_oracle.c in a temporary copy -- a dropped
+term, a wrong sign, a shifted index, a transposed or reversed operand -- compiles it, and runs
+every pin against it.  The real oracle is never modified.  All mutations keep memory accesses
+in bounds so a broken copy cannot crash the test process.
+"""
+import os
+
+import pytest
+
+import oracle
+import pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "w4a16_oracle.c")
+
+MUTATIONS = [
+    ("sign of q - zp", "return (q - zp) * s;", "return (zp - q) * s;"),
+    ("u4b8 bias 7", "? 8.0 : orc_half_to_double(zeros[(long)g * n + col]);",
+     "? 7.0 : orc_half_to_double(zeros[(long)g * n + col]);"),
+    ("nibble order high first", "return (int)((word >> (4 * (row % 8))) & 0xFu);",
+     "return (int)((word >> (4 * (7 - row % 8))) & 0xFu);"),
+    ("group off by one row", "    return row / group_size;\n}",
+     "    return (row > 0 ? row - 1 : 0) / group_size;\n}"),
+    ("scale column reversed", "double s = orc_half_to_double(scales[(long)g * n + col]);",
+     "double s = orc_half_to_double(scales[(long)g * n + (n - 1 - col)]);"),
+    ("zero point column dropped", "? 8.0 : orc_half_to_double(zeros[(long)g * n + col]);",
+     "? 8.0 : orc_half_to_double(zeros[(long)g * n]);"),
+    ("g_idx ignored", "    if (g_idx)\n        return g_idx[row];\n", "\n"),
+    ("dropped accumulation", "acc[j] += av * orc_weight(", "acc[j] = av * orc_weight("),
+    ("A reversed along K", "double av = orc_half_to_double(jb->a[(long)i * jb->lda + row]);",
+     "double av = orc_half_to_double(jb->a[(long)i * jb->lda + (jb->k - 1 - row)]);"),
+    ("half exponent bias", "v = ldexp(1.0 + frac / 1024.0, expo - 15);",
+     "v = ldexp(1.0 + frac / 1024.0, expo - 14);"),
+    ("half subnormal scale", "v = ldexp((double)frac, -24);", "v = ldexp((double)frac, -23);"),
+    ("tile nibble placement", "word |= code << (4 * (e / 2) + 16 * (e % 2));",
+     "word |= code << (4 * e);"),
+    ("tile half order", "out[base + h * 512 + c * 4 + j] = (int32_t)word;",
+     "out[base + (1 - h) * 512 + c * 4 + j] = (int32_t)word;"),
+    ("csr pair ids", "ex_pairs[cursor[selected[p]]++] = p;", "ex_pairs[cursor[selected[p]]++] = pair_tok[p];"),
+    ("csr offsets", "ex_off[active] = (int32_t)cursor[e];", "ex_off[active] = (int32_t)cursor[e + 1];"),
+    ("qzeros plus one dropped", "zero_points[(long)g * n + col] = (double)raw + 1.0;",
+     "zero_points[(long)g * n + col] = (double)raw;"),
+    ("group count ignores divisibility", "group_size % 16 != 0 || k % group_size != 0",
+     "group_size % 16 != 0"),
+    ("by-groups scale dropped", "c[(long)i * n + j] += orc_half_to_double(scales[(long)g * n + j]) * t[j];",
+     "c[(long)i * n + j] += t[j];"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_mutation_is_caught(tmp_path, name, old, new):
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation anchor not unique/present: {old!r}"
+    mutated = tmp_path / "mutant.c"
+    mutated.write_text(src.replace(old, new))
+    lib = oracle.build(force=True, src=str(mutated), out=str(tmp_path / "libmutant.so"))
+    orc = oracle.Oracle(lib)
+    failures = [p.__name__ for p in pins.ALL_PINS if p(orc) is not None]
+    assert failures, f"no pin caught the planted mistake: {name}"
