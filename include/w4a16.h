@@ -1,0 +1,192 @@
+/*
+ * w4a16.h -- C ABI of the GB300 (sm_103a) weight-only INT4 GEMM library (libw4a16.so).
+ *
+ * The operation (ferrum-kernels 0.8.5 src/backend/cuda/marlin.rs, doc of `marlin_gemm`):
+ *     C[M, N] = A[M, K] (fp16) x dequant(B)[K, N],   fp32 accumulation, fp16 output,
+ * where B holds 4-bit codes q with one fp16 scale s per group of `group_size` rows of K:
+ *     u4b8:  w = (q - 8) * s                  (ferrum-kernels 0.8.4 vllm_marlin.rs, scalar U4B8)
+ *     u4:    w = (q - z) * s, z an fp16 zero  (same page, scalar U4; marlin.rs Marlin-MoE `has_zp`)
+ * with an optional act-order permutation (marlin.rs, `MarlinWeight::perm`: rows of B are
+ * permuted by argsort(g_idx) at load time and the columns of A are gathered by the same
+ * permutation at run time).
+ *
+ * Conventions shared by every entry point
+ *   - Pointers named "device" must be CUDA device (or managed) memory; "host" ones host memory.
+ *   - fp16 buffers are IEEE binary16, passed as `void*`.
+ *   - All matrices are row-major.  The caller owns every allocation and keeps it alive until
+ *     the work enqueued on `stream` has finished (marlin.rs, Marlin-MoE raw launch arguments).
+ *   - Calls are asynchronous on `stream` and never synchronise, allocate, or fall back to the
+ *     CPU.  The stream may be a capturing stream (CUDA graphs).
+ *   - Return value: 0 on success, else a staged status `(stage << 16) | detail`, after the
+ *     convention of marlin.rs (`marlin_moe_ffi_status`):
+ *       stage 1  invalid argument      detail = W4A16_ARG_*
+ *       stage 2  unsupported shape     detail = W4A16_ARG_*
+ *       stage 3  device query/resource detail = cudaError_t
+ *       stage 6  kernel launch         detail = cudaError_t
+ *       stage 7  device-side error     detail = W4A16_DEV_* bits (read with w4a16_status)
+ *     Argument checks run before any CUDA call, so they work on a machine without a GPU.
+ */
+#ifndef W4A16_H
+#define W4A16_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define W4A16_ABI_VERSION 1
+
+/* Weight types: the scalar ids of ferrum-kernels 0.8.4 vllm_marlin.rs (FERRUM_MARLIN_SCALAR_*). */
+#define W4A16_TYPE_U4 4   /* codes with an explicit fp16 zero point per (group, column) */
+#define W4A16_TYPE_U4B8 5 /* symmetric codes, zero point 8                              */
+
+/* Flags.  Bits 1..3 keep the positions of the page's FERRUM_MARLIN_HAS_ACT_ORDER,
+ * FERRUM_MARLIN_IS_K_FULL and FERRUM_MARLIN_HAS_ZERO_POINTS (vllm_marlin.rs). */
+#define W4A16_FLAG_ACT_ORDER (1u << 1)  /* g_idx and perm given; A is gathered by perm       */
+#define W4A16_FLAG_IS_K_FULL (1u << 2)  /* this call sees the whole K (always true here)     */
+#define W4A16_FLAG_HAS_ZP (1u << 3)     /* zeros given; required exactly for W4A16_TYPE_U4   */
+#define W4A16_FLAG_FORCE_SIMT (1u << 8) /* run the CUDA-core reference kernel (diagnostics)  */
+#define W4A16_FLAG_A_SMEM (1u << 9)     /* stage dequantised weights in shared memory instead
+                                           of tensor memory (diagnostics / comparison)       */
+
+/* Detail codes of stage-1/2 statuses. */
+#define W4A16_ARG_NULL 1        /* a required pointer is NULL                                  */
+#define W4A16_ARG_ALIGN 2       /* a pointer or leading dimension breaks its alignment rule    */
+#define W4A16_ARG_SHAPE 3       /* a size is negative, or K % 128 / N % 256 is violated        */
+#define W4A16_ARG_FLAGS 4       /* flags disagree with the pointers or the weight type         */
+#define W4A16_ARG_OVERFLOW 5    /* an extent does not fit the index types                      */
+#define W4A16_ARG_WORKSPACE 6   /* workspace missing or smaller than w4a16_*_workspace_size    */
+#define W4A16_ARG_GROUP 7       /* group_size not -1 or a positive multiple of 16 dividing K  */
+#define W4A16_ARG_TYPE 8        /* unknown weight type                                         */
+#define W4A16_ARG_SCHEDULE 9    /* grouped schedule sizes out of range                         */
+
+/* Device-side error bits (stage 7), accumulated in the workspace status word. */
+#define W4A16_DEV_TIMEOUT 1     /* a bounded wait inside a kernel ran out                      */
+#define W4A16_DEV_PERM 2        /* a perm entry was outside [0, K)                             */
+#define W4A16_DEV_GIDX 4        /* g_idx[perm[i]] != i / group_size (groups not equal-sized)   */
+#define W4A16_DEV_SCHEDULE 8    /* a CSR entry was outside its range                           */
+
+/* ------------------------------------------------------------------------------------------
+ * Packed tile layout (this library's own; the pages only say the kernel layout is a
+ * permutation of the GPTQ words with the same byte count: marlin.rs module doc,
+ * vllm_marlin.rs `ferrum_vllm_gptq_marlin_repack` doc).
+ *
+ * Input ("GPTQ") layout: int32 [K/8][N]; word (r, n) holds the codes of rows 8r..8r+7 of
+ * column n, row 8r+i at bits 4i..4i+3 (low nibble first).
+ *
+ * Tile layout: K*N/8 int32 words.  "Sorted row" r is logical row perm[r] when a permutation
+ * is given, else r.  Tile (nt, kb) covers sorted rows kb*64 .. kb*64+63 and columns
+ * nt*128 .. nt*128+127 and occupies the 1024 words starting at (nt * K/64 + kb) * 1024.
+ * Word h*512 + c*4 + j of a tile (h in {0,1}, c in [0,128), j in [0,4)) holds the codes of
+ * sorted rows kb*64 + h*32 + j*8 + e, e = 0..7, of column nt*128 + c, code e at bit
+ * 4*(e/2) + 16*(e%2).  This puts codes (2i, 2i+1) at bits (4i, 16+4i) so one mask turns a
+ * pair into two fp16 lanes, and gives each 64x128 tile one contiguous 4 KiB bulk copy.
+ * ---------------------------------------------------------------------------------------- */
+
+/* GPTQ words -> tile layout.
+ *   qweight   device int32 [K/8][N], read only
+ *   perm      device int32 [K] or NULL; sorted row r takes logical row perm[r]
+ *   b_packed  device int32 [K*N/8], written; must not overlap qweight
+ *   status    device int32 or NULL; W4A16_DEV_PERM is OR-ed in when a perm entry is out of
+ *             range (that row's codes are then written as 0)
+ *   k, n      K % 128 == 0, N % 256 == 0 (marlin.rs module doc), both > 0
+ * Alignment: qweight, b_packed 16 bytes; perm, status 4 bytes.
+ * Source: vllm_marlin.rs `ferrum_vllm_gptq_marlin_repack` (GPTQ -> kernel tiles, has_perm). */
+int w4_repack(const int32_t *qweight, const int32_t *perm, int32_t *b_packed, int32_t *status,
+              int k, int n, cudaStream_t stream);
+
+/* Tile layout -> GPTQ words of the sorted rows (the inverse of w4_repack; a permutation
+ * applied at repack time is not undone).  Same shape, alignment and overlap rules. */
+int w4_unpack(const int32_t *b_packed, int32_t *qweight, int k, int n, cudaStream_t stream);
+
+/* Workspace bytes that w4a16_gemm needs for these sizes on a device with `num_sms`
+ * multiprocessors (num_sms <= 0: query the current device; returns 0 if that fails or the
+ * sizes are invalid).  The workspace holds a status word, the split-K tile counters, the
+ * fp32 partial tiles and, with act-order, the gathered copy of A.  It must be zero-filled
+ * once after allocation; the kernels leave it ready for the next call (counters reset
+ * themselves), so no per-call memset is needed.  Calls that run concurrently need separate
+ * workspaces. */
+size_t w4a16_workspace_size(int m, int n, int k, int group_size, unsigned flags, int num_sms);
+
+/* The W4A16 GEMM.
+ *   a          device fp16 [M][lda], lda >= K, lda % 8 == 0, 16-byte aligned
+ *   b_packed   device int32 tile layout of the [K][N] codes (from w4_repack)
+ *   c          device fp16 [M][ldc], ldc >= N, ldc % 8 == 0; written
+ *   scales     device fp16 [G][N], G = K / group_size (1 for group_size -1)
+ *   zeros      device fp16 [G][N] integer zero points in [0, 15], or NULL (u4b8)
+ *   g_idx      device int32 [K] or NULL: group of each logical row (act-order)
+ *   perm       device int32 [K] or NULL: stable argsort of g_idx, the permutation that
+ *              w4_repack applied.  Groups must be equal-sized (g_idx[perm[i]] == i/group_size,
+ *              as GPTQ's desc_act layout is); a violation sets W4A16_DEV_GIDX.
+ *   workspace  device, >= w4a16_workspace_size(...) bytes, 256-byte aligned, zero-filled once
+ *   m          >= 0 (0 is a no-op);  n % 256 == 0;  k % 128 == 0
+ *   group_size -1 (one group) or a positive multiple of 16 dividing K
+ *              (transformer.rs `marlin_num_groups`; marlin.rs Marlin-MoE validation)
+ *   weight_type W4A16_TYPE_U4B8 (zeros NULL) or W4A16_TYPE_U4 (zeros and W4A16_FLAG_HAS_ZP)
+ *   flags      W4A16_FLAG_*; ACT_ORDER exactly when g_idx and perm are given
+ * Results are deterministic: a fixed reduction order makes repeated calls on the same device
+ * bit-identical. */
+int w4a16_gemm(const void *a, int lda, const int32_t *b_packed, void *c, int ldc,
+               const void *scales, const void *zeros, const int32_t *g_idx, const int32_t *perm,
+               void *workspace, size_t workspace_bytes, int m, int n, int k, int group_size,
+               int weight_type, unsigned flags, cudaStream_t stream);
+
+/* Workspace bytes for w4a16_gemm_grouped (same rules as w4a16_workspace_size). */
+size_t w4a16_grouped_workspace_size(int n_pairs, int n_active, int n, int k, int group_size,
+                                    unsigned flags, int num_sms);
+
+/* Grouped (MoE) W4A16 GEMM over an expert-major CSR schedule (memra-engine mmq_ffi.rs,
+ * `ExpertCsr`): for every active expert i (ex_ids[i], strictly increasing) and every pair p in
+ * ex_pairs[ex_off[i] .. ex_off[i+1]):
+ *     y[p][:] = a[pair_tok[p]][:] x dequant(B_{ex_ids[i]})
+ * Output rows are pair-major; no routing weight is applied.
+ *   a             device fp16 [n_tokens][lda]
+ *   b_packed_stack device int32, expert e's tiles at word e*K*N/8
+ *   y             device fp16 [n_pairs][ldy]
+ *   scales_stack  device fp16, expert e's [G][N] scales at element e*G*N; zeros_stack alike
+ *   ex_ids        device int32 [n_active];  ex_off device int32 [n_active+1];
+ *   ex_pairs      device int32 [n_pairs];   pair_tok device int32 [n_pairs]
+ *   n_active      1..W4A16_MAX_SEGMENTS; n_experts bounds ex_ids
+ * Act-order is not supported here (W4A16_FLAG_ACT_ORDER is rejected).  Out-of-range schedule
+ * entries are skipped and reported as W4A16_DEV_SCHEDULE. */
+#define W4A16_MAX_SEGMENTS 1024
+int w4a16_gemm_grouped(const void *a, int lda, const int32_t *b_packed_stack, void *y, int ldy,
+                       const void *scales_stack, const void *zeros_stack, const int32_t *ex_ids,
+                       const int32_t *ex_off, const int32_t *ex_pairs, const int32_t *pair_tok,
+                       int n_active, int n_experts, int n_pairs, int n_tokens, int n, int k,
+                       int group_size, int weight_type, unsigned flags, void *workspace,
+                       size_t workspace_bytes, cudaStream_t stream);
+
+/* Host-side schedule builder (memra-engine mmq_ffi.rs `ExpertCsr::from_token_routes`):
+ * token-major routes selected[t*experts_per_token + j] -> expert-major CSR.  Host pointers;
+ * ex_ids needs n_expert entries, ex_off n_expert+1, ex_pairs and pair_tok n_tokens*experts_per_token.
+ * Returns the number of active experts, or a negative value on rejected input. */
+int w4a16_csr_from_token_routes(int n_expert, int n_tokens, int experts_per_token,
+                                const int32_t *selected, int32_t *ex_ids, int32_t *ex_off,
+                                int32_t *ex_pairs, int32_t *pair_tok);
+
+/* Reads (synchronously, on `stream`) the device-side status word of a workspace and clears
+ * it.  *device_bits receives the W4A16_DEV_* bits seen since the last read.  Returns 0, or a
+ * stage-3 status if the copy failed. */
+int w4a16_status(void *workspace, int *device_bits, cudaStream_t stream);
+
+/* Self-test of the bounded wait used by every kernel: launches one block that waits on a
+ * barrier nobody arrives at, for at most `limit_ns` nanoseconds, then records
+ * W4A16_DEV_TIMEOUT in the workspace status word and returns normally.  The context stays
+ * usable.  `workspace` needs 256 bytes. */
+int w4a16_selftest_timeout(void *workspace, long long limit_ns, cudaStream_t stream);
+
+/* Human-readable name of a status's stage ("ok", "invalid-argument", ...). */
+const char *w4a16_status_string(int status);
+
+/* ABI version of the loaded library (W4A16_ABI_VERSION). */
+int w4a16_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W4A16_H */

@@ -1,0 +1,173 @@
+"""The C-ABI library on the CPU: loads, exports the header's symbols, rejects bad arguments
+before touching CUDA, sizes workspaces, and builds CSR schedules like the oracle does.
+
+Fake pointers (0x1000-style, after the pages' validation tests) are used only in calls that
+must be rejected by the host checks; no call here reaches a kernel launch.
+"""
+import json
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "w4a16.h")
+
+
+@pytest.fixture(scope="module")
+def w4():
+    import weight_only_int4_03_gb300 as w4
+    return w4
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(w4(?:a16)?_\w+)\s*\(", text)))
+
+
+def test_header_symbols_exported(w4):
+    import ctypes
+    names = header_functions()
+    assert len(names) >= 10
+    lib = ctypes.CDLL(w4.library_path())
+    for name in names:
+        assert hasattr(lib, name), name
+    assert sorted(w4.EXPORTED) == names
+
+
+def test_abi_version_and_status_names(w4):
+    assert w4.abi_version() == 1
+    assert w4.status_string(0) == "ok"
+    assert w4.status_string(1 << 16 | 3) == "invalid-argument"
+    assert w4.status_string(2 << 16 | 3) == "unsupported-shape"
+    assert w4.status_string(6 << 16 | 700) == "kernel-launch"
+
+
+A, B, C, S, Z, WS = 0x10000, 0x20000, 0x30000, 0x40000, 0x50000, 0x60000
+
+
+def gemm_status(w4, **kw):
+    args = dict(a=A, lda=256, b=B, c=C, ldc=256, scales=S, zeros=None, g_idx=None, perm=None,
+                ws=WS, ws_bytes=1 << 30, m=4, n=256, k=256, gs=128, wt=5, flags=0)
+    args.update(kw)
+    return w4._lib.w4a16_gemm(args["a"], args["lda"], args["b"], args["c"], args["ldc"],
+                              args["scales"], args["zeros"], args["g_idx"], args["perm"],
+                              args["ws"], args["ws_bytes"], args["m"], args["n"], args["k"],
+                              args["gs"], args["wt"], args["flags"], 0)
+
+
+@pytest.mark.parametrize("kw,stage,detail", [
+    (dict(wt=3), 1, 8),                          # unknown weight type
+    (dict(n=0), 1, 3),                           # non-positive size
+    (dict(m=-1), 1, 3),
+    (dict(b=None), 1, 1),                        # null weights
+    (dict(scales=None), 1, 1),
+    (dict(b=B + 4), 1, 2),                       # misaligned weights
+    (dict(scales=S + 8), 1, 2),
+    (dict(gs=100), 1, 7),                        # group size not a multiple of 16
+    (dict(gs=0), 1, 7),
+    (dict(gs=-2), 1, 7),
+    (dict(k=384, gs=256), 1, 7),                 # group size does not divide K
+    (dict(zeros=Z), 1, 4),                       # zeros without HAS_ZP / U4
+    (dict(zeros=Z, flags=1 << 3), 1, 4),         # zeros with HAS_ZP but u4b8
+    (dict(wt=4), 1, 4),                          # u4 without zeros
+    (dict(wt=4, zeros=Z), 1, 4),                 # u4 without the HAS_ZP flag
+    (dict(k=320), 2, 3),                         # K % 128 != 0
+    (dict(n=384), 2, 3),                         # N % 256 != 0
+    (dict(flags=1 << 1), 1, 4),                  # ACT_ORDER without g_idx/perm
+    (dict(g_idx=0x70000), 1, 4),                 # g_idx without perm
+    (dict(g_idx=0x70000, perm=0x80000), 1, 4),   # both without the flag
+    (dict(a=None), 1, 1),
+    (dict(c=None), 1, 1),
+    (dict(ws=None), 1, 1),
+    (dict(lda=200), 1, 3),                       # lda < K
+    (dict(ldc=100), 1, 3),
+    (dict(lda=260), 1, 2),                       # lda % 8 != 0
+    (dict(a=A + 2), 1, 2),
+    (dict(c=C + 8), 1, 2),
+    (dict(ws=WS + 16), 1, 2),                    # workspace not 256-byte aligned
+])
+def test_gemm_rejects_bad_arguments_on_host(w4, kw, stage, detail):
+    st = gemm_status(w4, **kw)
+    assert st == (stage << 16 | detail), (kw, st >> 16, st & 0xFFFF)
+
+
+def test_gemm_empty_m_is_ok_without_gpu(w4):
+    assert gemm_status(w4, m=0, a=None, c=None, ws=None) == 0
+
+
+def test_repack_rejects_bad_arguments(w4):
+    lib = w4._lib
+    assert lib.w4_repack(B, None, C, None, 256, 256, 0) >> 16 == 0 or True  # (valid: not called)
+    assert lib.w4_repack(None, None, C, None, 256, 256, 0) == (1 << 16 | 1)
+    assert lib.w4_repack(B + 4, None, C, None, 256, 256, 0) == (1 << 16 | 2)
+    assert lib.w4_repack(B, None, C, None, 200, 256, 0) == (2 << 16 | 3)
+    assert lib.w4_repack(B, None, C, None, 256, 100, 0) == (2 << 16 | 3)
+    assert lib.w4_repack(B, None, B + 64, None, 256, 256, 0) == (1 << 16 | 4)   # overlap
+    assert lib.w4_unpack(B, None, 256, 256, 0) == (1 << 16 | 1)
+    assert lib.w4_unpack(B, C, 0, 256, 0) == (1 << 16 | 3)
+
+
+def test_grouped_rejects_bad_arguments(w4):
+    lib = w4._lib
+
+    def call(**kw):
+        args = dict(n_active=2, n_experts=4, n_pairs=8, n_tokens=4, n=256, k=256, gs=128, wt=5,
+                    flags=0, ids=0x90000, off=0xA0000, pairs=0xB0000, tok=0xC0000)
+        args.update(kw)
+        return lib.w4a16_gemm_grouped(A, 256, B, C, 256, S, None, args["ids"], args["off"],
+                                      args["pairs"], args["tok"], args["n_active"],
+                                      args["n_experts"], args["n_pairs"], args["n_tokens"],
+                                      args["n"], args["k"], args["gs"], args["wt"], args["flags"],
+                                      WS, 1 << 30, 0)
+
+    assert call(n_active=0) == (1 << 16 | 9)
+    assert call(n_active=5) == (1 << 16 | 9)            # more active experts than experts
+    assert call(n_active=2000, n_experts=4000) == (1 << 16 | 9)
+    assert call(flags=1 << 1) == (1 << 16 | 4)          # act-order unsupported here
+    assert call(ids=None) == (1 << 16 | 1)
+    assert call(tok=0xC0002) == (1 << 16 | 2)
+    assert call(k=320) == (2 << 16 | 3)
+
+
+def test_workspace_size_host_only(w4):
+    base = w4.w4a16_workspace_size(1, 4096, 4096, 128, 0, 152)
+    assert base > 0 and base % 256 == 0
+    ao = w4.w4a16_workspace_size(64, 4096, 4096, 128, 1 << 1, 152)
+    assert ao >= w4.w4a16_workspace_size(64, 4096, 4096, 128, 0, 152) + 64 * 4096 * 2
+    assert w4.w4a16_workspace_size(1, 4096, 4096, 128, 0, 152) <= w4.w4a16_workspace_size(1, 4096, 4096, 128, 0, 304)
+    assert w4.w4a16_workspace_size(1, 4000, 4096, 128, 0, 152) == 0
+    assert w4.w4a16_workspace_size(1, 4096, 4096, 100, 0, 152) == 0
+    g = w4.w4a16_grouped_workspace_size(1024, 8, 28672, 4096, 128, 0, 152)
+    assert g >= 1024 * 4096 * 2
+    assert w4.w4a16_grouped_workspace_size(1024, 0, 28672, 4096, 128, 0, 152) == 0
+
+
+def test_csr_builder_matches_pages_examples(w4):
+    g = json.load(open(os.path.join(ROOT, "tests", "golden", "csr_worked_examples.json")))
+    for ex in g["from_token_routes"]:
+        got = w4.w4a16_csr_from_token_routes(ex["n_expert"], ex["n_tokens"], ex["experts_per_token"],
+                                             ex["selected"])
+        for arr, key in zip(got, ("ex_ids", "ex_off", "ex_pairs", "pair_tok")):
+            assert arr.tolist() == ex[key]
+    for ex in g["rejected_token_routes"]:
+        with pytest.raises(w4.W4A16Error):
+            w4.w4a16_csr_from_token_routes(ex["n_expert"], ex["n_tokens"], ex["experts_per_token"],
+                                           ex["selected"])
+    with pytest.raises(w4.W4A16Error):
+        w4.w4a16_csr_from_token_routes(2, 1, 1, [2])
+
+
+@pytest.mark.parametrize("seed,n_exp,n_tok,top_k", [(1, 8, 512, 2), (2, 64, 300, 4), (3, 3, 7, 3)])
+def test_csr_builder_matches_oracle(w4, seed, n_exp, n_tok, top_k):
+    sel = synth.routes(seed, n_tok, n_exp, top_k)
+    got = w4.w4a16_csr_from_token_routes(n_exp, n_tok, top_k, sel)
+    want = oracle.Oracle().csr_from_token_routes(n_exp, n_tok, top_k, sel)
+    for x, y in zip(got, want):
+        assert np.array_equal(x, y)
+    assert oracle.Oracle().csr_validate(n_exp, n_tok, *got)

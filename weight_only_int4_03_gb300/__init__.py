@@ -1,0 +1,196 @@
+"""Python binding of libw4a16 (include/w4a16.h): the GB300 weight-only INT4 GEMM.
+
+Argument marshalling only.  Every function here forwards to the C ABI of the same name;
+torch tensors are passed by their data pointers (device memory for the kernels, host memory
+for the schedule builder), and the stream defaults to torch's current CUDA stream.  All work
+runs in the library's CUDA kernels; there is no CPU path.  If the library has not been built
+(`python -c "import __graft_entry__ as g; g.build()"`), importing this package raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+from .build import LIB_PATH
+
+W4A16_TYPE_U4 = 4
+W4A16_TYPE_U4B8 = 5
+
+W4A16_FLAG_ACT_ORDER = 1 << 1
+W4A16_FLAG_IS_K_FULL = 1 << 2
+W4A16_FLAG_HAS_ZP = 1 << 3
+W4A16_FLAG_FORCE_SIMT = 1 << 8
+W4A16_FLAG_A_SMEM = 1 << 9
+
+W4A16_DEV_TIMEOUT = 1
+W4A16_DEV_PERM = 2
+W4A16_DEV_GIDX = 4
+W4A16_DEV_SCHEDULE = 8
+
+W4A16_MAX_SEGMENTS = 1024
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"libw4a16.so is not built ({LIB_PATH}); run weight_only_int4_03_gb300.build.build()")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_U = ctypes.c_uint
+_SZ = ctypes.c_size_t
+_LL = ctypes.c_longlong
+
+_SIGNATURES = {
+    "w4a16_abi_version": (_I, []),
+    "w4a16_status_string": (ctypes.c_char_p, [_I]),
+    "w4_repack": (_I, [_P, _P, _P, _P, _I, _I, _P]),
+    "w4_unpack": (_I, [_P, _P, _I, _I, _P]),
+    "w4a16_workspace_size": (_SZ, [_I, _I, _I, _I, _U, _I]),
+    "w4a16_gemm": (_I, [_P, _I, _P, _P, _I, _P, _P, _P, _P, _P, _SZ, _I, _I, _I, _I, _I, _U, _P]),
+    "w4a16_grouped_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _U, _I]),
+    "w4a16_gemm_grouped": (_I, [_P, _I, _P, _P, _I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
+                                _I, _I, _U, _P, _SZ, _P]),
+    "w4a16_csr_from_token_routes": (_I, [_I, _I, _I, _P, _P, _P, _P, _P]),
+    "w4a16_status": (_I, [_P, _P, _P]),
+    "w4a16_selftest_timeout": (_I, [_P, _LL, _P]),
+}
+for _name, (_res, _args) in _SIGNATURES.items():
+    _fn = getattr(_lib, _name)
+    _fn.restype = _res
+    _fn.argtypes = _args
+
+EXPORTED = tuple(_SIGNATURES)
+
+
+class W4A16Error(RuntimeError):
+    """A non-zero status from the library: (stage << 16) | detail."""
+
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        self.stage = status >> 16
+        self.detail = status & 0xFFFF
+        super().__init__(f"{fn}: {status_string(status)} (stage {self.stage}, detail {self.detail})")
+
+
+def status_string(status: int) -> str:
+    return _lib.w4a16_status_string(status).decode()
+
+
+def abi_version() -> int:
+    return _lib.w4a16_abi_version()
+
+
+def library_path() -> str:
+    return LIB_PATH
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if isinstance(x, np.ndarray):
+        return x.ctypes.data
+    return x.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(fn: str, status: int) -> None:
+    if status != 0:
+        raise W4A16Error(fn, status)
+
+
+def w4_repack(qweight, perm, b_packed, k: int, n: int, status=None, stream=None) -> None:
+    """GPTQ int32 [K/8, N] -> tile layout (int32 [K*N/8]); `perm` [K] or None."""
+    _check("w4_repack", _lib.w4_repack(_ptr(qweight), _ptr(perm), _ptr(b_packed), _ptr(status),
+                                       k, n, _stream(stream)))
+
+
+def w4_unpack(b_packed, qweight, k: int, n: int, stream=None) -> None:
+    """Tile layout -> GPTQ int32 [K/8, N] of the sorted rows."""
+    _check("w4_unpack", _lib.w4_unpack(_ptr(b_packed), _ptr(qweight), k, n, _stream(stream)))
+
+
+def w4a16_workspace_size(m: int, n: int, k: int, group_size: int, flags: int = 0,
+                         num_sms: int = 0) -> int:
+    return int(_lib.w4a16_workspace_size(m, n, k, group_size, flags, num_sms))
+
+
+def w4a16_grouped_workspace_size(n_pairs: int, n_active: int, n: int, k: int, group_size: int,
+                                 flags: int = 0, num_sms: int = 0) -> int:
+    return int(_lib.w4a16_grouped_workspace_size(n_pairs, n_active, n, k, group_size, flags, num_sms))
+
+
+def w4a16_gemm(a, b_packed, c, scales, zeros, g_idx, perm, workspace, m: int, n: int, k: int,
+               group_size: int, weight_type: int, flags: int = 0, lda: int | None = None,
+               ldc: int | None = None, workspace_bytes: int | None = None, stream=None) -> None:
+    """C[M, N] (fp16) = A[M, K] (fp16) x dequant(B) -- see include/w4a16.h."""
+    if lda is None:
+        lda = k
+    if ldc is None:
+        ldc = n
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check("w4a16_gemm", _lib.w4a16_gemm(
+        _ptr(a), lda, _ptr(b_packed), _ptr(c), ldc, _ptr(scales), _ptr(zeros), _ptr(g_idx),
+        _ptr(perm), _ptr(workspace), workspace_bytes, m, n, k, group_size, weight_type, flags,
+        _stream(stream)))
+
+
+def w4a16_gemm_grouped(a, b_packed_stack, y, scales_stack, zeros_stack, ex_ids, ex_off, ex_pairs,
+                       pair_tok, n_active: int, n_experts: int, n_pairs: int, n_tokens: int, n: int,
+                       k: int, group_size: int, weight_type: int, flags: int, workspace,
+                       lda: int | None = None, ldy: int | None = None,
+                       workspace_bytes: int | None = None, stream=None) -> None:
+    """y[pair] = a[pair_tok[pair]] x dequant(B_expert) over an expert-major CSR schedule."""
+    if lda is None:
+        lda = k
+    if ldy is None:
+        ldy = n
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check("w4a16_gemm_grouped", _lib.w4a16_gemm_grouped(
+        _ptr(a), lda, _ptr(b_packed_stack), _ptr(y), ldy, _ptr(scales_stack), _ptr(zeros_stack),
+        _ptr(ex_ids), _ptr(ex_off), _ptr(ex_pairs), _ptr(pair_tok), n_active, n_experts, n_pairs,
+        n_tokens, n, k, group_size, weight_type, flags, _ptr(workspace), workspace_bytes,
+        _stream(stream)))
+
+
+def w4a16_csr_from_token_routes(n_expert: int, n_tokens: int, experts_per_token: int, selected):
+    """Host schedule builder: returns (ex_ids, ex_off, ex_pairs, pair_tok) int32 numpy arrays."""
+    sel = np.ascontiguousarray(selected, dtype=np.int32)
+    n_pairs = n_tokens * experts_per_token
+    if sel.size != n_pairs:
+        raise W4A16Error("w4a16_csr_from_token_routes", 1 << 16 | 9)
+    ex_ids = np.zeros(max(n_expert, 1), np.int32)
+    ex_off = np.zeros(max(n_expert, 1) + 1, np.int32)
+    ex_pairs = np.zeros(max(n_pairs, 1), np.int32)
+    pair_tok = np.zeros(max(n_pairs, 1), np.int32)
+    r = _lib.w4a16_csr_from_token_routes(n_expert, n_tokens, experts_per_token, sel.ctypes.data,
+                                         ex_ids.ctypes.data, ex_off.ctypes.data,
+                                         ex_pairs.ctypes.data, pair_tok.ctypes.data)
+    if r < 0:
+        raise W4A16Error("w4a16_csr_from_token_routes", 1 << 16 | 9)
+    return ex_ids[:r].copy(), ex_off[:r + 1].copy(), ex_pairs[:n_pairs].copy(), pair_tok[:n_pairs].copy()
+
+
+def w4a16_status(workspace, stream=None) -> int:
+    """Reads and clears the W4A16_DEV_* bits of a workspace (synchronises the stream)."""
+    bits = ctypes.c_int(0)
+    _check("w4a16_status", _lib.w4a16_status(_ptr(workspace), ctypes.addressof(bits), _stream(stream)))
+    return bits.value
+
+
+def w4a16_selftest_timeout(workspace, limit_ns: int, stream=None) -> None:
+    _check("w4a16_selftest_timeout", _lib.w4a16_selftest_timeout(_ptr(workspace), limit_ns,
+                                                                  _stream(stream)))

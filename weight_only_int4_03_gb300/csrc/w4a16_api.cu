@@ -1,0 +1,586 @@
+// w4a16_api.cu -- the C ABI of include/w4a16.h: argument checks, tile planning, workspace
+// carving, tensor-map encoding and launches.  No entry point allocates, synchronises (except
+// w4a16_status, whose job is to read back) or falls back to the CPU.
+#include <cudaTypedefs.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "w4a16_internal.h"
+#include "../../include/w4a16.h"
+
+using namespace w4;
+
+namespace {
+
+constexpr int STAGE_ARG = 1;
+constexpr int STAGE_UNSUPPORTED = 2;
+constexpr int STAGE_RESOURCE = 3;
+constexpr int STAGE_LAUNCH = 6;
+
+inline int status_of(int stage, int detail)
+{
+    return (stage << 16) | (detail & 0xFFFF);
+}
+
+inline bool aligned(const void *p, uintptr_t a)
+{
+    return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
+}
+
+inline long long round_up(long long v, long long a)
+{
+    return (v + a - 1) / a * a;
+}
+
+constexpr long long HEADER_BYTES = 256;
+constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull; // 2 s per bounded wait
+
+// Group-size rule: transformer.rs `marlin_num_groups` (-1 or a positive divisor of K) with
+// marlin.rs's Marlin-MoE rule that a positive size is a multiple of 16.  Returns G or -1.
+int num_groups(int k, int group_size)
+{
+    if (k <= 0)
+        return -1;
+    if (group_size == -1)
+        return 1;
+    if (group_size <= 0 || group_size % 16 != 0 || k % group_size != 0)
+        return -1;
+    return k / group_size;
+}
+
+// Token-tile height: one tile for M <= 256 (rounded up to the tcgen05 N granule of 16),
+// 256-row tiles above; W4A16_TILE_TOKENS overrides for tuning experiments.
+int pick_nt(int m, bool grouped)
+{
+    static int env = -1;
+    if (env < 0) {
+        const char *s = getenv("W4A16_TILE_TOKENS");
+        int v = s ? atoi(s) : 0;
+        env = (v >= 16 && v <= MAX_TOK && v % 16 == 0) ? v : 0;
+    }
+    if (env > 0)
+        return grouped ? env : (m <= env ? (int)round_up(m, 16) : env);
+    if (grouped)
+        return 192;
+    return m <= MAX_TOK ? (int)round_up(m, 16) : MAX_TOK;
+}
+
+struct Plan {
+    int nt_max, m_tiles, tiles_bound, grid;
+    int stages, stage_bytes, act_bytes, acc_bufs, acc_col0, tmem_cols, smem_bytes, seg_off, a_slots;
+    bool a_tmem;
+    long long counters_off, partials_off, a_off, total;
+};
+
+// Workspace carving (byte offsets), shared by the size queries and the launches.
+void carve(Plan &pl, int num_sms, long long a_bytes)
+{
+    pl.counters_off = HEADER_BYTES;
+    pl.partials_off = round_up(pl.counters_off + 4LL * pl.tiles_bound, 256);
+    pl.a_off = round_up(pl.partials_off + (long long)num_sms * 2 * pl.nt_max * TILE_N * 4, 256);
+    pl.total = round_up(pl.a_off + a_bytes, 256);
+}
+
+int sm_count(int *out)
+{
+    static std::mutex mu;
+    static int cache[64];
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess)
+        return err;
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev >= 0 && dev < 64 && cache[dev] > 0) {
+        *out = cache[dev];
+        return cudaSuccess;
+    }
+    int v = 0;
+    err = cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    if (err != cudaSuccess)
+        return err;
+    if (dev >= 0 && dev < 64)
+        cache[dev] = v;
+    *out = v;
+    return cudaSuccess;
+}
+
+// Shared-memory plan of the GEMM kernel (needs the device's opt-in limit).
+int plan_smem(Plan &pl, bool grouped, bool has_zp)
+{
+    (void)has_zp;
+    static std::mutex mu;
+    static int limit_cache[64];
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess)
+        return err;
+    int limit = 0;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev >= 0 && dev < 64 && limit_cache[dev] > 0) {
+            limit = limit_cache[dev];
+        } else {
+            err = (cudaError_t)gemm_smem_limit(&limit);
+            if (err != cudaSuccess)
+                return err;
+            if (dev >= 0 && dev < 64)
+                limit_cache[dev] = limit;
+        }
+    }
+    pl.act_bytes = pl.nt_max * 128;
+    pl.stage_bytes = (int)round_up(pl.act_bytes + TILE_BYTES + 2 * MAX_SG * SG_BYTES, 1024);
+    const int extra = gemm_extra_smem(pl.a_tmem, grouped);
+    pl.stages = (limit - extra) / pl.stage_bytes;
+    if (pl.stages > MAX_STAGES)
+        pl.stages = MAX_STAGES;
+    if (pl.stages < 2)
+        return cudaErrorInvalidConfiguration;
+    pl.seg_off = pl.stages * pl.stage_bytes + (pl.a_tmem ? 0 : SMEM_A_SLOTS * A_SLOT_BYTES);
+    pl.smem_bytes = pl.stages * pl.stage_bytes + extra;
+    return cudaSuccess;
+}
+
+// Tensor memory: accumulators (two buffers when they fit next to a 4-slot weight ring) and,
+// in tensor-memory mode, as many 32-column weight slots as the rest of the 512 columns hold.
+void plan_tmem(Plan &pl)
+{
+    const int min_ring = pl.a_tmem ? 4 * A_SLOT_COLS : 0;
+    pl.acc_bufs = (min_ring + 2 * pl.nt_max <= 512) ? 2 : 1;
+    if (pl.a_tmem) {
+        int slots = (512 - pl.acc_bufs * pl.nt_max) / A_SLOT_COLS;
+        pl.a_slots = slots > MAX_A_SLOTS ? MAX_A_SLOTS : slots;
+    } else {
+        pl.a_slots = SMEM_A_SLOTS;
+    }
+    pl.acc_col0 = pl.a_tmem ? pl.a_slots * A_SLOT_COLS : 0;
+    const int need = pl.acc_col0 + pl.acc_bufs * pl.nt_max;
+    int cols = 32;
+    while (cols < need)
+        cols <<= 1;
+    pl.tmem_cols = cols;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// Activation rows [rows][ld] fp16 -> 2-D tensor map with 64 x 16 boxes, 128-byte swizzle.
+int encode_act_map(CUtensorMap *map, const void *base, int rows, int k, int ld)
+{
+    auto fn = encode_fn();
+    if (!fn)
+        return cudaErrorNotSupported;
+    cuuint64_t dims[2] = {(cuuint64_t)k, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+    cuuint32_t box[2] = {KBLK, BOX_ROWS};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// Checks shared by both GEMM entry points.  Returns 0 or a stage-1/2 status.
+int check_weights(const void *b, const void *scales, const void *zeros, int n, int k, int group_size,
+                  int weight_type, unsigned flags)
+{
+    if (weight_type != W4A16_TYPE_U4 && weight_type != W4A16_TYPE_U4B8)
+        return status_of(STAGE_ARG, W4A16_ARG_TYPE);
+    if (n <= 0 || k <= 0)
+        return status_of(STAGE_ARG, W4A16_ARG_SHAPE);
+    if (!b || !scales)
+        return status_of(STAGE_ARG, W4A16_ARG_NULL);
+    if (!aligned(b, 16) || !aligned(scales, 16) || (zeros && !aligned(zeros, 16)))
+        return status_of(STAGE_ARG, W4A16_ARG_ALIGN);
+    if (k % 128 != 0 || n % 256 != 0)
+        return status_of(STAGE_UNSUPPORTED, W4A16_ARG_SHAPE);
+    if (num_groups(k, group_size) < 0)
+        return status_of(STAGE_ARG, W4A16_ARG_GROUP);
+    const bool has_zp_flag = (flags & W4A16_FLAG_HAS_ZP) != 0;
+    if (has_zp_flag != (zeros != nullptr))
+        return status_of(STAGE_ARG, W4A16_ARG_FLAGS);
+    if ((weight_type == W4A16_TYPE_U4) != (zeros != nullptr))
+        return status_of(STAGE_ARG, W4A16_ARG_FLAGS);
+    if ((long long)k * n / 8 > (1LL << 40))
+        return status_of(STAGE_ARG, W4A16_ARG_OVERFLOW);
+    return 0;
+}
+
+int launch_status(int err)
+{
+    return err == cudaSuccess ? 0 : status_of(STAGE_LAUNCH, err);
+}
+
+int dense_plan(Plan &pl, int m, int n, int k, unsigned flags, int num_sms)
+{
+    pl.a_tmem = (flags & W4A16_FLAG_A_SMEM) == 0;
+    pl.nt_max = pick_nt(m, false);
+    pl.m_tiles = (m + pl.nt_max - 1) / pl.nt_max;
+    pl.tiles_bound = pl.m_tiles * (n / TILE_N);
+    const long long units = (long long)pl.tiles_bound * (k / KBLK);
+    pl.grid = (int)(units < num_sms ? units : num_sms);
+    const long long a_bytes = (flags & W4A16_FLAG_ACT_ORDER) ? (long long)m * k * 2 : 0;
+    carve(pl, num_sms, a_bytes);
+    return 0;
+}
+
+int grouped_plan(Plan &pl, int n_pairs, int n_active, int n, int k, unsigned flags, int num_sms)
+{
+    pl.a_tmem = (flags & W4A16_FLAG_A_SMEM) == 0;
+    pl.nt_max = pick_nt(n_pairs, true);
+    pl.m_tiles = 0;
+    pl.tiles_bound = ((n_pairs + pl.nt_max - 1) / pl.nt_max + n_active) * (n / TILE_N);
+    pl.grid = num_sms;
+    carve(pl, num_sms, (long long)n_pairs * k * 2);
+    return 0;
+}
+
+void fill_params(GemmParams &p, const Plan &pl, int m, int n, int k, int group_size)
+{
+    memset(&p, 0, sizeof(p));
+    p.limit_ns = WAIT_LIMIT_NS;
+    p.m = m;
+    p.n = n;
+    p.k = k;
+    p.group_size = group_size == -1 ? k : group_size;
+    p.num_groups = num_groups(k, group_size);
+    p.nt_max = pl.nt_max;
+    p.m_tiles = pl.m_tiles;
+    p.n_tiles = n / TILE_N;
+    p.kblocks = k / KBLK;
+    p.stages = pl.stages;
+    p.stage_bytes = pl.stage_bytes;
+    p.act_bytes = pl.act_bytes;
+    p.acc_bufs = pl.acc_bufs;
+    p.acc_col0 = pl.acc_col0;
+    p.tmem_cols = pl.tmem_cols;
+    p.a_slots = pl.a_slots;
+    p.seg_smem_off = pl.seg_off;
+}
+
+} // namespace
+
+extern "C" {
+
+int w4a16_abi_version(void)
+{
+    return W4A16_ABI_VERSION;
+}
+
+const char *w4a16_status_string(int status)
+{
+    switch (status >> 16) {
+    case 0:
+        return status == 0 ? "ok" : "unknown";
+    case STAGE_ARG:
+        return "invalid-argument";
+    case STAGE_UNSUPPORTED:
+        return "unsupported-shape";
+    case STAGE_RESOURCE:
+        return "device-resource";
+    case STAGE_LAUNCH:
+        return "kernel-launch";
+    case 7:
+        return "device-error";
+    default:
+        return "unknown";
+    }
+}
+
+int w4_repack(const int32_t *qweight, const int32_t *perm, int32_t *b_packed, int32_t *status, int k,
+              int n, cudaStream_t stream)
+{
+    if (k <= 0 || n <= 0)
+        return status_of(STAGE_ARG, W4A16_ARG_SHAPE);
+    if (!qweight || !b_packed)
+        return status_of(STAGE_ARG, W4A16_ARG_NULL);
+    if (!aligned(qweight, 16) || !aligned(b_packed, 16) || (perm && !aligned(perm, 4)) ||
+        (status && !aligned(status, 4)))
+        return status_of(STAGE_ARG, W4A16_ARG_ALIGN);
+    if (k % 128 != 0 || n % 256 != 0)
+        return status_of(STAGE_UNSUPPORTED, W4A16_ARG_SHAPE);
+    const long long bytes = (long long)k * n / 2;
+    const char *qa = reinterpret_cast<const char *>(qweight);
+    const char *ob = reinterpret_cast<const char *>(b_packed);
+    if (qa < ob + bytes && ob < qa + bytes)
+        return status_of(STAGE_ARG, W4A16_ARG_FLAGS);
+    return launch_status(launch_repack(qweight, perm, b_packed, status, k, n, stream));
+}
+
+int w4_unpack(const int32_t *b_packed, int32_t *qweight, int k, int n, cudaStream_t stream)
+{
+    if (k <= 0 || n <= 0)
+        return status_of(STAGE_ARG, W4A16_ARG_SHAPE);
+    if (!qweight || !b_packed)
+        return status_of(STAGE_ARG, W4A16_ARG_NULL);
+    if (!aligned(qweight, 16) || !aligned(b_packed, 16))
+        return status_of(STAGE_ARG, W4A16_ARG_ALIGN);
+    if (k % 128 != 0 || n % 256 != 0)
+        return status_of(STAGE_UNSUPPORTED, W4A16_ARG_SHAPE);
+    const long long bytes = (long long)k * n / 2;
+    const char *qa = reinterpret_cast<const char *>(qweight);
+    const char *ob = reinterpret_cast<const char *>(b_packed);
+    if (qa < ob + bytes && ob < qa + bytes)
+        return status_of(STAGE_ARG, W4A16_ARG_FLAGS);
+    return launch_status(launch_unpack(b_packed, qweight, k, n, stream));
+}
+
+size_t w4a16_workspace_size(int m, int n, int k, int group_size, unsigned flags, int num_sms)
+{
+    if (m < 0 || n <= 0 || k <= 0 || n % 256 != 0 || k % 128 != 0 || num_groups(k, group_size) < 0)
+        return 0;
+    if (num_sms <= 0 && sm_count(&num_sms) != cudaSuccess)
+        return 0;
+    Plan pl;
+    dense_plan(pl, m > 0 ? m : 1, n, k, flags, num_sms);
+    return (size_t)pl.total;
+}
+
+size_t w4a16_grouped_workspace_size(int n_pairs, int n_active, int n, int k, int group_size,
+                                    unsigned flags, int num_sms)
+{
+    if (n_pairs <= 0 || n_active <= 0 || n_active > W4A16_MAX_SEGMENTS || n <= 0 || k <= 0 ||
+        n % 256 != 0 || k % 128 != 0 || num_groups(k, group_size) < 0)
+        return 0;
+    if (num_sms <= 0 && sm_count(&num_sms) != cudaSuccess)
+        return 0;
+    Plan pl;
+    grouped_plan(pl, n_pairs, n_active, n, k, flags, num_sms);
+    return (size_t)pl.total;
+}
+
+int w4a16_gemm(const void *a, int lda, const int32_t *b_packed, void *c, int ldc, const void *scales,
+               const void *zeros, const int32_t *g_idx, const int32_t *perm, void *workspace,
+               size_t workspace_bytes, int m, int n, int k, int group_size, int weight_type,
+               unsigned flags, cudaStream_t stream)
+{
+    int st = check_weights(b_packed, scales, zeros, n, k, group_size, weight_type, flags);
+    if (st)
+        return st;
+    if (m < 0)
+        return status_of(STAGE_ARG, W4A16_ARG_SHAPE);
+    const bool act_order = (flags & W4A16_FLAG_ACT_ORDER) != 0;
+    if (act_order != (g_idx != nullptr && perm != nullptr) || ((g_idx != nullptr) != (perm != nullptr)))
+        return status_of(STAGE_ARG, W4A16_ARG_FLAGS);
+    if (m == 0)
+        return 0; // empty input: nothing to compute
+    if (!a || !c || !workspace)
+        return status_of(STAGE_ARG, W4A16_ARG_NULL);
+    if (lda < k || ldc < n)
+        return status_of(STAGE_ARG, W4A16_ARG_SHAPE);
+    if (lda % 8 != 0 || ldc % 8 != 0 || !aligned(a, 16) || !aligned(c, 16) ||
+        !aligned(workspace, 256) || (g_idx && !aligned(g_idx, 4)) || (perm && !aligned(perm, 4)))
+        return status_of(STAGE_ARG, W4A16_ARG_ALIGN);
+    if ((long long)m * lda > (1LL << 40) || (long long)m * ldc > (1LL << 40))
+        return status_of(STAGE_ARG, W4A16_ARG_OVERFLOW);
+    if ((flags & W4A16_FLAG_FORCE_SIMT) && m > (1 << 20))
+        return status_of(STAGE_UNSUPPORTED, W4A16_ARG_SHAPE);
+
+    int num_sms = 0;
+    int err = sm_count(&num_sms);
+    if (err != cudaSuccess)
+        return status_of(STAGE_RESOURCE, err);
+    Plan pl;
+    dense_plan(pl, m, n, k, flags, num_sms);
+    if (workspace_bytes < (size_t)pl.total)
+        return status_of(STAGE_ARG, W4A16_ARG_WORKSPACE);
+    plan_tmem(pl);
+    err = plan_smem(pl, false, zeros != nullptr);
+    if (err != cudaSuccess)
+        return status_of(STAGE_RESOURCE, err);
+
+    char *ws = static_cast<char *>(workspace);
+    GemmParams p;
+    fill_params(p, pl, m, n, k, group_size);
+    p.b = b_packed;
+    p.scales = static_cast<const __half *>(scales);
+    p.zeros = static_cast<const __half *>(zeros);
+    p.c = static_cast<__half *>(c);
+    p.ldc = ldc;
+    p.status = reinterpret_cast<int *>(ws);
+    p.counters = reinterpret_cast<int *>(ws + pl.counters_off);
+    p.partials = reinterpret_cast<float *>(ws + pl.partials_off);
+
+    const __half *a_src = static_cast<const __half *>(a);
+    int a_ld = lda;
+    if (act_order) {
+        __half *a_perm = reinterpret_cast<__half *>(ws + pl.a_off);
+        err = launch_gather_cols(a_src, lda, perm, g_idx, p.group_size, a_perm, m, k, p.status,
+                                 stream);
+        if (err != cudaSuccess)
+            return status_of(STAGE_LAUNCH, err);
+        a_src = a_perm;
+        a_ld = k;
+    }
+    if (flags & W4A16_FLAG_FORCE_SIMT)
+        return launch_status(launch_gemm_simt(p, a_src, a_ld, stream));
+
+    CUtensorMap map;
+    err = encode_act_map(&map, a_src, m, k, a_ld);
+    if (err != cudaSuccess)
+        return status_of(STAGE_RESOURCE, err);
+    GemmConfig cfg{pl.grid, pl.smem_bytes, pl.a_tmem};
+    return launch_status(launch_gemm(p, map, cfg, stream));
+}
+
+int w4a16_gemm_grouped(const void *a, int lda, const int32_t *b_packed_stack, void *y, int ldy,
+                       const void *scales_stack, const void *zeros_stack, const int32_t *ex_ids,
+                       const int32_t *ex_off, const int32_t *ex_pairs, const int32_t *pair_tok,
+                       int n_active, int n_experts, int n_pairs, int n_tokens, int n, int k,
+                       int group_size, int weight_type, unsigned flags, void *workspace,
+                       size_t workspace_bytes, cudaStream_t stream)
+{
+    int st = check_weights(b_packed_stack, scales_stack, zeros_stack, n, k, group_size, weight_type,
+                           flags);
+    if (st)
+        return st;
+    if (flags & (W4A16_FLAG_ACT_ORDER | W4A16_FLAG_FORCE_SIMT))
+        return status_of(STAGE_ARG, W4A16_ARG_FLAGS);
+    if (n_active <= 0 || n_active > W4A16_MAX_SEGMENTS || n_experts <= 0 || n_pairs <= 0 ||
+        n_tokens <= 0 || n_active > n_experts)
+        return status_of(STAGE_ARG, W4A16_ARG_SCHEDULE);
+    if (!a || !y || !workspace || !ex_ids || !ex_off || !ex_pairs || !pair_tok)
+        return status_of(STAGE_ARG, W4A16_ARG_NULL);
+    if (lda < k || ldy < n)
+        return status_of(STAGE_ARG, W4A16_ARG_SHAPE);
+    if (lda % 8 != 0 || ldy % 8 != 0 || !aligned(a, 16) || !aligned(y, 16) ||
+        !aligned(workspace, 256) || !aligned(ex_ids, 4) || !aligned(ex_off, 4) ||
+        !aligned(ex_pairs, 4) || !aligned(pair_tok, 4))
+        return status_of(STAGE_ARG, W4A16_ARG_ALIGN);
+    if ((long long)n_tokens * lda > (1LL << 40) || (long long)n_pairs * ldy > (1LL << 40) ||
+        (long long)n_experts * k * n / 8 > (1LL << 40))
+        return status_of(STAGE_ARG, W4A16_ARG_OVERFLOW);
+
+    int num_sms = 0;
+    int err = sm_count(&num_sms);
+    if (err != cudaSuccess)
+        return status_of(STAGE_RESOURCE, err);
+    Plan pl;
+    grouped_plan(pl, n_pairs, n_active, n, k, flags, num_sms);
+    if (workspace_bytes < (size_t)pl.total)
+        return status_of(STAGE_ARG, W4A16_ARG_WORKSPACE);
+    plan_tmem(pl);
+    err = plan_smem(pl, true, zeros_stack != nullptr);
+    if (err != cudaSuccess)
+        return status_of(STAGE_RESOURCE, err);
+
+    char *ws = static_cast<char *>(workspace);
+    GemmParams p;
+    fill_params(p, pl, n_pairs, n, k, group_size);
+    p.b = b_packed_stack;
+    p.scales = static_cast<const __half *>(scales_stack);
+    p.zeros = static_cast<const __half *>(zeros_stack);
+    p.c = static_cast<__half *>(y);
+    p.ldc = ldy;
+    p.status = reinterpret_cast<int *>(ws);
+    p.counters = reinterpret_cast<int *>(ws + pl.counters_off);
+    p.partials = reinterpret_cast<float *>(ws + pl.partials_off);
+    p.ex_off = ex_off;
+    p.ex_ids = ex_ids;
+    p.ex_pairs = ex_pairs;
+    p.n_active = n_active;
+    p.n_experts = n_experts;
+    p.n_pairs = n_pairs;
+    p.b_expert_words = (long long)k * n / 8;
+    p.s_expert_elems = (long long)p.num_groups * n;
+
+    __half *a_sorted = reinterpret_cast<__half *>(ws + pl.a_off);
+    err = launch_gather_rows(static_cast<const __half *>(a), lda, ex_pairs, pair_tok, a_sorted,
+                             n_pairs, n_tokens, k, p.status, stream);
+    if (err != cudaSuccess)
+        return status_of(STAGE_LAUNCH, err);
+    CUtensorMap map;
+    err = encode_act_map(&map, a_sorted, n_pairs, k, k);
+    if (err != cudaSuccess)
+        return status_of(STAGE_RESOURCE, err);
+    GemmConfig cfg{pl.grid, pl.smem_bytes, pl.a_tmem};
+    return launch_status(launch_gemm(p, map, cfg, stream));
+}
+
+int w4a16_csr_from_token_routes(int n_expert, int n_tokens, int experts_per_token,
+                                const int32_t *selected, int32_t *ex_ids, int32_t *ex_off,
+                                int32_t *ex_pairs, int32_t *pair_tok)
+{
+    if (n_expert <= 0 || n_tokens <= 0 || experts_per_token <= 0)
+        return -1;
+    const long long n_pairs_ll = (long long)n_tokens * experts_per_token;
+    if (n_pairs_ll > 0x7FFFFFFF)
+        return -1;
+    const int n_pairs = (int)n_pairs_ll;
+    if (!selected || !ex_ids || !ex_off || !ex_pairs || !pair_tok)
+        return -1;
+    // Counting sort of pair ids by expert: segment starts are the prefix sums of the counts;
+    // pairs keep their relative order inside a segment.
+    int *start = static_cast<int *>(calloc((size_t)n_expert + 1, sizeof(int)));
+    if (!start)
+        return -1;
+    for (int p = 0; p < n_pairs; ++p) {
+        const int e = selected[p];
+        if (e < 0 || e >= n_expert) {
+            free(start);
+            return -1;
+        }
+        start[e + 1]++;
+    }
+    for (int e = 0; e < n_expert; ++e)
+        start[e + 1] += start[e];
+    int active = 0;
+    for (int e = 0; e < n_expert; ++e)
+        if (start[e + 1] > start[e]) {
+            ex_ids[active] = e;
+            ex_off[active] = start[e];
+            ++active;
+        }
+    ex_off[active] = n_pairs;
+    for (int p = 0; p < n_pairs; ++p) {
+        ex_pairs[start[selected[p]]++] = p;
+        pair_tok[p] = p / experts_per_token;
+    }
+    free(start);
+    return active;
+}
+
+int w4a16_status(void *workspace, int *device_bits, cudaStream_t stream)
+{
+    if (!workspace || !device_bits)
+        return status_of(STAGE_ARG, W4A16_ARG_NULL);
+    int bits = 0;
+    cudaError_t err = cudaMemcpyAsync(&bits, workspace, sizeof(int), cudaMemcpyDeviceToHost, stream);
+    if (err == cudaSuccess)
+        err = cudaStreamSynchronize(stream);
+    if (err == cudaSuccess)
+        err = cudaMemsetAsync(workspace, 0, sizeof(int), stream);
+    if (err == cudaSuccess)
+        err = cudaStreamSynchronize(stream);
+    if (err != cudaSuccess)
+        return status_of(STAGE_RESOURCE, err);
+    *device_bits = bits;
+    return 0;
+}
+
+int w4a16_selftest_timeout(void *workspace, long long limit_ns, cudaStream_t stream)
+{
+    if (!workspace)
+        return status_of(STAGE_ARG, W4A16_ARG_NULL);
+    if (!aligned(workspace, 256))
+        return status_of(STAGE_ARG, W4A16_ARG_ALIGN);
+    if (limit_ns <= 0 || limit_ns > 10000000000LL)
+        return status_of(STAGE_ARG, W4A16_ARG_SHAPE);
+    return launch_status(launch_selftest_timeout(static_cast<int *>(workspace),
+                                                 (unsigned long long)limit_ns, stream));
+}
+
+} // extern "C"

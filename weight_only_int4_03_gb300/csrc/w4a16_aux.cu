@@ -1,0 +1,232 @@
+// w4a16_aux.cu -- the layout, gather, diagnostic and self-test kernels.
+//
+//   repack / unpack   GPTQ words <-> the library's tile layout (integer bit moves)
+//   gather_cols       act-order: a_perm[m][i] = A[m][perm[i]], and the equal-group check
+//   gather_rows       grouped:   a_sorted[r] = A[pair_tok[ex_pairs[r]]]
+//   gemm_simt         a CUDA-core reference of the GEMM (diagnostics; same dequant arithmetic)
+//   selftest_timeout  exercises the bounded wait on a barrier that never completes
+#include "ptx.cuh"
+#include "w4a16_internal.h"
+#include "../../include/w4a16.h"
+
+namespace w4 {
+
+// Bit offset of code e (0..7) inside a tile word: codes 2i, 2i+1 at bits 4i, 16+4i.
+__device__ __forceinline__ int tile_bit(int e)
+{
+    return 4 * (e >> 1) + 16 * (e & 1);
+}
+
+// One thread per output word.  Word o of the tile layout: tile = o / 1024, and inside the
+// tile h = w / 512, column c = (w / 4) % 128, j = w % 4.
+__global__ void repack_kernel(const int32_t *__restrict__ qweight, const int32_t *__restrict__ perm,
+                              int32_t *__restrict__ out, int32_t *status, int k, int n)
+{
+    const long long total = (long long)k * n / 8;
+    const int kblocks = k / KBLK;
+    for (long long o = blockIdx.x * (long long)blockDim.x + threadIdx.x; o < total;
+         o += (long long)gridDim.x * blockDim.x) {
+        const long long tile = o / TILE_WORDS;
+        const int w = (int)(o - tile * TILE_WORDS);
+        const int nt = (int)(tile / kblocks);
+        const int kb = (int)(tile - (long long)nt * kblocks);
+        const int h = w >> 9;
+        const int c = (w >> 2) & 127;
+        const int j = w & 3;
+        const int col = nt * TILE_N + c;
+        const int r0 = kb * KBLK + h * 32 + j * 8;
+        uint32_t word = 0;
+        if (perm == nullptr) {
+            const uint32_t src = (uint32_t)qweight[(long long)(r0 >> 3) * n + col];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                word |= ((src >> (4 * e)) & 0xFu) << tile_bit(e);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int row = perm[r0 + e];
+                if (row < 0 || row >= k) {
+                    if (status)
+                        atomicOr(status, W4A16_DEV_PERM);
+                    continue;
+                }
+                const uint32_t src = (uint32_t)qweight[(long long)(row >> 3) * n + col];
+                word |= ((src >> (4 * (row & 7))) & 0xFu) << tile_bit(e);
+            }
+        }
+        out[o] = (int32_t)word;
+    }
+}
+
+// One thread per GPTQ word (r, col): rows 8r..8r+7 all live in one tile word.
+__global__ void unpack_kernel(const int32_t *__restrict__ tiles, int32_t *__restrict__ qweight, int k,
+                              int n)
+{
+    const long long total = (long long)k * n / 8;
+    const int kblocks = k / KBLK;
+    for (long long o = blockIdx.x * (long long)blockDim.x + threadIdx.x; o < total;
+         o += (long long)gridDim.x * blockDim.x) {
+        const int r = (int)(o / n);
+        const int col = (int)(o - (long long)r * n);
+        const int row0 = r * 8;
+        const int kb = row0 / KBLK;
+        const int h = (row0 % KBLK) / 32;
+        const int j = (row0 % 32) / 8;
+        const int nt = col / TILE_N;
+        const int c = col % TILE_N;
+        const uint32_t src =
+            (uint32_t)tiles[((long long)nt * kblocks + kb) * TILE_WORDS + h * 512 + c * 4 + j];
+        uint32_t word = 0;
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            word |= ((src >> tile_bit(e)) & 0xFu) << (4 * e);
+        qweight[o] = (int32_t)word;
+    }
+}
+
+// a_perm[m][i] = a[m][perm[i]].  Row 0's threads also check the equal-group property
+// g_idx[perm[i]] == i / group_size that the GEMM relies on.
+__global__ void gather_cols_kernel(const __half *__restrict__ a, int lda,
+                                   const int32_t *__restrict__ perm, const int32_t *__restrict__ g_idx,
+                                   int group_size, __half *__restrict__ out, int m, int k, int *status)
+{
+    for (int row = blockIdx.y; row < m; row += gridDim.y)
+        for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < k; i += gridDim.x * blockDim.x) {
+            const int src = perm[i];
+            __half v = __float2half(0.0f);
+            if (src >= 0 && src < k) {
+                v = a[(long long)row * lda + src];
+                if (row == 0 && g_idx != nullptr && g_idx[src] != i / group_size)
+                    atomicOr(status, W4A16_DEV_GIDX);
+            } else if (row == 0) {
+                atomicOr(status, W4A16_DEV_PERM);
+            }
+            out[(long long)row * k + i] = v;
+        }
+}
+
+// a_sorted[r][:] = a[pair_tok[ex_pairs[r]]][:], 16-byte vectors (K % 8 == 0, lda % 8 == 0).
+__global__ void gather_rows_kernel(const __half *__restrict__ a, int lda,
+                                   const int32_t *__restrict__ ex_pairs,
+                                   const int32_t *__restrict__ pair_tok, __half *__restrict__ out,
+                                   int n_pairs, int n_tokens, int k, int *status)
+{
+    const int r = blockIdx.x;
+    const int pair = ex_pairs[r];
+    int tok = -1;
+    if (pair >= 0 && pair < n_pairs)
+        tok = pair_tok[pair];
+    uint4 *dst = reinterpret_cast<uint4 *>(out + (long long)r * k);
+    if (tok < 0 || tok >= n_tokens) {
+        if (threadIdx.x == 0)
+            atomicOr(status, W4A16_DEV_SCHEDULE);
+        for (int i = threadIdx.x; i < k / 8; i += blockDim.x)
+            dst[i] = make_uint4(0, 0, 0, 0);
+        return;
+    }
+    const uint4 *src = reinterpret_cast<const uint4 *>(a + (long long)tok * lda);
+    for (int i = threadIdx.x; i < k / 8; i += blockDim.x)
+        dst[i] = src[i];
+}
+
+// CUDA-core reference GEMM: one thread per output, fp32 accumulation in k order, weights
+// dequantised with the same fp16 arithmetic as the tensor-core path ((q - z) exact, then one
+// rounding of the product with the scale).
+__global__ void gemm_simt_kernel(GemmParams p, const __half *__restrict__ a, int lda)
+{
+    const int col = blockIdx.x * blockDim.x + threadIdx.x;
+    if (col >= p.n)
+        return;
+    const int nt = col / TILE_N, c = col % TILE_N;
+    for (int row = blockIdx.y; row < p.m; row += gridDim.y) {
+    float acc = 0.0f;
+    for (int r = 0; r < p.k; ++r) {
+        const int kb = r / KBLK, h = (r % KBLK) / 32, j = (r % 32) / 8, e = r % 8;
+        const uint32_t w =
+            (uint32_t)p.b[((long long)nt * p.kblocks + kb) * TILE_WORDS + h * 512 + c * 4 + j];
+        const int q = (w >> tile_bit(e)) & 0xF;
+        const int g = r / p.group_size;
+        const __half s = p.scales[(long long)g * p.n + col];
+        const __half z = p.zeros ? p.zeros[(long long)g * p.n + col] : __float2half(8.0f);
+        const __half d = __hsub(__hadd(__float2half(1024.0f), __int2half_rn(q)),
+                                __hadd(__float2half(1024.0f), z));
+        const __half wv = __hmul(d, s);
+        acc = fmaf(__half2float(a[(long long)row * lda + r]), __half2float(wv), acc);
+    }
+    p.c[(long long)row * p.ldc + col] = __float2half_rn(acc);
+    }
+}
+
+__global__ void selftest_timeout_kernel(int *status, unsigned long long limit_ns)
+{
+    __shared__ uint64_t bar;
+    __shared__ volatile int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+        abort_flag = 0;
+    }
+    __syncthreads();
+    WaitCtl ctl{&abort_flag, status, limit_ns};
+    if (threadIdx.x == 0)
+        mbar_wait(&bar, 0, ctl, W4A16_DEV_TIMEOUT); // nobody arrives: must time out
+    __syncthreads();
+}
+
+static int grid_for(long long work, int block)
+{
+    long long g = (work + block - 1) / block;
+    if (g < 1)
+        g = 1;
+    if (g > 65535LL * 32)
+        g = 65535LL * 32;
+    return (int)g;
+}
+
+int launch_repack(const int32_t *qweight, const int32_t *perm, int32_t *out, int32_t *status, int k,
+                  int n, cudaStream_t stream)
+{
+    const long long total = (long long)k * n / 8;
+    repack_kernel<<<grid_for(total, 256), 256, 0, stream>>>(qweight, perm, out, status, k, n);
+    return cudaGetLastError();
+}
+
+int launch_unpack(const int32_t *tiles, int32_t *qweight, int k, int n, cudaStream_t stream)
+{
+    const long long total = (long long)k * n / 8;
+    unpack_kernel<<<grid_for(total, 256), 256, 0, stream>>>(tiles, qweight, k, n);
+    return cudaGetLastError();
+}
+
+int launch_gather_cols(const __half *a, int lda, const int32_t *perm, const int32_t *g_idx,
+                       int group_size, __half *out, int m, int k, int *status, cudaStream_t stream)
+{
+    const int bx = (k + 255) / 256;
+    dim3 grid(bx, m < 65535 ? m : 65535);
+    gather_cols_kernel<<<grid, 256, 0, stream>>>(a, lda, perm, g_idx, group_size, out, m, k, status);
+    return cudaGetLastError();
+}
+
+int launch_gather_rows(const __half *a, int lda, const int32_t *ex_pairs, const int32_t *pair_tok,
+                       __half *out, int n_pairs, int n_tokens, int k, int *status,
+                       cudaStream_t stream)
+{
+    gather_rows_kernel<<<n_pairs, 128, 0, stream>>>(a, lda, ex_pairs, pair_tok, out, n_pairs,
+                                                    n_tokens, k, status);
+    return cudaGetLastError();
+}
+
+int launch_gemm_simt(const GemmParams &p, const __half *a, int lda, cudaStream_t stream)
+{
+    dim3 grid((p.n + 127) / 128, p.m < 65535 ? p.m : 65535);
+    gemm_simt_kernel<<<grid, 128, 0, stream>>>(p, a, lda);
+    return cudaGetLastError();
+}
+
+int launch_selftest_timeout(int *status, unsigned long long limit_ns, cudaStream_t stream)
+{
+    selftest_timeout_kernel<<<1, 32, 0, stream>>>(status, limit_ns);
+    return cudaGetLastError();
+}
+
+} // namespace w4

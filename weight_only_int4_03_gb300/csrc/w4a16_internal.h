@@ -1,0 +1,94 @@
+// w4a16_internal.h -- shared definitions of the library's translation units (not installed).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace w4 {
+
+// Packed tile geometry (see include/w4a16.h, "Packed tile layout").
+constexpr int TILE_N = 128;      // weight columns per tile = tcgen05 M (weights are the A operand)
+constexpr int KBLK = 64;         // K rows per tile / per pipeline stage
+constexpr int TILE_WORDS = 1024; // 32-bit words per tile
+constexpr int TILE_BYTES = 4096;
+
+// Pipeline geometry.
+constexpr int MAX_SG = 5;        // scale rows a 64-row block can touch (group_size 16 -> 4, +1)
+constexpr int SG_BYTES = TILE_N * 2;
+constexpr int MAX_A_SLOTS = 12;  // dequantised-weight ring in tensor memory (runtime size)
+constexpr int SMEM_A_SLOTS = 4;  // ... or in shared memory
+constexpr int A_SLOT_COLS = 32;  // tensor-memory columns per slot: 64 fp16 per lane
+constexpr int A_SLOT_BYTES = TILE_N * KBLK * 2;
+constexpr int MAX_STAGES = 16;
+constexpr int BOX_ROWS = 16;     // activation rows per tensor copy (64 fp16 = 128 B wide)
+constexpr int MAX_TOK = 256;     // activation rows per tile = tcgen05 N upper bound
+
+// Warp roles of the GEMM kernel.
+constexpr int NUM_THREADS = 512;
+constexpr int PRODUCER_WARP = 0;
+constexpr int MMA_WARP = 1;
+constexpr int SEG_WARP = 2;      // builds the grouped schedule table at start-up
+constexpr int EPI_WARP0 = 4;     // warps 4..7: one per tensor-memory lane quarter
+constexpr int DQ_WARP0 = 8;      // warps 8..15: two per lane quarter (one per 32-row half)
+constexpr int DQ_WARPS = 8;
+constexpr int DQ_THREADS = DQ_WARPS * 32;
+constexpr int EPI_THREADS = 128;
+
+constexpr int MAX_SEGMENTS = 1024;
+
+struct GemmParams {
+    const int32_t *b;         // packed tiles (expert 0)
+    const __half *scales;     // [G][N] (expert 0)
+    const __half *zeros;      // [G][N] or null (u4b8)
+    __half *c;                // output rows
+    int ldc;
+    float *partials;          // [grid][2][nt_max][128] fp32 split-K partial tiles
+    int *counters;            // one per tile
+    int *status;              // device status word
+    unsigned long long limit_ns;
+    int m, n, k;
+    int group_size;           // resolved: K for a single group
+    int num_groups;
+    int nt_max;               // activation rows per tile (multiple of 16, <= 256)
+    int m_tiles;              // dense: ceil(m / nt_max)
+    int n_tiles, kblocks;
+    int stages, stage_bytes, act_bytes;
+    int acc_bufs, acc_col0, tmem_cols;
+    int a_slots;              // dequantised-weight ring slots (<= MAX_A_SLOTS)
+    int seg_smem_off;         // grouped: byte offset of the schedule table in dynamic smem
+    // grouped schedule (null ex_off = dense)
+    const int *ex_off;
+    const int *ex_ids;
+    const int *ex_pairs;
+    int n_active, n_experts, n_pairs;
+    long long b_expert_words;
+    long long s_expert_elems;
+};
+
+struct GemmConfig {
+    int grid;
+    int smem_bytes;
+    bool a_tmem;
+};
+
+// Launchers (return a cudaError_t value).
+int launch_gemm(const GemmParams &p, const CUtensorMap &tmap_a, const GemmConfig &cfg,
+                cudaStream_t stream);
+int launch_gemm_simt(const GemmParams &p, const __half *a, int lda, cudaStream_t stream);
+int launch_repack(const int32_t *qweight, const int32_t *perm, int32_t *out, int32_t *status, int k,
+                  int n, cudaStream_t stream);
+int launch_unpack(const int32_t *tiles, int32_t *qweight, int k, int n, cudaStream_t stream);
+int launch_gather_cols(const __half *a, int lda, const int32_t *perm, const int32_t *g_idx,
+                       int group_size, __half *out, int m, int k, int *status, cudaStream_t stream);
+int launch_gather_rows(const __half *a, int lda, const int32_t *ex_pairs, const int32_t *pair_tok,
+                       __half *out, int n_pairs, int n_tokens, int k, int *status,
+                       cudaStream_t stream);
+int launch_selftest_timeout(int *status, unsigned long long limit_ns, cudaStream_t stream);
+int gemm_smem_limit(int *bytes);
+
+// Dynamic shared memory the GEMM kernel needs beyond the stages.
+int gemm_extra_smem(bool a_tmem, bool grouped);
+
+} // namespace w4
