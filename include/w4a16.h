@@ -51,6 +51,9 @@ extern "C" {
 #define W4A16_FLAG_FORCE_SIMT (1u << 8) /* run the CUDA-core reference kernel (diagnostics)  */
 #define W4A16_FLAG_A_SMEM (1u << 9)     /* stage dequantised weights in shared memory instead
                                            of tensor memory (diagnostics / comparison)       */
+#define W4A16_FLAG_FORCE_TC (1u << 10)  /* always use the tcgen05 kernel (diagnostics)      */
+#define W4A16_FLAG_FORCE_MMA (1u << 11) /* always use the small-M register-fragment kernel;
+                                           M above 64 is then rejected (unsupported-shape)   */
 
 /* Detail codes of stage-1/2 statuses. */
 #define W4A16_ARG_NULL 1        /* a required pointer is NULL                                  */
@@ -80,10 +83,13 @@ extern "C" {
  * Tile layout: K*N/8 int32 words.  "Sorted row" r is logical row perm[r] when a permutation
  * is given, else r.  Tile (nt, kb) covers sorted rows kb*64 .. kb*64+63 and columns
  * nt*128 .. nt*128+127 and occupies the 1024 words starting at (nt * K/64 + kb) * 1024.
- * Word h*512 + c*4 + j of a tile (h in {0,1}, c in [0,128), j in [0,4)) holds the codes of
- * sorted rows kb*64 + h*32 + j*8 + e, e = 0..7, of column nt*128 + c, code e at bit
- * 4*(e/2) + 16*(e%2).  This puts codes (2i, 2i+1) at bits (4i, 16+4i) so one mask turns a
- * pair into two fp16 lanes, and gives each 64x128 tile one contiguous 4 KiB bulk copy.
+ * Word h*512 + c*4 + j of a tile (h in {0,1}, c in [0,128), j in [0,4)) holds eight codes
+ * of column nt*128 + c: for p in 0..3 and e in 0..1, the code of sorted row
+ * kb*64 + h*32 + 8p + 2j + e sits at bit 4p + 16e.  One mask then turns the row pair
+ * (8p + 2j, 8p + 2j + 1) into two fp16 lanes, a word is exactly what one thread of an
+ * m16n8k16 register fragment needs for two 16-row k steps, the four words of one
+ * (half, column) are one 16-byte load of 32 rows, and each 64x128 tile is one contiguous
+ * 4 KiB bulk copy.
  * ---------------------------------------------------------------------------------------- */
 
 /* GPTQ words -> tile layout.

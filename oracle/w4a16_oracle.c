@@ -259,9 +259,9 @@ void orc_gemm_by_groups(const uint16_t *a, long lda, int m, const int32_t *qweig
  * argsort(g_idx)), else row r.  The K x N code matrix is cut into tiles of 64 sorted rows x
  * 128 columns; tile (column tile nt, row block kb) is 1024 consecutive words starting at
  * word (nt * K/64 + kb) * 1024.  Inside a tile, word (h, c, j) for h in {0,1},
- * c in [0,128), j in [0,4) sits at h*512 + c*4 + j and holds the 8 codes of sorted rows
- * kb*64 + h*32 + j*8 + e (e = 0..7) of column nt*128 + c; code e sits at bit
- * 4*(e/2) + 16*(e%2).
+ * c in [0,128), j in [0,4) sits at h*512 + c*4 + j and holds 8 codes of column nt*128 + c:
+ * for p in 0..3 and e in 0..1, the code of sorted row kb*64 + h*32 + 2*j + 8*p + e sits at
+ * bit 4*p + 16*e.
  * ------------------------------------------------------------------------------------- */
 void orc_repack_tiles(const int32_t *qweight, const int32_t *perm, int k, int n, int32_t *out)
 {
@@ -273,12 +273,13 @@ void orc_repack_tiles(const int32_t *qweight, const int32_t *perm, int k, int n,
                 for (int c = 0; c < 128; ++c)
                     for (int j = 0; j < 4; ++j) {
                         uint32_t word = 0;
-                        for (int e = 0; e < 8; ++e) {
-                            int sorted_row = kb * 64 + h * 32 + j * 8 + e;
-                            int row = perm ? perm[sorted_row] : sorted_row;
-                            uint32_t code = (uint32_t)orc_code(qweight, n, row, nt * 128 + c);
-                            word |= code << (4 * (e / 2) + 16 * (e % 2));
-                        }
+                        for (int p = 0; p < 4; ++p)
+                            for (int e = 0; e < 2; ++e) {
+                                int sorted_row = kb * 64 + h * 32 + 2 * j + 8 * p + e;
+                                int row = perm ? perm[sorted_row] : sorted_row;
+                                uint32_t code = (uint32_t)orc_code(qweight, n, row, nt * 128 + c);
+                                word |= code << (4 * p + 16 * e);
+                            }
                         out[base + h * 512 + c * 4 + j] = (int32_t)word;
                     }
         }
@@ -296,12 +297,13 @@ void orc_unpack_tiles(const int32_t *tiles, int k, int n, int32_t *qweight)
                 for (int c = 0; c < 128; ++c)
                     for (int j = 0; j < 4; ++j) {
                         uint32_t word = (uint32_t)tiles[base + h * 512 + c * 4 + j];
-                        for (int e = 0; e < 8; ++e) {
-                            int row = kb * 64 + h * 32 + j * 8 + e;
-                            uint32_t code = (word >> (4 * (e / 2) + 16 * (e % 2))) & 0xFu;
-                            long at = (long)(row / 8) * n + nt * 128 + c;
-                            qweight[at] = (int32_t)((uint32_t)qweight[at] | (code << (4 * (row % 8))));
-                        }
+                        for (int p = 0; p < 4; ++p)
+                            for (int e = 0; e < 2; ++e) {
+                                int row = kb * 64 + h * 32 + 2 * j + 8 * p + e;
+                                uint32_t code = (word >> (4 * p + 16 * e)) & 0xFu;
+                                long at = (long)(row / 8) * n + nt * 128 + c;
+                                qweight[at] = (int32_t)((uint32_t)qweight[at] | (code << (4 * (row % 8))));
+                            }
                     }
         }
 }

@@ -13,6 +13,8 @@ FLAG_IS_K_FULL = 1 << 2
 FLAG_HAS_ZP = 1 << 3
 FLAG_FORCE_SIMT = 1 << 8
 FLAG_A_SMEM = 1 << 9
+FLAG_FORCE_TC = 1 << 10
+FLAG_FORCE_MMA = 1 << 11
 
 RTOL = 1e-2
 ATOL = 1e-2

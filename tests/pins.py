@@ -309,9 +309,10 @@ def tile_word_index(row: int, col: int, k: int) -> tuple[int, int]:
     nt, c = divmod(col, 128)
     kb, r = divmod(row, 64)
     h, r = divmod(r, 32)
-    j, e = divmod(r, 8)
+    p, r = divmod(r, 8)          # r = 2*j + e inside the 8-row group p
+    j, e = divmod(r, 2)
     word = (nt * kblocks + kb) * 1024 + h * 512 + c * 4 + j
-    return word, 4 * (e // 2) + 16 * (e % 2)
+    return word, 4 * p + 16 * e
 
 
 def pin_tile_layout_closed_form(orc):

@@ -4,7 +4,7 @@ import pytest
 
 import oracle
 import synth
-from helpers import (ATOL, FLAG_A_SMEM, FLAG_FORCE_SIMT, RTOL, U4, U4B8, DeviceProblem, make_problem,
+from helpers import (ATOL, FLAG_A_SMEM, FLAG_FORCE_MMA, FLAG_FORCE_SIMT, FLAG_FORCE_TC, RTOL, U4, U4B8, DeviceProblem, make_problem,
                      oracle_ref, repack_device, torch_dev, within_tol)
 
 pytestmark = pytest.mark.gpu
@@ -110,6 +110,65 @@ def test_alternate_paths(w4, orc, flag, m):
     dp = DeviceProblem(w4, make_problem(500 + m, m, 512, 512, weight_type=U4), flags_extra=flag)
     dp.run()
     check(dp, orc)
+
+
+# --- the two kernels: small-M register-fragment kernel and tcgen05 kernel, each forced -------
+
+@pytest.mark.parametrize("flag", [FLAG_FORCE_MMA, FLAG_FORCE_TC])
+@pytest.mark.parametrize("m", [1, 2, 5, 8, 9, 15, 16, 24, 31, 32, 33, 48, 63, 64])
+def test_small_m_both_kernels(w4, orc, flag, m):
+    """Every small M through both kernels; K=1024 (16 row blocks, 2 stages), N=768 (6 column
+    tiles, so stream-K splits tiles over several CTAs)."""
+    dp = DeviceProblem(w4, make_problem(1000 + m, m, 1024, 768), flags_extra=flag)
+    dp.run()
+    check(dp, orc)
+
+
+@pytest.mark.parametrize("gs", [16, 32, 64, 128, 512, -1])
+@pytest.mark.parametrize("m", [1, 8, 40])
+def test_small_m_kernel_group_sizes(w4, orc, gs, m):
+    dp = DeviceProblem(w4, make_problem(1100 + m + max(gs, 0), m, 1024, 512, group_size=gs),
+                       flags_extra=FLAG_FORCE_MMA)
+    dp.run()
+    check(dp, orc)
+
+
+@pytest.mark.parametrize("m", [1, 7, 16, 64])
+def test_small_m_kernel_zero_points(w4, orc, m):
+    dp = DeviceProblem(w4, make_problem(1200 + m, m, 768, 512, weight_type=U4, sigma=0.5),
+                       flags_extra=FLAG_FORCE_MMA)
+    dp.run()
+    check(dp, orc)
+
+
+@pytest.mark.parametrize("m,gs", [(1, 128), (8, 32), (33, 64)])
+def test_small_m_kernel_act_order(w4, orc, m, gs):
+    dp = DeviceProblem(w4, make_problem(1300 + m, m, 1024, 512, group_size=gs, act_order=True),
+                       flags_extra=FLAG_FORCE_MMA)
+    dp.run()
+    check(dp, orc)
+
+
+@pytest.mark.parametrize("m", [1, 8, 16, 64])
+def test_small_m_kernel_repeatable(w4, m):
+    dp = DeviceProblem(w4, make_problem(1400 + m, m, 2048, 1024), flags_extra=FLAG_FORCE_MMA)
+    dp.run()
+    first = dp.c.cpu().numpy().copy()
+    for _ in range(3):
+        dp.run()
+        assert np.array_equal(dp.c.cpu().numpy().view(np.uint16), first.view(np.uint16))
+
+
+def test_kernel_flags_rejected(w4):
+    pb = make_problem(1500, 65, 256, 256)
+    dp = DeviceProblem(w4, pb, flags_extra=FLAG_FORCE_MMA)
+    with pytest.raises(w4.W4A16Error) as e:
+        dp.run()
+    assert e.value.stage == 2
+    dp = DeviceProblem(w4, make_problem(1501, 4, 256, 256), flags_extra=FLAG_FORCE_MMA | FLAG_FORCE_TC)
+    with pytest.raises(w4.W4A16Error) as e:
+        dp.run()
+    assert e.value.stage == 1 and e.value.detail == 4
 
 
 def test_large_k_many_tiles(w4, orc):

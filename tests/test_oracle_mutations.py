@@ -33,8 +33,10 @@ MUTATIONS = [
     ("half exponent bias", "v = ldexp(1.0 + frac / 1024.0, expo - 15);",
      "v = ldexp(1.0 + frac / 1024.0, expo - 14);"),
     ("half subnormal scale", "v = ldexp((double)frac, -24);", "v = ldexp((double)frac, -23);"),
-    ("tile nibble placement", "word |= code << (4 * (e / 2) + 16 * (e % 2));",
-     "word |= code << (4 * e);"),
+    ("tile nibble placement", "word |= code << (4 * p + 16 * e);",
+     "word |= code << (4 * (2 * p + e));"),
+    ("tile row pairing", "int sorted_row = kb * 64 + h * 32 + 2 * j + 8 * p + e;",
+     "int sorted_row = kb * 64 + h * 32 + 8 * j + 2 * p + e;"),
     ("tile half order", "out[base + h * 512 + c * 4 + j] = (int32_t)word;",
      "out[base + (1 - h) * 512 + c * 4 + j] = (int32_t)word;"),
     ("csr pair ids", "ex_pairs[cursor[selected[p]]++] = p;", "ex_pairs[cursor[selected[p]]++] = pair_tok[p];"),

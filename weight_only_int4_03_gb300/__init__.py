@@ -23,6 +23,8 @@ W4A16_FLAG_IS_K_FULL = 1 << 2
 W4A16_FLAG_HAS_ZP = 1 << 3
 W4A16_FLAG_FORCE_SIMT = 1 << 8
 W4A16_FLAG_A_SMEM = 1 << 9
+W4A16_FLAG_FORCE_TC = 1 << 10
+W4A16_FLAG_FORCE_MMA = 1 << 11
 
 W4A16_DEV_TIMEOUT = 1
 W4A16_DEV_PERM = 2

@@ -48,15 +48,20 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar)
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// Test for completion of the phase with the given parity.  The suspend-time hint lets the
+// hardware park the thread until the phase completes (or the hint runs out) rather than have
+// it spin on the barrier unit.
+constexpr uint32_t SUSPEND_HINT_NS = 1000000u;
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}\n"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "r"(SUSPEND_HINT_NS)
         : "memory");
     return ok != 0;
 }
@@ -71,20 +76,19 @@ struct WaitCtl {
 };
 
 static __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, const WaitCtl &ctl,
-                                       int timeout_bit)
+                                              int timeout_bit)
 {
     const uint64_t t0 = global_timer_ns();
-    for (uint32_t i = 1;; ++i) {
+    for (;;) {
         if (mbar_try_wait(bar, parity))
             return true;
-        if ((i & 63u) == 0) {
-            if (*ctl.abort_flag)
-                return false;
-            if (global_timer_ns() - t0 > ctl.limit_ns) {
-                *ctl.abort_flag = 1;
+        if (*ctl.abort_flag)
+            return false;
+        if (global_timer_ns() - t0 > ctl.limit_ns) {
+            *ctl.abort_flag = 1;
+            if (ctl.status)
                 atomicOr(ctl.status, timeout_bit);
-                return false;
-            }
+            return false;
         }
     }
 }
@@ -140,6 +144,16 @@ __device__ __forceinline__ void tensor_load_2d(void *dst, const CUtensorMap *map
         : "memory");
 }
 
+__device__ __forceinline__ void tensor_load_3d(void *dst, const CUtensorMap *map, int x, int y, int z,
+                                               uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+        "l"(map), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+        : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map)
 {
     asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
@@ -152,9 +166,16 @@ __device__ __forceinline__ void fence_proxy_async_smem()
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-__device__ __forceinline__ void named_barrier(int id, int threads)
+// Programmatic dependent launch: let the next kernel of the stream start its prologue, and
+// wait until the previous kernel's memory operations are complete and visible.
+__device__ __forceinline__ void pdl_launch_dependents()
 {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // ---------------------------------------------------------------------------------------

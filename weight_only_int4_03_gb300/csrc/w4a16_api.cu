@@ -8,7 +8,7 @@
 #include <mutex>
 
 #include "w4a16_internal.h"
-#include "../../include/w4a16.h"
+#include "w4a16.h"
 
 using namespace w4;
 
@@ -50,31 +50,16 @@ int num_groups(int k, int group_size)
     return k / group_size;
 }
 
-// Token-tile height: one tile for M <= 256 (rounded up to the tcgen05 N granule of 16),
-// 256-row tiles above; W4A16_TILE_TOKENS overrides for tuning experiments.
-int pick_nt(int m, bool grouped)
-{
-    static int env = -1;
-    if (env < 0) {
-        const char *s = getenv("W4A16_TILE_TOKENS");
-        int v = s ? atoi(s) : 0;
-        env = (v >= 16 && v <= MAX_TOK && v % 16 == 0) ? v : 0;
-    }
-    if (env > 0)
-        return grouped ? env : (m <= env ? (int)round_up(m, 16) : env);
-    if (grouped)
-        return 192;
-    return m <= MAX_TOK ? (int)round_up(m, 16) : MAX_TOK;
-}
-
 struct Plan {
     int nt_max, m_tiles, tiles_bound, grid;
-    int stages, stage_bytes, act_bytes, acc_bufs, acc_col0, tmem_cols, smem_bytes, seg_off, a_slots;
-    bool a_tmem;
+    int kbs, sg_box, act_kb_bytes, packed_off, scales_off, zeros_off;
+    int stages, stage_bytes, acc_bufs, acc_col0, tmem_cols, smem_bytes, seg_off, a_slots;
+    bool a_tmem, mma; // mma: the small-M register-fragment kernel instead of tcgen05
     long long counters_off, partials_off, a_off, total;
 };
 
-// Workspace carving (byte offsets), shared by the size queries and the launches.
+// Workspace carving (byte offsets), shared by the size queries and the launches.  The
+// partial-tile area is sized for the largest tile height either kernel may pick.
 void carve(Plan &pl, int num_sms, long long a_bytes)
 {
     pl.counters_off = HEADER_BYTES;
@@ -106,50 +91,135 @@ int sm_count(int *out)
     return cudaSuccess;
 }
 
-// Shared-memory plan of the GEMM kernel (needs the device's opt-in limit).
-int plan_smem(Plan &pl, bool grouped, bool has_zp)
+int env_int(const char *name, int lo, int hi, int dflt)
 {
-    (void)has_zp;
+    const char *s = getenv(name);
+    if (!s)
+        return dflt;
+    const int v = atoi(s);
+    return (v >= lo && v <= hi) ? v : dflt;
+}
+
+// 64-row blocks per pipeline stage.  A TMA copy has a large fixed cost, so the packed codes
+// of a stage travel as one bulk copy of kbs * 4 KiB; 8 blocks (32 KiB) is the default,
+// W4A16_STAGE_BLOCKS overrides it for tuning.
+int stage_blocks_default()
+{
+    static int v = env_int("W4A16_STAGE_BLOCKS", 1, MAX_STAGES, 8);
+    return v;
+}
+
+// Largest M the small-M kernel takes by default (W4A16_DECODE_ROWS overrides, 0..64).
+int decode_rows_default()
+{
+    static int v = env_int("W4A16_DECODE_ROWS", 0, 64, 32);
+    return v;
+}
+
+// Token-tile height of the tcgen05 kernel: one tile for M <= 256 (rounded up to the tcgen05
+// N granule of 16), 256-row tiles above; W4A16_TILE_TOKENS overrides for tuning.
+int pick_nt(int m, bool grouped)
+{
+    static int env = [] {
+        const int v = env_int("W4A16_TILE_TOKENS", 16, MAX_TOK, 0);
+        return v % 16 == 0 ? v : 0;
+    }();
+    if (env > 0)
+        return grouped ? env : (m <= env ? (int)round_up(m, 16) : env);
+    if (grouped)
+        return 192;
+    return m <= MAX_TOK ? (int)round_up(m, 16) : MAX_TOK;
+}
+
+// Token-tile height of the small-M kernel: 8 rows (one m16n8 fragment's useful half) for
+// M <= 8, else M rounded up to the m16 fragment height.
+int pick_nt_mma(int m)
+{
+    return m <= 8 ? 8 : (int)round_up(m, 16);
+}
+
+// Stage geometry: [activations kbs x nt_max x 128 B | packed kbs x 4 KiB | scales | zeros].
+// The activation part starts the stage (1024-byte aligned for the 128-byte swizzle); the
+// scale rows a stage touches are at most ceil(kbs*64 / gs) + 1 (a group may straddle the
+// stage start), never more than the tensor's rows.
+void stage_layout(Plan &pl, int kbs, int group_size, int g_rows, bool has_zp)
+{
+    pl.kbs = kbs;
+    pl.act_kb_bytes = pl.nt_max * 128;
+    const int sg = (kbs * KBLK + group_size - 1) / group_size + 1;
+    pl.sg_box = sg < g_rows ? sg : g_rows;
+    pl.packed_off = kbs * pl.act_kb_bytes;
+    pl.scales_off = pl.packed_off + kbs * TILE_BYTES;
+    pl.zeros_off = pl.scales_off + (int)round_up((long long)pl.sg_box * SG_BYTES, 128);
+    const int end = has_zp ? pl.zeros_off + pl.sg_box * SG_BYTES : pl.zeros_off;
+    pl.stage_bytes = (int)round_up(end, 1024);
+}
+
+int smem_limit(int *limit)
+{
     static std::mutex mu;
     static int limit_cache[64];
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess)
         return err;
-    int limit = 0;
-    {
-        std::lock_guard<std::mutex> lock(mu);
-        if (dev >= 0 && dev < 64 && limit_cache[dev] > 0) {
-            limit = limit_cache[dev];
-        } else {
-            err = (cudaError_t)gemm_smem_limit(&limit);
-            if (err != cudaSuccess)
-                return err;
-            if (dev >= 0 && dev < 64)
-                limit_cache[dev] = limit;
-        }
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev >= 0 && dev < 64 && limit_cache[dev] > 0) {
+        *limit = limit_cache[dev];
+        return cudaSuccess;
     }
-    pl.act_bytes = pl.nt_max * 128;
-    pl.stage_bytes = (int)round_up(pl.act_bytes + TILE_BYTES + 2 * MAX_SG * SG_BYTES, 1024);
-    const int extra = gemm_extra_smem(pl.a_tmem, grouped);
-    pl.stages = (limit - extra) / pl.stage_bytes;
+    err = (cudaError_t)gemm_smem_limit(limit);
+    if (err != cudaSuccess)
+        return err;
+    if (dev >= 0 && dev < 64)
+        limit_cache[dev] = *limit;
+    return cudaSuccess;
+}
+
+// Shared-memory plan: the largest stage (up to the default block count, and for the tcgen05
+// kernel no more blocks than the dequantised-weight ring holds) that still leaves three
+// stages in flight; two at the very least.
+int plan_smem(Plan &pl, bool grouped, bool has_zp, int group_size, int g_rows)
+{
+    int limit = 0;
+    int err = smem_limit(&limit);
+    if (err != cudaSuccess)
+        return err;
+    const int extra = pl.mma ? decode_extra_smem() : gemm_extra_smem(pl.a_tmem, grouped);
+    int kbs = stage_blocks_default();
+    if (!pl.mma && kbs > pl.a_slots)
+        kbs = pl.a_slots;
+    for (;; kbs = kbs > 1 ? kbs / 2 : 0) {
+        if (kbs == 0)
+            return cudaErrorInvalidConfiguration;
+        stage_layout(pl, kbs, group_size, g_rows, has_zp);
+        pl.stages = (limit - extra) / pl.stage_bytes;
+        if (pl.stages >= 3 || (kbs == 1 && pl.stages >= 2))
+            break;
+    }
     if (pl.stages > MAX_STAGES)
         pl.stages = MAX_STAGES;
-    if (pl.stages < 2)
-        return cudaErrorInvalidConfiguration;
-    pl.seg_off = pl.stages * pl.stage_bytes + (pl.a_tmem ? 0 : SMEM_A_SLOTS * A_SLOT_BYTES);
+    pl.seg_off = pl.stages * pl.stage_bytes + (!pl.mma && !pl.a_tmem ? SMEM_A_SLOTS * A_SLOT_BYTES : 0);
     pl.smem_bytes = pl.stages * pl.stage_bytes + extra;
     return cudaSuccess;
 }
 
-// Tensor memory: accumulators (two buffers when they fit next to a 4-slot weight ring) and,
-// in tensor-memory mode, as many 32-column weight slots as the rest of the 512 columns hold.
+// Tensor memory of the tcgen05 kernel: accumulators (two buffers when they fit next to a
+// 4-slot weight ring) and, in tensor-memory mode, as many 32-column weight slots as the rest
+// of the 512 columns hold (at most MAX_A_SLOTS).
 void plan_tmem(Plan &pl)
 {
+    if (pl.mma) {
+        pl.acc_bufs = 1;
+        pl.a_slots = 0;
+        pl.acc_col0 = 0;
+        pl.tmem_cols = 0;
+        return;
+    }
     const int min_ring = pl.a_tmem ? 4 * A_SLOT_COLS : 0;
     pl.acc_bufs = (min_ring + 2 * pl.nt_max <= 512) ? 2 : 1;
     if (pl.a_tmem) {
-        int slots = (512 - pl.acc_bufs * pl.nt_max) / A_SLOT_COLS;
+        const int slots = (512 - pl.acc_bufs * pl.nt_max) / A_SLOT_COLS;
         pl.a_slots = slots > MAX_A_SLOTS ? MAX_A_SLOTS : slots;
     } else {
         pl.a_slots = SMEM_A_SLOTS;
@@ -177,18 +247,35 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
     return fn;
 }
 
-// Activation rows [rows][ld] fp16 -> 2-D tensor map with 64 x 16 boxes, 128-byte swizzle.
-int encode_act_map(CUtensorMap *map, const void *base, int rows, int k, int ld)
+// Activation rows [rows][ld] fp16 viewed as [K/64][rows][64]: one copy brings kbs column
+// blocks of nt_max rows, each landing as an [nt_max x 128 B] tile in the 128-byte swizzle.
+int encode_act_map(CUtensorMap *map, const void *base, int rows, int k, int ld, int nt, int kbs)
 {
     auto fn = encode_fn();
     if (!fn)
         return cudaErrorNotSupported;
-    cuuint64_t dims[2] = {(cuuint64_t)k, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
-    cuuint32_t box[2] = {KBLK, BOX_ROWS};
+    cuuint64_t dims[3] = {(cuuint64_t)KBLK, (cuuint64_t)rows, (cuuint64_t)(k / KBLK)};
+    cuuint64_t strides[2] = {(cuuint64_t)ld * 2, (cuuint64_t)KBLK * 2};
+    cuuint32_t box[3] = {KBLK, (cuuint32_t)nt, (cuuint32_t)kbs};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(base), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// Scale (or zero) rows [g_rows][n] fp16: boxes of 128 columns x sg_box group rows.
+int encode_group_map(CUtensorMap *map, const void *base, int g_rows, int n, int sg_box)
+{
+    auto fn = encode_fn();
+    if (!fn)
+        return cudaErrorNotSupported;
+    cuuint64_t dims[2] = {(cuuint64_t)n, (cuuint64_t)g_rows};
+    cuuint64_t strides[1] = {(cuuint64_t)n * 2};
+    cuuint32_t box[2] = {TILE_N, (cuuint32_t)sg_box};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides,
-                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
@@ -224,28 +311,55 @@ int launch_status(int err)
     return err == cudaSuccess ? 0 : status_of(STAGE_LAUNCH, err);
 }
 
-int dense_plan(Plan &pl, int m, int n, int k, unsigned flags, int num_sms)
+// Kernel choice of a dense call: 1 = small-M register-fragment kernel, 0 = tcgen05, or a
+// negative status when the flags conflict or force the small-M kernel beyond its rows.
+int choose_mma(int m, unsigned flags)
 {
-    pl.a_tmem = (flags & W4A16_FLAG_A_SMEM) == 0;
-    pl.nt_max = pick_nt(m, false);
-    pl.m_tiles = (m + pl.nt_max - 1) / pl.nt_max;
-    pl.tiles_bound = pl.m_tiles * (n / TILE_N);
-    const long long units = (long long)pl.tiles_bound * (k / KBLK);
-    pl.grid = (int)(units < num_sms ? units : num_sms);
-    const long long a_bytes = (flags & W4A16_FLAG_ACT_ORDER) ? (long long)m * k * 2 : 0;
-    carve(pl, num_sms, a_bytes);
-    return 0;
+    const unsigned other = W4A16_FLAG_FORCE_TC | W4A16_FLAG_A_SMEM | W4A16_FLAG_FORCE_SIMT;
+    if (flags & W4A16_FLAG_FORCE_MMA) {
+        if (flags & other)
+            return -status_of(STAGE_ARG, W4A16_ARG_FLAGS);
+        if (m > decode_max_rows())
+            return -status_of(STAGE_UNSUPPORTED, W4A16_ARG_SHAPE);
+        return 1;
+    }
+    if (flags & other)
+        return 0;
+    return m <= decode_rows_default() ? 1 : 0;
 }
 
-int grouped_plan(Plan &pl, int n_pairs, int n_active, int n, int k, unsigned flags, int num_sms)
+// Dense plan.  The workspace is carved for the larger tile of the two kernels, so a size
+// query answers for whichever kernel the call then picks.
+void dense_plan(Plan &pl, int m, int n, int k, unsigned flags, int num_sms, bool mma)
 {
+    pl.mma = mma;
+    pl.a_tmem = (flags & W4A16_FLAG_A_SMEM) == 0;
+    const int nt_tc = pick_nt(m, false);
+    const int nt_mma = m <= decode_max_rows() ? pick_nt_mma(m) : nt_tc;
+    const int nt_ws = nt_tc > nt_mma ? nt_tc : nt_mma;
+    const int mt_ws = (m + (nt_tc < nt_mma ? nt_tc : nt_mma) - 1) / (nt_tc < nt_mma ? nt_tc : nt_mma);
+    pl.nt_max = mma ? nt_mma : nt_tc;
+    pl.m_tiles = (m + pl.nt_max - 1) / pl.nt_max;
+    const long long units = (long long)pl.m_tiles * (n / TILE_N) * (k / KBLK);
+    pl.grid = (int)(units < num_sms ? units : num_sms);
+    // carve() sizes counters by tiles_bound and partials by nt_max: use the bounds of both.
+    const int nt_keep = pl.nt_max;
+    pl.tiles_bound = mt_ws * (n / TILE_N);
+    pl.nt_max = nt_ws;
+    const long long a_bytes = (flags & W4A16_FLAG_ACT_ORDER) ? (long long)m * k * 2 : 0;
+    carve(pl, num_sms, a_bytes);
+    pl.nt_max = nt_keep;
+}
+
+void grouped_plan(Plan &pl, int n_pairs, int n_active, int n, int k, unsigned flags, int num_sms)
+{
+    pl.mma = false;
     pl.a_tmem = (flags & W4A16_FLAG_A_SMEM) == 0;
     pl.nt_max = pick_nt(n_pairs, true);
     pl.m_tiles = 0;
     pl.tiles_bound = ((n_pairs + pl.nt_max - 1) / pl.nt_max + n_active) * (n / TILE_N);
     pl.grid = num_sms;
     carve(pl, num_sms, (long long)n_pairs * k * 2);
-    return 0;
 }
 
 void fill_params(GemmParams &p, const Plan &pl, int m, int n, int k, int group_size)
@@ -263,12 +377,35 @@ void fill_params(GemmParams &p, const Plan &pl, int m, int n, int k, int group_s
     p.kblocks = k / KBLK;
     p.stages = pl.stages;
     p.stage_bytes = pl.stage_bytes;
-    p.act_bytes = pl.act_bytes;
+    p.kbs = pl.kbs;
+    p.act_kb_bytes = pl.act_kb_bytes;
+    p.packed_off = pl.packed_off;
+    p.scales_off = pl.scales_off;
+    p.zeros_off = pl.zeros_off;
+    p.sg_box = pl.sg_box;
     p.acc_bufs = pl.acc_bufs;
     p.acc_col0 = pl.acc_col0;
     p.tmem_cols = pl.tmem_cols;
     p.a_slots = pl.a_slots;
     p.seg_smem_off = pl.seg_off;
+}
+
+// Tensor maps of one launch: activations (3-D, swizzled) and the scale / zero rows.  With no
+// zero points the zero map is a copy of the scale map that the kernels never read.
+int encode_maps(const Plan &pl, const void *act, int rows, int k, int ld, const void *scales,
+                const void *zeros, int g_rows, int n, CUtensorMap *ma, CUtensorMap *ms,
+                CUtensorMap *mz)
+{
+    int err = encode_act_map(ma, act, rows, k, ld, pl.nt_max, pl.kbs);
+    if (err == cudaSuccess)
+        err = encode_group_map(ms, scales, g_rows, n, pl.sg_box);
+    if (err == cudaSuccess) {
+        if (zeros)
+            err = encode_group_map(mz, zeros, g_rows, n, pl.sg_box);
+        else
+            *mz = *ms;
+    }
+    return err;
 }
 
 } // namespace
@@ -345,7 +482,7 @@ size_t w4a16_workspace_size(int m, int n, int k, int group_size, unsigned flags,
     if (num_sms <= 0 && sm_count(&num_sms) != cudaSuccess)
         return 0;
     Plan pl;
-    dense_plan(pl, m > 0 ? m : 1, n, k, flags, num_sms);
+    dense_plan(pl, m > 0 ? m : 1, n, k, flags, num_sms, false);
     return (size_t)pl.total;
 }
 
@@ -389,16 +526,21 @@ int w4a16_gemm(const void *a, int lda, const int32_t *b_packed, void *c, int ldc
     if ((flags & W4A16_FLAG_FORCE_SIMT) && m > (1 << 20))
         return status_of(STAGE_UNSUPPORTED, W4A16_ARG_SHAPE);
 
+    const int mma = choose_mma(m, flags);
+    if (mma < 0)
+        return -mma;
+
     int num_sms = 0;
     int err = sm_count(&num_sms);
     if (err != cudaSuccess)
         return status_of(STAGE_RESOURCE, err);
     Plan pl;
-    dense_plan(pl, m, n, k, flags, num_sms);
+    dense_plan(pl, m, n, k, flags, num_sms, mma == 1);
     if (workspace_bytes < (size_t)pl.total)
         return status_of(STAGE_ARG, W4A16_ARG_WORKSPACE);
+    const int g = num_groups(k, group_size);
     plan_tmem(pl);
-    err = plan_smem(pl, false, zeros != nullptr);
+    err = plan_smem(pl, false, zeros != nullptr, group_size == -1 ? k : group_size, g);
     if (err != cudaSuccess)
         return status_of(STAGE_RESOURCE, err);
 
@@ -428,12 +570,14 @@ int w4a16_gemm(const void *a, int lda, const int32_t *b_packed, void *c, int ldc
     if (flags & W4A16_FLAG_FORCE_SIMT)
         return launch_status(launch_gemm_simt(p, a_src, a_ld, stream));
 
-    CUtensorMap map;
-    err = encode_act_map(&map, a_src, m, k, a_ld);
+    CUtensorMap ma, ms, mz;
+    err = encode_maps(pl, a_src, m, k, a_ld, scales, zeros, g, n, &ma, &ms, &mz);
     if (err != cudaSuccess)
         return status_of(STAGE_RESOURCE, err);
     GemmConfig cfg{pl.grid, pl.smem_bytes, pl.a_tmem};
-    return launch_status(launch_gemm(p, map, cfg, stream));
+    if (pl.mma)
+        return launch_status(launch_decode(p, ma, ms, mz, cfg, stream));
+    return launch_status(launch_gemm(p, ma, ms, mz, cfg, stream));
 }
 
 int w4a16_gemm_grouped(const void *a, int lda, const int32_t *b_packed_stack, void *y, int ldy,
@@ -447,7 +591,7 @@ int w4a16_gemm_grouped(const void *a, int lda, const int32_t *b_packed_stack, vo
                            flags);
     if (st)
         return st;
-    if (flags & (W4A16_FLAG_ACT_ORDER | W4A16_FLAG_FORCE_SIMT))
+    if (flags & (W4A16_FLAG_ACT_ORDER | W4A16_FLAG_FORCE_SIMT | W4A16_FLAG_FORCE_MMA))
         return status_of(STAGE_ARG, W4A16_ARG_FLAGS);
     if (n_active <= 0 || n_active > W4A16_MAX_SEGMENTS || n_experts <= 0 || n_pairs <= 0 ||
         n_tokens <= 0 || n_active > n_experts)
@@ -472,8 +616,10 @@ int w4a16_gemm_grouped(const void *a, int lda, const int32_t *b_packed_stack, vo
     grouped_plan(pl, n_pairs, n_active, n, k, flags, num_sms);
     if (workspace_bytes < (size_t)pl.total)
         return status_of(STAGE_ARG, W4A16_ARG_WORKSPACE);
+    const int g = num_groups(k, group_size);
     plan_tmem(pl);
-    err = plan_smem(pl, true, zeros_stack != nullptr);
+    err = plan_smem(pl, true, zeros_stack != nullptr, group_size == -1 ? k : group_size,
+                    g * n_experts);
     if (err != cudaSuccess)
         return status_of(STAGE_RESOURCE, err);
 
@@ -502,12 +648,13 @@ int w4a16_gemm_grouped(const void *a, int lda, const int32_t *b_packed_stack, vo
                              n_pairs, n_tokens, k, p.status, stream);
     if (err != cudaSuccess)
         return status_of(STAGE_LAUNCH, err);
-    CUtensorMap map;
-    err = encode_act_map(&map, a_sorted, n_pairs, k, k);
+    CUtensorMap ma, ms, mz;
+    err = encode_maps(pl, a_sorted, n_pairs, k, k, scales_stack, zeros_stack, g * n_experts, n, &ma,
+                      &ms, &mz);
     if (err != cudaSuccess)
         return status_of(STAGE_RESOURCE, err);
     GemmConfig cfg{pl.grid, pl.smem_bytes, pl.a_tmem};
-    return launch_status(launch_gemm(p, map, cfg, stream));
+    return launch_status(launch_gemm(p, ma, ms, mz, cfg, stream));
 }
 
 int w4a16_csr_from_token_routes(int n_expert, int n_tokens, int experts_per_token,

@@ -7,18 +7,15 @@
 //   selftest_timeout  exercises the bounded wait on a barrier that never completes
 #include "ptx.cuh"
 #include "w4a16_internal.h"
-#include "../../include/w4a16.h"
+#include "w4a16.h"
 
 namespace w4 {
 
-// Bit offset of code e (0..7) inside a tile word: codes 2i, 2i+1 at bits 4i, 16+4i.
-__device__ __forceinline__ int tile_bit(int e)
-{
-    return 4 * (e >> 1) + 16 * (e & 1);
-}
+// Tile words (include/w4a16.h, "Packed tile layout"): word (h, c, j) of a 64 x 128 tile holds,
+// for p in 0..3 and e in 0..1, the code of row 32h + 2j + 8p + e at bit 4p + 16e.
 
-// One thread per output word.  Word o of the tile layout: tile = o / 1024, and inside the
-// tile h = w / 512, column c = (w / 4) % 128, j = w % 4.
+// One thread per output word.  Word o: tile = o / 1024; inside the tile h = w / 512,
+// column c = (w / 4) % 128, j = w % 4.
 __global__ void repack_kernel(const int32_t *__restrict__ qweight, const int32_t *__restrict__ perm,
                               int32_t *__restrict__ out, int32_t *status, int k, int n)
 {
@@ -34,31 +31,37 @@ __global__ void repack_kernel(const int32_t *__restrict__ qweight, const int32_t
         const int c = (w >> 2) & 127;
         const int j = w & 3;
         const int col = nt * TILE_N + c;
-        const int r0 = kb * KBLK + h * 32 + j * 8;
+        const int r0 = kb * KBLK + h * 32 + 2 * j;
         uint32_t word = 0;
         if (perm == nullptr) {
-            const uint32_t src = (uint32_t)qweight[(long long)(r0 >> 3) * n + col];
+            // rows r0 + 8p + {0,1} are nibbles 2j, 2j+1 of GPTQ word (r0 + 8p) / 8
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-                word |= ((src >> (4 * e)) & 0xFu) << tile_bit(e);
+            for (int p = 0; p < 4; ++p) {
+                const uint32_t src = (uint32_t)qweight[(long long)((r0 >> 3) + p) * n + col];
+                word |= ((src >> (8 * j)) & 0xFu) << (4 * p);
+                word |= ((src >> (8 * j + 4)) & 0xFu) << (4 * p + 16);
+            }
         } else {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int row = perm[r0 + e];
-                if (row < 0 || row >= k) {
-                    if (status)
-                        atomicOr(status, W4A16_DEV_PERM);
-                    continue;
+            for (int p = 0; p < 4; ++p)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int row = perm[r0 + 8 * p + e];
+                    if (row < 0 || row >= k) {
+                        if (status)
+                            atomicOr(status, W4A16_DEV_PERM);
+                        continue;
+                    }
+                    const uint32_t src = (uint32_t)qweight[(long long)(row >> 3) * n + col];
+                    word |= ((src >> (4 * (row & 7))) & 0xFu) << (4 * p + 16 * e);
                 }
-                const uint32_t src = (uint32_t)qweight[(long long)(row >> 3) * n + col];
-                word |= ((src >> (4 * (row & 7))) & 0xFu) << tile_bit(e);
-            }
         }
         out[o] = (int32_t)word;
     }
 }
 
-// One thread per GPTQ word (r, col): rows 8r..8r+7 all live in one tile word.
+// One thread per GPTQ word (rows 8r..8r+7 of one column): they are pair p = r % 4 of the four
+// tile words j = 0..3 of their (block, half, column).
 __global__ void unpack_kernel(const int32_t *__restrict__ tiles, int32_t *__restrict__ qweight, int k,
                               int n)
 {
@@ -68,18 +71,19 @@ __global__ void unpack_kernel(const int32_t *__restrict__ tiles, int32_t *__rest
          o += (long long)gridDim.x * blockDim.x) {
         const int r = (int)(o / n);
         const int col = (int)(o - (long long)r * n);
-        const int row0 = r * 8;
-        const int kb = row0 / KBLK;
-        const int h = (row0 % KBLK) / 32;
-        const int j = (row0 % 32) / 8;
+        const int kb = r / 8;
+        const int h = (r % 8) / 4;
+        const int p = r % 4;
         const int nt = col / TILE_N;
         const int c = col % TILE_N;
-        const uint32_t src =
-            (uint32_t)tiles[((long long)nt * kblocks + kb) * TILE_WORDS + h * 512 + c * 4 + j];
+        const int32_t *src = tiles + ((long long)nt * kblocks + kb) * TILE_WORDS + h * 512 + c * 4;
         uint32_t word = 0;
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-            word |= ((src >> tile_bit(e)) & 0xFu) << (4 * e);
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t t = (uint32_t)src[j];
+            word |= ((t >> (4 * p)) & 0xFu) << (8 * j);
+            word |= ((t >> (4 * p + 16)) & 0xFu) << (8 * j + 4);
+        }
         qweight[o] = (int32_t)word;
     }
 }
@@ -90,6 +94,8 @@ __global__ void gather_cols_kernel(const __half *__restrict__ a, int lda,
                                    const int32_t *__restrict__ perm, const int32_t *__restrict__ g_idx,
                                    int group_size, __half *__restrict__ out, int m, int k, int *status)
 {
+    pdl_launch_dependents();
+    pdl_wait();
     for (int row = blockIdx.y; row < m; row += gridDim.y)
         for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < k; i += gridDim.x * blockDim.x) {
             const int src = perm[i];
@@ -111,6 +117,8 @@ __global__ void gather_rows_kernel(const __half *__restrict__ a, int lda,
                                    const int32_t *__restrict__ pair_tok, __half *__restrict__ out,
                                    int n_pairs, int n_tokens, int k, int *status)
 {
+    pdl_launch_dependents();
+    pdl_wait();
     const int r = blockIdx.x;
     const int pair = ex_pairs[r];
     int tok = -1;
@@ -141,10 +149,11 @@ __global__ void gemm_simt_kernel(GemmParams p, const __half *__restrict__ a, int
     for (int row = blockIdx.y; row < p.m; row += gridDim.y) {
     float acc = 0.0f;
     for (int r = 0; r < p.k; ++r) {
-        const int kb = r / KBLK, h = (r % KBLK) / 32, j = (r % 32) / 8, e = r % 8;
+        const int kb = r / KBLK, h = (r % KBLK) / 32, r32 = r % 32;
+        const int pp = r32 / 8, j = (r32 % 8) / 2, e = r32 % 2;
         const uint32_t w =
             (uint32_t)p.b[((long long)nt * p.kblocks + kb) * TILE_WORDS + h * 512 + c * 4 + j];
-        const int q = (w >> tile_bit(e)) & 0xF;
+        const int q = (w >> (4 * pp + 16 * e)) & 0xF;
         const int g = r / p.group_size;
         const __half s = p.scales[(long long)g * p.n + col];
         const __half z = p.zeros ? p.zeros[(long long)g * p.n + col] : __float2half(8.0f);

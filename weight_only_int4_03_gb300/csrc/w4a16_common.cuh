@@ -1,0 +1,429 @@
+// w4a16_common.cuh -- device code shared by the W4A16 GEMM kernels: dequantisation of a tile
+// word, the data-parallel + stream-K work schedule, the grouped schedule table, the TMA
+// producer and the fixed-order split-K reduction.
+#pragma once
+
+#include "ptx.cuh"
+#include "w4a16_internal.h"
+#include "w4a16.h"
+
+namespace w4 {
+
+// ---------------------------------------------------------------------------------------
+// Dequantisation of one tile word (8 codes, 4 pairs) into 4 fp16 pairs (q - z) * s.
+// Pair p sits at bits (4p, 16+4p).  OR-ing a code into the mantissa of 1024.0 (0x6400) gives
+// 1024 + q exactly; a code in the upper nibble of a byte gives 1024 + 16 q, which one FMA by
+// 1/16 turns into 64 + q.  Subtracting (1024 + z) or (64 + z) is exact for integer zero
+// points, so the only rounding is the final product with the scale.  Each pair takes its own
+// scale and zero (the pairs of one word belong to two groups when group_size is 16).
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ __half2 u32_as_h2(uint32_t v)
+{
+    return *reinterpret_cast<__half2 *>(&v);
+}
+
+__device__ __forceinline__ uint32_t h2_as_u32(__half2 v)
+{
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+__device__ __forceinline__ void dequant_word(uint32_t x, const __half2 (&zlo)[4],
+                                             const __half2 (&zhi)[4], const __half2 (&s2)[4],
+                                             uint32_t (&out)[4])
+{
+    const uint32_t magic = 0x64006400u;
+    const __half2 sixteenth = __halves2half2(__ushort_as_half(0x2C00), __ushort_as_half(0x2C00));
+    const uint32_t t0 = (x & 0x000F000Fu) | magic;
+    const uint32_t t1 = (x & 0x00F000F0u) | magic;
+    const uint32_t x8 = x >> 8;
+    const uint32_t t2 = (x8 & 0x000F000Fu) | magic;
+    const uint32_t t3 = (x8 & 0x00F000F0u) | magic;
+    const __half2 v0 = __hsub2(u32_as_h2(t0), zlo[0]);
+    const __half2 v1 = __hfma2(u32_as_h2(t1), sixteenth, zhi[1]);
+    const __half2 v2 = __hsub2(u32_as_h2(t2), zlo[2]);
+    const __half2 v3 = __hfma2(u32_as_h2(t3), sixteenth, zhi[3]);
+    out[0] = h2_as_u32(__hmul2(v0, s2[0]));
+    out[1] = h2_as_u32(__hmul2(v1, s2[1]));
+    out[2] = h2_as_u32(__hmul2(v2, s2[2]));
+    out[3] = h2_as_u32(__hmul2(v3, s2[3]));
+}
+
+// Scales (and zeros) of the four 8-row groups p of half h of a 64-row block: one division per
+// block when a group spans whole blocks (the usual group sizes), else one per 8-row group.
+__device__ __forceinline__ void load_scales(const GemmParams &p, const __half *ssm, const __half *zsm,
+                                            bool has_zp, int kb, int h, int g_first, int gs_kb,
+                                            int col, __half2 (&s2)[4], __half2 (&zlo)[4],
+                                            __half2 (&zhi)[4])
+{
+    if (gs_kb) {
+        const int idx = (kb / gs_kb - g_first) * TILE_N + col;
+        const __half2 s = __half2half2(ssm[idx]);
+        __half2 lo = __float2half2_rn(1032.0f), hi = __float2half2_rn(-72.0f);
+        if (has_zp) {
+            const __half z = zsm[idx];
+            lo = __half2half2(__hadd(__float2half(1024.0f), z));
+            hi = __half2half2(__hneg(__hadd(__float2half(64.0f), z)));
+        }
+#pragma unroll
+        for (int pp = 0; pp < 4; ++pp) {
+            s2[pp] = s;
+            zlo[pp] = lo;
+            zhi[pp] = hi;
+        }
+        return;
+    }
+#pragma unroll
+    for (int pp = 0; pp < 4; ++pp) {
+        const int gl = (kb * KBLK + h * 32 + pp * 8) / p.group_size - g_first;
+        const int idx = gl * TILE_N + col;
+        s2[pp] = __half2half2(ssm[idx]);
+        if (has_zp) {
+            const __half z = zsm[idx];
+            zlo[pp] = __half2half2(__hadd(__float2half(1024.0f), z));
+            zhi[pp] = __half2half2(__hneg(__hadd(__float2half(64.0f), z)));
+        } else {
+            zlo[pp] = __float2half2_rn(1032.0f);
+            zhi[pp] = __float2half2_rn(-72.0f);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------------------
+// Work schedule shared by every role: whole tiles round-robin while at least two full waves
+// remain, then contiguous ranges of (tile, 64-row block) units ("stream-K").
+// ---------------------------------------------------------------------------------------
+
+// 64-bit division is a long software sequence on the GPU; use 32 bits when the operands fit.
+__device__ __forceinline__ long long div_fast(long long a, long long b, bool small)
+{
+    return small ? (long long)((uint32_t)a / (uint32_t)b) : a / b;
+}
+
+struct Sched {
+    int grid, cta, tiles, kblocks, dp_tiles, dp_next;
+    long long sk_units, u, u_end, u_begin;
+    bool small; // sk_units * (grid + 1) fits in 32 bits
+
+    // CTAs beyond the number of work units get nothing, so that the CTAs sharing a split
+    // tile are always consecutive (the fixed-order reduction walks them by index).
+    __device__ void init(int tiles_, int kblocks_)
+    {
+        tiles = tiles_;
+        kblocks = kblocks_;
+        const long long units = (long long)tiles * kblocks;
+        grid = (int)min((long long)gridDim.x, max(units, 1LL));
+        cta = blockIdx.x;
+        const int waves = tiles / grid;
+        if (tiles % grid == 0)
+            dp_tiles = tiles;
+        else
+            dp_tiles = waves >= 2 ? (waves - 1) * grid : 0;
+        dp_next = cta;
+        sk_units = (long long)(tiles - dp_tiles) * kblocks;
+        small = sk_units * (long long)(grid + 1) < (1LL << 32);
+        const bool idle = cta >= grid;
+        u = (sk_units && !idle) ? begin_of(cta) : 0;
+        u_end = (sk_units && !idle) ? begin_of(cta + 1) : 0;
+        u_begin = u;
+        if (idle)
+            dp_next = dp_tiles;
+    }
+
+    // First stream-K unit of CTA c.
+    __device__ __forceinline__ long long begin_of(int c) const
+    {
+        return div_fast((long long)c * sk_units, grid, small);
+    }
+
+    // Next segment of work: tile index and its 64-row block range [kb0, kb1).
+    __device__ bool next(int &tile, int &kb0, int &kb1)
+    {
+        if (dp_next < dp_tiles) {
+            tile = dp_next;
+            kb0 = 0;
+            kb1 = kblocks;
+            dp_next += grid;
+            return true;
+        }
+        if (u < u_end) {
+            const long long t = div_fast(u, kblocks, small);
+            kb0 = (int)(u - t * kblocks);
+            const long long stop = min((t + 1) * kblocks, u_end);
+            kb1 = kb0 + (int)(stop - u);
+            tile = dp_tiles + (int)t;
+            u = stop;
+            return true;
+        }
+        return false;
+    }
+
+    // CTA that owns stream-K unit `unit`.
+    __device__ int owner(long long unit) const
+    {
+        return (int)div_fast((unit + 1) * grid - 1, sk_units, small);
+    }
+};
+
+struct TileInfo {
+    int n0;      // first weight column
+    int row0;    // first activation row (in the tensor map's row space)
+    int rows;    // valid rows
+    int ntok;    // rows rounded up to 16 (tcgen05 N)
+    int expert;  // weight stack index
+};
+
+// Grouped schedule table in shared memory: tile prefix, row offsets, expert ids.
+struct SegTable {
+    int *tile_prefix; // [n_active + 1]
+    int *row_off;     // [n_active + 1]
+    int *expert;      // [n_active]
+};
+
+__device__ __forceinline__ TileInfo tile_info(const GemmParams &p, const SegTable &seg, int tile)
+{
+    TileInfo ti;
+    if (p.ex_off == nullptr) {
+        const int nt = tile / p.m_tiles;
+        const int mt = tile - nt * p.m_tiles;
+        ti.n0 = nt * TILE_N;
+        ti.row0 = mt * p.nt_max;
+        ti.rows = min(p.nt_max, p.m - ti.row0);
+        ti.expert = 0;
+    } else {
+        int lo = 0, hi = p.n_active - 1; // last segment with tile_prefix <= tile
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (seg.tile_prefix[mid] <= tile)
+                lo = mid;
+            else
+                hi = mid - 1;
+        }
+        const int local = tile - seg.tile_prefix[lo];
+        const int cnt = seg.row_off[lo + 1] - seg.row_off[lo];
+        const int mtiles = max(1, (cnt + p.nt_max - 1) / p.nt_max);
+        const int nt = local / mtiles;
+        const int mt = local - nt * mtiles;
+        ti.n0 = nt * TILE_N;
+        ti.row0 = seg.row_off[lo] + mt * p.nt_max;
+        ti.rows = min(p.nt_max, cnt - mt * p.nt_max);
+        ti.expert = seg.expert[lo];
+    }
+    ti.ntok = (ti.rows + 15) & ~15;
+    return ti;
+}
+
+// Ring position and phase, advanced incrementally (no division in the loops).
+struct Ring {
+    int idx = 0;
+    uint32_t phase = 0;
+    __device__ __forceinline__ void advance(int size)
+    {
+        if (++idx == size) {
+            idx = 0;
+            phase ^= 1u;
+        }
+    }
+};
+
+// ---------------------------------------------------------------------------------------
+// TMA producer (one thread).  A stage holds up to p.kbs consecutive 64-row blocks of one
+// segment: their packed codes (one contiguous bulk copy -- copies have a large fixed cost, so
+// they are made as big as the stage allows), the scale/zero rows they touch (one tensor copy
+// each) and their activation rows (one 3-D tensor copy, p.kbs blocks deep).
+// ---------------------------------------------------------------------------------------
+static __device__ void run_producer(const GemmParams &p, const CUtensorMap *tmap_a,
+                                    const CUtensorMap *tmap_s, const CUtensorMap *tmap_z,
+                                    const SegTable &seg, Sched sched, uint8_t *smem,
+                                    uint64_t *full_bars, uint64_t *empty_bars, const WaitCtl &ctl)
+{
+    const bool has_zp = p.zeros != nullptr;
+    const uint32_t fixed_bytes = (uint32_t)p.sg_box * SG_BYTES * (has_zp ? 2u : 1u) +
+                                 (uint32_t)p.kbs * (uint32_t)p.act_kb_bytes;
+    Ring ring;
+    uint32_t issued = 0;
+    int tile, kb0, kb1;
+    bool ok = true;
+    while (ok && sched.next(tile, kb0, kb1)) {
+        const TileInfo ti = tile_info(p, seg, tile);
+        const int32_t *bw = p.b + ti.expert * p.b_expert_words +
+                            ((long long)(ti.n0 / TILE_N) * p.kblocks) * TILE_WORDS;
+        const int grow0 = ti.expert * p.num_groups;
+        for (int kb = kb0; kb < kb1; kb += p.kbs) {
+            const int nkb = min(p.kbs, kb1 - kb);
+            if (!mbar_wait(&empty_bars[ring.idx], ring.phase ^ 1u, ctl, W4A16_DEV_TIMEOUT)) {
+                ok = false;
+                break;
+            }
+            uint64_t *full = &full_bars[ring.idx];
+            uint8_t *st = smem + (size_t)ring.idx * p.stage_bytes;
+            mbar_arrive_expect_tx(full, fixed_bytes + nkb * (uint32_t)TILE_BYTES);
+            bulk_load(st + p.packed_off, bw + (long long)kb * TILE_WORDS, nkb * TILE_BYTES, full);
+            const int g_first = grow0 + (kb * KBLK) / p.group_size;
+            tensor_load_2d(st + p.scales_off, tmap_s, ti.n0, g_first, full);
+            if (has_zp)
+                tensor_load_2d(st + p.zeros_off, tmap_z, ti.n0, g_first, full);
+            // 64 columns x nt_max rows x kbs column blocks, landing as kbs consecutive
+            // [nt_max x 128 B] tiles in the 128-byte swizzle.
+            tensor_load_3d(st, tmap_a, 0, ti.row0, kb, full);
+            ring.advance(p.stages);
+            ++issued;
+        }
+    }
+    // Leave no copy in flight: wait (bounded, ignoring the abort flag) for the last stages.
+    WaitCtl drain_ctl = ctl;
+    volatile int no_abort = 0;
+    drain_ctl.abort_flag = &no_abort;
+    const uint32_t n = issued < (uint32_t)p.stages ? issued : (uint32_t)p.stages;
+    for (uint32_t i = 0; i < n; ++i) {
+        int idx = ring.idx - 1 - (int)i;
+        uint32_t ph = ring.phase;
+        if (idx < 0) {
+            idx += p.stages;
+            ph ^= 1u;
+        }
+        mbar_wait(&full_bars[idx], ph, drain_ctl, W4A16_DEV_TIMEOUT);
+    }
+}
+
+// Builds the grouped schedule table (warp-wide): per active segment its row range, expert
+// and number of tiles; returns the total tile count.  The offsets must form a non-decreasing
+// chain inside [0, n_pairs] and the expert ids must be in range; otherwise the whole schedule
+// is treated as empty and W4A16_DEV_SCHEDULE is reported, so no tile can index past the
+// workspace's counters.
+static __device__ int build_segments(const GemmParams &p, SegTable &seg, int lane)
+{
+    bool bad = false;
+    for (int base = 0; base < p.n_active; base += 32) {
+        const int i = base + lane;
+        bool b = false;
+        if (i < p.n_active) {
+            const int lo = p.ex_off[i], hi = p.ex_off[i + 1], e = p.ex_ids[i];
+            b = lo < 0 || hi < lo || hi > p.n_pairs || e < 0 || e >= p.n_experts;
+        }
+        bad |= __any_sync(0xffffffffu, b);
+    }
+    if (bad) {
+        if (lane == 0)
+            atomicOr(p.status, W4A16_DEV_SCHEDULE);
+        return 0;
+    }
+    int running = 0;
+    for (int base = 0; base < p.n_active; base += 32) {
+        const int i = base + lane;
+        int tiles_i = 0;
+        if (i < p.n_active) {
+            const int lo = p.ex_off[i], hi = p.ex_off[i + 1];
+            seg.row_off[i] = lo;
+            seg.expert[i] = p.ex_ids[i];
+            if (i == p.n_active - 1)
+                seg.row_off[i + 1] = hi;
+            tiles_i = ((hi - lo + p.nt_max - 1) / p.nt_max) * p.n_tiles;
+        }
+        int incl = tiles_i; // inclusive warp scan
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, d);
+            if (lane >= d)
+                incl += v;
+        }
+        if (i < p.n_active)
+            seg.tile_prefix[i] = running + incl - tiles_i;
+        running += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0)
+        seg.tile_prefix[p.n_active] = running;
+    __syncwarp();
+    return running;
+}
+
+// ---------------------------------------------------------------------------------------
+// Split (stream-K) tiles.  Every CTA that covers part of a tile's 64-row blocks writes an
+// fp32 partial into one of its two workspace slots (0: the tile where its range starts,
+// 1: its last tile); the last of them to arrive sums all partials in CTA order.
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ float *partial_slot(const GemmParams &p, int cta, int slot)
+{
+    return p.partials + ((long long)(cta * 2 + slot) * p.nt_max) * TILE_N;
+}
+
+// This CTA's slot for stream-K tile st_tile.
+__device__ __forceinline__ int own_slot(const GemmParams &p, const Sched &sched, long long st_tile)
+{
+    return sched.u_begin >= st_tile * p.kblocks ? 0 : 1;
+}
+
+// Output row of tile row `row`: dense rows are in place; grouped rows go to pair ex_pairs[.].
+// Returns -1 (and reports) for an out-of-range pair.
+__device__ __forceinline__ int output_row(const GemmParams &p, const TileInfo &ti, int row)
+{
+    int out_row = ti.row0 + row;
+    if (p.ex_off != nullptr) {
+        out_row = p.ex_pairs[out_row];
+        if (out_row < 0 || out_row >= p.n_pairs) {
+            atomicOr(p.status, W4A16_DEV_SCHEDULE);
+            return -1;
+        }
+    }
+    return out_row;
+}
+
+// Contributors c_lo..c_hi of stream-K tile st_tile and the slot of the first one (the others
+// start inside the tile, so they use slot 0).
+struct Contributors {
+    int lo, hi, lo_slot;
+};
+
+__device__ __forceinline__ Contributors contributors(const GemmParams &p, const Sched &sched,
+                                                     long long st_tile)
+{
+    const long long u0 = st_tile * p.kblocks;
+    Contributors c;
+    c.lo = sched.owner(u0);
+    c.hi = sched.owner(u0 + p.kblocks - 1);
+    c.lo_slot = sched.begin_of(c.lo) >= u0 ? 0 : 1;
+    return c;
+}
+
+// Sum the partials of a split tile in contributor order and write fp16 C.  Thread `tid` of
+// `nthreads` takes (row, 4-column quad) items; loads of up to four contributors are issued
+// together so that their latencies overlap.
+static __device__ void reduce_tile(const GemmParams &p, const TileInfo &ti, const Contributors &cb,
+                                   int tid, int nthreads)
+{
+    for (int item = tid; item < ti.rows * (TILE_N / 4); item += nthreads) {
+        const int row = item / (TILE_N / 4);
+        const int cq = item % (TILE_N / 4);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int c0 = cb.lo; c0 <= cb.hi; c0 += 4) {
+            float4 v[4];
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                const int c = c0 + cc;
+                const float4 *pc = reinterpret_cast<const float4 *>(
+                    partial_slot(p, c, c == cb.lo ? cb.lo_slot : 0));
+                v[cc] = (c <= cb.hi) ? __ldcg(pc + row * (TILE_N / 4) + cq)
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                if (c0 + cc > cb.hi)
+                    break;
+                acc.x += v[cc].x;
+                acc.y += v[cc].y;
+                acc.z += v[cc].z;
+                acc.w += v[cc].w;
+            }
+        }
+        const int out_row = output_row(p, ti, row);
+        if (out_row < 0)
+            continue;
+        const __half2 lo = __floats2half2_rn(acc.x, acc.y);
+        const __half2 hi = __floats2half2_rn(acc.z, acc.w);
+        uint2 packed;
+        packed.x = *reinterpret_cast<const uint32_t *>(&lo);
+        packed.y = *reinterpret_cast<const uint32_t *>(&hi);
+        *reinterpret_cast<uint2 *>(p.c + (long long)out_row * p.ldc + ti.n0 + 4 * cq) = packed;
+    }
+}
+
+} // namespace w4

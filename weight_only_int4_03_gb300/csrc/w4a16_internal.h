@@ -10,30 +10,27 @@ namespace w4 {
 
 // Packed tile geometry (see include/w4a16.h, "Packed tile layout").
 constexpr int TILE_N = 128;      // weight columns per tile = tcgen05 M (weights are the A operand)
-constexpr int KBLK = 64;         // K rows per tile / per pipeline stage
+constexpr int KBLK = 64;         // K rows per tile
 constexpr int TILE_WORDS = 1024; // 32-bit words per tile
 constexpr int TILE_BYTES = 4096;
 
 // Pipeline geometry.
-constexpr int MAX_SG = 5;        // scale rows a 64-row block can touch (group_size 16 -> 4, +1)
-constexpr int SG_BYTES = TILE_N * 2;
-constexpr int MAX_A_SLOTS = 12;  // dequantised-weight ring in tensor memory (runtime size)
-constexpr int SMEM_A_SLOTS = 4;  // ... or in shared memory
-constexpr int A_SLOT_COLS = 32;  // tensor-memory columns per slot: 64 fp16 per lane
+constexpr int SG_BYTES = TILE_N * 2; // one scale (or zero) row of a column tile
+constexpr int MAX_A_SLOTS = 12;      // dequantised-weight ring in tensor memory (runtime size)
+constexpr int SMEM_A_SLOTS = 4;      // ... or in shared memory
+constexpr int A_SLOT_COLS = 32;      // tensor-memory columns per slot: 64 fp16 per lane
 constexpr int A_SLOT_BYTES = TILE_N * KBLK * 2;
 constexpr int MAX_STAGES = 16;
-constexpr int BOX_ROWS = 16;     // activation rows per tensor copy (64 fp16 = 128 B wide)
-constexpr int MAX_TOK = 256;     // activation rows per tile = tcgen05 N upper bound
+constexpr int MAX_TOK = 256;         // activation rows per tile = tcgen05 N upper bound
 
-// Warp roles of the GEMM kernel.
+// Warp roles of the tcgen05 GEMM kernel.
 constexpr int NUM_THREADS = 512;
 constexpr int PRODUCER_WARP = 0;
 constexpr int MMA_WARP = 1;
 constexpr int SEG_WARP = 2;      // builds the grouped schedule table at start-up
 constexpr int EPI_WARP0 = 4;     // warps 4..7: one per tensor-memory lane quarter
-constexpr int DQ_WARP0 = 8;      // warps 8..15: two per lane quarter (one per 32-row half)
+constexpr int DQ_WARP0 = 8;      // warps 8..15: two sets of four (one warp per lane quarter)
 constexpr int DQ_WARPS = 8;
-constexpr int DQ_THREADS = DQ_WARPS * 32;
 constexpr int EPI_THREADS = 128;
 
 constexpr int MAX_SEGMENTS = 1024;
@@ -54,7 +51,11 @@ struct GemmParams {
     int nt_max;               // activation rows per tile (multiple of 16, <= 256)
     int m_tiles;              // dense: ceil(m / nt_max)
     int n_tiles, kblocks;
-    int stages, stage_bytes, act_bytes;
+    int stages, stage_bytes;
+    int kbs;                  // 64-row blocks per pipeline stage
+    int act_kb_bytes;         // activation bytes per block in a stage (nt_max rows x 128 B)
+    int packed_off, scales_off, zeros_off; // byte offsets inside a stage
+    int sg_box;               // scale rows copied per stage
     int acc_bufs, acc_col0, tmem_cols;
     int a_slots;              // dequantised-weight ring slots (<= MAX_A_SLOTS)
     int seg_smem_off;         // grouped: byte offset of the schedule table in dynamic smem
@@ -74,8 +75,10 @@ struct GemmConfig {
 };
 
 // Launchers (return a cudaError_t value).
-int launch_gemm(const GemmParams &p, const CUtensorMap &tmap_a, const GemmConfig &cfg,
-                cudaStream_t stream);
+int launch_gemm(const GemmParams &p, const CUtensorMap &tmap_a, const CUtensorMap &tmap_s,
+                const CUtensorMap &tmap_z, const GemmConfig &cfg, cudaStream_t stream);
+int launch_decode(const GemmParams &p, const CUtensorMap &tmap_a, const CUtensorMap &tmap_s,
+                  const CUtensorMap &tmap_z, const GemmConfig &cfg, cudaStream_t stream);
 int launch_gemm_simt(const GemmParams &p, const __half *a, int lda, cudaStream_t stream);
 int launch_repack(const int32_t *qweight, const int32_t *perm, int32_t *out, int32_t *status, int k,
                   int n, cudaStream_t stream);
@@ -88,7 +91,9 @@ int launch_gather_rows(const __half *a, int lda, const int32_t *ex_pairs, const 
 int launch_selftest_timeout(int *status, unsigned long long limit_ns, cudaStream_t stream);
 int gemm_smem_limit(int *bytes);
 
-// Dynamic shared memory the GEMM kernel needs beyond the stages.
+// Dynamic shared memory the kernels need beyond the stages.
 int gemm_extra_smem(bool a_tmem, bool grouped);
+int decode_extra_smem();
+int decode_max_rows();
 
 } // namespace w4
