@@ -65,6 +65,7 @@ extern "C" {
 #define W4A16_ARG_GROUP 7       /* group_size not -1 or a positive multiple of 16 dividing K  */
 #define W4A16_ARG_TYPE 8        /* unknown weight type                                         */
 #define W4A16_ARG_SCHEDULE 9    /* grouped schedule sizes out of range                         */
+#define W4A16_ARG_SCRATCH 10    /* w4a16_gemm_noalloc: the call needs more scratch than it has */
 
 /* Device-side error bits (stage 7), accumulated in the workspace status word. */
 #define W4A16_DEV_TIMEOUT 1     /* a bounded wait inside a kernel ran out                      */
@@ -139,6 +140,31 @@ int w4a16_gemm(const void *a, int lda, const int32_t *b_packed, void *c, int ldc
                const void *scales, const void *zeros, const int32_t *g_idx, const int32_t *perm,
                void *workspace, size_t workspace_bytes, int m, int n, int k, int group_size,
                int weight_type, unsigned flags, cudaStream_t stream);
+
+/* Device scratch of w4a16_gemm_noalloc, per GPU that loads the library (held until exit). */
+#define W4A16_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+/* w4a16_gemm without a workspace argument, for callers that cannot allocate device memory
+ * (code running inside a host callback or an allocator hook, under a framework's sealed
+ * memory pool, or in a plug-in whose host offers neither an allocator nor a workspace).  It
+ * allocates nothing: the scratch that w4a16_gemm keeps in the caller's workspace lives in a
+ * fixed device array of W4A16_NOALLOC_SCRATCH_BYTES inside the library.  The pages have no
+ * counterpart of this entry point; it is this library's own.
+ *   Arguments as w4a16_gemm, minus workspace / workspace_bytes, plus
+ *   status_out  device int32 or NULL, 4-byte aligned: receives (stream-ordered) the call's
+ *               device-side error bits (W4A16_DEV_*), 0 when all went well
+ * A call whose w4a16_workspace_size exceeds the array (on a 152-multiprocessor GPU: M above
+ * 96 rows, fewer with act-order, whose copy of A adds M*K*2 bytes) returns stage 2 with
+ * detail W4A16_ARG_SCRATCH and launches nothing.
+ * The first call on a device looks up the array's device address (once per device); make
+ * that first call before any stream capture.  Each call clears the status word and tile
+ * counters it needs on `stream` before its kernels run.  All calls on one device share the
+ * array: calls whose work overlaps on the GPU (other streams, other host threads) race and
+ * produce wrong results, so serialise them. */
+int w4a16_gemm_noalloc(const void *a, int lda, const int32_t *b_packed, void *c, int ldc,
+                       const void *scales, const void *zeros, const int32_t *g_idx,
+                       const int32_t *perm, int32_t *status_out, int m, int n, int k,
+                       int group_size, int weight_type, unsigned flags, cudaStream_t stream);
 
 /* Workspace bytes for w4a16_gemm_grouped (same rules as w4a16_workspace_size). */
 size_t w4a16_grouped_workspace_size(int n_pairs, int n_active, int n, int k, int group_size,

@@ -32,6 +32,8 @@ W4A16_DEV_GIDX = 4
 W4A16_DEV_SCHEDULE = 8
 
 W4A16_MAX_SEGMENTS = 1024
+W4A16_ARG_SCRATCH = 10
+W4A16_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"libw4a16.so is not built ({LIB_PATH}); run weight_only_int4_03_gb300.build.build()")
@@ -51,6 +53,7 @@ _SIGNATURES = {
     "w4_unpack": (_I, [_P, _P, _I, _I, _P]),
     "w4a16_workspace_size": (_SZ, [_I, _I, _I, _I, _U, _I]),
     "w4a16_gemm": (_I, [_P, _I, _P, _P, _I, _P, _P, _P, _P, _P, _SZ, _I, _I, _I, _I, _I, _U, _P]),
+    "w4a16_gemm_noalloc": (_I, [_P, _I, _P, _P, _I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _U, _P]),
     "w4a16_grouped_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _U, _I]),
     "w4a16_gemm_grouped": (_I, [_P, _I, _P, _P, _I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
                                 _I, _I, _U, _P, _SZ, _P]),
@@ -147,6 +150,21 @@ def w4a16_gemm(a, b_packed, c, scales, zeros, g_idx, perm, workspace, m: int, n:
         _ptr(a), lda, _ptr(b_packed), _ptr(c), ldc, _ptr(scales), _ptr(zeros), _ptr(g_idx),
         _ptr(perm), _ptr(workspace), workspace_bytes, m, n, k, group_size, weight_type, flags,
         _stream(stream)))
+
+
+def w4a16_gemm_noalloc(a, b_packed, c, scales, zeros, g_idx, perm, m: int, n: int, k: int,
+                       group_size: int, weight_type: int, flags: int = 0, status_out=None,
+                       lda: int | None = None, ldc: int | None = None, stream=None) -> None:
+    """w4a16_gemm with no workspace argument, for callers that cannot allocate device memory:
+    the scratch is a fixed array inside the library (include/w4a16.h).  `status_out`, a
+    device int32 tensor or None, receives the call's W4A16_DEV_* bits."""
+    if lda is None:
+        lda = k
+    if ldc is None:
+        ldc = n
+    _check("w4a16_gemm_noalloc", _lib.w4a16_gemm_noalloc(
+        _ptr(a), lda, _ptr(b_packed), _ptr(c), ldc, _ptr(scales), _ptr(zeros), _ptr(g_idx),
+        _ptr(perm), _ptr(status_out), m, n, k, group_size, weight_type, flags, _stream(stream)))
 
 
 def w4a16_gemm_grouped(a, b_packed_stack, y, scales_stack, zeros_stack, ex_ids, ex_off, ex_pairs,
