@@ -75,20 +75,30 @@ struct WaitCtl {
     unsigned long long limit_ns;
 };
 
+// Slow path.  A waiting warp would otherwise keep issuing (the hardware parks try_wait only
+// briefly), taking issue slots and integer-pipe cycles from the warps that have work; so it
+// backs off with a growing sleep (32 .. 256 ns) and looks at the abort flag and the clock
+// only every 8th round.
 static __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, const WaitCtl &ctl,
                                               int timeout_bit)
 {
     const uint64_t t0 = global_timer_ns();
-    for (;;) {
+    uint32_t sleep_ns = 32;
+    for (uint32_t round = 1;; ++round) {
+        __nanosleep(sleep_ns);
+        if (sleep_ns < 256)
+            sleep_ns <<= 1;
         if (mbar_try_wait(bar, parity))
             return true;
-        if (*ctl.abort_flag)
-            return false;
-        if (global_timer_ns() - t0 > ctl.limit_ns) {
-            *ctl.abort_flag = 1;
-            if (ctl.status)
-                atomicOr(ctl.status, timeout_bit);
-            return false;
+        if ((round & 7) == 0) {
+            if (*ctl.abort_flag)
+                return false;
+            if (global_timer_ns() - t0 > ctl.limit_ns) {
+                *ctl.abort_flag = 1;
+                if (ctl.status)
+                    atomicOr(ctl.status, timeout_bit);
+                return false;
+            }
         }
     }
 }

@@ -131,11 +131,13 @@ int pick_nt(int m, bool grouped)
     return m <= MAX_TOK ? (int)round_up(m, 16) : MAX_TOK;
 }
 
-// Token-tile height of the small-M kernel: 8 rows (one m16n8 fragment's useful half) for
-// M <= 8, else M rounded up to the m16 fragment height.
+// Token-tile height of the small-M kernel: the smallest of 8, 16, 32, 64 rows that holds M.
 int pick_nt_mma(int m)
 {
-    return m <= 8 ? 8 : (int)round_up(m, 16);
+    int nt = 8;
+    while (nt < m)
+        nt <<= 1;
+    return nt;
 }
 
 // Stage geometry: [activations kbs x nt_max x 128 B | packed kbs x 4 KiB | scales | zeros].
@@ -185,7 +187,7 @@ int plan_smem(Plan &pl, bool grouped, bool has_zp, int group_size, int g_rows)
     int err = smem_limit(&limit);
     if (err != cudaSuccess)
         return err;
-    const int extra = pl.mma ? decode_extra_smem() : gemm_extra_smem(pl.a_tmem, grouped);
+    const int extra = pl.mma ? decode_extra_smem(pl.nt_max) : gemm_extra_smem(pl.a_tmem, grouped);
     int kbs = stage_blocks_default();
     if (!pl.mma && kbs > pl.a_slots)
         kbs = pl.a_slots;

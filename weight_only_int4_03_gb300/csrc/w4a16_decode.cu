@@ -1,24 +1,35 @@
 // w4a16_decode.cu -- the small-M W4A16 GEMM: weights dequantised in registers straight into
 // warp-level mma.sync (m16n8k16), for decode-sized M (up to 64 rows).
 //
-// Why a second kernel: at small M the job is to stream the packed weights at HBM speed.  The
-// tcgen05 kernel stages every dequantised weight in tensor (or shared) memory and reads it
-// back as an MMA operand, and a 128x16x16 tcgen05.mma costs about as much as a 128x64x16 one;
-// both cap the weight rate well below the HBM rate.  Here each thread converts the 8 codes of
-// one tile word -- which the tile layout makes exactly its m16n8k16 B fragment for two 16-row
-// steps -- and feeds the fp16 registers to mma.sync directly; the activations (A, m16 x k16 per
-// step) come from shared memory through ldmatrix.  Only the 4-bit codes, scales and
-// activations move on chip.
+// Why a second kernel: at small M the job is to stream the packed weights at HBM speed, which
+// leaves a budget of roughly 20 warp instructions per 32-bit word of codes.  The tcgen05
+// kernel stages every dequantised weight in tensor (or shared) memory and reads it back as an
+// MMA operand, and a 128x16x16 tcgen05.mma costs about as much as a 128x64x16 one; both cap
+// the weight rate well below the HBM rate.  Here the weights never leave registers.
 //
-// CTA: one TMA producer warp (the producer of w4a16_common.cuh) and 16 compute warps, warp g
-// owning the 8 weight columns 8g..8g+7 of the 128-column tile.  Work is split over CTAs with
-// the same data-parallel + stream-K schedule; split tiles are reduced in a fixed order by the
-// last contributor.
+// Operand roles ("swap-AB", as in the tcgen05 kernel): the weights are the MMA's A operand
+// (16 weight columns x 16 k), the activations its B operand (16 k x 8 tokens), so one MMA
+// consumes 256 weights whatever M is, and one B fragment (loaded from the swizzled stage by
+// ldmatrix) serves a whole warp's 16 columns.  The tile layout puts in each 32-bit word
+// exactly what one lane needs of an A fragment for two 16-row k steps: word j of column c
+// holds rows 8p + 2j + {0,1}, p = 0..3, i.e. fragment registers a0 / a2 of step 0 (p = 0, 1)
+// and of step 1 (p = 2, 3); column c + 8 gives a1 / a3.
+//
+// Budget: the integer pipe is the limit, so the loop is kept to the dequantisation proper
+// (13 instructions per 8 codes, 5 of them integer), two shared loads, one ldmatrix and two
+// MMAs per 64-row block.  When a group covers whole blocks (group_size % 64 == 0) a lane's
+// scale and zero change only where a group ends, which a per-stage bit mask marks.
+//
+// CTA: one TMA producer warp (the producer of w4a16_common.cuh) and 16 compute warps; warp w
+// owns 16 weight columns (w & 7) and one 32-row half (w >> 3) of every 64-row block.  The two
+// halves are summed through shared memory at the end of a segment.  Work is split over CTAs
+// with the same data-parallel + stream-K schedule as the tcgen05 kernel; split tiles are
+// reduced in a fixed order by the last contributor.
 #include "w4a16_common.cuh"
 
 namespace w4 {
 
-constexpr int DEC_WARPS = 16;                 // compute warps (one 8-column group each)
+constexpr int DEC_WARPS = 16; // compute warps
 constexpr int DEC_THREADS = (DEC_WARPS + 1) * 32;
 
 struct DecBars {
@@ -34,37 +45,107 @@ __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t (&r)[4])
                  : "r"(addr));
 }
 
-__device__ __forceinline__ void ldmatrix_x2(uint32_t addr, uint32_t &r0, uint32_t &r1)
+__device__ __forceinline__ uint32_t lds32(uint32_t addr)
 {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];"
-                 : "=r"(r0), "=r"(r1)
-                 : "r"(addr));
+    uint32_t v;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
 }
 
-// D (f32 16x8) += A (f16 16x16, row) * B (f16 16x8, col)
-__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                          uint32_t b1)
+// D (f32 16x8) += A (f16 16x16, row) * B (f16 16x8, col).  Registers only, so the compiler
+// may schedule it freely.
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1)
 {
-    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
                  "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
                  : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// MT m16 row tiles; HALF: at most 8 rows, held as 8-row activation tiles (the MMA's rows
-// 8..15 are zero registers).
-template <int MT, bool HALF>
-__device__ void run_compute(const GemmParams &p, Sched sched, uint8_t *smem, DecBars &bars,
-                            const WaitCtl &ctl, int g, int lane, volatile int *last_flag)
+// Codes -> fp16 pairs (q - z) * s for one column (one scale and zero for all 8 codes): pair p
+// of word x sits at bits (4p, 16 + 4p).  (q - z) is exact; the product is rounded once.
+__device__ __forceinline__ void dequant_word_col(uint32_t x, __half2 zlo, __half2 zhi, __half2 s,
+                                                 uint32_t (&out)[4])
+{
+    const uint32_t magic = 0x64006400u;
+    const __half2 sixteenth = __halves2half2(__ushort_as_half(0x2C00), __ushort_as_half(0x2C00));
+    const uint32_t x8 = x >> 8;
+    out[0] = h2_as_u32(__hmul2(__hsub2(u32_as_h2((x & 0x000F000Fu) | magic), zlo), s));
+    out[1] = h2_as_u32(__hmul2(__hfma2(u32_as_h2((x & 0x00F000F0u) | magic), sixteenth, zhi), s));
+    out[2] = h2_as_u32(__hmul2(__hsub2(u32_as_h2((x8 & 0x000F000Fu) | magic), zlo), s));
+    out[3] = h2_as_u32(__hmul2(__hfma2(u32_as_h2((x8 & 0x00F000F0u) | magic), sixteenth, zhi), s));
+}
+
+// Scale (as a broadcast pair) and (1024 + z), -(64 + z) of column `col` in group row `grp` of
+// a stage; the zero offsets are constants for u4b8 (z = 8).
+struct ColGroup {
+    __half2 s, zlo, zhi;
+};
+
+__device__ __forceinline__ ColGroup col_group(bool has_zp, const __half *ssm, const __half *zsm,
+                                              int idx)
+{
+    ColGroup cgp;
+    cgp.s = __half2half2(ssm[idx]);
+    if (has_zp) {
+        const __half z = zsm[idx];
+        cgp.zlo = __half2half2(__hadd(__ushort_as_half(0x6400), z));         // 1024 + z
+        cgp.zhi = __half2half2(__hneg(__hadd(__ushort_as_half(0x5400), z))); // -(64 + z)
+    } else {
+        cgp.zlo = __half2half2(__ushort_as_half(0x6408)); // 1032
+        cgp.zhi = __half2half2(__ushort_as_half(0xD480)); // -72
+    }
+    return cgp;
+}
+
+// One 64-row block of a warp's 16 columns x 32 rows: two code words per lane (columns col0
+// and col0 + 8) dequantised into A fragments for two k steps, times the B fragments of every
+// 8-token tile.  `w_addr` / `act` are shared-memory addresses of the lane's first word and of
+// its ldmatrix row in the block.
+template <int NT>
+__device__ __forceinline__ void block_mma(uint32_t w_addr, uint32_t act, const ColGroup &c0,
+                                          const ColGroup &c1, float (&acc)[NT][4])
+{
+    uint32_t a0[4], a1[4];
+    dequant_word_col(lds32(w_addr), c0.zlo, c0.zhi, c0.s, a0);
+    dequant_word_col(lds32(w_addr + 128), c1.zlo, c1.zhi, c1.s, a1);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        uint32_t b[4];
+        ldmatrix_x4(act + nt * 1024, b);
+        mma_16816(acc[nt], a0[0], a1[0], a0[1], a1[1], b[0], b[1]);
+        mma_16816(acc[nt], a0[2], a1[2], a0[3], a1[3], b[2], b[3]);
+    }
+}
+
+constexpr int DEC_UNROLL = 8; // stages of exactly this many blocks take the unrolled path
+
+// NT: 8-token tiles per CTA tile (nt_max = 8 * NT).  BLOCK_GROUPS: group_size is a multiple
+// of 64, so a group covers whole blocks and one scale serves all of a lane's codes in a
+// block; otherwise each 8-row pair looks up its own group (slow, general path).
+template <int NT, bool BLOCK_GROUPS>
+__device__ void run_compute(const GemmParams &p, Sched sched, uint8_t *smem, float *red,
+                            DecBars &bars, const WaitCtl &ctl, int w, int lane,
+                            volatile int *last_flag)
 {
     const bool has_zp = p.zeros != nullptr;
     const int gs = p.group_size;
-    const int gs_kb = (gs % KBLK == 0) ? gs / KBLK : 0;
-    const int col_in_tile = 8 * g + (lane >> 2);   // B / scale column of this thread
-    // ldmatrix: matrix i = lane / 8 covers rows 8*(i&1).. and 16-byte chunk (i>>1) of a step
-    // (x4); for the 8-row tiles, matrix i = lane / 8 (0, 1) is chunk i of rows 0..7 (x2).
-    const int lm_row = HALF ? (lane & 7) : (lane & 7) + 8 * ((lane >> 3) & 1);
-    const int lm_chunk = HALF ? ((lane >> 3) & 1) : (lane >> 4);
+    const int gs_kb = BLOCK_GROUPS ? gs / KBLK : 1;
+    const bool gs_pow2 = (gs_kb & (gs_kb - 1)) == 0;
+    // Bit b of ends64: block b (counted from a group start) is the last of its group.
+    unsigned long long ends64 = 0;
+    if (gs_kb <= 32)
+        for (int b = gs_kb - 1; b < 64; b += gs_kb)
+            ends64 |= 1ull << b;
+    const int cg = w & 7, h = w >> 3;
+    const int t = lane & 3;
+    const int col0 = cg * 16 + (lane >> 2); // this lane's weight columns: col0 and col0 + 8
+    const uint32_t w_off = (uint32_t)(h * 512 + col0 * 4 + t) * 4u;
+    // ldmatrix.x4: matrix i = lane / 8 is 16-byte chunk h*4 + i of token rows 0..7 of an
+    // 8-token tile, so registers (0, 1) are the B fragment of k step 0 and (2, 3) of step 1.
+    const uint32_t lm_off = (uint32_t)((lane & 7) * 128 + (((h * 4 + (lane >> 3)) ^ (lane & 7)) << 4));
+    float *my_red = red + (cg * 32 + lane) * NT * 4;
     Ring ring;
     uint32_t nsync = 0;
     auto rendezvous = [&]() -> bool {
@@ -79,12 +160,13 @@ __device__ void run_compute(const GemmParams &p, Sched sched, uint8_t *smem, Dec
     int tile, kb0, kb1;
     while (sched.next(tile, kb0, kb1)) {
         const TileInfo ti = tile_info(p, no_seg, tile);
-        float acc[MT][4];
+        float acc[NT][4];
 #pragma unroll
-        for (int mt = 0; mt < MT; ++mt)
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int i = 0; i < 4; ++i)
-                acc[mt][i] = 0.f;
+                acc[nt][i] = 0.f;
+        int in_grp = BLOCK_GROUPS ? kb0 % gs_kb : 0; // blocks of the current group before kb
         for (int kb = kb0; kb < kb1; kb += p.kbs) {
             const int nkb = min(p.kbs, kb1 - kb);
             if (!mbar_wait(&bars.full[ring.idx], ring.phase, ctl, W4A16_DEV_TIMEOUT))
@@ -92,39 +174,61 @@ __device__ void run_compute(const GemmParams &p, Sched sched, uint8_t *smem, Dec
             const uint8_t *st = smem + (size_t)ring.idx * p.stage_bytes;
             const __half *ssm = reinterpret_cast<const __half *>(st + p.scales_off);
             const __half *zsm = reinterpret_cast<const __half *>(st + p.zeros_off);
-            const int g_first = (kb * KBLK) / gs;
-            for (int j = 0; j < nkb; ++j) {
-                const int kbj = kb + j;
-                const uint32_t act = smem_u32(st + j * p.act_kb_bytes);
-                const uint32_t *packed =
-                    reinterpret_cast<const uint32_t *>(st + p.packed_off + j * TILE_BYTES);
-                const uint32_t w0 = packed[32 * g + lane];
-                const uint32_t w1 = packed[512 + 32 * g + lane];
+            const uint32_t w_addr = smem_u32(st + p.packed_off) + w_off;
+            const uint32_t act = smem_u32(st) + lm_off;
+            if (BLOCK_GROUPS) {
+                // Bit j of gend: block kb + j is the last of its group.
+                uint32_t gend;
+                if (gs_kb <= 32) {
+                    gend = (uint32_t)(ends64 >> in_grp);
+                } else {
+                    const int e = gs_kb - 1 - in_grp;
+                    gend = e < 32 ? 1u << e : 0u;
+                }
+                in_grp += nkb;
+                if (in_grp >= gs_kb)
+                    in_grp = gs_pow2 ? (in_grp & (gs_kb - 1)) : in_grp % gs_kb;
+                int gidx = col0; // scale index of the current group (relative to the stage's)
+                ColGroup c0 = col_group(has_zp, ssm, zsm, gidx);
+                ColGroup c1 = col_group(has_zp, ssm, zsm, gidx + 8);
+                auto next_group = [&]() {
+                    gidx += TILE_N;
+                    c0 = col_group(has_zp, ssm, zsm, gidx);
+                    c1 = col_group(has_zp, ssm, zsm, gidx + 8);
+                };
+                if (nkb == DEC_UNROLL) {
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    __half2 s2[4], zlo[4], zhi[4];
-                    load_scales(p, ssm, zsm, has_zp, kbj, h, g_first, gs_kb, col_in_tile, s2, zlo,
-                                zhi);
-                    uint32_t b[4];
-                    dequant_word(h ? w1 : w0, zlo, zhi, s2, b);
-#pragma unroll
-                    for (int step = 0; step < 2; ++step) {
-                        const int chunk = (h * 2 + step) * 2 + lm_chunk;
-#pragma unroll
-                        for (int mt = 0; mt < MT; ++mt) {
-                            const int r = mt * 16 + lm_row;
-                            const uint32_t addr = act + r * 128 + ((chunk ^ (r & 7)) << 4);
-                            uint32_t a[4];
-                            if (HALF) {
-                                ldmatrix_x2(addr, a[0], a[2]);
-                                a[1] = 0u;
-                                a[3] = 0u;
-                            } else {
-                                ldmatrix_x4(addr, a);
-                            }
-                            mma_16816(acc[mt], a, b[2 * step], b[2 * step + 1]);
-                        }
+                    for (int j = 0; j < DEC_UNROLL; ++j) {
+                        block_mma<NT>(w_addr + j * TILE_BYTES, act + j * p.act_kb_bytes, c0, c1, acc);
+                        if (j + 1 < DEC_UNROLL && (gend & (1u << j)))
+                            next_group();
                     }
+                } else {
+                    for (int j = 0; j < nkb; ++j) {
+                        block_mma<NT>(w_addr + j * TILE_BYTES, act + j * p.act_kb_bytes, c0, c1, acc);
+                        if (j + 1 < nkb && (gend & (1u << j)))
+                            next_group();
+                    }
+                }
+            } else {
+                const int g_first = (kb * KBLK) / gs;
+                const uint32_t *pw = reinterpret_cast<const uint32_t *>(st + p.packed_off) + w_off / 4;
+                for (int j = 0; j < nkb; ++j) {
+                    uint32_t a0[4], a1[4];
+                    __half2 s2[4], zl[4], zh[4];
+                    load_scales(p, ssm, zsm, has_zp, kb + j, h, g_first, 0, col0, s2, zl, zh);
+                    dequant_word(pw[0], zl, zh, s2, a0);
+                    load_scales(p, ssm, zsm, has_zp, kb + j, h, g_first, 0, col0 + 8, s2, zl, zh);
+                    dequant_word(pw[32], zl, zh, s2, a1);
+                    const uint32_t actj = act + j * p.act_kb_bytes;
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        uint32_t b[4];
+                        ldmatrix_x4(actj + nt * 1024, b);
+                        mma_16816(acc[nt], a0[0], a1[0], a0[1], a1[1], b[0], b[1]);
+                        mma_16816(acc[nt], a0[2], a1[2], a0[3], a1[3], b[2], b[3]);
+                    }
+                    pw += TILE_WORDS;
                 }
             }
             __syncwarp();
@@ -133,34 +237,44 @@ __device__ void run_compute(const GemmParams &p, Sched sched, uint8_t *smem, Dec
             ring.advance(p.stages);
         }
 
-        // Segment end: fp16 C for a whole tile, else an fp32 partial and the split protocol.
-        const bool whole = (kb0 == 0 && kb1 == p.kblocks);
-        const long long st_tile = (long long)tile - sched.dp_tiles;
-        const int col = ti.n0 + 8 * g + 2 * (lane & 3);
-        float *part = whole ? nullptr : partial_slot(p, sched.cta, own_slot(p, sched, st_tile));
+        // Segment end.  Half 1 hands its sums to half 0 through shared memory.
+        if (h == 1) {
 #pragma unroll
-        for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-            for (int hr = 0; hr < 2; ++hr) {
-                const int row = mt * 16 + (lane >> 2) + 8 * hr;
-                if (row >= ti.rows)
-                    continue;
-                if (whole) {
-                    const int out_row = output_row(p, ti, row);
-                    if (out_row >= 0)
-                        *reinterpret_cast<__half2 *>(p.c + (long long)out_row * p.ldc + col) =
-                            __floats2half2_rn(acc[mt][2 * hr], acc[mt][2 * hr + 1]);
-                } else {
-                    __stcg(reinterpret_cast<float2 *>(part + row * TILE_N + (col - ti.n0)),
-                           make_float2(acc[mt][2 * hr], acc[mt][2 * hr + 1]));
-                }
-            }
-        if (whole)
-            continue;
+            for (int nt = 0; nt < NT; ++nt)
+                *reinterpret_cast<float4 *>(my_red + nt * 4) =
+                    make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
+        }
         if (!rendezvous())
             return;
+        const bool whole = (kb0 == 0 && kb1 == p.kblocks);
+        const long long st_tile = (long long)tile - sched.dp_tiles;
+        if (h == 0) {
+            float *part = whole ? nullptr : partial_slot(p, sched.cta, own_slot(p, sched, st_tile));
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const float4 o = *reinterpret_cast<const float4 *>(my_red + nt * 4);
+                const float v[4] = {acc[nt][0] + o.x, acc[nt][1] + o.y, acc[nt][2] + o.z,
+                                    acc[nt][3] + o.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int row = nt * 8 + 2 * t + (i & 1);
+                    const int col = col0 + 8 * (i >> 1);
+                    if (row >= ti.rows)
+                        continue;
+                    if (whole)
+                        p.c[(long long)(ti.row0 + row) * p.ldc + ti.n0 + col] = __float2half_rn(v[i]);
+                    else
+                        __stcg(part + row * TILE_N + col, v[i]);
+                }
+            }
+        }
+        // Half 0 has read the exchange buffer (and written its partial) before anyone moves on.
+        if (!rendezvous())
+            return;
+        if (whole)
+            continue;
         const Contributors cb = contributors(p, sched, st_tile);
-        if (g == 0 && lane == 0) {
+        if (w == 0 && lane == 0) {
             __threadfence();
             const int old = atomicAdd(&p.counters[tile], 1);
             const int last = old == (cb.hi - cb.lo);
@@ -172,13 +286,13 @@ __device__ void run_compute(const GemmParams &p, Sched sched, uint8_t *smem, Dec
             return;
         if (!*last_flag)
             continue;
-        reduce_tile(p, ti, cb, g * 32 + lane, DEC_WARPS * 32);
-        if (g == 0 && lane == 0)
+        reduce_tile(p, ti, cb, w * 32 + lane, DEC_WARPS * 32);
+        if (w == 0 && lane == 0)
             p.counters[tile] = 0;
     }
 }
 
-template <int MT, bool HALF>
+template <int NT, bool BLOCK_GROUPS>
 __global__ void __launch_bounds__(DEC_THREADS, 1)
     w4a16_decode_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap tmap_a,
                         const __grid_constant__ CUtensorMap tmap_s, const __grid_constant__ CUtensorMap tmap_z)
@@ -192,6 +306,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
     const int lane = threadIdx.x & 31;
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    float *red = reinterpret_cast<float *>(smem + (size_t)p.stages * p.stage_bytes);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.stages; ++s) {
@@ -220,7 +335,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
             run_producer(p, &tmap_a, &tmap_s, &tmap_z, no_seg, sched, smem, bars.full, bars.empty,
                          ctl);
     } else {
-        run_compute<MT, HALF>(p, sched, smem, bars, ctl, warp - 1, lane, &last_sh);
+        run_compute<NT, BLOCK_GROUPS>(p, sched, smem, red, bars, ctl, warp - 1, lane, &last_sh);
     }
     __syncwarp();
     __syncthreads();
@@ -231,26 +346,34 @@ int decode_max_rows()
     return 64;
 }
 
-int decode_extra_smem()
+// Alignment slack plus the half-sum exchange buffer: 8 column groups x 32 lanes x
+// (nt_max / 8) x 4 floats.
+int decode_extra_smem(int nt_max)
 {
-    return 1024; // alignment slack
+    return 1024 + 8 * 32 * (nt_max / 8) * 4 * (int)sizeof(float);
 }
 
 int launch_decode(const GemmParams &p, const CUtensorMap &tmap_a, const CUtensorMap &tmap_s,
                   const CUtensorMap &tmap_z, const GemmConfig &cfg, cudaStream_t stream)
 {
-    static int attr_done[5][64];
+    static int attr_done[8][64];
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess)
         return err;
-    // variant 0: 8-row tiles; 1..4: MT m16 tiles
-    const int variant = p.nt_max == 8 ? 0 : p.nt_max / 16;
-    if (variant < 0 || variant > 4 || (variant > 0 && p.nt_max % 16 != 0))
-        return cudaErrorInvalidValue;
-    void (*kernels[5])(GemmParams, CUtensorMap, CUtensorMap, CUtensorMap) = {
-        w4a16_decode_kernel<1, true>, w4a16_decode_kernel<1, false>, w4a16_decode_kernel<2, false>,
-        w4a16_decode_kernel<3, false>, w4a16_decode_kernel<4, false>};
+    int v;
+    switch (p.nt_max) {
+    case 8: v = 0; break;
+    case 16: v = 1; break;
+    case 32: v = 2; break;
+    case 64: v = 3; break;
+    default: return cudaErrorInvalidValue;
+    }
+    void (*kernels[8])(GemmParams, CUtensorMap, CUtensorMap, CUtensorMap) = {
+        w4a16_decode_kernel<1, true>,  w4a16_decode_kernel<2, true>,  w4a16_decode_kernel<4, true>,
+        w4a16_decode_kernel<8, true>,  w4a16_decode_kernel<1, false>, w4a16_decode_kernel<2, false>,
+        w4a16_decode_kernel<4, false>, w4a16_decode_kernel<8, false>};
+    const int variant = v + (p.group_size % KBLK == 0 ? 0 : 4);
     auto kernel = kernels[variant];
     if (dev < 64 && attr_done[variant][dev] < cfg.smem_bytes) {
         err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

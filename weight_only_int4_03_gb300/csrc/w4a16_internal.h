@@ -93,7 +93,7 @@ int gemm_smem_limit(int *bytes);
 
 // Dynamic shared memory the kernels need beyond the stages.
 int gemm_extra_smem(bool a_tmem, bool grouped);
-int decode_extra_smem();
+int decode_extra_smem(int nt_max);
 int decode_max_rows();
 
 } // namespace w4
