@@ -142,7 +142,7 @@ int w4a16_gemm(const void *a, int lda, const int32_t *b_packed, void *c, int ldc
                int weight_type, unsigned flags, cudaStream_t stream);
 
 /* Device scratch of w4a16_gemm_noalloc, per GPU that loads the library (held until exit). */
-#define W4A16_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+#define W4A16_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
 
 /* w4a16_gemm without a workspace argument, for callers that cannot allocate device memory
  * (code running inside a host callback or an allocator hook, under a framework's sealed
@@ -154,7 +154,7 @@ int w4a16_gemm(const void *a, int lda, const int32_t *b_packed, void *c, int ldc
  *   status_out  device int32 or NULL, 4-byte aligned: receives (stream-ordered) the call's
  *               device-side error bits (W4A16_DEV_*), 0 when all went well
  * A call whose w4a16_workspace_size exceeds the array (on a 152-multiprocessor GPU: M above
- * 96 rows, fewer with act-order, whose copy of A adds M*K*2 bytes) returns stage 2 with
+ * 208 rows, fewer with act-order, whose copy of A adds M*K*2 bytes) returns stage 2 with
  * detail W4A16_ARG_SCRATCH and launches nothing.
  * The first call on a device looks up the array's device address (once per device); make
  * that first call before any stream capture.  Each call clears the status word and tile

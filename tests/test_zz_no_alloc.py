@@ -28,6 +28,7 @@ CASES = [
     dict(m=33, k=768, n=512, weight_type=U4, sigma=0.5),
     dict(m=64, k=1024, n=1024),
     dict(m=96, k=512, n=256, flags=FLAG_FORCE_TC),
+    dict(m=200, k=1024, n=512),
 ]
 
 

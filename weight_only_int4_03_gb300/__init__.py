@@ -33,7 +33,7 @@ W4A16_DEV_SCHEDULE = 8
 
 W4A16_MAX_SEGMENTS = 1024
 W4A16_ARG_SCRATCH = 10
-W4A16_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
+W4A16_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"libw4a16.so is not built ({LIB_PATH}); run weight_only_int4_03_gb300.build.build()")

@@ -59,12 +59,13 @@ struct Plan {
 };
 
 // Workspace carving (byte offsets), shared by the size queries and the launches.  The
-// partial-tile area is sized for the largest tile height either kernel may pick.
-void carve(Plan &pl, int num_sms, long long a_bytes)
+// partial-tile area holds two [slot_rows x 128] fp32 slots per CTA: slot_cta_rows is the
+// largest (CTAs x tile rows) of the kernels the call may pick.
+void carve(Plan &pl, long long slot_cta_rows, long long a_bytes)
 {
     pl.counters_off = HEADER_BYTES;
     pl.partials_off = round_up(pl.counters_off + 4LL * pl.tiles_bound, 256);
-    pl.a_off = round_up(pl.partials_off + (long long)num_sms * 2 * pl.nt_max * TILE_N * 4, 256);
+    pl.a_off = round_up(pl.partials_off + slot_cta_rows * 2 * TILE_N * 4, 256);
     pl.total = round_up(pl.a_off + a_bytes, 256);
 }
 
@@ -157,24 +158,26 @@ void stage_layout(Plan &pl, int kbs, int group_size, int g_rows, bool has_zp)
     pl.stage_bytes = (int)round_up(end, 1024);
 }
 
-int smem_limit(int *limit)
+// Dynamic shared memory a CTA may use: the tcgen05 kernel (one CTA per SM) or the small-M
+// kernel (several per SM).  Cached per device.
+int smem_limit(int *limit, bool mma)
 {
     static std::mutex mu;
-    static int limit_cache[64];
+    static int limit_cache[2][64];
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess)
         return err;
     std::lock_guard<std::mutex> lock(mu);
-    if (dev >= 0 && dev < 64 && limit_cache[dev] > 0) {
-        *limit = limit_cache[dev];
+    if (dev >= 0 && dev < 64 && limit_cache[mma][dev] > 0) {
+        *limit = limit_cache[mma][dev];
         return cudaSuccess;
     }
-    err = (cudaError_t)gemm_smem_limit(limit);
+    err = (cudaError_t)(mma ? decode_smem_limit(limit) : gemm_smem_limit(limit));
     if (err != cudaSuccess)
         return err;
     if (dev >= 0 && dev < 64)
-        limit_cache[dev] = *limit;
+        limit_cache[mma][dev] = *limit;
     return cudaSuccess;
 }
 
@@ -184,7 +187,7 @@ int smem_limit(int *limit)
 int plan_smem(Plan &pl, bool grouped, bool has_zp, int group_size, int g_rows)
 {
     int limit = 0;
-    int err = smem_limit(&limit);
+    int err = smem_limit(&limit, pl.mma);
     if (err != cudaSuccess)
         return err;
     const int extra = pl.mma ? decode_extra_smem(pl.nt_max) : gemm_extra_smem(pl.a_tmem, grouped);
@@ -336,21 +339,26 @@ void dense_plan(Plan &pl, int m, int n, int k, unsigned flags, int num_sms, bool
 {
     pl.mma = mma;
     pl.a_tmem = (flags & W4A16_FLAG_A_SMEM) == 0;
+    const bool mma_ok = m <= decode_max_rows();
     const int nt_tc = pick_nt(m, false);
-    const int nt_mma = m <= decode_max_rows() ? pick_nt_mma(m) : nt_tc;
-    const int nt_ws = nt_tc > nt_mma ? nt_tc : nt_mma;
-    const int mt_ws = (m + (nt_tc < nt_mma ? nt_tc : nt_mma) - 1) / (nt_tc < nt_mma ? nt_tc : nt_mma);
+    const int nt_mma = mma_ok ? pick_nt_mma(m) : nt_tc;
+    const int nt_small = nt_tc < nt_mma ? nt_tc : nt_mma;
     pl.nt_max = mma ? nt_mma : nt_tc;
     pl.m_tiles = (m + pl.nt_max - 1) / pl.nt_max;
     const long long units = (long long)pl.m_tiles * (n / TILE_N) * (k / KBLK);
-    pl.grid = (int)(units < num_sms ? units : num_sms);
-    // carve() sizes counters by tiles_bound and partials by nt_max: use the bounds of both.
-    const int nt_keep = pl.nt_max;
-    pl.tiles_bound = mt_ws * (n / TILE_N);
-    pl.nt_max = nt_ws;
+    const int ctas = mma ? num_sms * decode_ctas_per_sm() : num_sms;
+    pl.grid = (int)(units < ctas ? units : ctas);
+    // The workspace serves whichever kernel a call picks: counters for the smaller tile
+    // height, partial slots for the larger CTA count x tile height.
+    pl.tiles_bound = ((m + nt_small - 1) / nt_small) * (n / TILE_N);
+    long long slot_rows = (long long)num_sms * nt_tc;
+    if (mma_ok) {
+        const long long r = (long long)num_sms * decode_ctas_per_sm() * nt_mma;
+        if (r > slot_rows)
+            slot_rows = r;
+    }
     const long long a_bytes = (flags & W4A16_FLAG_ACT_ORDER) ? (long long)m * k * 2 : 0;
-    carve(pl, num_sms, a_bytes);
-    pl.nt_max = nt_keep;
+    carve(pl, slot_rows, a_bytes);
 }
 
 void grouped_plan(Plan &pl, int n_pairs, int n_active, int n, int k, unsigned flags, int num_sms)
@@ -361,7 +369,7 @@ void grouped_plan(Plan &pl, int n_pairs, int n_active, int n, int k, unsigned fl
     pl.m_tiles = 0;
     pl.tiles_bound = ((n_pairs + pl.nt_max - 1) / pl.nt_max + n_active) * (n / TILE_N);
     pl.grid = num_sms;
-    carve(pl, num_sms, (long long)n_pairs * k * 2);
+    carve(pl, (long long)num_sms * pl.nt_max, (long long)n_pairs * k * 2);
 }
 
 void fill_params(GemmParams &p, const Plan &pl, int m, int n, int k, int group_size)

@@ -16,21 +16,23 @@
 // and of step 1 (p = 2, 3); column c + 8 gives a1 / a3.
 //
 // Budget: the integer pipe is the limit, so the loop is kept to the dequantisation proper
-// (13 instructions per 8 codes, 5 of them integer), two shared loads, one ldmatrix and two
-// MMAs per 64-row block.  When a group covers whole blocks (group_size % 64 == 0) a lane's
-// scale and zero change only where a group ends, which a per-stage bit mask marks.
+// (13 instructions per 8 codes, 5 of them integer), one shared load per word, one ldmatrix
+// per 32 rows and one MMA per word.  When a group covers whole blocks (group_size % 64 == 0)
+// a lane's scale and zero change only where a group ends, which a per-stage bit mask marks.
 //
-// CTA: one TMA producer warp (the producer of w4a16_common.cuh) and 16 compute warps; warp w
-// owns 16 weight columns (w & 7) and one 32-row half (w >> 3) of every 64-row block.  The two
-// halves are summed through shared memory at the end of a segment.  Work is split over CTAs
-// with the same data-parallel + stream-K schedule as the tcgen05 kernel; split tiles are
-// reduced in a fixed order by the last contributor.
+// CTA: one TMA producer warp (the producer of w4a16_common.cuh) and 8 compute warps; warp w
+// owns 16 weight columns of every 64-row block (16 columns x 64 rows = 4 words per lane).
+// Two CTAs share an SM, so one CTA's segment epilogue (partials, the split counter, the
+// reduction) overlaps the other's streaming.  Work is split over CTAs with the same
+// data-parallel + stream-K schedule as the tcgen05 kernel; split tiles are reduced in a fixed
+// order by the last contributor.
 #include "w4a16_common.cuh"
 
 namespace w4 {
 
-constexpr int DEC_WARPS = 16; // compute warps
+constexpr int DEC_WARPS = 8; // compute warps
 constexpr int DEC_THREADS = (DEC_WARPS + 1) * 32;
+constexpr int DEC_CTAS_PER_SM = 2;
 
 struct DecBars {
     uint64_t full[MAX_STAGES];
@@ -99,35 +101,41 @@ __device__ __forceinline__ ColGroup col_group(bool has_zp, const __half *ssm, co
     return cgp;
 }
 
-// One 64-row block of a warp's 16 columns x 32 rows: two code words per lane (columns col0
-// and col0 + 8) dequantised into A fragments for two k steps, times the B fragments of every
-// 8-token tile.  `w_addr` / `act` are shared-memory addresses of the lane's first word and of
-// its ldmatrix row in the block.
+// One 64-row block of a warp's 16 columns: per lane four code words (columns col0 and
+// col0 + 8, rows 0..31 and 32..63), dequantised into A fragments for four k steps, times the B
+// fragments of every 8-token tile.  `w_addr` is the shared address of the lane's first word,
+// `act0` / `act1` of its ldmatrix rows for the two 32-row halves.  The halves accumulate
+// separately (two independent MMA chains) and are summed at the segment end.
 template <int NT>
-__device__ __forceinline__ void block_mma(uint32_t w_addr, uint32_t act, const ColGroup &c0,
-                                          const ColGroup &c1, float (&acc)[NT][4])
+__device__ __forceinline__ void block_mma(uint32_t w_addr, uint32_t act0, uint32_t act1,
+                                          const ColGroup &c0, const ColGroup &c1,
+                                          float (&acc0)[NT][4], float (&acc1)[NT][4])
 {
-    uint32_t a0[4], a1[4];
+    uint32_t a0[4], a1[4], a2[4], a3[4];
     dequant_word_col(lds32(w_addr), c0.zlo, c0.zhi, c0.s, a0);
     dequant_word_col(lds32(w_addr + 128), c1.zlo, c1.zhi, c1.s, a1);
+    dequant_word_col(lds32(w_addr + 2048), c0.zlo, c0.zhi, c0.s, a2);
+    dequant_word_col(lds32(w_addr + 2048 + 128), c1.zlo, c1.zhi, c1.s, a3);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-        uint32_t b[4];
-        ldmatrix_x4(act + nt * 1024, b);
-        mma_16816(acc[nt], a0[0], a1[0], a0[1], a1[1], b[0], b[1]);
-        mma_16816(acc[nt], a0[2], a1[2], a0[3], a1[3], b[2], b[3]);
+        uint32_t b[4], e[4];
+        ldmatrix_x4(act0 + nt * 1024, b);
+        ldmatrix_x4(act1 + nt * 1024, e);
+        mma_16816(acc0[nt], a0[0], a1[0], a0[1], a1[1], b[0], b[1]);
+        mma_16816(acc1[nt], a2[0], a3[0], a2[1], a3[1], e[0], e[1]);
+        mma_16816(acc0[nt], a0[2], a1[2], a0[3], a1[3], b[2], b[3]);
+        mma_16816(acc1[nt], a2[2], a3[2], a2[3], a3[3], e[2], e[3]);
     }
 }
 
-constexpr int DEC_UNROLL = 8; // stages of exactly this many blocks take the unrolled path
+constexpr int DEC_UNROLL = 4; // stages of exactly this many blocks take the unrolled path
 
 // NT: 8-token tiles per CTA tile (nt_max = 8 * NT).  BLOCK_GROUPS: group_size is a multiple
 // of 64, so a group covers whole blocks and one scale serves all of a lane's codes in a
 // block; otherwise each 8-row pair looks up its own group (slow, general path).
 template <int NT, bool BLOCK_GROUPS>
-__device__ void run_compute(const GemmParams &p, Sched sched, uint8_t *smem, float *red,
-                            DecBars &bars, const WaitCtl &ctl, int w, int lane,
-                            volatile int *last_flag)
+__device__ void run_compute(const GemmParams &p, Sched sched, uint8_t *smem, DecBars &bars,
+                            const WaitCtl &ctl, int w, int lane, volatile int *last_flag)
 {
     const bool has_zp = p.zeros != nullptr;
     const int gs = p.group_size;
@@ -138,14 +146,13 @@ __device__ void run_compute(const GemmParams &p, Sched sched, uint8_t *smem, flo
     if (gs_kb <= 32)
         for (int b = gs_kb - 1; b < 64; b += gs_kb)
             ends64 |= 1ull << b;
-    const int cg = w & 7, h = w >> 3;
     const int t = lane & 3;
-    const int col0 = cg * 16 + (lane >> 2); // this lane's weight columns: col0 and col0 + 8
-    const uint32_t w_off = (uint32_t)(h * 512 + col0 * 4 + t) * 4u;
-    // ldmatrix.x4: matrix i = lane / 8 is 16-byte chunk h*4 + i of token rows 0..7 of an
-    // 8-token tile, so registers (0, 1) are the B fragment of k step 0 and (2, 3) of step 1.
-    const uint32_t lm_off = (uint32_t)((lane & 7) * 128 + (((h * 4 + (lane >> 3)) ^ (lane & 7)) << 4));
-    float *my_red = red + (cg * 32 + lane) * NT * 4;
+    const int col0 = w * 16 + (lane >> 2); // this lane's weight columns: col0 and col0 + 8
+    const uint32_t w_off = (uint32_t)(col0 * 4 + t) * 4u;
+    // ldmatrix.x4: matrix i = lane / 8 is 16-byte chunk 4h + i of token rows 0..7 of an
+    // 8-token tile, so registers (0, 1) are the B fragment of k step 2h and (2, 3) of 2h + 1.
+    const uint32_t lm_off0 = (uint32_t)((lane & 7) * 128 + ((((lane >> 3)) ^ (lane & 7)) << 4));
+    const uint32_t lm_off1 = (uint32_t)((lane & 7) * 128 + (((4 + (lane >> 3)) ^ (lane & 7)) << 4));
     Ring ring;
     uint32_t nsync = 0;
     auto rendezvous = [&]() -> bool {
@@ -160,12 +167,17 @@ __device__ void run_compute(const GemmParams &p, Sched sched, uint8_t *smem, flo
     int tile, kb0, kb1;
     while (sched.next(tile, kb0, kb1)) {
         const TileInfo ti = tile_info(p, no_seg, tile);
-        float acc[NT][4];
+        // The two 32-row halves of a block feed separate accumulators when NT is small, so
+        // that two MMA chains run side by side; larger NT has enough independent chains.
+        float acc[NT][4], acc_h1[NT][4];
+        float(&acc1)[NT][4] = NT <= 2 ? acc_h1 : acc;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
+            for (int i = 0; i < 4; ++i) {
                 acc[nt][i] = 0.f;
+                acc_h1[nt][i] = 0.f;
+            }
         int in_grp = BLOCK_GROUPS ? kb0 % gs_kb : 0; // blocks of the current group before kb
         for (int kb = kb0; kb < kb1; kb += p.kbs) {
             const int nkb = min(p.kbs, kb1 - kb);
@@ -175,7 +187,8 @@ __device__ void run_compute(const GemmParams &p, Sched sched, uint8_t *smem, flo
             const __half *ssm = reinterpret_cast<const __half *>(st + p.scales_off);
             const __half *zsm = reinterpret_cast<const __half *>(st + p.zeros_off);
             const uint32_t w_addr = smem_u32(st + p.packed_off) + w_off;
-            const uint32_t act = smem_u32(st) + lm_off;
+            const uint32_t act0 = smem_u32(st) + lm_off0;
+            const uint32_t act1 = smem_u32(st) + lm_off1;
             if (BLOCK_GROUPS) {
                 // Bit j of gend: block kb + j is the last of its group.
                 uint32_t gend;
@@ -199,13 +212,15 @@ __device__ void run_compute(const GemmParams &p, Sched sched, uint8_t *smem, flo
                 if (nkb == DEC_UNROLL) {
 #pragma unroll
                     for (int j = 0; j < DEC_UNROLL; ++j) {
-                        block_mma<NT>(w_addr + j * TILE_BYTES, act + j * p.act_kb_bytes, c0, c1, acc);
+                        block_mma<NT>(w_addr + j * TILE_BYTES, act0 + j * p.act_kb_bytes,
+                                      act1 + j * p.act_kb_bytes, c0, c1, acc, acc1);
                         if (j + 1 < DEC_UNROLL && (gend & (1u << j)))
                             next_group();
                     }
                 } else {
                     for (int j = 0; j < nkb; ++j) {
-                        block_mma<NT>(w_addr + j * TILE_BYTES, act + j * p.act_kb_bytes, c0, c1, acc);
+                        block_mma<NT>(w_addr + j * TILE_BYTES, act0 + j * p.act_kb_bytes,
+                                      act1 + j * p.act_kb_bytes, c0, c1, acc, acc1);
                         if (j + 1 < nkb && (gend & (1u << j)))
                             next_group();
                     }
@@ -214,19 +229,22 @@ __device__ void run_compute(const GemmParams &p, Sched sched, uint8_t *smem, flo
                 const int g_first = (kb * KBLK) / gs;
                 const uint32_t *pw = reinterpret_cast<const uint32_t *>(st + p.packed_off) + w_off / 4;
                 for (int j = 0; j < nkb; ++j) {
-                    uint32_t a0[4], a1[4];
-                    __half2 s2[4], zl[4], zh[4];
-                    load_scales(p, ssm, zsm, has_zp, kb + j, h, g_first, 0, col0, s2, zl, zh);
-                    dequant_word(pw[0], zl, zh, s2, a0);
-                    load_scales(p, ssm, zsm, has_zp, kb + j, h, g_first, 0, col0 + 8, s2, zl, zh);
-                    dequant_word(pw[32], zl, zh, s2, a1);
-                    const uint32_t actj = act + j * p.act_kb_bytes;
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        uint32_t b[4];
-                        ldmatrix_x4(actj + nt * 1024, b);
-                        mma_16816(acc[nt], a0[0], a1[0], a0[1], a1[1], b[0], b[1]);
-                        mma_16816(acc[nt], a0[2], a1[2], a0[3], a1[3], b[2], b[3]);
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t a0[4], a1[4];
+                        __half2 s2[4], zl[4], zh[4];
+                        load_scales(p, ssm, zsm, has_zp, kb + j, h, g_first, 0, col0, s2, zl, zh);
+                        dequant_word(pw[h * 512], zl, zh, s2, a0);
+                        load_scales(p, ssm, zsm, has_zp, kb + j, h, g_first, 0, col0 + 8, s2, zl, zh);
+                        dequant_word(pw[h * 512 + 32], zl, zh, s2, a1);
+                        const uint32_t actj = (h ? act1 : act0) + j * p.act_kb_bytes;
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) {
+                            uint32_t b[4];
+                            ldmatrix_x4(actj + nt * 1024, b);
+                            mma_16816(acc[nt], a0[0], a1[0], a0[1], a1[1], b[0], b[1]);
+                            mma_16816(acc[nt], a0[2], a1[2], a0[3], a1[3], b[2], b[3]);
+                        }
                     }
                     pw += TILE_WORDS;
                 }
@@ -237,42 +255,28 @@ __device__ void run_compute(const GemmParams &p, Sched sched, uint8_t *smem, flo
             ring.advance(p.stages);
         }
 
-        // Segment end.  Half 1 hands its sums to half 0 through shared memory.
-        if (h == 1) {
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-                *reinterpret_cast<float4 *>(my_red + nt * 4) =
-                    make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
-        }
-        if (!rendezvous())
-            return;
+        // Segment end: fp16 C for a whole tile, else an fp32 partial and the split protocol.
         const bool whole = (kb0 == 0 && kb1 == p.kblocks);
         const long long st_tile = (long long)tile - sched.dp_tiles;
-        if (h == 0) {
-            float *part = whole ? nullptr : partial_slot(p, sched.cta, own_slot(p, sched, st_tile));
+        float *part = whole ? nullptr : partial_slot(p, sched.cta, own_slot(p, sched, st_tile));
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                const float4 o = *reinterpret_cast<const float4 *>(my_red + nt * 4);
-                const float v[4] = {acc[nt][0] + o.x, acc[nt][1] + o.y, acc[nt][2] + o.z,
-                                    acc[nt][3] + o.w};
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int row = nt * 8 + 2 * t + (i & 1);
-                    const int col = col0 + 8 * (i >> 1);
-                    if (row >= ti.rows)
-                        continue;
-                    if (whole)
-                        p.c[(long long)(ti.row0 + row) * p.ldc + ti.n0 + col] = __float2half_rn(v[i]);
-                    else
-                        __stcg(part + row * TILE_N + col, v[i]);
-                }
+            for (int i = 0; i < 4; ++i) {
+                const int row = nt * 8 + 2 * t + (i & 1);
+                const int col = col0 + 8 * (i >> 1);
+                const float v = NT <= 2 ? acc[nt][i] + acc_h1[nt][i] : acc[nt][i];
+                if (row >= ti.rows)
+                    continue;
+                if (whole)
+                    p.c[(long long)(ti.row0 + row) * p.ldc + ti.n0 + col] = __float2half_rn(v);
+                else
+                    __stcg(part + row * TILE_N + col, v);
             }
-        }
-        // Half 0 has read the exchange buffer (and written its partial) before anyone moves on.
-        if (!rendezvous())
-            return;
         if (whole)
             continue;
+        if (!rendezvous())
+            return;
         const Contributors cb = contributors(p, sched, st_tile);
         if (w == 0 && lane == 0) {
             __threadfence();
@@ -293,7 +297,7 @@ __device__ void run_compute(const GemmParams &p, Sched sched, uint8_t *smem, flo
 }
 
 template <int NT, bool BLOCK_GROUPS>
-__global__ void __launch_bounds__(DEC_THREADS, 1)
+__global__ void __launch_bounds__(DEC_THREADS, DEC_CTAS_PER_SM)
     w4a16_decode_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap tmap_a,
                         const __grid_constant__ CUtensorMap tmap_s, const __grid_constant__ CUtensorMap tmap_z)
 {
@@ -306,7 +310,6 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
     const int lane = threadIdx.x & 31;
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-    float *red = reinterpret_cast<float *>(smem + (size_t)p.stages * p.stage_bytes);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.stages; ++s) {
@@ -335,7 +338,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
             run_producer(p, &tmap_a, &tmap_s, &tmap_z, no_seg, sched, smem, bars.full, bars.empty,
                          ctl);
     } else {
-        run_compute<NT, BLOCK_GROUPS>(p, sched, smem, red, bars, ctl, warp - 1, lane, &last_sh);
+        run_compute<NT, BLOCK_GROUPS>(p, sched, smem, bars, ctl, warp - 1, lane, &last_sh);
     }
     __syncwarp();
     __syncthreads();
@@ -346,11 +349,35 @@ int decode_max_rows()
     return 64;
 }
 
-// Alignment slack plus the half-sum exchange buffer: 8 column groups x 32 lanes x
-// (nt_max / 8) x 4 floats.
+// Alignment slack only (the stages are all the dynamic shared memory).
 int decode_extra_smem(int nt_max)
 {
-    return 1024 + 8 * 32 * (nt_max / 8) * 4 * (int)sizeof(float);
+    (void)nt_max;
+    return 1024;
+}
+
+// CTAs of the small-M kernel per SM, and the dynamic shared memory each may use so that they
+// all fit: the SM's shared memory split evenly, less each CTA's reserved and static part.
+int decode_ctas_per_sm()
+{
+    return DEC_CTAS_PER_SM;
+}
+
+int decode_smem_limit(int *bytes)
+{
+    int dev = 0, per_sm = 0, reserved = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err == cudaSuccess)
+        err = cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    if (err == cudaSuccess)
+        err = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+    cudaFuncAttributes fa;
+    if (err == cudaSuccess)
+        err = cudaFuncGetAttributes(&fa, w4a16_decode_kernel<1, true>);
+    if (err != cudaSuccess)
+        return err;
+    *bytes = per_sm / DEC_CTAS_PER_SM - reserved - (int)fa.sharedSizeBytes - 256;
+    return cudaSuccess;
 }
 
 int launch_decode(const GemmParams &p, const CUtensorMap &tmap_a, const CUtensorMap &tmap_s,

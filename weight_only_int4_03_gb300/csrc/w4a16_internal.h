@@ -95,5 +95,7 @@ int gemm_smem_limit(int *bytes);
 int gemm_extra_smem(bool a_tmem, bool grouped);
 int decode_extra_smem(int nt_max);
 int decode_max_rows();
+int decode_ctas_per_sm();
+int decode_smem_limit(int *bytes);
 
 } // namespace w4

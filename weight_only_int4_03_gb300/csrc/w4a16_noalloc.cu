@@ -8,7 +8,7 @@
 // workspace to w4a16_gemm.  This entry point takes none.  Nothing here calls cudaMalloc,
 // cudaFree or any routine that allocates.
 //
-// The array is W4A16_NOALLOC_SCRATCH_BYTES (16 MiB) of device memory per GPU that loads the
+// The array is W4A16_NOALLOC_SCRATCH_BYTES (32 MiB) of device memory per GPU that loads the
 // library, held until the process exits.  Every call on a device shares it, so calls whose
 // kernels overlap on the GPU (two streams, or two host threads) race and give wrong results;
 // serialise them.
