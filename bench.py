@@ -110,17 +110,17 @@ def kernel_source_hash() -> str:
 
 
 def recorded_traffic(workload: str):
-    """DRAM bytes per launch of the dominant kernel from the committed ncu summary, or None
-    if it is missing or was taken on a different kernel source."""
-    path = os.path.join(ROOT, "profiles", "traffic.json")
+    """DRAM bytes per launch of the hot-path kernels from the committed ncu summary
+    (profiles/traffic.txt), or None if it is missing or was taken on other kernel sources."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(path):
         return None
     with open(path) as f:
-        rec = json.load(f)
-    entry = rec.get(workload)
-    if not entry or entry.get("kernel_source_hash") != kernel_source_hash():
-        return None
-    return entry.get("dram_bytes_per_launch")
+        for line in f:
+            parts = line.split()
+            if len(parts) == 3 and not line.startswith("#") and parts[0] == workload:
+                return int(parts[2]) if parts[1] == kernel_source_hash() else None
+    return None
 
 
 # ---------------------------------------------------------------------------------------------
@@ -321,6 +321,17 @@ def grouped_accounting(s):
     return wb, wb + rows * s["k"] * 2 + n_pairs * s["n"] * 2, 2 * n_pairs * s["n"] * s["k"]
 
 
+def select_shape(specs, shape):
+    """The GEMMs of `specs` whose (m, k, n) equal the "M,K,N" string `shape` (all if None)."""
+    if not shape:
+        return specs
+    m, k, n = (int(v) for v in shape.split(","))
+    picked = [s for s in specs if (s.get("m"), s["k"], s["n"]) == (m, k, n)]
+    if not picked:
+        raise SystemExit(f"no GEMM {shape} in this workload")
+    return picked
+
+
 def run_ours(args, rank, world, local):
     import torch
     import weight_only_int4_03_gb300 as w4
@@ -329,7 +340,7 @@ def run_ours(args, rank, world, local):
     torch.cuda.set_device(dev)
     props = torch.cuda.get_device_properties(dev)
     l2 = getattr(props, "L2_cache_size", 0) or 126 * 1024 * 1024
-    specs = workload_specs(args.workload)
+    specs = select_shape(workload_specs(args.workload), args.shape)
     gemms = []
     for s in specs:
         if s.get("grouped"):
@@ -506,7 +517,8 @@ def run_ours(args, rank, world, local):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(max_ms / args.steps, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16 x u4 -> f32 acc",
         "data": "synthetic (seeded LCG; shapes and distributions of the W4A16 configurations)",
-        "config": {"workload": WORKLOAD_TEXT[args.workload], "gemms_per_step": len(gemms),
+        "config": {"workload": WORKLOAD_TEXT[args.workload] + (f" (only {args.shape})" if args.shape else ""),
+                   "gemms_per_step": len(gemms),
                    "l2_defeat": "weight-copy ring >= 3x L2 per shape", "graph": "CUDA graph of all steps",
                    "parallelism": f"replicas x{world}"},
         "tflops": round(step_flops * args.steps / sec / 1e12, 2),
@@ -525,78 +537,55 @@ def run_ours(args, rank, world, local):
 # The oracle (CPU) as a reported baseline and as the reference arm
 # ---------------------------------------------------------------------------------------------
 
+def _oracle_inputs(s, rows: int):
+    """Oracle inputs of one GEMM of the workload with `rows` activation rows (for a grouped
+    GEMM: one expert's weights, rows standing for (token, expert) pairs)."""
+    k, n = s["k"], s["n"]
+    g = synth.group_count(k, s["gs"])
+    if s.get("grouped"):
+        qw = synth.qweight(s["seed"] * 100, k, n)
+        a = synth.activations(s["seed"], rows, k)
+        return a, qw, synth.scales(s["seed"], g, n), None
+    qw = synth.qweight(s["seed"], k, n)
+    z = synth.zeros(s["seed"], g, n) if s["wt"] == U4 else None
+    return synth.activations(s["seed"], rows, k, sigma=s["sigma"]), qw, synth.scales(s["seed"], g, n), z
+
+
 def oracle_sample(workload: str, budget_s: float):
-    """Times the oracle on a bounded sample of one step of the workload: `r` rows of every
-    GEMM, then extrapolates the step time linearly in the rows (the oracle's cost is linear
-    in M).  Returns (step_seconds_estimate, units_per_step, unit, threads, sample_text)."""
+    """Times the oracle on a bounded sample of one step of the workload: r output rows of every
+    GEMM (r sized so the sample takes about `budget_s`), then extrapolates the step time
+    linearly in the rows (the oracle's cost is linear in M).
+    Returns (step_seconds_estimate, units_per_step, unit, threads, sample_text)."""
     import oracle
     orc = oracle.Oracle()
     threads = oracle.default_threads()
     specs = workload_specs(workload)
-    est = 0.0
-    units = 0.0
+
+    def row_seconds(s, r):
+        a, qw, sc, z = _oracle_inputs(s, r)
+        t0 = time.time()
+        orc.gemm(a, qw, sc, z, None, s["gs"], s["wt"], threads=threads)
+        return (time.time() - t0) / r
+
+    # Calibrate with one row per GEMM, then spend the budget on r rows of each.
+    calib = sum(row_seconds(s, 1) for s in specs)
+    r = max(1, int(budget_s / max(calib, 1e-9)))
+    hbm = workload == "decode"
+    est = units = 0.0
     sample_rows = 0
-    per_row = []
     for s in specs:
+        rows_total = s["n_tok"] * s["top_k"] if s.get("grouped") else s["m"]
+        rr = min(r, rows_total)
+        est += row_seconds(s, rr) * rows_total
+        sample_rows += rr
         if s.get("grouped"):
-            k, n, g = s["k"], s["n"], synth.group_count(s["k"], s["gs"])
-            rows_total = s["n_tok"] * s["top_k"]
-            qw = synth.qweight(s["seed"] * 100, k, n)
-            sc = synth.scales(s["seed"], g, n)
-            wt = s["wt"]
-            z = None
-            a = synth.activations(s["seed"], 1, k)
             wb, _, f = grouped_accounting(s)
         else:
-            k, n, g = s["k"], s["n"], synth.group_count(s["k"], s["gs"])
-            rows_total = s["m"]
-            qw = synth.qweight(s["seed"], k, n)
-            sc = synth.scales(s["seed"], g, n)
-            wt = s["wt"]
-            z = synth.zeros(s["seed"], g, n) if wt == U4 else None
-            a = synth.activations(s["seed"], 1, k, sigma=s["sigma"])
             wb, f = weight_bytes(s), gemm_flops(s)
-        t0 = time.time()
-        orc.gemm(a, qw, sc, z, None, s["gs"], wt, threads=threads)
-        t_row = time.time() - t0
-        per_row.append((t_row, rows_total, wb, f))
-        sample_rows += 1
-    # Spend the remaining budget on more rows, spread evenly.
-    spent = sum(p[0] for p in per_row)
-    extra = max(0, int((budget_s - spent) / max(spent, 1e-9)))
-    if extra:
-        t0 = time.time()
-        for _ in range(extra):
-            for s in specs:
-                pass
-        # Re-time with `extra+1` rows of every GEMM for a steadier per-row figure.
-        per_row2 = []
-        for (t_row, rows_total, wb, f), s in zip(per_row, specs):
-            r = min(extra + 1, rows_total)
-            if s.get("grouped"):
-                k, n, g = s["k"], s["n"], synth.group_count(s["k"], s["gs"])
-                qw = synth.qweight(s["seed"] * 100, k, n)
-                sc = synth.scales(s["seed"], g, n)
-                a = synth.activations(s["seed"], r, k)
-                z = None
-            else:
-                k, n, g = s["k"], s["n"], synth.group_count(s["k"], s["gs"])
-                qw = synth.qweight(s["seed"], k, n)
-                sc = synth.scales(s["seed"], g, n)
-                z = synth.zeros(s["seed"], g, n) if s["wt"] == U4 else None
-                a = synth.activations(s["seed"], r, k, sigma=s["sigma"])
-            t1 = time.time()
-            orc.gemm(a, qw, sc, z, None, s["gs"], s["wt"], threads=threads)
-            per_row2.append(((time.time() - t1) / r, rows_total, wb, f))
-            sample_rows += r
-        per_row = per_row2
-    hbm = workload == "decode"
-    for t_row, rows_total, wb, f in per_row:
-        est += t_row * rows_total
         units += wb if hbm else f
     unit = "GB/s (weight stream)" if hbm else "TFLOP/s"
-    text = (f"{sample_rows} output rows over the {len(specs)} GEMMs of one step, fp64, "
-            f"extrapolated linearly to all rows of the step")
+    text = (f"{sample_rows} output rows over the {len(specs)} GEMMs of one step (at most {r} per "
+            f"GEMM), fp64 on {threads} threads, extrapolated linearly to all rows of the step")
     return est, units, unit, threads, text
 
 
@@ -648,6 +637,8 @@ def main(argv=None):
     ap.add_argument("--workload", choices=list(WORKLOAD_TEXT), default="decode")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-detail", action="store_true")
+    ap.add_argument("--shape", default=None,
+                    help="M,K,N: run only this GEMM of the workload (for profiling one kernel)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
