@@ -134,6 +134,13 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
         : "memory");
 }
 
+// Bulk prefetch of global memory into L2 (a hint: it fills no shared memory and signals
+// nothing).  Address and size must be multiples of 16 bytes.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void bulk_load_hint(void *dst, const void *src, uint32_t bytes,
                                                uint64_t *bar, uint64_t policy)
 {

@@ -231,9 +231,10 @@ struct Ring {
 // they are made as big as the stage allows), the scale/zero rows they touch (one tensor copy
 // each) and their activation rows (one 3-D tensor copy, p.kbs blocks deep).
 // ---------------------------------------------------------------------------------------
+template <class SCHED>
 static __device__ void run_producer(const GemmParams &p, const CUtensorMap *tmap_a,
                                     const CUtensorMap *tmap_s, const CUtensorMap *tmap_z,
-                                    const SegTable &seg, Sched sched, uint8_t *smem,
+                                    const SegTable &seg, SCHED sched, uint8_t *smem,
                                     uint64_t *full_bars, uint64_t *empty_bars, const WaitCtl &ctl)
 {
     const bool has_zp = p.zeros != nullptr;
@@ -282,6 +283,26 @@ static __device__ void run_producer(const GemmParams &p, const CUtensorMap *tmap
             ph ^= 1u;
         }
         mbar_wait(&full_bars[idx], ph, drain_ctl, W4A16_DEV_TIMEOUT);
+    }
+}
+
+// L2 prefetch of the packed codes of this CTA's first `budget` bytes of work (dense schedule
+// only).  The weights never depend on the kernel that precedes this one on the stream, so the
+// prefetch may run before the programmatic-dependency wait and overlap that kernel's tail; it
+// only warms L2 (the coherence point), and the real loads still come after the wait.
+template <class SCHED>
+static __device__ void prefetch_first_codes(const GemmParams &p, SCHED sched, uint32_t budget)
+{
+    SegTable no_seg{nullptr, nullptr, nullptr};
+    int tile, kb0, kb1;
+    while (budget > 0 && sched.next(tile, kb0, kb1)) {
+        const TileInfo ti = tile_info(p, no_seg, tile);
+        const int32_t *bw = p.b + ((long long)(ti.n0 / TILE_N) * p.kblocks + kb0) * TILE_WORDS;
+        uint32_t bytes = (uint32_t)(kb1 - kb0) * TILE_BYTES;
+        if (bytes > budget)
+            bytes = budget;
+        bulk_prefetch_l2(bw, bytes);
+        budget -= bytes;
     }
 }
 
@@ -384,36 +405,69 @@ __device__ __forceinline__ Contributors contributors(const GemmParams &p, const 
     return c;
 }
 
-// Sum the partials of a split tile in contributor order and write fp16 C.  Thread `tid` of
-// `nthreads` takes (row, 4-column quad) items; loads of up to four contributors are issued
-// together so that their latencies overlap.
+// Split-tile counter: one acquire-release atomic at GPU scope.  The CTA's partial stores
+// happen before it through the CTA-wide rendezvous that precedes it, and release is
+// cumulative, so they are visible to whoever reads the counter's later value; the acquire half
+// makes the other contributors' partials visible to the last arriver (and, through the
+// rendezvous that follows, to the rest of its CTA).
+__device__ __forceinline__ int split_counter_arrive(int *counter)
+{
+    int old;
+    asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], 1;" : "=r"(old) : "l"(counter) : "memory");
+    return old;
+}
+
+// Sum the partials of a split tile and write fp16 C.  Work items are (row, 4-column quad);
+// when there are fewer items than threads, `ways` consecutive threads share an item, thread j
+// summing contributors lo + j, lo + j + ways, ... and a fixed shuffle tree combining the ways
+// -- a fixed order, so results are bit-identical from run to run.  Up to eight contributor
+// loads of a thread are in flight together.  `nthreads` must be a multiple of 32.
 static __device__ void reduce_tile(const GemmParams &p, const TileInfo &ti, const Contributors &cb,
                                    int tid, int nthreads)
 {
-    for (int item = tid; item < ti.rows * (TILE_N / 4); item += nthreads) {
+    const int items = ti.rows * (TILE_N / 4);
+    const int ncontrib = cb.hi - cb.lo + 1;
+    int ways = 1;
+    while (ways < 16 && ways * 2 <= ncontrib && items * ways * 2 <= nthreads)
+        ways *= 2;
+    const int slots = items * ways;
+    const int rounds = (slots + nthreads - 1) / nthreads;
+    for (int r = 0; r < rounds; ++r) {
+        const int slot = r * nthreads + tid;
+        const bool active = slot < slots;
+        const int item = slot / ways;
+        const int j = slot - item * ways;
         const int row = item / (TILE_N / 4);
-        const int cq = item % (TILE_N / 4);
+        const int cq = item - row * (TILE_N / 4);
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int c0 = cb.lo; c0 <= cb.hi; c0 += 4) {
-            float4 v[4];
+        if (active) {
+            for (int c0 = cb.lo + j; c0 <= cb.hi; c0 += 8 * ways) {
+                float4 v[8];
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-                const int c = c0 + cc;
-                const float4 *pc = reinterpret_cast<const float4 *>(
-                    partial_slot(p, c, c == cb.lo ? cb.lo_slot : 0));
-                v[cc] = (c <= cb.hi) ? __ldcg(pc + row * (TILE_N / 4) + cq)
-                                     : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
+                for (int u = 0; u < 8; ++u) {
+                    const int c = c0 + u * ways;
+                    const float4 *pc = reinterpret_cast<const float4 *>(
+                        partial_slot(p, c, c == cb.lo ? cb.lo_slot : 0));
+                    v[u] = (c <= cb.hi) ? __ldcg(pc + row * (TILE_N / 4) + cq)
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-                if (c0 + cc > cb.hi)
-                    break;
-                acc.x += v[cc].x;
-                acc.y += v[cc].y;
-                acc.z += v[cc].z;
-                acc.w += v[cc].w;
+                for (int u = 0; u < 8; ++u) {
+                    acc.x += v[u].x;
+                    acc.y += v[u].y;
+                    acc.z += v[u].z;
+                    acc.w += v[u].w;
+                }
             }
         }
+        for (int off = 1; off < ways; off <<= 1) {
+            acc.x += __shfl_xor_sync(0xffffffffu, acc.x, off);
+            acc.y += __shfl_xor_sync(0xffffffffu, acc.y, off);
+            acc.z += __shfl_xor_sync(0xffffffffu, acc.z, off);
+            acc.w += __shfl_xor_sync(0xffffffffu, acc.w, off);
+        }
+        if (!active || j != 0)
+            continue;
         const int out_row = output_row(p, ti, row);
         if (out_row < 0)
             continue;

@@ -279,11 +279,8 @@ __device__ void run_compute(const GemmParams &p, Sched sched, uint8_t *smem, Dec
             return;
         const Contributors cb = contributors(p, sched, st_tile);
         if (w == 0 && lane == 0) {
-            __threadfence();
-            const int old = atomicAdd(&p.counters[tile], 1);
+            const int old = split_counter_arrive(&p.counters[tile]);
             const int last = old == (cb.hi - cb.lo);
-            if (last)
-                __threadfence();
             *last_flag = last;
         }
         if (!rendezvous())
@@ -325,6 +322,9 @@ __global__ void __launch_bounds__(DEC_THREADS, DEC_CTAS_PER_SM)
         if (p.zeros != nullptr)
             prefetch_tensormap(&tmap_z);
         pdl_launch_dependents();
+        Sched pre;
+        pre.init(p.m_tiles * p.n_tiles, p.kblocks);
+        prefetch_first_codes(p, pre, (uint32_t)p.stages * p.kbs * TILE_BYTES);
     }
     pdl_wait();
     __syncthreads();

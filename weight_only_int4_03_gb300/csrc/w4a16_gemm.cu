@@ -267,11 +267,8 @@ __device__ void run_epilogue(const GemmParams &p, const SegTable &seg, Sched sch
             return;
         const Contributors cb = contributors(p, sched, st_tile);
         if (warp == EPI_WARP0 && lane == 0) {
-            __threadfence();
-            const int old = atomicAdd(&p.counters[tile], 1);
+            const int old = split_counter_arrive(&p.counters[tile]);
             const int last = old == (cb.hi - cb.lo);
-            if (last)
-                __threadfence();
             *last_flag = last;
         }
         if (!rendezvous())
