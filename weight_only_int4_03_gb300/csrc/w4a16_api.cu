@@ -53,7 +53,7 @@ int num_groups(int k, int group_size)
 struct Plan {
     int nt_max, m_tiles, tiles_bound, grid;
     int kbs, sg_box, act_kb_bytes, packed_off, scales_off, zeros_off;
-    int stages, stage_bytes, acc_bufs, acc_col0, tmem_cols, smem_bytes, seg_off, a_slots;
+    int stages, stage_bytes, acc_bufs, acc_col0, tmem_cols, smem_bytes, seg_off, epi_off, a_slots;
     bool a_tmem, mma; // mma: the small-M register-fragment kernel instead of tcgen05
     long long counters_off, partials_off, a_off, total;
 };
@@ -204,7 +204,8 @@ int plan_smem(Plan &pl, bool grouped, bool has_zp, int group_size, int g_rows)
     }
     if (pl.stages > MAX_STAGES)
         pl.stages = MAX_STAGES;
-    pl.seg_off = pl.stages * pl.stage_bytes + (!pl.mma && !pl.a_tmem ? SMEM_A_SLOTS * A_SLOT_BYTES : 0);
+    pl.epi_off = pl.stages * pl.stage_bytes + (!pl.mma && !pl.a_tmem ? SMEM_A_SLOTS * A_SLOT_BYTES : 0);
+    pl.seg_off = pl.epi_off + (pl.mma ? 0 : EPI_STAGE_BYTES);
     pl.smem_bytes = pl.stages * pl.stage_bytes + extra;
     return cudaSuccess;
 }
@@ -398,6 +399,7 @@ void fill_params(GemmParams &p, const Plan &pl, int m, int n, int k, int group_s
     p.tmem_cols = pl.tmem_cols;
     p.a_slots = pl.a_slots;
     p.seg_smem_off = pl.seg_off;
+    p.epi_smem_off = pl.epi_off;
 }
 
 // Tensor maps of one launch: activations (3-D, swizzled) and the scale / zero rows.  With no

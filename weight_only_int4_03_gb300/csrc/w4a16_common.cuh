@@ -48,30 +48,12 @@ __device__ __forceinline__ void dequant_word(uint32_t x, const __half2 (&zlo)[4]
     out[3] = h2_as_u32(__hmul2(v3, s2[3]));
 }
 
-// Scales (and zeros) of the four 8-row groups p of half h of a 64-row block: one division per
-// block when a group spans whole blocks (the usual group sizes), else one per 8-row group.
+// Scales (and zeros) of the four 8-row pairs p of half h of a 64-row block, each pair looking
+// up its own group (general group sizes; one division per pair).
 __device__ __forceinline__ void load_scales(const GemmParams &p, const __half *ssm, const __half *zsm,
-                                            bool has_zp, int kb, int h, int g_first, int gs_kb,
-                                            int col, __half2 (&s2)[4], __half2 (&zlo)[4],
-                                            __half2 (&zhi)[4])
+                                            bool has_zp, int kb, int h, int g_first, int col,
+                                            __half2 (&s2)[4], __half2 (&zlo)[4], __half2 (&zhi)[4])
 {
-    if (gs_kb) {
-        const int idx = (kb / gs_kb - g_first) * TILE_N + col;
-        const __half2 s = __half2half2(ssm[idx]);
-        __half2 lo = __float2half2_rn(1032.0f), hi = __float2half2_rn(-72.0f);
-        if (has_zp) {
-            const __half z = zsm[idx];
-            lo = __half2half2(__hadd(__float2half(1024.0f), z));
-            hi = __half2half2(__hneg(__hadd(__float2half(64.0f), z)));
-        }
-#pragma unroll
-        for (int pp = 0; pp < 4; ++pp) {
-            s2[pp] = s;
-            zlo[pp] = lo;
-            zhi[pp] = hi;
-        }
-        return;
-    }
 #pragma unroll
     for (int pp = 0; pp < 4; ++pp) {
         const int gl = (kb * KBLK + h * 32 + pp * 8) / p.group_size - g_first;
@@ -79,13 +61,42 @@ __device__ __forceinline__ void load_scales(const GemmParams &p, const __half *s
         s2[pp] = __half2half2(ssm[idx]);
         if (has_zp) {
             const __half z = zsm[idx];
-            zlo[pp] = __half2half2(__hadd(__float2half(1024.0f), z));
-            zhi[pp] = __half2half2(__hneg(__hadd(__float2half(64.0f), z)));
+            zlo[pp] = __half2half2(__hadd(__ushort_as_half(0x6400), z));
+            zhi[pp] = __half2half2(__hneg(__hadd(__ushort_as_half(0x5400), z)));
         } else {
-            zlo[pp] = __float2half2_rn(1032.0f);
-            zhi[pp] = __float2half2_rn(-72.0f);
+            zlo[pp] = __half2half2(__ushort_as_half(0x6408));
+            zhi[pp] = __half2half2(__ushort_as_half(0xD480));
         }
     }
+}
+
+// Uniform case (a group spans whole 64-row blocks): scale and zero offsets of one group row
+// `grp_rel` (relative to the stage's first group row), the same for all four pairs.
+__device__ __forceinline__ void load_scales_row(const __half *ssm, const __half *zsm, bool has_zp,
+                                                int grp_rel, int col, __half2 (&s2)[4],
+                                                __half2 (&zlo)[4], __half2 (&zhi)[4])
+{
+    const int idx = grp_rel * TILE_N + col;
+    const __half2 s = __half2half2(ssm[idx]);
+    __half2 lo = __half2half2(__ushort_as_half(0x6408)); // 1032
+    __half2 hi = __half2half2(__ushort_as_half(0xD480)); // -72
+    if (has_zp) {
+        const __half z = zsm[idx];
+        lo = __half2half2(__hadd(__ushort_as_half(0x6400), z));         // 1024 + z
+        hi = __half2half2(__hneg(__hadd(__ushort_as_half(0x5400), z))); // -(64 + z)
+    }
+#pragma unroll
+    for (int pp = 0; pp < 4; ++pp) {
+        s2[pp] = s;
+        zlo[pp] = lo;
+        zhi[pp] = hi;
+    }
+}
+
+// log2 of the blocks per group when that is a power of two, else -1.
+__device__ __forceinline__ int group_shift(int gs_kb)
+{
+    return (gs_kb > 0 && (gs_kb & (gs_kb - 1)) == 0) ? __ffs(gs_kb) - 1 : -1;
 }
 
 // ---------------------------------------------------------------------------------------

@@ -233,9 +233,9 @@ __device__ void run_compute(const GemmParams &p, Sched sched, uint8_t *smem, Dec
                     for (int h = 0; h < 2; ++h) {
                         uint32_t a0[4], a1[4];
                         __half2 s2[4], zl[4], zh[4];
-                        load_scales(p, ssm, zsm, has_zp, kb + j, h, g_first, 0, col0, s2, zl, zh);
+                        load_scales(p, ssm, zsm, has_zp, kb + j, h, g_first, col0, s2, zl, zh);
                         dequant_word(pw[h * 512], zl, zh, s2, a0);
-                        load_scales(p, ssm, zsm, has_zp, kb + j, h, g_first, 0, col0 + 8, s2, zl, zh);
+                        load_scales(p, ssm, zsm, has_zp, kb + j, h, g_first, col0 + 8, s2, zl, zh);
                         dequant_word(pw[h * 512 + 32], zl, zh, s2, a1);
                         const uint32_t actj = (h ? act1 : act0) + j * p.act_kb_bytes;
 #pragma unroll

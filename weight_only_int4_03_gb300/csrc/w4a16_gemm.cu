@@ -100,16 +100,21 @@ __device__ void run_mma(const GemmParams &p, const SegTable &seg, Sched sched, u
 // tensor-memory columns.
 constexpr int DQ_SETS = DQ_WARPS / 4;
 
+// grp_rel >= 0: the block lies in one group, row grp_rel of the stage's scales; otherwise
+// each 8-row pair looks up its own group.
 template <bool A_TMEM>
 __device__ __forceinline__ void dequant_block(const GemmParams &p, const uint8_t *packed,
                                               const __half *ssm, const __half *zsm, int kb,
-                                              int g_first, int gs_kb, int nl, bool has_zp,
+                                              int g_first, int grp_rel, int nl, bool has_zp,
                                               uint32_t dst_tmem, uint8_t *dst_smem)
 {
+    __half2 s2[4], zlo[4], zhi[4];
+    if (grp_rel >= 0)
+        load_scales_row(ssm, zsm, has_zp, grp_rel, nl, s2, zlo, zhi);
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-        __half2 s2[4], zlo[4], zhi[4];
-        load_scales(p, ssm, zsm, has_zp, kb, h, g_first, gs_kb, nl, s2, zlo, zhi);
+        if (grp_rel < 0)
+            load_scales(p, ssm, zsm, has_zp, kb, h, g_first, nl, s2, zlo, zhi);
         const uint4 wv = *reinterpret_cast<const uint4 *>(packed + (h * 512 + nl * 4) * 4);
         const uint32_t words[4] = {wv.x, wv.y, wv.z, wv.w};
         uint32_t out[16];
@@ -147,6 +152,7 @@ __device__ void run_dequant(const GemmParams &p, Sched sched, uint8_t *smem, uin
     const bool has_zp = p.zeros != nullptr;
     const int gs = p.group_size;
     const int gs_kb = (gs % KBLK == 0) ? gs / KBLK : 0; // 64-row blocks per group, or 0
+    const int gs_sh = group_shift(gs_kb);
     Ring ring, apos;
     int owner_set = 0; // dequant set of the next 64-row block
     int tile, kb0, kb1;
@@ -169,8 +175,12 @@ __device__ void run_dequant(const GemmParams &p, Sched sched, uint8_t *smem, uin
                     if (!mbar_wait(&bars.aempty[a.idx], a.phase ^ 1u, ctl, W4A16_DEV_TIMEOUT))
                         return;
                     tc_fence_after();
-                    dequant_block<A_TMEM>(p, st + p.packed_off + j * TILE_BYTES, ssm, zsm, kb + j,
-                                          g_first, gs_kb, nl, has_zp,
+                    const int kbj = kb + j;
+                    const int grp_rel = gs_kb == 0   ? -1
+                                        : gs_sh >= 0 ? (kbj >> gs_sh) - g_first
+                                                     : kbj / gs_kb - g_first;
+                    dequant_block<A_TMEM>(p, st + p.packed_off + j * TILE_BYTES, ssm, zsm, kbj,
+                                          g_first, grp_rel, nl, has_zp,
                                           tmem_base + lane_base + a.idx * A_SLOT_COLS,
                                           aring + a.idx * A_SLOT_BYTES);
                     mine |= 1u << j;
@@ -205,10 +215,11 @@ __device__ void run_dequant(const GemmParams &p, Sched sched, uint8_t *smem, uin
 }
 
 __device__ void run_epilogue(const GemmParams &p, const SegTable &seg, Sched sched, Bars &bars,
-                             uint32_t tmem_base, const WaitCtl &ctl, int warp, int lane,
-                             volatile int *last_flag)
+                             uint32_t tmem_base, uint8_t *smem, const WaitCtl &ctl, int warp,
+                             int lane, volatile int *last_flag)
 {
     const int q = warp & 3;
+    __half *stg = reinterpret_cast<__half *>(smem + p.epi_smem_off) + q * EPI_ROWS * 32;
     const int nl = q * 32 + lane;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     uint32_t seg_i = 0, nsync = 0;
@@ -231,25 +242,42 @@ __device__ void run_epilogue(const GemmParams &p, const SegTable &seg, Sched sch
         tc_fence_after();
         const uint32_t taddr = tmem_base + lane_base + p.acc_col0 + abuf * p.nt_max;
         const bool whole = (kb0 == 0 && kb1 == p.kblocks);
-        const int col = ti.n0 + nl;
         const long long st_tile = (long long)tile - sched.dp_tiles;
         float *part = whole ? nullptr : partial_slot(p, sched.cta, own_slot(p, sched, st_tile));
-        for (int c0 = 0; c0 < ti.ntok; c0 += 16) {
-            uint32_t v[16];
-            tmem_ld16(taddr + c0, v);
+        // Batches of 32 token rows: two tensor-memory loads per wait.  A whole tile goes out
+        // through this warp's staging buffer (its 32 columns x 32 rows as fp16), so that each
+        // lane writes 16-byte runs of a C row instead of single halves.
+        for (int c0 = 0; c0 < ti.ntok; c0 += EPI_ROWS) {
+            uint32_t v[32];
+            tmem_ld16(taddr + c0, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+            if (c0 + 16 < ti.ntok)
+                tmem_ld16(taddr + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
             tmem_ld_wait();
+            if (whole) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const int row = c0 + j;
-                if (row < ti.rows) {
-                    const float f = __uint_as_float(v[j]);
-                    if (whole) {
+                for (int j = 0; j < EPI_ROWS; ++j)
+                    stg[j * 32 + lane] = __float2half_rn(__uint_as_float(v[j]));
+                __syncwarp();
+#pragma unroll
+                for (int i = 0; i < EPI_ROWS / 8; ++i) {
+                    const int r = i * 8 + (lane >> 2);
+                    const int cseg = (lane & 3) * 8;
+                    const uint4 val = *reinterpret_cast<const uint4 *>(stg + r * 32 + cseg);
+                    const int row = c0 + r;
+                    if (row < ti.rows) {
                         const int out_row = output_row(p, ti, row);
                         if (out_row >= 0)
-                            p.c[(long long)out_row * p.ldc + col] = __float2half_rn(f);
-                    } else {
-                        __stcg(part + row * TILE_N + nl, f);
+                            *reinterpret_cast<uint4 *>(p.c + (long long)out_row * p.ldc + ti.n0 +
+                                                       q * 32 + cseg) = val;
                     }
+                }
+                __syncwarp();
+            } else {
+#pragma unroll
+                for (int j = 0; j < EPI_ROWS; ++j) {
+                    const int row = c0 + j;
+                    if (row < ti.rows)
+                        __stcg(part + row * TILE_N + nl, __uint_as_float(v[j]));
                 }
             }
         }
@@ -358,7 +386,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (lane == 0)
             run_mma<A_TMEM>(p, seg, sched, smem, aring, bars, tmem_base, ctl);
     } else if (warp >= EPI_WARP0 && warp < EPI_WARP0 + 4) {
-        run_epilogue(p, seg, sched, bars, tmem_base, ctl, warp, lane, &last_sh);
+        run_epilogue(p, seg, sched, bars, tmem_base, smem, ctl, warp, lane, &last_sh);
     } else if (warp >= DQ_WARP0) {
         run_dequant<A_TMEM>(p, sched, smem, aring, bars, tmem_base, ctl, warp, lane);
     }
@@ -374,7 +402,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 int gemm_extra_smem(bool a_tmem, bool grouped)
 {
-    int bytes = 1024; // alignment slack
+    int bytes = 1024 + EPI_STAGE_BYTES; // alignment slack, epilogue staging
     if (!a_tmem)
         bytes += SMEM_A_SLOTS * A_SLOT_BYTES;
     if (grouped)

@@ -32,6 +32,8 @@ constexpr int EPI_WARP0 = 4;     // warps 4..7: one per tensor-memory lane quart
 constexpr int DQ_WARP0 = 8;      // warps 8..15: two sets of four (one warp per lane quarter)
 constexpr int DQ_WARPS = 8;
 constexpr int EPI_THREADS = 128;
+constexpr int EPI_ROWS = 32;                               // token rows per epilogue batch
+constexpr int EPI_STAGE_BYTES = 4 * EPI_ROWS * 32 * 2;     // per warp: 32 rows x 32 columns fp16
 
 constexpr int MAX_SEGMENTS = 1024;
 
@@ -59,6 +61,7 @@ struct GemmParams {
     int acc_bufs, acc_col0, tmem_cols;
     int a_slots;              // dequantised-weight ring slots (<= MAX_A_SLOTS)
     int seg_smem_off;         // grouped: byte offset of the schedule table in dynamic smem
+    int epi_smem_off;         // tcgen05 kernel: byte offset of the epilogue's staging buffer
     // grouped schedule (null ex_off = dense)
     const int *ex_off;
     const int *ex_ids;
