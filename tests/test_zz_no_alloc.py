@@ -29,6 +29,7 @@ CASES = [
     dict(m=64, k=1024, n=1024),
     dict(m=96, k=512, n=256, flags=FLAG_FORCE_TC),
     dict(m=200, k=1024, n=512),
+    dict(m=600, k=1024, n=512),
 ]
 
 
@@ -58,7 +59,7 @@ def test_noalloc_matches_workspace_entry_point(w4, case):
 
 def test_noalloc_rejects_calls_beyond_its_scratch(w4):
     import torch
-    m, k, n = 1024, 4096, 4096
+    m, k, n = 240, 4096, 4096   # one 240-row token tile: the partial slots exceed the scratch
     assert w4.w4a16_workspace_size(m, n, k, 128) > w4.W4A16_NOALLOC_SCRATCH_BYTES
     a = torch.zeros((m, k), dtype=torch.float16, device="cuda")
     b = torch.zeros(k * n // 8, dtype=torch.int32, device="cuda")

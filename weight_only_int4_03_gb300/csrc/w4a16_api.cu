@@ -118,7 +118,9 @@ int decode_rows_default()
 }
 
 // Token-tile height of the tcgen05 kernel: one tile for M <= 256 (rounded up to the tcgen05
-// N granule of 16), 256-row tiles above; W4A16_TILE_TOKENS overrides for tuning.
+// N granule of 16); above that 192-row tiles, the tallest for which two accumulator buffers
+// fit in tensor memory beside the dequantised-weight ring, so a tile's epilogue overlaps the
+// next tile's MMAs.  W4A16_TILE_TOKENS overrides for tuning.
 int pick_nt(int m, bool grouped)
 {
     static int env = [] {
@@ -129,7 +131,7 @@ int pick_nt(int m, bool grouped)
         return grouped ? env : (m <= env ? (int)round_up(m, 16) : env);
     if (grouped)
         return 192;
-    return m <= MAX_TOK ? (int)round_up(m, 16) : MAX_TOK;
+    return m <= MAX_TOK ? (int)round_up(m, 16) : 192;
 }
 
 // Token-tile height of the small-M kernel: the smallest of 8, 16, 32, 64 rows that holds M.
