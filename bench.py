@@ -38,6 +38,8 @@ import synth  # noqa: E402
 METRIC = "W4A16 GEMM TFLOP/s and weight HBM GB/s vs M=1..4096 (fraction of roofline)"
 U4, U4B8 = 4, 5
 FLAG_ACT_ORDER, FLAG_IS_K_FULL, FLAG_HAS_ZP = 1 << 1, 1 << 2, 1 << 3
+# Inference weights are written once, long before the GEMMs that read them.
+FLAG_STATIC_WEIGHTS = 1 << 12
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -232,7 +234,7 @@ class DenseGemm:
         self.scales = [scales] + [scales.clone() for _ in range(copies - 1)]
         self.zeros = None if zeros is None else [zeros] + [zeros.clone() for _ in range(copies - 1)]
         self.perm, self.g_idx = perm, g_idx
-        self.flags = FLAG_IS_K_FULL | (FLAG_HAS_ZP if zeros is not None else 0) | (
+        self.flags = FLAG_IS_K_FULL | FLAG_STATIC_WEIGHTS | (FLAG_HAS_ZP if zeros is not None else 0) | (
             FLAG_ACT_ORDER if perm is not None else 0)
         self.a_host = torch.from_numpy(a).pin_memory()
         self.a = self.a_host.to(dev)

@@ -4,7 +4,7 @@ import pytest
 
 import oracle
 import synth
-from helpers import (ATOL, FLAG_A_SMEM, FLAG_FORCE_MMA, FLAG_FORCE_SIMT, FLAG_FORCE_TC, RTOL, U4, U4B8, DeviceProblem, make_problem,
+from helpers import (ATOL, FLAG_A_SMEM, FLAG_FORCE_MMA, FLAG_FORCE_SIMT, FLAG_FORCE_TC, FLAG_STATIC_WEIGHTS, RTOL, U4, U4B8, DeviceProblem, make_problem,
                      oracle_ref, repack_device, torch_dev, within_tol)
 
 pytestmark = pytest.mark.gpu
@@ -157,6 +157,23 @@ def test_small_m_kernel_repeatable(w4, m):
     for _ in range(3):
         dp.run()
         assert np.array_equal(dp.c.cpu().numpy().view(np.uint16), first.view(np.uint16))
+
+
+@pytest.mark.parametrize("m,k,n,kw", [(1, 4096, 4096, {}), (16, 1024, 768, dict(weight_type=U4, sigma=0.5)),
+                                      (8, 2048, 512, dict(act_order=True)), (300, 512, 512, {})])
+def test_static_weights_flag(w4, orc, m, k, n, kw):
+    """Weights read before the preceding kernel completes: same results, several calls in a row
+    (the stages issued early wrap around the ring)."""
+    pb = make_problem(1600 + m, m, k, n, **kw)
+    dp = DeviceProblem(w4, pb, flags_extra=FLAG_STATIC_WEIGHTS)
+    for _ in range(3):
+        dp.run()
+    check(dp, orc)
+    plain = DeviceProblem(w4, pb)
+    plain.run()
+    import torch
+    torch.cuda.synchronize()
+    assert np.array_equal(dp.c.cpu().numpy().view(np.uint16), plain.c.cpu().numpy().view(np.uint16))
 
 
 def test_kernel_flags_rejected(w4):

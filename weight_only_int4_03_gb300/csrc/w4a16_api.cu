@@ -402,6 +402,7 @@ void fill_params(GemmParams &p, const Plan &pl, int m, int n, int k, int group_s
     p.a_slots = pl.a_slots;
     p.seg_smem_off = pl.seg_off;
     p.epi_smem_off = pl.epi_off;
+    p.static_weights = 0;
 }
 
 // Tensor maps of one launch: activations (3-D, swizzled) and the scale / zero rows.  With no
@@ -566,6 +567,7 @@ int w4a16_gemm(const void *a, int lda, const int32_t *b_packed, void *c, int ldc
     p.zeros = static_cast<const __half *>(zeros);
     p.c = static_cast<__half *>(c);
     p.ldc = ldc;
+    p.static_weights = (flags & W4A16_FLAG_STATIC_WEIGHTS) ? 1 : 0;
     p.status = reinterpret_cast<int *>(ws);
     p.counters = reinterpret_cast<int *>(ws + pl.counters_off);
     p.partials = reinterpret_cast<float *>(ws + pl.partials_off);

@@ -242,38 +242,81 @@ struct Ring {
 // they are made as big as the stage allows), the scale/zero rows they touch (one tensor copy
 // each) and their activation rows (one 3-D tensor copy, p.kbs blocks deep).
 // ---------------------------------------------------------------------------------------
-template <class SCHED>
-static __device__ void run_producer(const GemmParams &p, const CUtensorMap *tmap_a,
-                                    const CUtensorMap *tmap_s, const CUtensorMap *tmap_z,
-                                    const SegTable &seg, SCHED sched, uint8_t *smem,
-                                    uint64_t *full_bars, uint64_t *empty_bars, const WaitCtl &ctl)
+// The weight part of one stage (packed codes, scale rows, zero rows), arming its barrier for
+// the whole stage including the activation rows that follow separately.
+static __device__ __forceinline__ void issue_stage_weights(const GemmParams &p,
+                                                           const CUtensorMap *tmap_s,
+                                                           const CUtensorMap *tmap_z,
+                                                           const TileInfo &ti, int kb, int nkb,
+                                                           uint8_t *st, uint64_t *full)
 {
     const bool has_zp = p.zeros != nullptr;
     const uint32_t fixed_bytes = (uint32_t)p.sg_box * SG_BYTES * (has_zp ? 2u : 1u) +
                                  (uint32_t)p.kbs * (uint32_t)p.act_kb_bytes;
+    const int32_t *bw = p.b + ti.expert * p.b_expert_words +
+                        ((long long)(ti.n0 / TILE_N) * p.kblocks) * TILE_WORDS;
+    mbar_arrive_expect_tx(full, fixed_bytes + nkb * (uint32_t)TILE_BYTES);
+    // The codes are read once per call: first to leave L2, so that what is re-read (the
+    // activations, scales, split partials, the kernel's own instructions) stays.
+    bulk_load_hint(st + p.packed_off, bw + (long long)kb * TILE_WORDS, nkb * TILE_BYTES, full,
+                   policy_evict_first());
+    const int g_first = ti.expert * p.num_groups + (kb * KBLK) / p.group_size;
+    tensor_load_2d(st + p.scales_off, tmap_s, ti.n0, g_first, full);
+    if (has_zp)
+        tensor_load_2d(st + p.zeros_off, tmap_z, ti.n0, g_first, full);
+}
+
+// With static weights (W4A16_FLAG_STATIC_WEIGHTS) the weight part of the first ring's worth
+// of stages is issued before the programmatic-dependency wait: nothing the preceding kernel
+// writes is read.  Returns the number of stages so issued (their activation rows are still
+// to come, from run_producer).
+template <class SCHED>
+static __device__ int issue_static_weights(const GemmParams &p, const CUtensorMap *tmap_s,
+                                           const CUtensorMap *tmap_z, const SegTable &seg,
+                                           SCHED sched, uint8_t *smem, uint64_t *full_bars)
+{
+    int n = 0;
+    int tile, kb0, kb1;
+    while (n < p.stages && sched.next(tile, kb0, kb1)) {
+        const TileInfo ti = tile_info(p, seg, tile);
+        for (int kb = kb0; kb < kb1 && n < p.stages; kb += p.kbs, ++n)
+            issue_stage_weights(p, tmap_s, tmap_z, ti, kb, min(p.kbs, kb1 - kb),
+                                smem + (size_t)n * p.stage_bytes, &full_bars[n]);
+    }
+    return n;
+}
+
+// `pre`: leading stages whose weight part issue_static_weights already issued.  `dep_wait`:
+// the caller has not yet waited on the preceding kernel; wait before the first copy that may
+// read its output (any copy, unless the weights are static; else the first activation copy).
+template <class SCHED>
+static __device__ void run_producer(const GemmParams &p, const CUtensorMap *tmap_a,
+                                    const CUtensorMap *tmap_s, const CUtensorMap *tmap_z,
+                                    const SegTable &seg, SCHED sched, uint8_t *smem,
+                                    uint64_t *full_bars, uint64_t *empty_bars, const WaitCtl &ctl,
+                                    int pre = 0, bool dep_wait = false)
+{
+    if (dep_wait && !p.static_weights)
+        pdl_wait();
     Ring ring;
     uint32_t issued = 0;
     int tile, kb0, kb1;
     bool ok = true;
     while (ok && sched.next(tile, kb0, kb1)) {
         const TileInfo ti = tile_info(p, seg, tile);
-        const int32_t *bw = p.b + ti.expert * p.b_expert_words +
-                            ((long long)(ti.n0 / TILE_N) * p.kblocks) * TILE_WORDS;
-        const int grow0 = ti.expert * p.num_groups;
         for (int kb = kb0; kb < kb1; kb += p.kbs) {
             const int nkb = min(p.kbs, kb1 - kb);
-            if (!mbar_wait(&empty_bars[ring.idx], ring.phase ^ 1u, ctl, W4A16_DEV_TIMEOUT)) {
-                ok = false;
-                break;
-            }
             uint64_t *full = &full_bars[ring.idx];
             uint8_t *st = smem + (size_t)ring.idx * p.stage_bytes;
-            mbar_arrive_expect_tx(full, fixed_bytes + nkb * (uint32_t)TILE_BYTES);
-            bulk_load(st + p.packed_off, bw + (long long)kb * TILE_WORDS, nkb * TILE_BYTES, full);
-            const int g_first = grow0 + (kb * KBLK) / p.group_size;
-            tensor_load_2d(st + p.scales_off, tmap_s, ti.n0, g_first, full);
-            if (has_zp)
-                tensor_load_2d(st + p.zeros_off, tmap_z, ti.n0, g_first, full);
+            if ((int)issued >= pre) {
+                if (!mbar_wait(&empty_bars[ring.idx], ring.phase ^ 1u, ctl, W4A16_DEV_TIMEOUT)) {
+                    ok = false;
+                    break;
+                }
+                issue_stage_weights(p, tmap_s, tmap_z, ti, kb, nkb, st, full);
+            }
+            if (dep_wait && issued == 0 && p.static_weights)
+                pdl_wait();
             // 64 columns x nt_max rows x kbs column blocks, landing as kbs consecutive
             // [nt_max x 128 B] tiles in the 128-byte swizzle.
             tensor_load_3d(st, tmap_a, 0, ti.row0, kb, full);

@@ -256,6 +256,8 @@ __device__ void run_compute(const GemmParams &p, Sched sched, uint8_t *smem, Dec
         }
 
         // Segment end: fp16 C for a whole tile, else an fp32 partial and the split protocol.
+        // (Nothing of the preceding kernel may still read C or this workspace.)
+        pdl_wait();
         const bool whole = (kb0 == 0 && kb1 == p.kblocks);
         const long long st_tile = (long long)tile - sched.dp_tiles;
         float *part = whole ? nullptr : partial_slot(p, sched.cta, own_slot(p, sched, st_tile));
@@ -308,6 +310,7 @@ __global__ void __launch_bounds__(DEC_THREADS, DEC_CTAS_PER_SM)
     const uint32_t raw = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
 
+    int pre = 0; // stages whose weight part went out before the dependency wait (thread 0)
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.stages; ++s) {
             mbar_init(&bars.full[s], 1);
@@ -322,11 +325,18 @@ __global__ void __launch_bounds__(DEC_THREADS, DEC_CTAS_PER_SM)
         if (p.zeros != nullptr)
             prefetch_tensormap(&tmap_z);
         pdl_launch_dependents();
-        Sched pre;
-        pre.init(p.m_tiles * p.n_tiles, p.kblocks);
-        prefetch_first_codes(p, pre, (uint32_t)p.stages * p.kbs * TILE_BYTES);
+        Sched first;
+        first.init(p.m_tiles * p.n_tiles, p.kblocks);
+        SegTable none{nullptr, nullptr, nullptr};
+        if (p.static_weights)
+            pre = issue_static_weights(p, &tmap_s, &tmap_z, none, first, smem, bars.full);
+        else
+            prefetch_first_codes(p, first, (uint32_t)p.stages * p.kbs * TILE_BYTES);
     }
-    pdl_wait();
+    // No programmatic-dependency wait here: the set-up below reads nothing the preceding
+    // kernel writes, so it overlaps that kernel's tail.  The producer waits before its first
+    // activation copy (and, without static weights, before any copy), the compute warps
+    // before their first global write.
     __syncthreads();
     WaitCtl ctl{&abort_sh, p.status, p.limit_ns};
     Sched sched;
@@ -336,7 +346,7 @@ __global__ void __launch_bounds__(DEC_THREADS, DEC_CTAS_PER_SM)
     if (warp == 0) {
         if (lane == 0)
             run_producer(p, &tmap_a, &tmap_s, &tmap_z, no_seg, sched, smem, bars.full, bars.empty,
-                         ctl);
+                         ctl, pre, true);
     } else {
         run_compute<NT, BLOCK_GROUPS>(p, sched, smem, bars, ctl, warp - 1, lane, &last_sh);
     }
