@@ -319,6 +319,26 @@ int launch_status(int err)
     return err == cudaSuccess ? 0 : status_of(STAGE_LAUNCH, err);
 }
 
+// CTA count for `tiles` output tiles of `kblocks` 64-row blocks on `ctas` CTA slots.  When
+// every tile can be split into s equal K-ranges (s dividing kblocks) with tiles * s CTAs
+// covering at least 80 % of the slots, use exactly that: no CTA's range then straddles two
+// tiles, so none runs two split-tile protocols back to back (M=8, 4096x4096: 9.9 -> 7.6 us).
+// Otherwise fill the slots and let ranges straddle.
+int aligned_grid(int tiles, int kblocks, int ctas)
+{
+    const long long units = (long long)tiles * kblocks;
+    if (units <= ctas)
+        return (int)(units > 0 ? units : 1);
+    const int s_max = tiles > 0 ? ctas / tiles : 0;
+    for (int s = s_max; s >= 1; --s)
+        if (kblocks % s == 0) {
+            if ((long long)tiles * s * 5 >= (long long)ctas * 4)
+                return tiles * s;
+            break;
+        }
+    return ctas;
+}
+
 // Kernel choice of a dense call: 1 = small-M register-fragment kernel, 0 = tcgen05, or a
 // negative status when the flags conflict or force the small-M kernel beyond its rows.
 int choose_mma(int m, unsigned flags)
@@ -350,7 +370,7 @@ void dense_plan(Plan &pl, int m, int n, int k, unsigned flags, int num_sms, bool
     pl.m_tiles = (m + pl.nt_max - 1) / pl.nt_max;
     const long long units = (long long)pl.m_tiles * (n / TILE_N) * (k / KBLK);
     const int ctas = mma ? num_sms * decode_ctas_per_sm() : num_sms;
-    pl.grid = (int)(units < ctas ? units : ctas);
+    pl.grid = aligned_grid(pl.m_tiles * (n / TILE_N), k / KBLK, ctas);
     // The workspace serves whichever kernel a call picks: counters for the smaller tile
     // height, partial slots for the larger CTA count x tile height.
     pl.tiles_bound = ((m + nt_small - 1) / nt_small) * (n / TILE_N);
