@@ -35,7 +35,7 @@ __device__ __forceinline__ void dequant_word(uint32_t x, const __half2 (&zlo)[4]
     const __half2 sixteenth = __halves2half2(__ushort_as_half(0x2C00), __ushort_as_half(0x2C00));
     const uint32_t t0 = (x & 0x000F000Fu) | magic;
     const uint32_t t1 = (x & 0x00F000F0u) | magic;
-    const uint32_t x8 = x >> 8;
+    const uint32_t x8 = __umulhi(x, 1u << 24); // x >> 8, on the FMA pipe (the integer pipe is the busy one)
     const uint32_t t2 = (x8 & 0x000F000Fu) | magic;
     const uint32_t t3 = (x8 & 0x00F000F0u) | magic;
     const __half2 v0 = __hsub2(u32_as_h2(t0), zlo[0]);

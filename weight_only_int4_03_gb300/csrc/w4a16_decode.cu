@@ -47,11 +47,14 @@ __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t (&r)[4])
                  : "r"(addr));
 }
 
+// A plain shared-memory load (not inline assembly), so the compiler may schedule the code
+// words of later blocks early; the stage's mbarrier wait (a memory clobber) keeps them after
+// the data has landed.
 __device__ __forceinline__ uint32_t lds32(uint32_t addr)
 {
-    uint32_t v;
-    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
-    return v;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t base = (uint32_t)__cvta_generic_to_shared(smem_raw);
+    return *reinterpret_cast<const uint32_t *>(smem_raw + (addr - base));
 }
 
 // D (f32 16x8) += A (f16 16x16, row) * B (f16 16x8, col).  Registers only, so the compiler
@@ -72,7 +75,7 @@ __device__ __forceinline__ void dequant_word_col(uint32_t x, __half2 zlo, __half
 {
     const uint32_t magic = 0x64006400u;
     const __half2 sixteenth = __halves2half2(__ushort_as_half(0x2C00), __ushort_as_half(0x2C00));
-    const uint32_t x8 = x >> 8;
+    const uint32_t x8 = __umulhi(x, 1u << 24); // x >> 8, on the FMA pipe (the integer pipe is the busy one)
     out[0] = h2_as_u32(__hmul2(__hsub2(u32_as_h2((x & 0x000F000Fu) | magic), zlo), s));
     out[1] = h2_as_u32(__hmul2(__hfma2(u32_as_h2((x & 0x00F000F0u) | magic), sixteenth, zhi), s));
     out[2] = h2_as_u32(__hmul2(__hsub2(u32_as_h2((x8 & 0x000F000Fu) | magic), zlo), s));
