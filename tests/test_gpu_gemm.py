@@ -176,6 +176,17 @@ def test_static_weights_flag(w4, orc, m, k, n, kw):
     assert np.array_equal(dp.c.cpu().numpy().view(np.uint16), plain.c.cpu().numpy().view(np.uint16))
 
 
+@pytest.mark.parametrize("m,k,n,flag", [(1, 4096, 4096, 0), (13, 4224, 4096, 0), (5, 1152, 12288, 0),
+                                        (64, 4096, 4096, FLAG_FORCE_TC), (40, 2176, 4096, FLAG_FORCE_MMA)])
+def test_tile_aligned_split_schedule(w4, orc, m, k, n, flag):
+    """Shapes whose tiles x CTAs-per-tile cover most of the GPU run one near-equal K-range per
+    CTA (uneven when the split does not divide the 64-row blocks: 66 blocks over 9, 18 over 3)."""
+    dp = DeviceProblem(w4, make_problem(1700 + m, m, k, n), flags_extra=flag)
+    for _ in range(2):
+        dp.run()
+    check(dp, orc)
+
+
 def test_kernel_flags_rejected(w4):
     pb = make_problem(1500, 65, 256, 256)
     dp = DeviceProblem(w4, pb, flags_extra=FLAG_FORCE_MMA)

@@ -55,6 +55,7 @@ struct Plan {
     int kbs, sg_box, act_kb_bytes, packed_off, scales_off, zeros_off;
     int stages, stage_bytes, acc_bufs, acc_col0, tmem_cols, smem_bytes, seg_off, epi_off, a_slots;
     bool a_tmem, mma; // mma: the small-M register-fragment kernel instead of tcgen05
+    int split = 0;    // tile-aligned split factor (0: stream-K)
     long long counters_off, partials_off, a_off, total;
 };
 
@@ -319,23 +320,24 @@ int launch_status(int err)
     return err == cudaSuccess ? 0 : status_of(STAGE_LAUNCH, err);
 }
 
-// CTA count for `tiles` output tiles of `kblocks` 64-row blocks on `ctas` CTA slots.  When
-// every tile can be split into s equal K-ranges (s dividing kblocks) with tiles * s CTAs
-// covering at least 80 % of the slots, use exactly that: no CTA's range then straddles two
-// tiles, so none runs two split-tile protocols back to back (M=8, 4096x4096: 9.9 -> 7.6 us).
-// Otherwise fill the slots and let ranges straddle.
-int aligned_grid(int tiles, int kblocks, int ctas)
+// CTA count for `tiles` output tiles of `kblocks` 64-row blocks on `ctas` CTA slots, and the
+// split factor (0: stream-K).  When every tile can take s >= 1 CTAs (s <= kblocks), each with
+// one near-equal K-range, and tiles * s CTAs cover at least 80 % of the slots, launch exactly
+// that: no CTA's range then straddles two tiles, so none runs two split-tile protocols back to
+// back (M=8, 4096x4096: 9.9 -> 7.6 us).  Otherwise stream-K over all slots.
+int aligned_grid(int tiles, int kblocks, int ctas, int *split)
 {
+    *split = 0;
     const long long units = (long long)tiles * kblocks;
     if (units <= ctas)
         return (int)(units > 0 ? units : 1);
-    const int s_max = tiles > 0 ? ctas / tiles : 0;
-    for (int s = s_max; s >= 1; --s)
-        if (kblocks % s == 0) {
-            if ((long long)tiles * s * 5 >= (long long)ctas * 4)
-                return tiles * s;
-            break;
-        }
+    int s = tiles > 0 ? ctas / tiles : 0;
+    if (s > kblocks)
+        s = kblocks;
+    if (s >= 1 && (long long)tiles * s * 5 >= (long long)ctas * 4) {
+        *split = s;
+        return tiles * s;
+    }
     return ctas;
 }
 
@@ -370,7 +372,7 @@ void dense_plan(Plan &pl, int m, int n, int k, unsigned flags, int num_sms, bool
     pl.m_tiles = (m + pl.nt_max - 1) / pl.nt_max;
     const long long units = (long long)pl.m_tiles * (n / TILE_N) * (k / KBLK);
     const int ctas = mma ? num_sms * decode_ctas_per_sm() : num_sms;
-    pl.grid = aligned_grid(pl.m_tiles * (n / TILE_N), k / KBLK, ctas);
+    pl.grid = aligned_grid(pl.m_tiles * (n / TILE_N), k / KBLK, ctas, &pl.split);
     // The workspace serves whichever kernel a call picks: counters for the smaller tile
     // height, partial slots for the larger CTA count x tile height.
     pl.tiles_bound = ((m + nt_small - 1) / nt_small) * (n / TILE_N);
@@ -423,6 +425,7 @@ void fill_params(GemmParams &p, const Plan &pl, int m, int n, int k, int group_s
     p.seg_smem_off = pl.seg_off;
     p.epi_smem_off = pl.epi_off;
     p.static_weights = 0;
+    p.split = pl.split;
 }
 
 // Tensor maps of one launch: activations (3-D, swizzled) and the scale / zero rows.  With no

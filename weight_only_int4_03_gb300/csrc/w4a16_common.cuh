@@ -114,13 +114,31 @@ struct Sched {
     int grid, cta, tiles, kblocks, dp_tiles, dp_next;
     long long sk_units, u, u_end, u_begin;
     bool small; // sk_units * (grid + 1) fits in 32 bits
+    // Split mode (split > 0, grid = tiles * split): CTA c takes the (c % split)-th of `split`
+    // near-equal K-ranges of tile c / split -- one segment, never straddling two tiles.
+    int split, split_tile, kb_lo, kb_hi;
+    bool split_done;
 
     // CTAs beyond the number of work units get nothing, so that the CTAs sharing a split
     // tile are always consecutive (the fixed-order reduction walks them by index).
-    __device__ void init(int tiles_, int kblocks_)
+    __device__ void init(int tiles_, int kblocks_, int split_ = 0)
     {
         tiles = tiles_;
         kblocks = kblocks_;
+        split = split_;
+        if (split > 0) {
+            grid = (int)gridDim.x;
+            cta = (int)blockIdx.x;
+            dp_tiles = dp_next = 0;
+            sk_units = u = u_end = u_begin = 0;
+            small = true;
+            const int r = cta % split;
+            split_tile = cta / split;
+            kb_lo = (int)((long long)r * kblocks / split);
+            kb_hi = (int)((long long)(r + 1) * kblocks / split);
+            split_done = split_tile >= tiles || kb_lo >= kb_hi;
+            return;
+        }
         const long long units = (long long)tiles * kblocks;
         grid = (int)min((long long)gridDim.x, max(units, 1LL));
         cta = blockIdx.x;
@@ -149,6 +167,15 @@ struct Sched {
     // Next segment of work: tile index and its 64-row block range [kb0, kb1).
     __device__ bool next(int &tile, int &kb0, int &kb1)
     {
+        if (split > 0) {
+            if (split_done)
+                return false;
+            tile = split_tile;
+            kb0 = kb_lo;
+            kb1 = kb_hi;
+            split_done = true;
+            return true;
+        }
         if (dp_next < dp_tiles) {
             tile = dp_next;
             kb0 = 0;
@@ -424,6 +451,8 @@ __device__ __forceinline__ float *partial_slot(const GemmParams &p, int cta, int
 // This CTA's slot for stream-K tile st_tile.
 __device__ __forceinline__ int own_slot(const GemmParams &p, const Sched &sched, long long st_tile)
 {
+    if (sched.split > 0)
+        return 0; // one segment per CTA
     return sched.u_begin >= st_tile * p.kblocks ? 0 : 1;
 }
 
@@ -451,8 +480,14 @@ struct Contributors {
 __device__ __forceinline__ Contributors contributors(const GemmParams &p, const Sched &sched,
                                                      long long st_tile)
 {
-    const long long u0 = st_tile * p.kblocks;
     Contributors c;
+    if (sched.split > 0) {
+        c.lo = (int)st_tile * sched.split;
+        c.hi = c.lo + sched.split - 1;
+        c.lo_slot = 0;
+        return c;
+    }
+    const long long u0 = st_tile * p.kblocks;
     c.lo = sched.owner(u0);
     c.hi = sched.owner(u0 + p.kblocks - 1);
     c.lo_slot = sched.begin_of(c.lo) >= u0 ? 0 : 1;

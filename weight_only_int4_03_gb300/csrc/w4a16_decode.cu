@@ -329,7 +329,7 @@ __global__ void __launch_bounds__(DEC_THREADS, DEC_CTAS_PER_SM)
             prefetch_tensormap(&tmap_z);
         pdl_launch_dependents();
         Sched first;
-        first.init(p.m_tiles * p.n_tiles, p.kblocks);
+        first.init(p.m_tiles * p.n_tiles, p.kblocks, p.split);
         SegTable none{nullptr, nullptr, nullptr};
         if (p.static_weights)
             pre = issue_static_weights(p, &tmap_s, &tmap_z, none, first, smem, bars.full);
@@ -343,7 +343,7 @@ __global__ void __launch_bounds__(DEC_THREADS, DEC_CTAS_PER_SM)
     __syncthreads();
     WaitCtl ctl{&abort_sh, p.status, p.limit_ns};
     Sched sched;
-    sched.init(p.m_tiles * p.n_tiles, p.kblocks);
+    sched.init(p.m_tiles * p.n_tiles, p.kblocks, p.split);
     SegTable no_seg{nullptr, nullptr, nullptr};
 
     if (warp == 0) {

@@ -377,7 +377,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t tmem_base = tmem_base_sh;
     WaitCtl ctl{&abort_sh, p.status, p.limit_ns};
     Sched sched;
-    sched.init(total_tiles_sh, p.kblocks);
+    sched.init(total_tiles_sh, p.kblocks, p.split);
 
     if (warp == PRODUCER_WARP) {
         if (lane == 0)

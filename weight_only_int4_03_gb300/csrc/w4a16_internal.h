@@ -63,6 +63,7 @@ struct GemmParams {
     int seg_smem_off;         // grouped: byte offset of the schedule table in dynamic smem
     int epi_smem_off;         // tcgen05 kernel: byte offset of the epilogue's staging buffer
     int static_weights;       // weights may be read before the preceding kernel completes
+    int split;                // > 0: tile-aligned split schedule (grid = tiles * split)
     // grouped schedule (null ex_off = dense)
     const int *ex_off;
     const int *ex_ids;
