@@ -506,28 +506,48 @@ __device__ __forceinline__ int split_counter_arrive(int *counter)
     return old;
 }
 
-// Sum the partials of a split tile and write fp16 C.  Work items are (row, 4-column quad);
-// when there are fewer items than threads, `ways` consecutive threads share an item, thread j
-// summing contributors lo + j, lo + j + ways, ... and a fixed shuffle tree combining the ways
-// -- a fixed order, so results are bit-identical from run to run.  Up to eight contributor
-// loads of a thread are in flight together.  `nthreads` must be a multiple of 32.
+// Sum the partials of a split tile and write fp16 C.  Work items are (row, 4-column quad).
+// With fewer items than threads, `ways` consecutive threads share an item, thread j summing
+// contributors lo + j, lo + j + ways, ... and a fixed shuffle tree combining the ways; with more
+// items than threads, each thread takes RB items per round and keeps their loads (up to
+// RB x CB partial quads) in flight together -- the partials sit in L2, so the reduction is
+// bound by load latency, not bandwidth.  Every order is fixed, so results are bit-identical from
+// run to run.  `nthreads` must be a multiple of 32.
+static __device__ __forceinline__ void store_quad(const GemmParams &p, const TileInfo &ti, int row,
+                                                  int cq, float4 acc)
+{
+    const int out_row = output_row(p, ti, row);
+    if (out_row < 0)
+        return;
+    const __half2 lo = __floats2half2_rn(acc.x, acc.y);
+    const __half2 hi = __floats2half2_rn(acc.z, acc.w);
+    uint2 packed;
+    packed.x = *reinterpret_cast<const uint32_t *>(&lo);
+    packed.y = *reinterpret_cast<const uint32_t *>(&hi);
+    *reinterpret_cast<uint2 *>(p.c + (long long)out_row * p.ldc + ti.n0 + 4 * cq) = packed;
+}
+
+__device__ __forceinline__ const float4 *partial_quads(const GemmParams &p, const Contributors &cb,
+                                                       int c)
+{
+    return reinterpret_cast<const float4 *>(partial_slot(p, c, c == cb.lo ? cb.lo_slot : 0));
+}
+
+template <int RB = 4>
 static __device__ void reduce_tile(const GemmParams &p, const TileInfo &ti, const Contributors &cb,
                                    int tid, int nthreads)
 {
-    const int items = ti.rows * (TILE_N / 4);
+    constexpr int QUADS = TILE_N / 4;
+    const int items = ti.rows * QUADS;
     const int ncontrib = cb.hi - cb.lo + 1;
-    int ways = 1;
-    while (ways < 16 && ways * 2 <= ncontrib && items * ways * 2 <= nthreads)
-        ways *= 2;
-    const int slots = items * ways;
-    const int rounds = (slots + nthreads - 1) / nthreads;
-    for (int r = 0; r < rounds; ++r) {
-        const int slot = r * nthreads + tid;
-        const bool active = slot < slots;
+    if (items * 2 <= nthreads) {
+        int ways = 1;
+        while (ways < 16 && ways * 2 <= ncontrib && items * ways * 2 <= nthreads)
+            ways *= 2;
+        const int slot = tid;
+        const bool active = slot < items * ways;
         const int item = slot / ways;
         const int j = slot - item * ways;
-        const int row = item / (TILE_N / 4);
-        const int cq = item - row * (TILE_N / 4);
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         if (active) {
             for (int c0 = cb.lo + j; c0 <= cb.hi; c0 += 8 * ways) {
@@ -535,10 +555,8 @@ static __device__ void reduce_tile(const GemmParams &p, const TileInfo &ti, cons
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
                     const int c = c0 + u * ways;
-                    const float4 *pc = reinterpret_cast<const float4 *>(
-                        partial_slot(p, c, c == cb.lo ? cb.lo_slot : 0));
-                    v[u] = (c <= cb.hi) ? __ldcg(pc + row * (TILE_N / 4) + cq)
-                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+                    v[u] = c <= cb.hi ? __ldcg(partial_quads(p, cb, c) + item)
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
@@ -555,17 +573,42 @@ static __device__ void reduce_tile(const GemmParams &p, const TileInfo &ti, cons
             acc.z += __shfl_xor_sync(0xffffffffu, acc.z, off);
             acc.w += __shfl_xor_sync(0xffffffffu, acc.w, off);
         }
-        if (!active || j != 0)
-            continue;
-        const int out_row = output_row(p, ti, row);
-        if (out_row < 0)
-            continue;
-        const __half2 lo = __floats2half2_rn(acc.x, acc.y);
-        const __half2 hi = __floats2half2_rn(acc.z, acc.w);
-        uint2 packed;
-        packed.x = *reinterpret_cast<const uint32_t *>(&lo);
-        packed.y = *reinterpret_cast<const uint32_t *>(&hi);
-        *reinterpret_cast<uint2 *>(p.c + (long long)out_row * p.ldc + ti.n0 + 4 * cq) = packed;
+        if (active && j == 0)
+            store_quad(p, ti, item / QUADS, item % QUADS, acc);
+        return;
+    }
+    constexpr int CB = 4; // RB items per round x CB contributors per batch in flight
+    for (int base = tid; base < items; base += nthreads * RB) {
+        float4 acc[RB];
+#pragma unroll
+        for (int r = 0; r < RB; ++r)
+            acc[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int c0 = cb.lo; c0 <= cb.hi; c0 += CB) {
+            float4 v[RB][CB];
+#pragma unroll
+            for (int r = 0; r < RB; ++r)
+#pragma unroll
+                for (int u = 0; u < CB; ++u) {
+                    const int item = base + r * nthreads, c = c0 + u;
+                    v[r][u] = (item < items && c <= cb.hi) ? __ldcg(partial_quads(p, cb, c) + item)
+                                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+            for (int r = 0; r < RB; ++r)
+#pragma unroll
+                for (int u = 0; u < CB; ++u) {
+                    acc[r].x += v[r][u].x;
+                    acc[r].y += v[r][u].y;
+                    acc[r].z += v[r][u].z;
+                    acc[r].w += v[r][u].w;
+                }
+        }
+#pragma unroll
+        for (int r = 0; r < RB; ++r) {
+            const int item = base + r * nthreads;
+            if (item < items)
+                store_quad(p, ti, item / QUADS, item % QUADS, acc[r]);
+        }
     }
 }
 

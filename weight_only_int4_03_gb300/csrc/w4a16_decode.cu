@@ -292,7 +292,7 @@ __device__ void run_compute(const GemmParams &p, Sched sched, uint8_t *smem, Dec
             return;
         if (!*last_flag)
             continue;
-        reduce_tile(p, ti, cb, w * 32 + lane, DEC_WARPS * 32);
+        reduce_tile<2>(p, ti, cb, w * 32 + lane, DEC_WARPS * 32); // lighter: keeps the main loop free of spills
         if (w == 0 && lane == 0)
             p.counters[tile] = 0;
     }
