@@ -25,7 +25,6 @@ struct Bars {
     uint64_t accfull[2];
     uint64_t accempty[2];
     uint64_t drain;
-    uint64_t epi;       // epilogue-group rendezvous (bounded, unlike a named barrier)
 };
 
 template <bool A_TMEM>
@@ -214,25 +213,18 @@ __device__ void run_dequant(const GemmParams &p, Sched sched, uint8_t *smem, uin
     }
 }
 
+// Split tiles get only their fp32 partial here; the counter and the reduction wait until the
+// whole CTA is done (see the kernel's end), when all of its threads can share the reduction.
 __device__ void run_epilogue(const GemmParams &p, const SegTable &seg, Sched sched, Bars &bars,
                              uint32_t tmem_base, uint8_t *smem, const WaitCtl &ctl, int warp,
-                             int lane, volatile int *last_flag)
+                             int lane, int *split_tiles, int *n_split)
 {
     const int q = warp & 3;
     __half *stg = reinterpret_cast<__half *>(smem + p.epi_smem_off) + q * EPI_ROWS * 32;
     const int nl = q * 32 + lane;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-    uint32_t seg_i = 0, nsync = 0;
+    uint32_t seg_i = 0;
     int tile, kb0, kb1;
-    // The four epilogue warps meet here; gives up (false) on abort instead of hanging.
-    auto rendezvous = [&]() -> bool {
-        __syncwarp();
-        if (lane == 0)
-            mbar_arrive(&bars.epi);
-        const bool ok = mbar_wait(&bars.epi, nsync & 1u, ctl, W4A16_DEV_TIMEOUT);
-        ++nsync;
-        return ok;
-    };
     while (sched.next(tile, kb0, kb1)) {
         const TileInfo ti = tile_info(p, seg, tile);
         const int abuf = seg_i % p.acc_bufs;
@@ -286,26 +278,8 @@ __device__ void run_epilogue(const GemmParams &p, const SegTable &seg, Sched sch
         if (lane == 0)
             mbar_arrive(&bars.accempty[abuf]);
         ++seg_i;
-        if (whole)
-            continue;
-        // Split tile: publish the partial, and let the last contributor reduce.  The
-        // rendezvous orders the group's stores before thread 0's device-scope fence and
-        // counter update (fences are cumulative), so one fence publishes the whole tile.
-        if (!rendezvous())
-            return;
-        const Contributors cb = contributors(p, sched, st_tile);
-        if (warp == EPI_WARP0 && lane == 0) {
-            const int old = split_counter_arrive(&p.counters[tile]);
-            const int last = old == (cb.hi - cb.lo);
-            *last_flag = last;
-        }
-        if (!rendezvous())
-            return;
-        if (!*last_flag)
-            continue;
-        reduce_tile(p, ti, cb, (warp - EPI_WARP0) * 32 + lane, EPI_THREADS);
-        if (warp == EPI_WARP0 && lane == 0)
-            p.counters[tile] = 0;
+        if (!whole && warp == EPI_WARP0 && lane == 0)
+            split_tiles[(*n_split)++] = tile;
     }
 }
 
@@ -318,7 +292,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     __shared__ Bars bars;
     __shared__ uint32_t tmem_base_sh;
     __shared__ volatile int abort_sh;
-    __shared__ volatile int last_sh;
+    __shared__ volatile int last_sh[2];
+    __shared__ int split_tiles_sh[2];
+    __shared__ int n_split_sh;
     __shared__ int total_tiles_sh;
 
     const int warp = threadIdx.x >> 5;
@@ -346,10 +322,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(&bars.accempty[s], EPI_THREADS / 32);
         }
         mbar_init(&bars.drain, 1);
-        mbar_init(&bars.epi, EPI_THREADS / 32);
         fence_mbar_init();
         abort_sh = 0;
-        last_sh = 0;
+        last_sh[0] = last_sh[1] = 0;
+        n_split_sh = 0;
         prefetch_tensormap(&tmap_a);
         prefetch_tensormap(&tmap_s);
         if (p.zeros != nullptr)
@@ -386,7 +362,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (lane == 0)
             run_mma<A_TMEM>(p, seg, sched, smem, aring, bars, tmem_base, ctl);
     } else if (warp >= EPI_WARP0 && warp < EPI_WARP0 + 4) {
-        run_epilogue(p, seg, sched, bars, tmem_base, smem, ctl, warp, lane, &last_sh);
+        run_epilogue(p, seg, sched, bars, tmem_base, smem, ctl, warp, lane, split_tiles_sh,
+                     &n_split_sh);
     } else if (warp >= DQ_WARP0) {
         run_dequant<A_TMEM>(p, sched, smem, aring, bars, tmem_base, ctl, warp, lane);
     }
@@ -397,6 +374,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp == MMA_WARP) {
         tc_fence_after();
         tmem_dealloc(tmem_base, p.tmem_cols);
+    }
+
+    // Split tiles of this CTA (at most two: where its range starts and ends).  The barrier
+    // above orders the partial stores before the counter atomics (release is cumulative); the
+    // last contributor of a tile sums the partials with all of the CTA's threads.
+    const int n_split = n_split_sh;
+    if (n_split == 0 || abort_sh)
+        return;
+    if (threadIdx.x < n_split) {
+        const int tile = split_tiles_sh[threadIdx.x];
+        const Contributors cb = contributors(p, sched, (long long)tile - sched.dp_tiles);
+        const int old = split_counter_arrive(&p.counters[tile]);
+        last_sh[threadIdx.x] = old == (cb.hi - cb.lo);
+    }
+    __syncthreads();
+    for (int i = 0; i < n_split; ++i) {
+        if (!last_sh[i])
+            continue;
+        const int tile = split_tiles_sh[i];
+        const TileInfo ti = tile_info(p, seg, tile);
+        const Contributors cb = contributors(p, sched, (long long)tile - sched.dp_tiles);
+        reduce_tile<4>(p, ti, cb, threadIdx.x, NUM_THREADS);
+        if (threadIdx.x == 0)
+            p.counters[tile] = 0;
     }
 }
 
