@@ -213,7 +213,9 @@ __device__ void run_compute(const GemmParams &p, Sched sched, uint8_t *smem, Dec
                     c1 = col_group(has_zp, ssm, zsm, gidx + 8);
                 };
                 if (nkb == DEC_UNROLL) {
-#pragma unroll
+                    // Taller tiles keep more accumulators live: unroll less there.
+                    constexpr int UNROLL = NT <= 2 ? DEC_UNROLL : 2;
+#pragma unroll UNROLL
                     for (int j = 0; j < DEC_UNROLL; ++j) {
                         block_mma<NT>(w_addr + j * TILE_BYTES, act0 + j * p.act_kb_bytes,
                                       act1 + j * p.act_kb_bytes, c0, c1, acc, acc1);
@@ -292,7 +294,7 @@ __device__ void run_compute(const GemmParams &p, Sched sched, uint8_t *smem, Dec
             return;
         if (!*last_flag)
             continue;
-        reduce_tile<2>(p, ti, cb, w * 32 + lane, DEC_WARPS * 32); // lighter: keeps the main loop free of spills
+        reduce_tile<(NT <= 2 ? 2 : 1)>(p, ti, cb, w * 32 + lane, DEC_WARPS * 32); // lighter: no spills
         if (w == 0 && lane == 0)
             p.counters[tile] = 0;
     }
