@@ -70,6 +70,24 @@ void carve(Plan &pl, long long slot_cta_rows, long long a_bytes)
     pl.total = round_up(pl.a_off + a_bytes, 256);
 }
 
+// L2 bytes of the current device (cached; 0 if the query fails).
+long long l2_bytes()
+{
+    static std::mutex mu;
+    static long long cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[dev] == 0) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrL2CacheSize, dev) != cudaSuccess)
+            return 0;
+        cache[dev] = v;
+    }
+    return cache[dev];
+}
+
 int sm_count(int *out)
 {
     static std::mutex mu;
@@ -591,6 +609,13 @@ int w4a16_gemm(const void *a, int lda, const int32_t *b_packed, void *c, int ldc
     p.c = static_cast<__half *>(c);
     p.ldc = ldc;
     p.static_weights = (flags & W4A16_FLAG_STATIC_WEIGHTS) ? 1 : 0;
+    // Tile order: walk token tiles outermost when the activations outweigh the weights and
+    // would not stay in L2 while every column tile passes over them (e.g. M=4096, K=11008:
+    // 90 MB of A, read 4.6 times from DRAM column-tile-major).
+    {
+        const long long a_bytes = (long long)m * k * 2, w_bytes = (long long)k * n / 2;
+        p.m_outer = (a_bytes > w_bytes && a_bytes * 2 > l2_bytes()) ? 1 : 0;
+    }
     p.status = reinterpret_cast<int *>(ws);
     p.counters = reinterpret_cast<int *>(ws + pl.counters_off);
     p.partials = reinterpret_cast<float *>(ws + pl.partials_off);

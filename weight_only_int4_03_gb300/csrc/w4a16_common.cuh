@@ -221,8 +221,10 @@ __device__ __forceinline__ TileInfo tile_info(const GemmParams &p, const SegTabl
 {
     TileInfo ti;
     if (p.ex_off == nullptr) {
-        const int nt = tile / p.m_tiles;
-        const int mt = tile - nt * p.m_tiles;
+        // Column-tile-major by default (the tiles running at once share weight columns);
+        // token-tile-major when A is the operand that would otherwise fall out of L2.
+        const int nt = p.m_outer ? tile % p.n_tiles : tile / p.m_tiles;
+        const int mt = p.m_outer ? tile / p.n_tiles : tile - nt * p.m_tiles;
         ti.n0 = nt * TILE_N;
         ti.row0 = mt * p.nt_max;
         ti.rows = min(p.nt_max, p.m - ti.row0);
@@ -345,8 +347,9 @@ static __device__ void run_producer(const GemmParams &p, const CUtensorMap *tmap
             if (dep_wait && issued == 0 && p.static_weights)
                 pdl_wait();
             // 64 columns x nt_max rows x kbs column blocks, landing as kbs consecutive
-            // [nt_max x 128 B] tiles in the 128-byte swizzle.
-            tensor_load_3d(st, tmap_a, 0, ti.row0, kb, full);
+            // [nt_max x 128 B] tiles in the 128-byte swizzle.  Activation rows are read again
+            // for every column tile: last to leave L2.
+            tensor_load_3d_hint(st, tmap_a, 0, ti.row0, kb, full, policy_evict_last());
             ring.advance(p.stages);
             ++issued;
         }

@@ -258,9 +258,10 @@ __device__ void run_epilogue(const GemmParams &p, const SegTable &seg, Sched sch
                     const int row = c0 + r;
                     if (row < ti.rows) {
                         const int out_row = output_row(p, ti, row);
-                        if (out_row >= 0)
-                            *reinterpret_cast<uint4 *>(p.c + (long long)out_row * p.ldc + ti.n0 +
-                                                       q * 32 + cseg) = val;
+                        if (out_row >= 0) // written once: streaming store (first out of L2)
+                            __stcs(reinterpret_cast<uint4 *>(p.c + (long long)out_row * p.ldc +
+                                                             ti.n0 + q * 32 + cseg),
+                                   val);
                     }
                 }
                 __syncwarp();

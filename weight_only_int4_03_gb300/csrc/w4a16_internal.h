@@ -64,6 +64,7 @@ struct GemmParams {
     int epi_smem_off;         // tcgen05 kernel: byte offset of the epilogue's staging buffer
     int static_weights;       // weights may be read before the preceding kernel completes
     int split;                // > 0: tile-aligned split schedule (grid = tiles * split)
+    int m_outer;              // dense: tile index runs token-tile-major
     // grouped schedule (null ex_off = dense)
     const int *ex_off;
     const int *ex_ids;
