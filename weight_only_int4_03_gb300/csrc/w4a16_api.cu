@@ -140,16 +140,14 @@ int decode_rows_default()
 // N granule of 16); above that 192-row tiles, the tallest for which two accumulator buffers
 // fit in tensor memory beside the dequantised-weight ring, so a tile's epilogue overlaps the
 // next tile's MMAs.  W4A16_TILE_TOKENS overrides for tuning.
-int pick_nt(int m, bool grouped)
+int pick_nt(int m)
 {
     static int env = [] {
         const int v = env_int("W4A16_TILE_TOKENS", 16, MAX_TOK, 0);
         return v % 16 == 0 ? v : 0;
     }();
     if (env > 0)
-        return grouped ? env : (m <= env ? (int)round_up(m, 16) : env);
-    if (grouped)
-        return 192;
+        return m <= env ? (int)round_up(m, 16) : env;
     return m <= MAX_TOK ? (int)round_up(m, 16) : 192;
 }
 
@@ -383,7 +381,7 @@ void dense_plan(Plan &pl, int m, int n, int k, unsigned flags, int num_sms, bool
     pl.mma = mma;
     pl.a_tmem = (flags & W4A16_FLAG_A_SMEM) == 0;
     const bool mma_ok = m <= decode_max_rows();
-    const int nt_tc = pick_nt(m, false);
+    const int nt_tc = pick_nt(m);
     const int nt_mma = mma_ok ? pick_nt_mma(m) : nt_tc;
     const int nt_small = nt_tc < nt_mma ? nt_tc : nt_mma;
     pl.nt_max = mma ? nt_mma : nt_tc;
@@ -404,11 +402,26 @@ void dense_plan(Plan &pl, int m, int n, int k, unsigned flags, int num_sms, bool
     carve(pl, slot_rows, a_bytes);
 }
 
+// Token-tile height of a grouped call: the average pairs per active expert plus an eighth
+// (segment sizes spread around the average), rounded up to 16 and capped at 192 -- a tile
+// per segment, little padding (8 experts, 1024 pairs: 144 rows, +12 % over 192-row tiles).
+int pick_nt_grouped(int n_pairs, int n_active)
+{
+    static const int env = env_int("W4A16_TILE_TOKENS", 16, MAX_TOK, 0) % 16 == 0
+                               ? env_int("W4A16_TILE_TOKENS", 16, MAX_TOK, 0)
+                               : 0;
+    if (env > 0)
+        return env;
+    const long long avg = (n_pairs + (long long)n_active - 1) / n_active;
+    const long long want = round_up(avg + avg / 8, 16);
+    return (int)(want < 16 ? 16 : want > 192 ? 192 : want);
+}
+
 void grouped_plan(Plan &pl, int n_pairs, int n_active, int n, int k, unsigned flags, int num_sms)
 {
     pl.mma = false;
     pl.a_tmem = (flags & W4A16_FLAG_A_SMEM) == 0;
-    pl.nt_max = pick_nt(n_pairs, true);
+    pl.nt_max = pick_nt_grouped(n_pairs, n_active);
     pl.m_tiles = 0;
     pl.tiles_bound = ((n_pairs + pl.nt_max - 1) / pl.nt_max + n_active) * (n / TILE_N);
     pl.grid = num_sms;
