@@ -159,10 +159,12 @@ int w4a16_gemm(const void *a, int lda, const int32_t *b_packed, void *c, int ldc
  *   Arguments as w4a16_gemm, minus workspace / workspace_bytes, plus
  *   status_out  device int32 or NULL, 4-byte aligned: receives (stream-ordered) the call's
  *               device-side error bits (W4A16_DEV_*), 0 when all went well
- * A call whose w4a16_workspace_size exceeds the array returns stage 2 with detail
- * W4A16_ARG_SCRATCH and launches nothing.  On a 152-multiprocessor GPU that is M from 209 to
- * 256 rows (one token tile that tall), and act-order calls whose copy of A (M*K*2 bytes) does
- * not fit beside the rest.
+ * It holds the tcgen05 kernel's token tiles to at most 192 rows (w4a16_gemm goes up to 256),
+ * so that their partial-tile slots fit the array for every shape; M above 192 then runs in
+ * tiles of 192 rows, a little slower than w4a16_gemm where that would pick taller tiles.  A
+ * call whose scratch still exceeds the array -- an act-order call whose copy of A (M*K*2
+ * bytes) does not fit beside the rest -- returns stage 2 with detail W4A16_ARG_SCRATCH and
+ * launches nothing.
  * The first call on a device looks up the array's device address (once per device); make
  * that first call before any stream capture.  Each call clears the status word and tile
  * counters it needs on `stream` before its kernels run.  All calls on one device share the

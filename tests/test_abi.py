@@ -148,6 +148,21 @@ def test_workspace_size_host_only(w4):
     assert w4.w4a16_grouped_workspace_size(1024, 0, 28672, 4096, 128, 0, 152) == 0
 
 
+def test_token_tile_height_from_workspace(w4):
+    """The tcgen05 kernel's token-tile height, read back from the workspace size on a 152-SM
+    device (the partial slots are 2 x nt x 128 fp32 per CTA): one tile up to 256 rows; above
+    that ceil(M / 224) equal tiles rounded up to 16 rows, never below 192."""
+    def nt_of(m, n=256):
+        total = w4.w4a16_workspace_size(m, n, 128, 128, 0, 152)
+        slots = 152 * 2 * 128 * 4
+        head = total % slots
+        assert head % 256 == 0
+        return total // slots
+    expect = {100: 112, 256: 256, 257: 192, 448: 224, 449: 192, 512: 192, 600: 208, 672: 224,
+              1024: 208, 2048: 208, 4096: 224, 8192: 224}
+    assert {m: nt_of(m) for m in expect} == expect
+
+
 def test_csr_builder_matches_pages_examples(w4):
     g = json.load(open(os.path.join(ROOT, "tests", "golden", "csr_worked_examples.json")))
     for ex in g["from_token_routes"]:

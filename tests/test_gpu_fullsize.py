@@ -31,7 +31,7 @@ def orc():
 
 def sample_rows(m: int):
     rows = {0, m - 1, m // 2}
-    for edge in (8, 16, 32, 64, 192, 256):   # token-tile heights of the two kernels
+    for edge in (8, 16, 32, 64, 192, 208, 224, 256):   # token-tile heights of the two kernels
         if edge < m:
             rows.update((edge - 1, edge))
     return sorted(r for r in rows if 0 <= r < m)

@@ -74,7 +74,7 @@ def test_tiny_config(w4, orc):
     check(dp, orc)
 
 
-@pytest.mark.parametrize("m", [1, 3, 16, 17, 32, 33, 64, 100, 128, 200, 256, 257, 300, 600])
+@pytest.mark.parametrize("m", [1, 3, 16, 17, 32, 33, 64, 100, 128, 200, 256, 257, 300, 600, 1000, 1500])
 def test_m_sweep_u4b8(w4, orc, m):
     """Ragged M across token tiles; K=512 (8 row blocks), N=512 (4 column tiles): stream-K splits."""
     dp = DeviceProblem(w4, make_problem(100 + m, m, 512, 512))
@@ -96,7 +96,7 @@ def test_zero_points_u4(w4, orc, m):
     check(dp, orc)
 
 
-@pytest.mark.parametrize("m,gs", [(1, 128), (16, 128), (200, 64), (33, 32)])
+@pytest.mark.parametrize("m,gs", [(1, 128), (16, 128), (200, 64), (33, 32), (1000, 128)])
 def test_act_order(w4, orc, m, gs):
     dp = DeviceProblem(w4, make_problem(400 + m, m, 1024, 512, group_size=gs, act_order=True))
     dp.run()

@@ -29,7 +29,9 @@ CASES = [
     dict(m=64, k=1024, n=1024),
     dict(m=96, k=512, n=256, flags=FLAG_FORCE_TC),
     dict(m=200, k=1024, n=512),
+    dict(m=240, k=4096, n=512),               # one 240-row tile in w4a16_gemm, two of 192 here
     dict(m=600, k=1024, n=512),
+    dict(m=1024, k=1024, n=768, group_size=64),  # 208-row tiles in w4a16_gemm, 192 here
 ]
 
 
@@ -58,16 +60,21 @@ def test_noalloc_matches_workspace_entry_point(w4, case):
 
 
 def test_noalloc_rejects_calls_beyond_its_scratch(w4):
+    """An act-order call whose copy of A (M*K*2 = 8 MiB here) does not fit beside the partial
+    slots is refused before anything launches."""
     import torch
-    m, k, n = 240, 4096, 4096   # one 240-row token tile: the partial slots exceed the scratch
-    assert w4.w4a16_workspace_size(m, n, k, 128) > w4.W4A16_NOALLOC_SCRATCH_BYTES
+    m, k, n, gs = 1024, 4096, 4096, 128
+    flags = w4.W4A16_FLAG_ACT_ORDER | w4.W4A16_FLAG_IS_K_FULL
+    assert w4.w4a16_workspace_size(m, n, k, gs, flags) > w4.W4A16_NOALLOC_SCRATCH_BYTES
     a = torch.zeros((m, k), dtype=torch.float16, device="cuda")
     b = torch.zeros(k * n // 8, dtype=torch.int32, device="cuda")
-    s = torch.ones((k // 128, n), dtype=torch.float16, device="cuda")
+    s = torch.ones((k // gs, n), dtype=torch.float16, device="cuda")
+    g_idx = (torch.arange(k, dtype=torch.int32, device="cuda") // gs).to(torch.int32)
+    perm = torch.arange(k, dtype=torch.int32, device="cuda")
     c = torch.full((m, n), 5.0, dtype=torch.float16, device="cuda")
     with pytest.raises(w4.W4A16Error) as e:
-        w4.w4a16_gemm_noalloc(a, b, c, s, None, None, None, m, n, k, 128, w4.W4A16_TYPE_U4B8,
-                              w4.W4A16_FLAG_IS_K_FULL)
+        w4.w4a16_gemm_noalloc(a, b, c, s, None, g_idx, perm, m, n, k, gs, w4.W4A16_TYPE_U4B8,
+                              flags)
     assert e.value.stage == 2 and e.value.detail == w4.W4A16_ARG_SCRATCH
     torch.cuda.synchronize()
     assert float(c.float().min()) == 5.0 and float(c.float().max()) == 5.0

@@ -136,19 +136,33 @@ int decode_rows_default()
     return v;
 }
 
-// Token-tile height of the tcgen05 kernel: one tile for M <= 256 (rounded up to the tcgen05
-// N granule of 16); above that 192-row tiles, the tallest for which two accumulator buffers
-// fit in tensor memory beside the dequantised-weight ring, so a tile's epilogue overlaps the
-// next tile's MMAs.  W4A16_TILE_TOKENS overrides for tuning.
-int pick_nt(int m)
+// Token-tile height of the tcgen05 kernel (a multiple of 16, at most cap rows): one tile for
+// M <= cap; above that M is cut into ceil(M / 224) tiles of equal height rounded up to 16, but
+// never below 192 rows.  Prefill is bound by the dequantisation of each weight tile, which is
+// done once per token tile, so fewer, taller tiles win while the tile count stays the same or
+// drops: M=1024 runs 5 tiles of 208 (6 of 192 before), M=4096 19 of 224 (22 of 192).  Up to
+// 192 rows two accumulator buffers fit in tensor memory beside the dequantised-weight ring
+// (the epilogue overlaps the next tile's MMAs); taller tiles trade that overlap for the
+// smaller tile count.  Below 192 rows per tile the kernel slows sharply (160-row tiles run at
+// two thirds of the rate), so M just above a multiple of 192 keeps 192-row tiles.
+// W4A16_TILE_TOKENS overrides for tuning.
+int pick_nt(int m, int cap)
 {
     static int env = [] {
         const int v = env_int("W4A16_TILE_TOKENS", 16, MAX_TOK, 0);
         return v % 16 == 0 ? v : 0;
     }();
-    if (env > 0)
-        return m <= env ? (int)round_up(m, 16) : env;
-    return m <= MAX_TOK ? (int)round_up(m, 16) : 192;
+    if (env > 0) {
+        const int e = env < cap ? env : cap;
+        return m <= e ? (int)round_up(m, 16) : e;
+    }
+    if (m <= cap)
+        return (int)round_up(m, 16);
+    const int hi = cap < TALL_TILE_TOK ? cap : TALL_TILE_TOK;
+    const int lo = hi < TWO_BUF_TILE_TOK ? hi : TWO_BUF_TILE_TOK;
+    const int tiles = (m + hi - 1) / hi;
+    const int nt = (int)round_up((m + tiles - 1) / tiles, 16);
+    return nt < lo ? lo : nt;
 }
 
 // Token-tile height of the small-M kernel: the smallest of 8, 16, 32, 64 rows that holds M.
@@ -376,12 +390,12 @@ int choose_mma(int m, unsigned flags)
 
 // Dense plan.  The workspace is carved for the larger tile of the two kernels, so a size
 // query answers for whichever kernel the call then picks.
-void dense_plan(Plan &pl, int m, int n, int k, unsigned flags, int num_sms, bool mma)
+void dense_plan(Plan &pl, int m, int n, int k, unsigned flags, int num_sms, bool mma, int tile_cap)
 {
     pl.mma = mma;
     pl.a_tmem = (flags & W4A16_FLAG_A_SMEM) == 0;
     const bool mma_ok = m <= decode_max_rows();
-    const int nt_tc = pick_nt(m);
+    const int nt_tc = pick_nt(m, tile_cap);
     const int nt_mma = mma_ok ? pick_nt_mma(m) : nt_tc;
     const int nt_small = nt_tc < nt_mma ? nt_tc : nt_mma;
     pl.nt_max = mma ? nt_mma : nt_tc;
@@ -479,6 +493,111 @@ int encode_maps(const Plan &pl, const void *act, int rows, int k, int ld, const 
 
 } // namespace
 
+namespace w4 {
+
+size_t dense_workspace_size(int m, int n, int k, int group_size, unsigned flags, int num_sms,
+                            int tile_cap)
+{
+    if (m < 0 || n <= 0 || k <= 0 || n % 256 != 0 || k % 128 != 0 || num_groups(k, group_size) < 0)
+        return 0;
+    if (num_sms <= 0 && sm_count(&num_sms) != cudaSuccess)
+        return 0;
+    Plan pl;
+    dense_plan(pl, m > 0 ? m : 1, n, k, flags, num_sms, false, tile_cap);
+    return (size_t)pl.total;
+}
+
+int dense_gemm(const void *a, int lda, const int32_t *b_packed, void *c, int ldc,
+               const void *scales, const void *zeros, const int32_t *g_idx, const int32_t *perm,
+               void *workspace, size_t workspace_bytes, int m, int n, int k, int group_size,
+               int weight_type, unsigned flags, cudaStream_t stream, int tile_cap)
+{
+    int st = check_weights(b_packed, scales, zeros, n, k, group_size, weight_type, flags);
+    if (st)
+        return st;
+    if (m < 0)
+        return status_of(STAGE_ARG, W4A16_ARG_SHAPE);
+    const bool act_order = (flags & W4A16_FLAG_ACT_ORDER) != 0;
+    if (act_order != (g_idx != nullptr && perm != nullptr) || ((g_idx != nullptr) != (perm != nullptr)))
+        return status_of(STAGE_ARG, W4A16_ARG_FLAGS);
+    if (m == 0)
+        return 0; // empty input: nothing to compute
+    if (!a || !c || !workspace)
+        return status_of(STAGE_ARG, W4A16_ARG_NULL);
+    if (lda < k || ldc < n)
+        return status_of(STAGE_ARG, W4A16_ARG_SHAPE);
+    if (lda % 8 != 0 || ldc % 8 != 0 || !aligned(a, 16) || !aligned(c, 16) ||
+        !aligned(workspace, 256) || (g_idx && !aligned(g_idx, 4)) || (perm && !aligned(perm, 4)))
+        return status_of(STAGE_ARG, W4A16_ARG_ALIGN);
+    if ((long long)m * lda > (1LL << 40) || (long long)m * ldc > (1LL << 40))
+        return status_of(STAGE_ARG, W4A16_ARG_OVERFLOW);
+    if ((flags & W4A16_FLAG_FORCE_SIMT) && m > (1 << 20))
+        return status_of(STAGE_UNSUPPORTED, W4A16_ARG_SHAPE);
+
+    const int mma = choose_mma(m, flags);
+    if (mma < 0)
+        return -mma;
+
+    int num_sms = 0;
+    int err = sm_count(&num_sms);
+    if (err != cudaSuccess)
+        return status_of(STAGE_RESOURCE, err);
+    Plan pl;
+    dense_plan(pl, m, n, k, flags, num_sms, mma == 1, tile_cap);
+    if (workspace_bytes < (size_t)pl.total)
+        return status_of(STAGE_ARG, W4A16_ARG_WORKSPACE);
+    const int g = num_groups(k, group_size);
+    plan_tmem(pl);
+    err = plan_smem(pl, false, zeros != nullptr, group_size == -1 ? k : group_size, g);
+    if (err != cudaSuccess)
+        return status_of(STAGE_RESOURCE, err);
+
+    char *ws = static_cast<char *>(workspace);
+    GemmParams p;
+    fill_params(p, pl, m, n, k, group_size);
+    p.b = b_packed;
+    p.scales = static_cast<const __half *>(scales);
+    p.zeros = static_cast<const __half *>(zeros);
+    p.c = static_cast<__half *>(c);
+    p.ldc = ldc;
+    p.static_weights = (flags & W4A16_FLAG_STATIC_WEIGHTS) ? 1 : 0;
+    // Tile order: walk token tiles outermost when the activations outweigh the weights and
+    // would not stay in L2 while every column tile passes over them (e.g. M=4096, K=11008:
+    // 90 MB of A, read 4.6 times from DRAM column-tile-major).
+    {
+        const long long a_bytes = (long long)m * k * 2, w_bytes = (long long)k * n / 2;
+        p.m_outer = (a_bytes > w_bytes && a_bytes * 2 > l2_bytes()) ? 1 : 0;
+    }
+    p.status = reinterpret_cast<int *>(ws);
+    p.counters = reinterpret_cast<int *>(ws + pl.counters_off);
+    p.partials = reinterpret_cast<float *>(ws + pl.partials_off);
+
+    const __half *a_src = static_cast<const __half *>(a);
+    int a_ld = lda;
+    if (act_order) {
+        __half *a_perm = reinterpret_cast<__half *>(ws + pl.a_off);
+        err = launch_gather_cols(a_src, lda, perm, g_idx, p.group_size, a_perm, m, k, p.status,
+                                 stream);
+        if (err != cudaSuccess)
+            return status_of(STAGE_LAUNCH, err);
+        a_src = a_perm;
+        a_ld = k;
+    }
+    if (flags & W4A16_FLAG_FORCE_SIMT)
+        return launch_status(launch_gemm_simt(p, a_src, a_ld, stream));
+
+    CUtensorMap ma, ms, mz;
+    err = encode_maps(pl, a_src, m, k, a_ld, scales, zeros, g, n, &ma, &ms, &mz);
+    if (err != cudaSuccess)
+        return status_of(STAGE_RESOURCE, err);
+    GemmConfig cfg{pl.grid, pl.smem_bytes, pl.a_tmem};
+    if (pl.mma)
+        return launch_status(launch_decode(p, ma, ms, mz, cfg, stream));
+    return launch_status(launch_gemm(p, ma, ms, mz, cfg, stream));
+}
+
+} // namespace w4
+
 extern "C" {
 
 int w4a16_abi_version(void)
@@ -546,13 +665,7 @@ int w4_unpack(const int32_t *b_packed, int32_t *qweight, int k, int n, cudaStrea
 
 size_t w4a16_workspace_size(int m, int n, int k, int group_size, unsigned flags, int num_sms)
 {
-    if (m < 0 || n <= 0 || k <= 0 || n % 256 != 0 || k % 128 != 0 || num_groups(k, group_size) < 0)
-        return 0;
-    if (num_sms <= 0 && sm_count(&num_sms) != cudaSuccess)
-        return 0;
-    Plan pl;
-    dense_plan(pl, m > 0 ? m : 1, n, k, flags, num_sms, false);
-    return (size_t)pl.total;
+    return w4::dense_workspace_size(m, n, k, group_size, flags, num_sms, w4::MAX_TOK);
 }
 
 size_t w4a16_grouped_workspace_size(int n_pairs, int n_active, int n, int k, int group_size,
@@ -573,90 +686,10 @@ int w4a16_gemm(const void *a, int lda, const int32_t *b_packed, void *c, int ldc
                size_t workspace_bytes, int m, int n, int k, int group_size, int weight_type,
                unsigned flags, cudaStream_t stream)
 {
-    int st = check_weights(b_packed, scales, zeros, n, k, group_size, weight_type, flags);
-    if (st)
-        return st;
-    if (m < 0)
-        return status_of(STAGE_ARG, W4A16_ARG_SHAPE);
-    const bool act_order = (flags & W4A16_FLAG_ACT_ORDER) != 0;
-    if (act_order != (g_idx != nullptr && perm != nullptr) || ((g_idx != nullptr) != (perm != nullptr)))
-        return status_of(STAGE_ARG, W4A16_ARG_FLAGS);
-    if (m == 0)
-        return 0; // empty input: nothing to compute
-    if (!a || !c || !workspace)
-        return status_of(STAGE_ARG, W4A16_ARG_NULL);
-    if (lda < k || ldc < n)
-        return status_of(STAGE_ARG, W4A16_ARG_SHAPE);
-    if (lda % 8 != 0 || ldc % 8 != 0 || !aligned(a, 16) || !aligned(c, 16) ||
-        !aligned(workspace, 256) || (g_idx && !aligned(g_idx, 4)) || (perm && !aligned(perm, 4)))
-        return status_of(STAGE_ARG, W4A16_ARG_ALIGN);
-    if ((long long)m * lda > (1LL << 40) || (long long)m * ldc > (1LL << 40))
-        return status_of(STAGE_ARG, W4A16_ARG_OVERFLOW);
-    if ((flags & W4A16_FLAG_FORCE_SIMT) && m > (1 << 20))
-        return status_of(STAGE_UNSUPPORTED, W4A16_ARG_SHAPE);
-
-    const int mma = choose_mma(m, flags);
-    if (mma < 0)
-        return -mma;
-
-    int num_sms = 0;
-    int err = sm_count(&num_sms);
-    if (err != cudaSuccess)
-        return status_of(STAGE_RESOURCE, err);
-    Plan pl;
-    dense_plan(pl, m, n, k, flags, num_sms, mma == 1);
-    if (workspace_bytes < (size_t)pl.total)
-        return status_of(STAGE_ARG, W4A16_ARG_WORKSPACE);
-    const int g = num_groups(k, group_size);
-    plan_tmem(pl);
-    err = plan_smem(pl, false, zeros != nullptr, group_size == -1 ? k : group_size, g);
-    if (err != cudaSuccess)
-        return status_of(STAGE_RESOURCE, err);
-
-    char *ws = static_cast<char *>(workspace);
-    GemmParams p;
-    fill_params(p, pl, m, n, k, group_size);
-    p.b = b_packed;
-    p.scales = static_cast<const __half *>(scales);
-    p.zeros = static_cast<const __half *>(zeros);
-    p.c = static_cast<__half *>(c);
-    p.ldc = ldc;
-    p.static_weights = (flags & W4A16_FLAG_STATIC_WEIGHTS) ? 1 : 0;
-    // Tile order: walk token tiles outermost when the activations outweigh the weights and
-    // would not stay in L2 while every column tile passes over them (e.g. M=4096, K=11008:
-    // 90 MB of A, read 4.6 times from DRAM column-tile-major).
-    {
-        const long long a_bytes = (long long)m * k * 2, w_bytes = (long long)k * n / 2;
-        p.m_outer = (a_bytes > w_bytes && a_bytes * 2 > l2_bytes()) ? 1 : 0;
-    }
-    p.status = reinterpret_cast<int *>(ws);
-    p.counters = reinterpret_cast<int *>(ws + pl.counters_off);
-    p.partials = reinterpret_cast<float *>(ws + pl.partials_off);
-
-    const __half *a_src = static_cast<const __half *>(a);
-    int a_ld = lda;
-    if (act_order) {
-        __half *a_perm = reinterpret_cast<__half *>(ws + pl.a_off);
-        err = launch_gather_cols(a_src, lda, perm, g_idx, p.group_size, a_perm, m, k, p.status,
-                                 stream);
-        if (err != cudaSuccess)
-            return status_of(STAGE_LAUNCH, err);
-        a_src = a_perm;
-        a_ld = k;
-    }
-    if (flags & W4A16_FLAG_FORCE_SIMT)
-        return launch_status(launch_gemm_simt(p, a_src, a_ld, stream));
-
-    CUtensorMap ma, ms, mz;
-    err = encode_maps(pl, a_src, m, k, a_ld, scales, zeros, g, n, &ma, &ms, &mz);
-    if (err != cudaSuccess)
-        return status_of(STAGE_RESOURCE, err);
-    GemmConfig cfg{pl.grid, pl.smem_bytes, pl.a_tmem};
-    if (pl.mma)
-        return launch_status(launch_decode(p, ma, ms, mz, cfg, stream));
-    return launch_status(launch_gemm(p, ma, ms, mz, cfg, stream));
+    return w4::dense_gemm(a, lda, b_packed, c, ldc, scales, zeros, g_idx, perm, workspace,
+                          workspace_bytes, m, n, k, group_size, weight_type, flags, stream,
+                          w4::MAX_TOK);
 }
-
 int w4a16_gemm_grouped(const void *a, int lda, const int32_t *b_packed_stack, void *y, int ldy,
                        const void *scales_stack, const void *zeros_stack, const int32_t *ex_ids,
                        const int32_t *ex_off, const int32_t *ex_pairs, const int32_t *pair_tok,

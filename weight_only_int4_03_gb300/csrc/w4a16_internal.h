@@ -22,6 +22,8 @@ constexpr int A_SLOT_COLS = 32;      // tensor-memory columns per slot: 64 fp16 
 constexpr int A_SLOT_BYTES = TILE_N * KBLK * 2;
 constexpr int MAX_STAGES = 16;
 constexpr int MAX_TOK = 256;         // activation rows per tile = tcgen05 N upper bound
+constexpr int TALL_TILE_TOK = 224;   // tallest token tile chosen for M above one tile
+constexpr int TWO_BUF_TILE_TOK = 192; // tallest token tile with two accumulator buffers
 
 // Warp roles of the tcgen05 GEMM kernel.
 constexpr int NUM_THREADS = 512;
@@ -103,5 +105,15 @@ int decode_extra_smem(int nt_max);
 int decode_max_rows();
 int decode_ctas_per_sm();
 int decode_smem_limit(int *bytes);
+
+// The dense entry points with the tcgen05 kernel's token tile held to at most tile_cap rows (a
+// multiple of 16, TWO_BUF_TILE_TOK..MAX_TOK): w4a16_workspace_size / w4a16_gemm use MAX_TOK;
+// a caller with a fixed scratch may ask for shorter tiles, whose partial slots take less.
+size_t dense_workspace_size(int m, int n, int k, int group_size, unsigned flags, int num_sms,
+                            int tile_cap);
+int dense_gemm(const void *a, int lda, const int32_t *b_packed, void *c, int ldc,
+               const void *scales, const void *zeros, const int32_t *g_idx, const int32_t *perm,
+               void *workspace, size_t workspace_bytes, int m, int n, int k, int group_size,
+               int weight_type, unsigned flags, cudaStream_t stream, int tile_cap);
 
 } // namespace w4

@@ -15,6 +15,7 @@
 #include <mutex>
 
 #include "w4a16.h"
+#include "w4a16_internal.h"
 
 static __device__ __align__(256) unsigned char g_scratch[W4A16_NOALLOC_SCRATCH_BYTES];
 
@@ -62,7 +63,11 @@ extern "C" int w4a16_gemm_noalloc(const void *a, int lda, const int32_t *b_packe
         // Same answers as w4a16_gemm for an empty or invalid shape (no scratch needed).
         return w4a16_gemm(a, lda, b_packed, c, ldc, scales, zeros, g_idx, perm, nullptr, 0, m, n, k,
                           group_size, weight_type, flags, stream);
-    const size_t need = w4a16_workspace_size(m, n, k, group_size, flags, 0);
+    // The tallest token tiles (up to 256 rows) take more partial-slot room than the scratch
+    // holds; tiles of at most 192 rows -- two accumulator buffers, the kernel's former default
+    // -- fit for every shape, so only an act-order copy of A can push a call over.
+    const int tile_cap = w4::TWO_BUF_TILE_TOK;
+    const size_t need = w4::dense_workspace_size(m, n, k, group_size, flags, 0, tile_cap);
     if (need == 0)
         // Invalid sizes: let the full argument checks of w4a16_gemm name the problem.
         return w4a16_gemm(a, lda, b_packed, c, ldc, scales, zeros, g_idx, perm, nullptr, 0, m, n, k,
@@ -88,9 +93,9 @@ extern "C" int w4a16_gemm_noalloc(const void *a, int lda, const int32_t *b_packe
     if (err != cudaSuccess)
         return (6 << 16) | (err & 0xFFFF);
 
-    const int st = w4a16_gemm(a, lda, b_packed, c, ldc, scales, zeros, g_idx, perm, ws,
-                              (size_t)W4A16_NOALLOC_SCRATCH_BYTES, m, n, k, group_size, weight_type,
-                              flags, stream);
+    const int st = w4::dense_gemm(a, lda, b_packed, c, ldc, scales, zeros, g_idx, perm, ws,
+                                  (size_t)W4A16_NOALLOC_SCRATCH_BYTES, m, n, k, group_size,
+                                  weight_type, flags, stream, tile_cap);
     if (st != 0 || !status_out)
         return st;
     // Hand the call's device-side error bits to the caller (stream-ordered, no host wait).
