@@ -136,6 +136,15 @@ int decode_rows_default()
     return v;
 }
 
+// CTAs per SM that one small-M launch fills (W4A16_DECODE_GRID overrides, 1..2).  Each CTA is
+// sized for half an SM either way; a launch that fills one leaves the other free for the next
+// launch of the stream, whose CTAs then start their weight copies while this one drains.
+int decode_grid_per_sm()
+{
+    static int v = env_int("W4A16_DECODE_GRID", 1, decode_ctas_per_sm(), decode_ctas_per_sm());
+    return v;
+}
+
 // Token-tile height of the tcgen05 kernel (a multiple of 16, at most cap rows): one tile for
 // M <= cap; above that M is cut into ceil(M / 224) tiles of equal height rounded up to 16, but
 // never below 192 rows.  Prefill is bound by the dequantisation of each weight tile, which is
@@ -401,7 +410,7 @@ void dense_plan(Plan &pl, int m, int n, int k, unsigned flags, int num_sms, bool
     pl.nt_max = mma ? nt_mma : nt_tc;
     pl.m_tiles = (m + pl.nt_max - 1) / pl.nt_max;
     const long long units = (long long)pl.m_tiles * (n / TILE_N) * (k / KBLK);
-    const int ctas = mma ? num_sms * decode_ctas_per_sm() : num_sms;
+    const int ctas = mma ? num_sms * decode_grid_per_sm() : num_sms;
     pl.grid = aligned_grid(pl.m_tiles * (n / TILE_N), k / KBLK, ctas, &pl.split);
     // The workspace serves whichever kernel a call picks: counters for the smaller tile
     // height, partial slots for the larger CTA count x tile height.

@@ -15,10 +15,18 @@
 // holds rows 8p + 2j + {0,1}, p = 0..3, i.e. fragment registers a0 / a2 of step 0 (p = 0, 1)
 // and of step 1 (p = 2, 3); column c + 8 gives a1 / a3.
 //
-// Budget: the integer pipe is the limit, so the loop is kept to the dequantisation proper
-// (13 instructions per 8 codes, 5 of them integer), one shared load per word, one ldmatrix
-// per 32 rows and one MMA per word.  When a group covers whole blocks (group_size % 64 == 0)
-// a lane's scale and zero change only where a group ends, which a per-stage bit mask marks.
+// Budget: the loop is kept to the dequantisation proper, one shared load per word, one
+// ldmatrix per 32 rows and one MMA per word.  When a group covers whole blocks
+// (group_size % 64 == 0) a lane's scale and zero change only where a group ends, which a
+// per-stage bit mask marks, and the scale leaves the loop altogether: the MMAs of a group
+// take the exact integers (q - z) and accumulate sum_k (q - z) a in fp32, and at the group's
+// end that sum is multiplied by the column's scale and added to the output accumulator --
+// the same product regrouped, since the scale is constant along K within a group (on the
+// MMA's M side, one per accumulator row).  That leaves 9 instructions per 8 codes (an
+// integer shift, four and-or, four fp16 add/fma) instead of 13, and it drops a rounding:
+// (q - z) s is never rounded to fp16.  Groups smaller than a block, and tiles of more than
+// 16 tokens (whose accumulators leave no registers for a second set), keep the scale in the
+// dequantisation.
 //
 // CTA: one TMA producer warp (the producer of w4a16_common.cuh) and 8 compute warps; warp w
 // owns 16 weight columns of every 64-row block (16 columns x 64 rows = 4 words per lane).
@@ -68,6 +76,20 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
                  : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// Codes -> fp16 pairs (q - z) for one column (one zero for all 8 codes), exact: pair p of
+// word x sits at bits (4p, 16 + 4p).
+__device__ __forceinline__ void dequant_word_int(uint32_t x, __half2 zlo, __half2 zhi,
+                                                 uint32_t (&out)[4])
+{
+    const uint32_t magic = 0x64006400u;
+    const __half2 sixteenth = __halves2half2(__ushort_as_half(0x2C00), __ushort_as_half(0x2C00));
+    const uint32_t x8 = __umulhi(x, 1u << 24); // x >> 8, on the FMA pipe (the integer pipe is the busy one)
+    out[0] = h2_as_u32(__hsub2(u32_as_h2((x & 0x000F000Fu) | magic), zlo));
+    out[1] = h2_as_u32(__hfma2(u32_as_h2((x & 0x00F000F0u) | magic), sixteenth, zhi));
+    out[2] = h2_as_u32(__hsub2(u32_as_h2((x8 & 0x000F000Fu) | magic), zlo));
+    out[3] = h2_as_u32(__hfma2(u32_as_h2((x8 & 0x00F000F0u) | magic), sixteenth, zhi));
+}
+
 // Codes -> fp16 pairs (q - z) * s for one column (one scale and zero for all 8 codes): pair p
 // of word x sits at bits (4p, 16 + 4p).  (q - z) is exact; the product is rounded once.
 __device__ __forceinline__ void dequant_word_col(uint32_t x, __half2 zlo, __half2 zhi, __half2 s,
@@ -105,20 +127,28 @@ __device__ __forceinline__ ColGroup col_group(bool has_zp, const __half *ssm, co
 }
 
 // One 64-row block of a warp's 16 columns: per lane four code words (columns col0 and
-// col0 + 8, rows 0..31 and 32..63), dequantised into A fragments for four k steps, times the B
+// col0 + 8, rows 0..31 and 32..63), dequantised into A fragments for four k steps -- exact
+// (q - z) when the scale is applied per group (SCALED false), else (q - z) s -- times the B
 // fragments of every 8-token tile.  `w_addr` is the shared address of the lane's first word,
-// `act0` / `act1` of its ldmatrix rows for the two 32-row halves.  The halves accumulate
-// separately (two independent MMA chains) and are summed at the segment end.
-template <int NT>
+// `act0` / `act1` of its ldmatrix rows for the two 32-row halves, which accumulate into acc0 /
+// acc1 (two independent MMA chains when they differ).
+template <int NT, bool SCALED>
 __device__ __forceinline__ void block_mma(uint32_t w_addr, uint32_t act0, uint32_t act1,
                                           const ColGroup &c0, const ColGroup &c1,
                                           float (&acc0)[NT][4], float (&acc1)[NT][4])
 {
     uint32_t a0[4], a1[4], a2[4], a3[4];
-    dequant_word_col(lds32(w_addr), c0.zlo, c0.zhi, c0.s, a0);
-    dequant_word_col(lds32(w_addr + 128), c1.zlo, c1.zhi, c1.s, a1);
-    dequant_word_col(lds32(w_addr + 2048), c0.zlo, c0.zhi, c0.s, a2);
-    dequant_word_col(lds32(w_addr + 2048 + 128), c1.zlo, c1.zhi, c1.s, a3);
+    if (SCALED) {
+        dequant_word_col(lds32(w_addr), c0.zlo, c0.zhi, c0.s, a0);
+        dequant_word_col(lds32(w_addr + 128), c1.zlo, c1.zhi, c1.s, a1);
+        dequant_word_col(lds32(w_addr + 2048), c0.zlo, c0.zhi, c0.s, a2);
+        dequant_word_col(lds32(w_addr + 2048 + 128), c1.zlo, c1.zhi, c1.s, a3);
+    } else {
+        dequant_word_int(lds32(w_addr), c0.zlo, c0.zhi, a0);
+        dequant_word_int(lds32(w_addr + 128), c1.zlo, c1.zhi, a1);
+        dequant_word_int(lds32(w_addr + 2048), c0.zlo, c0.zhi, a2);
+        dequant_word_int(lds32(w_addr + 2048 + 128), c1.zlo, c1.zhi, a3);
+    }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
         uint32_t b[4], e[4];
@@ -129,6 +159,23 @@ __device__ __forceinline__ void block_mma(uint32_t w_addr, uint32_t act0, uint32
         mma_16816(acc0[nt], a0[2], a1[2], a0[3], a1[3], b[2], b[3]);
         mma_16816(acc1[nt], a2[2], a3[2], a2[3], a3[3], e[2], e[3]);
     }
+}
+
+// End of a group: acc += s (g0 + g1) per accumulator row (registers 0, 1: column col0, scale
+// s0; 2, 3: column col0 + 8, scale s1), and the group accumulators restart from zero.
+template <int NT>
+__device__ __forceinline__ void flush_group(float (&acc)[NT][4], float (&g0)[NT][4],
+                                            float (&g1)[NT][4], float s0, float s1)
+{
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float sc = i < 2 ? s0 : s1;
+            acc[nt][i] = fmaf(g1[nt][i], sc, fmaf(g0[nt][i], sc, acc[nt][i]));
+            g0[nt][i] = 0.f;
+            g1[nt][i] = 0.f;
+        }
 }
 
 constexpr int DEC_UNROLL = 4; // stages of exactly this many blocks take the unrolled path
@@ -170,17 +217,24 @@ __device__ void run_compute(const GemmParams &p, Sched sched, uint8_t *smem, Dec
     int tile, kb0, kb1;
     while (sched.next(tile, kb0, kb1)) {
         const TileInfo ti = tile_info(p, no_seg, tile);
-        // The two 32-row halves of a block feed separate accumulators when NT is small, so
-        // that two MMA chains run side by side; larger NT has enough independent chains.
-        float acc[NT][4], acc_h1[NT][4];
-        float(&acc1)[NT][4] = NT <= 2 ? acc_h1 : acc;
+        // acc: the output accumulators.  With DEFER (whole-block groups, NT <= 2) the block
+        // MMAs go into g0 / g1, the unscaled sums of the current group, one per 32-row half so
+        // that two MMA chains run side by side; taller tiles (enough independent chains, and
+        // no registers to spare for a second set) scale in the dequantisation and accumulate
+        // straight into acc.
+        constexpr bool DEFER = BLOCK_GROUPS && NT <= 2;
+        float acc[NT][4], g0_own[NT][4], g1_own[NT][4];
+        float(&g0)[NT][4] = DEFER ? g0_own : acc;
+        float(&g1)[NT][4] = DEFER ? g1_own : acc;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 acc[nt][i] = 0.f;
-                acc_h1[nt][i] = 0.f;
+                g0_own[nt][i] = 0.f;
+                g1_own[nt][i] = 0.f;
             }
+        float s0 = 0.f, s1 = 0.f; // the current group's scales of columns col0, col0 + 8
         int in_grp = BLOCK_GROUPS ? kb0 % gs_kb : 0; // blocks of the current group before kb
         for (int kb = kb0; kb < kb1; kb += p.kbs) {
             const int nkb = min(p.kbs, kb1 - kb);
@@ -207,27 +261,39 @@ __device__ void run_compute(const GemmParams &p, Sched sched, uint8_t *smem, Dec
                 int gidx = col0; // scale index of the current group (relative to the stage's)
                 ColGroup c0 = col_group(has_zp, ssm, zsm, gidx);
                 ColGroup c1 = col_group(has_zp, ssm, zsm, gidx + 8);
+                s0 = __low2float(c0.s);
+                s1 = __low2float(c1.s);
                 auto next_group = [&]() {
                     gidx += TILE_N;
                     c0 = col_group(has_zp, ssm, zsm, gidx);
                     c1 = col_group(has_zp, ssm, zsm, gidx + 8);
+                    s0 = __low2float(c0.s);
+                    s1 = __low2float(c1.s);
                 };
                 if (nkb == DEC_UNROLL) {
                     // Taller tiles keep more accumulators live: unroll less there.
                     constexpr int UNROLL = NT <= 2 ? DEC_UNROLL : 2;
 #pragma unroll UNROLL
                     for (int j = 0; j < DEC_UNROLL; ++j) {
-                        block_mma<NT>(w_addr + j * TILE_BYTES, act0 + j * p.act_kb_bytes,
-                                      act1 + j * p.act_kb_bytes, c0, c1, acc, acc1);
-                        if (j + 1 < DEC_UNROLL && (gend & (1u << j)))
-                            next_group();
+                        block_mma<NT, !DEFER>(w_addr + j * TILE_BYTES, act0 + j * p.act_kb_bytes,
+                                              act1 + j * p.act_kb_bytes, c0, c1, g0, g1);
+                        if (gend & (1u << j)) {
+                            if (DEFER)
+                                flush_group<NT>(acc, g0, g1, s0, s1);
+                            if (j + 1 < DEC_UNROLL)
+                                next_group();
+                        }
                     }
                 } else {
                     for (int j = 0; j < nkb; ++j) {
-                        block_mma<NT>(w_addr + j * TILE_BYTES, act0 + j * p.act_kb_bytes,
-                                      act1 + j * p.act_kb_bytes, c0, c1, acc, acc1);
-                        if (j + 1 < nkb && (gend & (1u << j)))
-                            next_group();
+                        block_mma<NT, !DEFER>(w_addr + j * TILE_BYTES, act0 + j * p.act_kb_bytes,
+                                              act1 + j * p.act_kb_bytes, c0, c1, g0, g1);
+                        if (gend & (1u << j)) {
+                            if (DEFER)
+                                flush_group<NT>(acc, g0, g1, s0, s1);
+                            if (j + 1 < nkb)
+                                next_group();
+                        }
                     }
                 }
             } else {
@@ -260,6 +326,10 @@ __device__ void run_compute(const GemmParams &p, Sched sched, uint8_t *smem, Dec
             ring.advance(p.stages);
         }
 
+        // A segment may end inside a group: add what it holds of that group.
+        if (DEFER)
+            flush_group<NT>(acc, g0, g1, s0, s1);
+
         // Segment end: fp16 C for a whole tile, else an fp32 partial and the split protocol.
         // (Nothing of the preceding kernel may still read C or this workspace.)
         pdl_wait();
@@ -272,7 +342,7 @@ __device__ void run_compute(const GemmParams &p, Sched sched, uint8_t *smem, Dec
             for (int i = 0; i < 4; ++i) {
                 const int row = nt * 8 + 2 * t + (i & 1);
                 const int col = col0 + 8 * (i >> 1);
-                const float v = NT <= 2 ? acc[nt][i] + acc_h1[nt][i] : acc[nt][i];
+                const float v = acc[nt][i];
                 if (row >= ti.rows)
                     continue;
                 if (whole)
