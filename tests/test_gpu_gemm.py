@@ -133,6 +133,18 @@ def test_small_m_kernel_group_sizes(w4, orc, gs, m):
     check(dp, orc)
 
 
+@pytest.mark.parametrize("gs", [-1, 2112])
+@pytest.mark.parametrize("m", [1, 16])
+def test_small_m_kernel_long_groups(w4, orc, gs, m):
+    """Groups of more than 32 blocks (one group over K = 4224, or two of 33 blocks): the group
+    end is found by count, not by the per-stage mask, and split segments of a block or two end
+    inside a group, so each adds its share of the group's scaled sum."""
+    dp = DeviceProblem(w4, make_problem(1150 + m + max(gs, 0), m, 4224, 512, group_size=gs),
+                       flags_extra=FLAG_FORCE_MMA)
+    dp.run()
+    check(dp, orc)
+
+
 @pytest.mark.parametrize("m", [1, 7, 16, 64])
 def test_small_m_kernel_zero_points(w4, orc, m):
     dp = DeviceProblem(w4, make_problem(1200 + m, m, 768, 512, weight_type=U4, sigma=0.5),
