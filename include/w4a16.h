@@ -52,14 +52,20 @@ extern "C" {
 #define W4A16_FLAG_A_SMEM (1u << 9)     /* stage dequantised weights in shared memory instead
                                            of tensor memory (diagnostics / comparison)       */
 #define W4A16_FLAG_FORCE_TC (1u << 10)  /* always use the tcgen05 kernel (diagnostics)      */
-#define W4A16_FLAG_FORCE_MMA (1u << 11) /* always use the small-M register-fragment kernel;
-                                           M above 64 is then rejected (unsupported-shape)   */
+#define W4A16_FLAG_FORCE_MMA (1u << 11) /* always use the small-M split-K register-fragment
+                                           kernel; M above 64 is then rejected
+                                           (unsupported-shape)                               */
 #define W4A16_FLAG_STATIC_WEIGHTS (1u << 12) /* b_packed, scales and zeros are not written by the
                                            work that precedes this call on its stream, so the
                                            kernel may start reading them before that work has
                                            finished (it still waits before reading A or
                                            writing C or the workspace).  Without the flag
                                            weights are only prefetched into L2 early.        */
+#define W4A16_FLAG_FORCE_SLICE (1u << 13) /* always use the small-M column-slice kernel (each
+                                           CTA owns 16-column slices over all of K, no
+                                           split-K); M above 16 or a group size that is not
+                                           -1 or a multiple of 64 is then rejected
+                                           (unsupported-shape)                               */
 
 /* Detail codes of stage-1/2 statuses. */
 #define W4A16_ARG_NULL 1        /* a required pointer is NULL                                  */

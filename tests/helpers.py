@@ -15,6 +15,7 @@ FLAG_FORCE_SIMT = 1 << 8
 FLAG_A_SMEM = 1 << 9
 FLAG_FORCE_TC = 1 << 10
 FLAG_FORCE_MMA = 1 << 11
+FLAG_FORCE_SLICE = 1 << 13
 FLAG_STATIC_WEIGHTS = 1 << 12
 
 RTOL = 1e-2

@@ -91,6 +91,12 @@ def gemm_status(w4, **kw):
     (dict(a=A + 2), 1, 2),
     (dict(c=C + 8), 1, 2),
     (dict(ws=WS + 16), 1, 2),                    # workspace not 256-byte aligned
+    (dict(flags=1 << 13 | 1 << 11), 1, 4),       # FORCE_SLICE with FORCE_MMA
+    (dict(flags=1 << 13 | 1 << 10), 1, 4),       # FORCE_SLICE with FORCE_TC
+    (dict(flags=1 << 11 | 1 << 8), 1, 4),        # FORCE_MMA with FORCE_SIMT
+    (dict(flags=1 << 13, m=17), 2, 3),           # column-slice kernel: M <= 16 only
+    (dict(flags=1 << 13, gs=32), 2, 3),          # ... and groups of whole 64-row blocks
+    (dict(flags=1 << 11, m=65), 2, 3),           # split-K small-M kernel: M <= 64 only
 ])
 def test_gemm_rejects_bad_arguments_on_host(w4, kw, stage, detail):
     st = gemm_status(w4, **kw)

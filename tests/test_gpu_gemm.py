@@ -4,7 +4,8 @@ import pytest
 
 import oracle
 import synth
-from helpers import (ATOL, FLAG_A_SMEM, FLAG_FORCE_MMA, FLAG_FORCE_SIMT, FLAG_FORCE_TC, FLAG_STATIC_WEIGHTS, RTOL, U4, U4B8, DeviceProblem, make_problem,
+from helpers import (ATOL, FLAG_A_SMEM, FLAG_FORCE_MMA, FLAG_FORCE_SIMT, FLAG_FORCE_SLICE, FLAG_FORCE_TC,
+                     FLAG_STATIC_WEIGHTS, RTOL, U4, U4B8, DeviceProblem, make_problem,
                      oracle_ref, repack_device, torch_dev, within_tol)
 
 pytestmark = pytest.mark.gpu
@@ -143,6 +144,61 @@ def test_small_m_kernel_long_groups(w4, orc, gs, m):
                        flags_extra=FLAG_FORCE_MMA)
     dp.run()
     check(dp, orc)
+
+
+# --- column-slice small-M kernel (16-column slices over all of K, no split-K) ----------------
+
+@pytest.mark.parametrize("m,k,n,gs,kw", [
+    (1, 1024, 256, 128, {}),                                  # 2 stages of 8 blocks, 16 slices
+    (3, 2048, 512, -1, {}),                                   # one group over K
+    (8, 4224, 512, 64, {}),                                   # 66 blocks: last stage has 2
+    (9, 1536, 256, 512, dict(weight_type=U4, sigma=0.5)),     # u4 zeros, one group per stage
+    (16, 4224, 768, 192, dict(weight_type=U4, sigma=0.5)),    # groups straddle stages
+    (16, 4096, 4096, 128, {}),                                # 256 slices: one per CTA
+    (5, 4096, 12288, 128, {}),                                # 768 slices: 3 per CTA
+])
+def test_slice_kernel(w4, orc, m, k, n, gs, kw):
+    dp = DeviceProblem(w4, make_problem(1500 + m + k % 997, m, k, n, group_size=gs, **kw),
+                       flags_extra=FLAG_FORCE_SLICE)
+    dp.run()
+    rows = None if m * n <= 16 * 4096 else [0, m - 1]
+    check(dp, orc, rows)
+
+
+@pytest.mark.parametrize("m,gs", [(1, 128), (16, 64)])
+def test_slice_kernel_act_order(w4, orc, m, gs):
+    dp = DeviceProblem(w4, make_problem(1600 + m, m, 2048, 512, group_size=gs, act_order=True),
+                       flags_extra=FLAG_FORCE_SLICE)
+    dp.run()
+    check(dp, orc)
+
+
+@pytest.mark.parametrize("m", [1, 16])
+def test_slice_kernel_repeatable_and_static_weights(w4, m):
+    """Fixed-order cross-warp sums: repeated calls are bit-identical, with or without the
+    static-weights flag (weights read before the preceding kernel finishes)."""
+    pb = make_problem(1700 + m, m, 4096, 4096)
+    dp = DeviceProblem(w4, pb, flags_extra=FLAG_FORCE_SLICE)
+    dp.run()
+    first = dp.c.cpu().numpy().copy()
+    ds = DeviceProblem(w4, pb, flags_extra=FLAG_FORCE_SLICE | FLAG_STATIC_WEIGHTS)
+    for _ in range(3):
+        dp.run()
+        ds.run()
+        assert np.array_equal(dp.c.cpu().numpy().view(np.uint16), first.view(np.uint16))
+        assert np.array_equal(ds.c.cpu().numpy().view(np.uint16), first.view(np.uint16))
+    assert dp.status() == 0 and ds.status() == 0
+
+
+def test_slice_kernel_is_the_default_for_decode_shapes(w4):
+    """M <= 16 with whole-block groups and at least one slice per SM goes to the column-slice
+    kernel by default: the same bits as forcing it."""
+    pb = make_problem(1800, 4, 4096, 4096)
+    d0 = DeviceProblem(w4, pb)
+    d1 = DeviceProblem(w4, pb, flags_extra=FLAG_FORCE_SLICE)
+    d0.run()
+    d1.run()
+    assert np.array_equal(d0.c.cpu().numpy().view(np.uint16), d1.c.cpu().numpy().view(np.uint16))
 
 
 @pytest.mark.parametrize("m", [1, 7, 16, 64])

@@ -25,6 +25,7 @@ W4A16_FLAG_FORCE_SIMT = 1 << 8
 W4A16_FLAG_A_SMEM = 1 << 9
 W4A16_FLAG_FORCE_TC = 1 << 10
 W4A16_FLAG_FORCE_MMA = 1 << 11
+W4A16_FLAG_FORCE_SLICE = 1 << 13
 W4A16_FLAG_STATIC_WEIGHTS = 1 << 12
 
 W4A16_DEV_TIMEOUT = 1

@@ -179,6 +179,16 @@ __device__ __forceinline__ void tensor_load_3d(void *dst, const CUtensorMap *map
 }
 
 // The same with an L2 cache policy.
+__device__ __forceinline__ void tensor_load_2d_hint(void *dst, const CUtensorMap *map, int x, int y,
+                                                    uint64_t *bar, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+        "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
 __device__ __forceinline__ void tensor_load_3d_hint(void *dst, const CUtensorMap *map, int x, int y,
                                                     int z, uint64_t *bar, uint64_t policy)
 {

@@ -54,8 +54,11 @@ struct Plan {
     int nt_max, m_tiles, tiles_bound, grid;
     int kbs, sg_box, act_kb_bytes, packed_off, scales_off, zeros_off;
     int stages, stage_bytes, acc_bufs, acc_col0, tmem_cols, smem_bytes, seg_off, epi_off, a_slots;
-    bool a_tmem, mma; // mma: the small-M register-fragment kernel instead of tcgen05
+    bool a_tmem, mma; // mma: a small-M register-fragment kernel instead of tcgen05
+    bool slice = false; // ... the column-slice one (no split-K)
+    int act_rows = 0;   // rows of one activation box (slice kernel: M; others: nt_max)
     int split = 0;    // tile-aligned split factor (0: stream-K)
+    int n_slices = 0, slice_per = 0;
     long long counters_off, partials_off, a_off, total;
 };
 
@@ -233,6 +236,33 @@ int plan_smem(Plan &pl, bool grouped, bool has_zp, int group_size, int g_rows)
     if (err != cudaSuccess)
         return err;
     const int extra = pl.mma ? decode_extra_smem(pl.nt_max) : gemm_extra_smem(pl.a_tmem, grouped);
+    if (pl.slice) {
+        // Column-slice stage: [activations kbs x M rows x 128 B | codes kbs x 512 B | scale
+        // rows x 16 columns | zero rows], kbs = 8 warps x slice_bpw(nt_max) blocks.  The
+        // activation box is exactly M rows (the token rows an 8-token MMA tile has beyond M read
+        // a zero row instead).  After the stages: two buffers for the cross-warp sum of a slice
+        // (8 warps x nt_max/8 x 4 x 32 fp32 each), then the 128-byte zero row.
+        const int kbs = SLICE_WARPS * slice_bpw(pl.nt_max);
+        pl.kbs = kbs;
+        pl.act_kb_bytes = pl.act_rows * 128;
+        const int sg = (kbs * KBLK + group_size - 1) / group_size + 1;
+        pl.sg_box = sg < g_rows ? sg : g_rows;
+        pl.packed_off = (int)round_up((long long)kbs * pl.act_kb_bytes, 1024);
+        pl.scales_off = pl.packed_off + kbs * SLICE_BLOCK_BYTES;
+        pl.zeros_off = pl.scales_off + (int)round_up((long long)pl.sg_box * SLICE_N * 2, 128);
+        const int end = has_zp ? pl.zeros_off + pl.sg_box * SLICE_N * 2 : pl.zeros_off;
+        pl.stage_bytes = (int)round_up(end, 1024);
+        const int red = 2 * SLICE_WARPS * (pl.nt_max / 8) * 4 * 32 * 4 + 128;
+        pl.stages = (limit - extra - red) / pl.stage_bytes;
+        if (pl.stages < 2)
+            return cudaErrorInvalidConfiguration;
+        if (pl.stages > MAX_STAGES)
+            pl.stages = MAX_STAGES;
+        pl.epi_off = pl.stages * pl.stage_bytes;
+        pl.seg_off = pl.epi_off;
+        pl.smem_bytes = pl.stages * pl.stage_bytes + red + extra;
+        return cudaSuccess;
+    }
     int kbs = stage_blocks_default();
     if (!pl.mma && kbs > pl.a_slots)
         kbs = pl.a_slots;
@@ -312,17 +342,38 @@ int encode_act_map(CUtensorMap *map, const void *base, int rows, int k, int ld, 
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-// Scale (or zero) rows [g_rows][n] fp16: boxes of 128 columns x sg_box group rows.
-int encode_group_map(CUtensorMap *map, const void *base, int g_rows, int n, int sg_box)
+// Scale (or zero) rows [g_rows][n] fp16: boxes of box_n columns (128, or 16 for the
+// column-slice kernel) x sg_box group rows.
+int encode_group_map(CUtensorMap *map, const void *base, int g_rows, int n, int sg_box,
+                     int box_n = TILE_N)
 {
     auto fn = encode_fn();
     if (!fn)
         return cudaErrorNotSupported;
     cuuint64_t dims[2] = {(cuuint64_t)n, (cuuint64_t)g_rows};
     cuuint64_t strides[1] = {(cuuint64_t)n * 2};
-    cuuint32_t box[2] = {TILE_N, (cuuint32_t)sg_box};
+    cuuint32_t box[2] = {(cuuint32_t)box_n, (cuuint32_t)sg_box};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// Packed tiles viewed as [tiles x K/64 x 2][512] int32 rows (a row is one 32-row half of a
+// 64-row block of a 128-column tile: 128 columns x 4 words): a box of 64 words x 2*kbs rows
+// brings the codes of one 16-column slice for kbs consecutive blocks, 256 bytes per row.
+int encode_slice_weight_map(CUtensorMap *map, const void *base, int n, int k, int kbs)
+{
+    auto fn = encode_fn();
+    if (!fn)
+        return cudaErrorNotSupported;
+    cuuint64_t dims[2] = {(cuuint64_t)(TILE_WORDS / 2),
+                          (cuuint64_t)(n / TILE_N) * (cuuint64_t)(k / KBLK) * 2};
+    cuuint64_t strides[1] = {(cuuint64_t)TILE_BYTES / 2};
+    cuuint32_t box[2] = {(cuuint32_t)(SLICE_N * 4), (cuuint32_t)(2 * kbs)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, const_cast<void *>(base), dims, strides,
                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
@@ -380,38 +431,85 @@ int aligned_grid(int tiles, int kblocks, int ctas, int *split)
     return ctas;
 }
 
-// Kernel choice of a dense call: 1 = small-M register-fragment kernel, 0 = tcgen05, or a
-// negative status when the flags conflict or force the small-M kernel beyond its rows.
-int choose_mma(int m, unsigned flags)
+// Whether the column-slice kernel is picked by default where it applies (W4A16_SLICE=0 turns
+// it off, for comparison).
+bool slice_default()
+{
+    static int v = env_int("W4A16_SLICE", 0, 1, 1);
+    return v != 0;
+}
+
+// Kernel flags of a dense call, checked before anything touches the device: 0, or the status
+// of flags that conflict or force a small-M kernel beyond what it takes.  The column-slice
+// kernel needs M <= 16 and groups of whole 64-row blocks (`gs` resolved: K for one group); the
+// split-K small-M kernel M <= 64.
+int check_kernel_flags(int m, int gs, unsigned flags)
 {
     const unsigned other = W4A16_FLAG_FORCE_TC | W4A16_FLAG_A_SMEM | W4A16_FLAG_FORCE_SIMT;
+    if (flags & W4A16_FLAG_FORCE_SLICE) {
+        if (flags & (other | W4A16_FLAG_FORCE_MMA))
+            return status_of(STAGE_ARG, W4A16_ARG_FLAGS);
+        if (m > SLICE_MAX_ROWS || gs % KBLK != 0)
+            return status_of(STAGE_UNSUPPORTED, W4A16_ARG_SHAPE);
+    }
     if (flags & W4A16_FLAG_FORCE_MMA) {
         if (flags & other)
-            return -status_of(STAGE_ARG, W4A16_ARG_FLAGS);
+            return status_of(STAGE_ARG, W4A16_ARG_FLAGS);
         if (m > decode_max_rows())
-            return -status_of(STAGE_UNSUPPORTED, W4A16_ARG_SHAPE);
-        return 1;
+            return status_of(STAGE_UNSUPPORTED, W4A16_ARG_SHAPE);
     }
-    if (flags & other)
+    return 0;
+}
+
+// Kernel of a dense call whose flags passed check_kernel_flags: 2 = column-slice small-M
+// kernel, 1 = split-K small-M register-fragment kernel, 0 = tcgen05.  By default the
+// column-slice kernel takes M <= 16 with whole-block groups when there is at least one
+// 16-column slice per SM (measured at 4096x4096: M=1 5.3 us against 8.1 split-K; at
+// 4096x12288: 11.9 against 13.5); the split-K one the rest up to 32 rows.
+int choose_kernel(int m, int n, int gs, unsigned flags, int num_sms)
+{
+    if (flags & W4A16_FLAG_FORCE_SLICE)
+        return 2;
+    if (flags & W4A16_FLAG_FORCE_MMA)
+        return 1;
+    if (flags & (W4A16_FLAG_FORCE_TC | W4A16_FLAG_A_SMEM | W4A16_FLAG_FORCE_SIMT))
         return 0;
+    // 9..16 tokens (two 8-token tiles, a shallower ring) only while each CTA gets one slice:
+    // at N=12288 (3 slices per CTA) the split-K kernel is 3 % faster there.
+    const int slices = n / SLICE_N;
+    const bool fits = m <= 8 || slices <= num_sms * decode_grid_per_sm();
+    if (m <= SLICE_MAX_ROWS && gs % KBLK == 0 && slice_default() && slices >= num_sms && fits)
+        return 2;
     return m <= decode_rows_default() ? 1 : 0;
 }
 
 // Dense plan.  The workspace is carved for the larger tile of the two kernels, so a size
 // query answers for whichever kernel the call then picks.
-void dense_plan(Plan &pl, int m, int n, int k, unsigned flags, int num_sms, bool mma, int tile_cap)
+void dense_plan(Plan &pl, int m, int n, int k, unsigned flags, int num_sms, int kernel,
+                int tile_cap)
 {
+    const bool mma = kernel != 0;
     pl.mma = mma;
+    pl.slice = kernel == 2;
     pl.a_tmem = (flags & W4A16_FLAG_A_SMEM) == 0;
     const bool mma_ok = m <= decode_max_rows();
     const int nt_tc = pick_nt(m, tile_cap);
-    const int nt_mma = mma_ok ? pick_nt_mma(m) : nt_tc;
+    const int nt_mma = mma_ok || pl.slice ? pick_nt_mma(m) : nt_tc;
     const int nt_small = nt_tc < nt_mma ? nt_tc : nt_mma;
     pl.nt_max = mma ? nt_mma : nt_tc;
     pl.m_tiles = (m + pl.nt_max - 1) / pl.nt_max;
     const long long units = (long long)pl.m_tiles * (n / TILE_N) * (k / KBLK);
     const int ctas = mma ? num_sms * decode_grid_per_sm() : num_sms;
     pl.grid = aligned_grid(pl.m_tiles * (n / TILE_N), k / KBLK, ctas, &pl.split);
+    pl.act_rows = pl.slice ? m : pl.nt_max;
+    if (pl.slice) {
+        // Consecutive slices per CTA, as evenly as the CTA slots allow (N=12288: 768 slices,
+        // 3 each on 256 CTAs); no split-K, so no partial slots or counters are used.
+        pl.n_slices = n / SLICE_N;
+        pl.slice_per = (pl.n_slices + ctas - 1) / ctas;
+        pl.grid = (pl.n_slices + pl.slice_per - 1) / pl.slice_per;
+        pl.split = 0;
+    }
     // The workspace serves whichever kernel a call picks: counters for the smaller tile
     // height, partial slots for the larger CTA count x tile height.
     pl.tiles_bound = ((m + nt_small - 1) / nt_small) * (n / TILE_N);
@@ -445,6 +543,7 @@ void grouped_plan(Plan &pl, int n_pairs, int n_active, int n, int k, unsigned fl
     pl.mma = false;
     pl.a_tmem = (flags & W4A16_FLAG_A_SMEM) == 0;
     pl.nt_max = pick_nt_grouped(n_pairs, n_active);
+    pl.act_rows = pl.nt_max;
     pl.m_tiles = 0;
     pl.tiles_bound = ((n_pairs + pl.nt_max - 1) / pl.nt_max + n_active) * (n / TILE_N);
     pl.grid = num_sms;
@@ -480,6 +579,8 @@ void fill_params(GemmParams &p, const Plan &pl, int m, int n, int k, int group_s
     p.epi_smem_off = pl.epi_off;
     p.static_weights = 0;
     p.split = pl.split;
+    p.n_slices = pl.n_slices;
+    p.slice_per = pl.slice_per;
 }
 
 // Tensor maps of one launch: activations (3-D, swizzled) and the scale / zero rows.  With no
@@ -488,12 +589,13 @@ int encode_maps(const Plan &pl, const void *act, int rows, int k, int ld, const 
                 const void *zeros, int g_rows, int n, CUtensorMap *ma, CUtensorMap *ms,
                 CUtensorMap *mz)
 {
-    int err = encode_act_map(ma, act, rows, k, ld, pl.nt_max, pl.kbs);
+    const int box_n = pl.slice ? SLICE_N : TILE_N;
+    int err = encode_act_map(ma, act, rows, k, ld, pl.act_rows, pl.kbs);
     if (err == cudaSuccess)
-        err = encode_group_map(ms, scales, g_rows, n, pl.sg_box);
+        err = encode_group_map(ms, scales, g_rows, n, pl.sg_box, box_n);
     if (err == cudaSuccess) {
         if (zeros)
-            err = encode_group_map(mz, zeros, g_rows, n, pl.sg_box);
+            err = encode_group_map(mz, zeros, g_rows, n, pl.sg_box, box_n);
         else
             *mz = *ms;
     }
@@ -512,7 +614,7 @@ size_t dense_workspace_size(int m, int n, int k, int group_size, unsigned flags,
     if (num_sms <= 0 && sm_count(&num_sms) != cudaSuccess)
         return 0;
     Plan pl;
-    dense_plan(pl, m > 0 ? m : 1, n, k, flags, num_sms, false, tile_cap);
+    dense_plan(pl, m > 0 ? m : 1, n, k, flags, num_sms, 0, tile_cap);
     return (size_t)pl.total;
 }
 
@@ -543,16 +645,18 @@ int dense_gemm(const void *a, int lda, const int32_t *b_packed, void *c, int ldc
     if ((flags & W4A16_FLAG_FORCE_SIMT) && m > (1 << 20))
         return status_of(STAGE_UNSUPPORTED, W4A16_ARG_SHAPE);
 
-    const int mma = choose_mma(m, flags);
-    if (mma < 0)
-        return -mma;
+    const int gs_resolved = group_size == -1 ? k : group_size;
+    st = check_kernel_flags(m, gs_resolved, flags);
+    if (st)
+        return st;
 
     int num_sms = 0;
     int err = sm_count(&num_sms);
     if (err != cudaSuccess)
         return status_of(STAGE_RESOURCE, err);
+    const int kernel = choose_kernel(m, n, gs_resolved, flags, num_sms);
     Plan pl;
-    dense_plan(pl, m, n, k, flags, num_sms, mma == 1, tile_cap);
+    dense_plan(pl, m, n, k, flags, num_sms, kernel, tile_cap);
     if (workspace_bytes < (size_t)pl.total)
         return status_of(STAGE_ARG, W4A16_ARG_WORKSPACE);
     const int g = num_groups(k, group_size);
@@ -600,6 +704,13 @@ int dense_gemm(const void *a, int lda, const int32_t *b_packed, void *c, int ldc
     if (err != cudaSuccess)
         return status_of(STAGE_RESOURCE, err);
     GemmConfig cfg{pl.grid, pl.smem_bytes, pl.a_tmem};
+    if (pl.slice) {
+        CUtensorMap mw;
+        err = encode_slice_weight_map(&mw, b_packed, n, k, pl.kbs);
+        if (err != cudaSuccess)
+            return status_of(STAGE_RESOURCE, err);
+        return launch_status(launch_slice(p, ma, mw, ms, mz, cfg, stream));
+    }
     if (pl.mma)
         return launch_status(launch_decode(p, ma, ms, mz, cfg, stream));
     return launch_status(launch_gemm(p, ma, ms, mz, cfg, stream));

@@ -132,7 +132,9 @@ __device__ __forceinline__ ColGroup col_group(bool has_zp, const __half *ssm, co
 // fragments of every 8-token tile.  `w_addr` is the shared address of the lane's first word,
 // `act0` / `act1` of its ldmatrix rows for the two 32-row halves, which accumulate into acc0 /
 // acc1 (two independent MMA chains when they differ).
-template <int NT, bool SCALED>
+// HALF: bytes from a block's first 32-row half to its second (2048 in a 128-column tile, 256
+// in a 16-column slice); column col + 8 is always 128 bytes on.
+template <int NT, bool SCALED, int HALF = 2048>
 __device__ __forceinline__ void block_mma(uint32_t w_addr, uint32_t act0, uint32_t act1,
                                           const ColGroup &c0, const ColGroup &c1,
                                           float (&acc0)[NT][4], float (&acc1)[NT][4])
@@ -141,13 +143,13 @@ __device__ __forceinline__ void block_mma(uint32_t w_addr, uint32_t act0, uint32
     if (SCALED) {
         dequant_word_col(lds32(w_addr), c0.zlo, c0.zhi, c0.s, a0);
         dequant_word_col(lds32(w_addr + 128), c1.zlo, c1.zhi, c1.s, a1);
-        dequant_word_col(lds32(w_addr + 2048), c0.zlo, c0.zhi, c0.s, a2);
-        dequant_word_col(lds32(w_addr + 2048 + 128), c1.zlo, c1.zhi, c1.s, a3);
+        dequant_word_col(lds32(w_addr + HALF), c0.zlo, c0.zhi, c0.s, a2);
+        dequant_word_col(lds32(w_addr + HALF + 128), c1.zlo, c1.zhi, c1.s, a3);
     } else {
         dequant_word_int(lds32(w_addr), c0.zlo, c0.zhi, a0);
         dequant_word_int(lds32(w_addr + 128), c1.zlo, c1.zhi, a1);
-        dequant_word_int(lds32(w_addr + 2048), c0.zlo, c0.zhi, a2);
-        dequant_word_int(lds32(w_addr + 2048 + 128), c1.zlo, c1.zhi, a3);
+        dequant_word_int(lds32(w_addr + HALF), c0.zlo, c0.zhi, a2);
+        dequant_word_int(lds32(w_addr + HALF + 128), c1.zlo, c1.zhi, a3);
     }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
@@ -429,6 +431,299 @@ __global__ void __launch_bounds__(DEC_THREADS, DEC_CTAS_PER_SM)
     __syncthreads();
 }
 
+// ---------------------------------------------------------------------------------------
+// Column-slice kernel (M <= 16, groups of whole blocks).  The kernel above splits K across
+// CTAs, and the split tiles cost every call a tail of two L2 round trips (partial stores, the
+// counter, the last contributor's reduction) that sits on the critical path of back-to-back
+// calls.  Here a work item is one 16-column slice over all of K: a CTA takes a run of
+// consecutive slices, its 8 compute warps take 4 consecutive blocks each (2 for 9..16 tokens)
+// of every stage, and the warps' fp32 sums of a slice meet in shared memory (fixed order, so
+// repeated calls are bit-identical) and are written as fp16 C.  No partials, counters or
+// workspace traffic.  The per-lane work is the same as block_mma above, on the slice's 16
+// columns; a stage's activation box is exactly M rows, so little shared memory goes to the
+// token rows an 8-token MMA tile has past M.
+// ---------------------------------------------------------------------------------------
+static_assert(DEC_WARPS == SLICE_WARPS, "slice reduction buffers are sized for 8 warps");
+
+// One stage's codes and scale (and zero) rows, arming its barrier for the whole stage
+// including the activation rows that follow separately.
+static __device__ __forceinline__ void slice_issue_weights(const GemmParams &p,
+                                                           const CUtensorMap *tmap_w,
+                                                           const CUtensorMap *tmap_s,
+                                                           const CUtensorMap *tmap_z, int slice,
+                                                           int kb0, uint8_t *st, uint64_t *full)
+{
+    const bool has_zp = p.zeros != nullptr;
+    const uint32_t sg_bytes = (uint32_t)p.sg_box * SLICE_N * 2;
+    mbar_arrive_expect_tx(full, (uint32_t)p.kbs * (uint32_t)p.act_kb_bytes +
+                                    (uint32_t)p.kbs * SLICE_BLOCK_BYTES +
+                                    sg_bytes * (has_zp ? 2u : 1u));
+    constexpr int SLICES_PER_TILE = TILE_N / SLICE_N;
+    const int tile = slice / SLICES_PER_TILE;
+    const int x = (slice % SLICES_PER_TILE) * SLICE_N * 4; // word offset inside a half row
+    const int row = (tile * p.kblocks + kb0) * 2;
+    tensor_load_2d_hint(st + p.packed_off, tmap_w, x, row, full, policy_evict_first());
+    const int g0 = (kb0 * KBLK) / p.group_size;
+    tensor_load_2d(st + p.scales_off, tmap_s, slice * SLICE_N, g0, full);
+    if (has_zp)
+        tensor_load_2d(st + p.zeros_off, tmap_z, slice * SLICE_N, g0, full);
+}
+
+static __device__ void slice_producer(const GemmParams &p, const CUtensorMap *tmap_a,
+                                      const CUtensorMap *tmap_w, const CUtensorMap *tmap_s,
+                                      const CUtensorMap *tmap_z, int s_begin, int s_end, int n_st,
+                                      uint8_t *smem, DecBars &bars, const WaitCtl &ctl, int pre)
+{
+    if (!p.static_weights)
+        pdl_wait();
+    Ring ring;
+    int issued = 0;
+    bool ok = true;
+    for (int sl = s_begin; ok && sl < s_end; ++sl) {
+        for (int st = 0; st < n_st; ++st) {
+            uint64_t *full = &bars.full[ring.idx];
+            uint8_t *stp = smem + (size_t)ring.idx * p.stage_bytes;
+            if (issued >= pre) {
+                if (!mbar_wait(&bars.empty[ring.idx], ring.phase ^ 1u, ctl, W4A16_DEV_TIMEOUT)) {
+                    ok = false;
+                    break;
+                }
+                slice_issue_weights(p, tmap_w, tmap_s, tmap_z, sl, st * p.kbs, stp, full);
+            }
+            if (issued == 0 && p.static_weights)
+                pdl_wait();
+            // The M rows of A for the stage's blocks; blocks past K read zeros.
+            tensor_load_3d_hint(stp, tmap_a, 0, 0, st * p.kbs, full, policy_evict_last());
+            ring.advance(p.stages);
+            ++issued;
+        }
+    }
+    // Leave no copy in flight: wait (bounded, ignoring the abort flag) for the last stages.
+    WaitCtl drain_ctl = ctl;
+    volatile int no_abort = 0;
+    drain_ctl.abort_flag = &no_abort;
+    const int n = issued < p.stages ? issued : p.stages;
+    for (int i = 0; i < n; ++i) {
+        int idx = ring.idx - 1 - i;
+        uint32_t ph = ring.phase;
+        if (idx < 0) {
+            idx += p.stages;
+            ph ^= 1u;
+        }
+        mbar_wait(&bars.full[idx], ph, drain_ctl, W4A16_DEV_TIMEOUT);
+    }
+}
+
+// One 64-row block of the lane's two slice columns (c and c + 8) against NT 8-token tiles:
+// `w_addr` is the lane's first code word, act0[nt] / act1[nt] its ldmatrix row addresses for
+// the block's two 32-row halves.
+template <int NT>
+__device__ __forceinline__ void slice_block_mma(uint32_t w_addr, const uint32_t (&act0)[NT],
+                                                const uint32_t (&act1)[NT], const ColGroup &c0,
+                                                const ColGroup &c1, float (&acc0)[NT][4],
+                                                float (&acc1)[NT][4])
+{
+    constexpr uint32_t HALF = SLICE_N * 4 * 4; // 256 bytes: one 32-row half of the slice
+    uint32_t a0[4], a1[4], a2[4], a3[4];
+    dequant_word_col(lds32(w_addr), c0.zlo, c0.zhi, c0.s, a0);
+    dequant_word_col(lds32(w_addr + 128), c1.zlo, c1.zhi, c1.s, a1);
+    dequant_word_col(lds32(w_addr + HALF), c0.zlo, c0.zhi, c0.s, a2);
+    dequant_word_col(lds32(w_addr + HALF + 128), c1.zlo, c1.zhi, c1.s, a3);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        uint32_t b[4], e[4];
+        ldmatrix_x4(act0[nt], b);
+        ldmatrix_x4(act1[nt], e);
+        mma_16816(acc0[nt], a0[0], a1[0], a0[1], a1[1], b[0], b[1]);
+        mma_16816(acc1[nt], a2[0], a3[0], a2[1], a3[1], e[0], e[1]);
+        mma_16816(acc0[nt], a0[2], a1[2], a0[3], a1[3], b[2], b[3]);
+        mma_16816(acc1[nt], a2[2], a3[2], a2[3], a3[3], e[2], e[3]);
+    }
+}
+
+// Compute warp w of the column-slice kernel: blocks w*BPW .. w*BPW + BPW - 1 of every stage.
+// A stage's activations are kbs blocks x M rows of 128 bytes in the 128-byte swizzle (16-byte
+// chunk c of row j at j*128 + ((c ^ (j & 7)) << 4) from the 1024-aligned stage start); the
+// lanes of a token row at or past M point ldmatrix at the zero row instead.
+template <int NT>
+__device__ void slice_compute(const GemmParams &p, uint8_t *smem, DecBars &bars,
+                              const WaitCtl &ctl, int w, int lane, int s_begin, int s_end,
+                              int n_st)
+{
+    constexpr int BPW = slice_bpw(8 * NT);
+    constexpr int KBS = SLICE_WARPS * BPW;
+    const bool has_zp = p.zeros != nullptr;
+    const int t = lane & 3;
+    const int c = lane >> 2; // this lane's slice columns: c and c + 8
+    // Word of column c, half 0, of block bl: row 2*bl of 16 columns x 4 words.
+    const uint32_t w_lane = (uint32_t)((c * 4 + t) * 4);
+    constexpr int VALS = NT * 4 * 32; // one warp's accumulators
+    float *red = reinterpret_cast<float *>(smem + p.epi_smem_off);
+    const uint32_t zero_row = smem_u32(smem + p.epi_smem_off + 2 * SLICE_WARPS * VALS * 4);
+    const int m = p.m;
+    // ldmatrix row offsets (from the stage start) of this lane for block j of the warp's run,
+    // token tile nt and the block's two 32-row halves; valid bit (j, nt) clear: token row >= M.
+    uint32_t act_off0[BPW][NT], act_off1[BPW][NT];
+    uint32_t valid = 0;
+#pragma unroll
+    for (int j = 0; j < BPW; ++j)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int tok = nt * 8 + (lane & 7);
+            const int row = (w * BPW + j) * m + tok;
+            const uint32_t ch = (uint32_t)(lane >> 3);
+            const uint32_t sw = (uint32_t)(row & 7);
+            act_off0[j][nt] = (uint32_t)row * 128u + ((ch ^ sw) << 4);
+            act_off1[j][nt] = (uint32_t)row * 128u + (((4u + ch) ^ sw) << 4);
+            if (tok < m)
+                valid |= 1u << (j * NT + nt);
+        }
+    // Group of block kb relative to the stage's first group: a shift when the blocks per group
+    // are a power of two.
+    const int gs_kb = p.group_size / KBLK;
+    const int gsh = group_shift(gs_kb);
+    Ring ring;
+    uint32_t nsync = 0;
+    bool dep_done = false;
+    for (int sl = s_begin; sl < s_end; ++sl) {
+        float acc0[NT][4], acc1[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                acc0[nt][i] = 0.f;
+                acc1[nt][i] = 0.f;
+            }
+        for (int st = 0; st < n_st; ++st) {
+            if (!mbar_wait(&bars.full[ring.idx], ring.phase, ctl, W4A16_DEV_TIMEOUT))
+                return;
+            const uint8_t *stp = smem + (size_t)ring.idx * p.stage_bytes;
+            const uint32_t act_base = smem_u32(stp);
+            const uint32_t w_base = smem_u32(stp + p.packed_off) + w_lane;
+            const __half *ssm = reinterpret_cast<const __half *>(stp + p.scales_off);
+            const __half *zsm = reinterpret_cast<const __half *>(stp + p.zeros_off);
+            const int kb0 = st * KBS;
+            const int g_stage = gsh >= 0 ? kb0 >> gsh : kb0 / gs_kb;
+#pragma unroll
+            for (int j = 0; j < BPW; ++j) {
+                const int bl = w * BPW + j;
+                const int kb = kb0 + bl;
+                if (kb < p.kblocks) {
+                    const int g = (gsh >= 0 ? kb >> gsh : kb / gs_kb) - g_stage;
+                    const ColGroup c0 = col_group(has_zp, ssm, zsm, g * SLICE_N + c);
+                    const ColGroup c1 = col_group(has_zp, ssm, zsm, g * SLICE_N + c + 8);
+                    uint32_t act0[NT], act1[NT];
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        const bool ok = (valid >> (j * NT + nt)) & 1u;
+                        act0[nt] = ok ? act_base + act_off0[j][nt] : zero_row;
+                        act1[nt] = ok ? act_base + act_off1[j][nt] : zero_row;
+                    }
+                    slice_block_mma<NT>(w_base + (uint32_t)(bl * 2 * SLICE_N * 4 * 4), act0, act1,
+                                        c0, c1, acc0, acc1);
+                }
+            }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&bars.empty[ring.idx]);
+            ring.advance(p.stages);
+        }
+        // The warp's sums into this slice's buffer (two buffers alternate: a warp can be one
+        // slice ahead of the slowest reader, never two, since the rendezvous below needs all).
+        float *buf = red + ((sl - s_begin) & 1) * (SLICE_WARPS * VALS);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                buf[(w * NT * 4 + nt * 4 + i) * 32 + lane] = acc0[nt][i] + acc1[nt][i];
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(&bars.epi);
+        if (!mbar_wait(&bars.epi, nsync & 1u, ctl, W4A16_DEV_TIMEOUT))
+            return;
+        ++nsync;
+        if (!dep_done) {
+            pdl_wait(); // nothing of the preceding kernel may still read C
+            dep_done = true;
+        }
+        // Thread `id` sums value (register reg, lane ln) over the 8 warps in a fixed order.
+        const int id = w * 32 + lane;
+        if (id < VALS) {
+            const int reg = id >> 5, ln = id & 31;
+            float v = 0.f;
+#pragma unroll
+            for (int q = 0; q < SLICE_WARPS; ++q)
+                v += buf[(q * NT * 4 + reg) * 32 + ln];
+            const int nt = reg >> 2, i = reg & 3;
+            const int row = nt * 8 + 2 * (ln & 3) + (i & 1);
+            const int col = sl * SLICE_N + (ln >> 2) + 8 * (i >> 1);
+            if (row < m)
+                p.c[(long long)row * p.ldc + col] = __float2half_rn(v);
+        }
+    }
+}
+
+template <int NT>
+__global__ void __launch_bounds__(DEC_THREADS, DEC_CTAS_PER_SM)
+    w4a16_slice_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap tmap_a,
+                       const __grid_constant__ CUtensorMap tmap_w,
+                       const __grid_constant__ CUtensorMap tmap_s,
+                       const __grid_constant__ CUtensorMap tmap_z)
+{
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ DecBars bars;
+    __shared__ volatile int abort_sh;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    const int s_begin = blockIdx.x * p.slice_per;
+    const int s_end = min(s_begin + p.slice_per, p.n_slices);
+    const int n_st = (p.kblocks + p.kbs - 1) / p.kbs; // stages per slice
+
+    int pre = 0; // stages whose weight part went out before the dependency wait (thread 0)
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < p.stages; ++s) {
+            mbar_init(&bars.full[s], 1);
+            mbar_init(&bars.empty[s], DEC_WARPS);
+        }
+        mbar_init(&bars.epi, DEC_WARPS);
+        fence_mbar_init();
+        abort_sh = 0;
+        prefetch_tensormap(&tmap_a);
+        prefetch_tensormap(&tmap_w);
+        prefetch_tensormap(&tmap_s);
+        if (p.zeros != nullptr)
+            prefetch_tensormap(&tmap_z);
+        pdl_launch_dependents();
+        if (p.static_weights) {
+            const int total = (s_end - s_begin) * n_st;
+            for (; pre < p.stages && pre < total; ++pre)
+                slice_issue_weights(p, &tmap_w, &tmap_s, &tmap_z, s_begin + pre / n_st,
+                                    (pre % n_st) * p.kbs, smem + (size_t)pre * p.stage_bytes,
+                                    &bars.full[pre]);
+        }
+    }
+    // The zero row that ldmatrix reads for token rows past M.
+    if (warp == 1)
+        reinterpret_cast<uint32_t *>(smem + p.epi_smem_off + 2 * SLICE_WARPS * NT * 4 * 32 * 4)[lane] = 0u;
+    // As in the kernel above: no dependency wait before the set-up; the producer waits before
+    // its first activation copy (without static weights, before any copy), the compute warps
+    // before their first write of C.
+    __syncthreads();
+    WaitCtl ctl{&abort_sh, p.status, p.limit_ns};
+    if (warp == 0) {
+        if (lane == 0)
+            slice_producer(p, &tmap_a, &tmap_w, &tmap_s, &tmap_z, s_begin, s_end, n_st, smem, bars,
+                           ctl, pre);
+    } else {
+        slice_compute<NT>(p, smem, bars, ctl, warp - 1, lane, s_begin, s_end, n_st);
+    }
+    __syncwarp();
+    __syncthreads();
+}
+
 int decode_max_rows()
 {
     return 64;
@@ -456,12 +751,16 @@ int decode_smem_limit(int *bytes)
         err = cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
     if (err == cudaSuccess)
         err = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
-    cudaFuncAttributes fa;
+    cudaFuncAttributes fa, fs;
     if (err == cudaSuccess)
         err = cudaFuncGetAttributes(&fa, w4a16_decode_kernel<1, true>);
+    if (err == cudaSuccess)
+        err = cudaFuncGetAttributes(&fs, w4a16_slice_kernel<1>);
     if (err != cudaSuccess)
         return err;
-    *bytes = per_sm / DEC_CTAS_PER_SM - reserved - (int)fa.sharedSizeBytes - 256;
+    const int stat = (int)(fa.sharedSizeBytes > fs.sharedSizeBytes ? fa.sharedSizeBytes
+                                                                     : fs.sharedSizeBytes);
+    *bytes = per_sm / DEC_CTAS_PER_SM - reserved - stat - 256;
     return cudaSuccess;
 }
 
@@ -505,6 +804,44 @@ int launch_decode(const GemmParams &p, const CUtensorMap &tmap_a, const CUtensor
     lc.attrs = attr;
     lc.numAttrs = 1;
     return cudaLaunchKernelEx(&lc, kernel, p, tmap_a, tmap_s, tmap_z);
+}
+
+int launch_slice(const GemmParams &p, const CUtensorMap &tmap_a, const CUtensorMap &tmap_w,
+                 const CUtensorMap &tmap_s, const CUtensorMap &tmap_z, const GemmConfig &cfg,
+                 cudaStream_t stream)
+{
+    static int attr_done[2][64];
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess)
+        return err;
+    int v;
+    switch (p.nt_max) {
+    case 8: v = 0; break;
+    case 16: v = 1; break;
+    default: return cudaErrorInvalidValue;
+    }
+    void (*kernels[2])(GemmParams, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap) = {
+        w4a16_slice_kernel<1>, w4a16_slice_kernel<2>};
+    auto kernel = kernels[v];
+    if (dev < 64 && attr_done[v][dev] < cfg.smem_bytes) {
+        err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   cfg.smem_bytes);
+        if (err != cudaSuccess)
+            return err;
+        attr_done[v][dev] = cfg.smem_bytes;
+    }
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(cfg.grid);
+    lc.blockDim = dim3(DEC_THREADS);
+    lc.dynamicSmemBytes = cfg.smem_bytes;
+    lc.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    return cudaLaunchKernelEx(&lc, kernel, p, tmap_a, tmap_w, tmap_s, tmap_z);
 }
 
 } // namespace w4

@@ -39,6 +39,14 @@ constexpr int EPI_STAGE_BYTES = 4 * EPI_ROWS * 32 * 2;     // per warp: 32 rows 
 
 constexpr int MAX_SEGMENTS = 1024;
 
+// Column-slice small-M kernel: 16 weight columns over all of K per work item; a pipeline
+// stage holds slice_bpw consecutive blocks for each of the 8 compute warps.
+constexpr int SLICE_N = 16;
+__host__ __device__ constexpr int slice_bpw(int nt_max) { return nt_max <= 8 ? 4 : 2; }
+constexpr int SLICE_BLOCK_BYTES = SLICE_N * KBLK / 2; // codes of one block of a slice
+constexpr int SLICE_MAX_ROWS = 16;
+constexpr int SLICE_WARPS = 8; // compute warps of the small-M kernels
+
 struct GemmParams {
     const int32_t *b;         // packed tiles (expert 0)
     const __half *scales;     // [G][N] (expert 0)
@@ -67,6 +75,7 @@ struct GemmParams {
     int static_weights;       // weights may be read before the preceding kernel completes
     int split;                // > 0: tile-aligned split schedule (grid = tiles * split)
     int m_outer;              // dense: tile index runs token-tile-major
+    int n_slices, slice_per;  // column-slice kernel: N / 16 slices, consecutive slices per CTA
     // grouped schedule (null ex_off = dense)
     const int *ex_off;
     const int *ex_ids;
@@ -87,6 +96,9 @@ int launch_gemm(const GemmParams &p, const CUtensorMap &tmap_a, const CUtensorMa
                 const CUtensorMap &tmap_z, const GemmConfig &cfg, cudaStream_t stream);
 int launch_decode(const GemmParams &p, const CUtensorMap &tmap_a, const CUtensorMap &tmap_s,
                   const CUtensorMap &tmap_z, const GemmConfig &cfg, cudaStream_t stream);
+int launch_slice(const GemmParams &p, const CUtensorMap &tmap_a, const CUtensorMap &tmap_w,
+                 const CUtensorMap &tmap_s, const CUtensorMap &tmap_z, const GemmConfig &cfg,
+                 cudaStream_t stream);
 int launch_gemm_simt(const GemmParams &p, const __half *a, int lda, cudaStream_t stream);
 int launch_repack(const int32_t *qweight, const int32_t *perm, int32_t *out, int32_t *status, int k,
                   int n, cudaStream_t stream);
