@@ -604,24 +604,34 @@ __device__ void slice_compute(const GemmParams &p, uint8_t *smem, DecBars &bars,
             const __half *zsm = reinterpret_cast<const __half *>(stp + p.zeros_off);
             const int kb0 = st * KBS;
             const int g_stage = gsh >= 0 ? kb0 >> gsh : kb0 / gs_kb;
-#pragma unroll
-            for (int j = 0; j < BPW; ++j) {
+            auto block = [&](int j) {
                 const int bl = w * BPW + j;
                 const int kb = kb0 + bl;
-                if (kb < p.kblocks) {
-                    const int g = (gsh >= 0 ? kb >> gsh : kb / gs_kb) - g_stage;
-                    const ColGroup c0 = col_group(has_zp, ssm, zsm, g * SLICE_N + c);
-                    const ColGroup c1 = col_group(has_zp, ssm, zsm, g * SLICE_N + c + 8);
-                    uint32_t act0[NT], act1[NT];
+                const int g = (gsh >= 0 ? kb >> gsh : kb / gs_kb) - g_stage;
+                const ColGroup c0 = col_group(has_zp, ssm, zsm, g * SLICE_N + c);
+                const ColGroup c1 = col_group(has_zp, ssm, zsm, g * SLICE_N + c + 8);
+                uint32_t act0[NT], act1[NT];
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        const bool ok = (valid >> (j * NT + nt)) & 1u;
-                        act0[nt] = ok ? act_base + act_off0[j][nt] : zero_row;
-                        act1[nt] = ok ? act_base + act_off1[j][nt] : zero_row;
-                    }
-                    slice_block_mma<NT>(w_base + (uint32_t)(bl * 2 * SLICE_N * 4 * 4), act0, act1,
-                                        c0, c1, acc0, acc1);
+                for (int nt = 0; nt < NT; ++nt) {
+                    const bool ok = (valid >> (j * NT + nt)) & 1u;
+                    act0[nt] = ok ? act_base + act_off0[j][nt] : zero_row;
+                    act1[nt] = ok ? act_base + act_off1[j][nt] : zero_row;
                 }
+                slice_block_mma<NT>(w_base + (uint32_t)(bl * 2 * SLICE_N * 4 * 4), act0, act1, c0,
+                                    c1, acc0, acc1);
+            };
+            if (kb0 + KBS <= p.kblocks) {
+                // A full stage: no per-block bound in the unrolled loop.
+#pragma unroll
+                for (int j = 0; j < BPW; ++j)
+                    block(j);
+            } else {
+                // The last, partial stage of a slice: blocks past K are skipped (their scale
+                // rows were never loaded).
+#pragma unroll
+                for (int j = 0; j < BPW; ++j)
+                    if (kb0 + w * BPW + j < p.kblocks)
+                        block(j);
             }
             __syncwarp();
             if (lane == 0)
