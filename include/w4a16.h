@@ -63,7 +63,7 @@ extern "C" {
                                            weights are only prefetched into L2 early.        */
 #define W4A16_FLAG_FORCE_SLICE (1u << 13) /* always use the small-M column-slice kernel (each
                                            CTA owns 16-column slices over all of K, no
-                                           split-K); M above 16 or a group size that is not
+                                           split-K); M above 32 or a group size that is not
                                            -1 or a multiple of 64 is then rejected
                                            (unsupported-shape)                               */
 

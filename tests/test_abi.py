@@ -94,7 +94,7 @@ def gemm_status(w4, **kw):
     (dict(flags=1 << 13 | 1 << 11), 1, 4),       # FORCE_SLICE with FORCE_MMA
     (dict(flags=1 << 13 | 1 << 10), 1, 4),       # FORCE_SLICE with FORCE_TC
     (dict(flags=1 << 11 | 1 << 8), 1, 4),        # FORCE_MMA with FORCE_SIMT
-    (dict(flags=1 << 13, m=17), 2, 3),           # column-slice kernel: M <= 16 only
+    (dict(flags=1 << 13, m=33), 2, 3),           # column-slice kernel: M <= 32 only
     (dict(flags=1 << 13, gs=32), 2, 3),          # ... and groups of whole 64-row blocks
     (dict(flags=1 << 11, m=65), 2, 3),           # split-K small-M kernel: M <= 64 only
 ])

@@ -156,12 +156,15 @@ def test_small_m_kernel_long_groups(w4, orc, gs, m):
     (16, 4224, 768, 192, dict(weight_type=U4, sigma=0.5)),    # groups straddle stages
     (16, 4096, 4096, 128, {}),                                # 256 slices: one per CTA
     (5, 4096, 12288, 128, {}),                                # 768 slices: 3 per CTA
+    (24, 4224, 768, 192, dict(weight_type=U4, sigma=0.5)),    # four 8-token tiles, ragged
+    (32, 4096, 4096, 128, {}),                                # four full tiles, 256 slices
+    (17, 1024, 256, -1, {}),
 ])
 def test_slice_kernel(w4, orc, m, k, n, gs, kw):
     dp = DeviceProblem(w4, make_problem(1500 + m + k % 997, m, k, n, group_size=gs, **kw),
                        flags_extra=FLAG_FORCE_SLICE)
     dp.run()
-    rows = None if m * n <= 16 * 4096 else [0, m - 1]
+    rows = None if m * n <= 32 * 4096 else [0, m - 1]
     check(dp, orc, rows)
 
 

@@ -441,7 +441,7 @@ bool slice_default()
 
 // Kernel flags of a dense call, checked before anything touches the device: 0, or the status
 // of flags that conflict or force a small-M kernel beyond what it takes.  The column-slice
-// kernel needs M <= 16 and groups of whole 64-row blocks (`gs` resolved: K for one group); the
+// kernel needs M <= 32 and groups of whole 64-row blocks (`gs` resolved: K for one group); the
 // split-K small-M kernel M <= 64.
 int check_kernel_flags(int m, int gs, unsigned flags)
 {
@@ -463,7 +463,7 @@ int check_kernel_flags(int m, int gs, unsigned flags)
 
 // Kernel of a dense call whose flags passed check_kernel_flags: 2 = column-slice small-M
 // kernel, 1 = split-K small-M register-fragment kernel, 0 = tcgen05.  By default the
-// column-slice kernel takes M <= 16 with whole-block groups when there is at least one
+// column-slice kernel takes M <= 32 with whole-block groups when there is at least one
 // 16-column slice per SM (measured at 4096x4096: M=1 5.3 us against 8.1 split-K; at
 // 4096x12288: 11.9 against 13.5); the split-K one the rest up to 32 rows.
 int choose_kernel(int m, int n, int gs, unsigned flags, int num_sms)
@@ -474,8 +474,8 @@ int choose_kernel(int m, int n, int gs, unsigned flags, int num_sms)
         return 1;
     if (flags & (W4A16_FLAG_FORCE_TC | W4A16_FLAG_A_SMEM | W4A16_FLAG_FORCE_SIMT))
         return 0;
-    // 9..16 tokens (two 8-token tiles, a shallower ring) only while each CTA gets one slice:
-    // at N=12288 (3 slices per CTA) the split-K kernel is 3 % faster there.
+    // 9..32 tokens (two or four 8-token tiles, a shallower ring) only while each CTA gets one
+    // slice: at N=12288 (3 slices per CTA) the split-K kernel is faster at M=16.
     const int slices = n / SLICE_N;
     const bool fits = m <= 8 || slices <= num_sms * decode_grid_per_sm();
     if (m <= SLICE_MAX_ROWS && gs % KBLK == 0 && slice_default() && slices >= num_sms && fits)

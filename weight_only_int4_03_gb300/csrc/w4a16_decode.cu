@@ -432,12 +432,12 @@ __global__ void __launch_bounds__(DEC_THREADS, DEC_CTAS_PER_SM)
 }
 
 // ---------------------------------------------------------------------------------------
-// Column-slice kernel (M <= 16, groups of whole blocks).  The kernel above splits K across
+// Column-slice kernel (M <= 32, groups of whole blocks).  The kernel above splits K across
 // CTAs, and the split tiles cost every call a tail of two L2 round trips (partial stores, the
 // counter, the last contributor's reduction) that sits on the critical path of back-to-back
 // calls.  Here a work item is one 16-column slice over all of K: a CTA takes a run of
-// consecutive slices, its 8 compute warps take 4 consecutive blocks each (2 for 9..16 tokens)
-// of every stage, and the warps' fp32 sums of a slice meet in shared memory (fixed order, so
+// consecutive slices, its 8 compute warps take 4 consecutive blocks each (2 for 9..16 tokens,
+// 1 for 17..32) of every stage, and the warps' fp32 sums of a slice meet in shared memory (fixed order, so
 // repeated calls are bit-identical) and are written as fp16 C.  No partials, counters or
 // workspace traffic.  The per-lane work is the same as block_mma above, on the slice's 16
 // columns; a stage's activation box is exactly M rows, so little shared memory goes to the
@@ -656,9 +656,9 @@ __device__ void slice_compute(const GemmParams &p, uint8_t *smem, DecBars &bars,
             pdl_wait(); // nothing of the preceding kernel may still read C
             dep_done = true;
         }
-        // Thread `id` sums value (register reg, lane ln) over the 8 warps in a fixed order.
-        const int id = w * 32 + lane;
-        if (id < VALS) {
+        // Thread `id` sums values (register reg, lane ln) over the 8 warps in a fixed order;
+        // with four token tiles (512 values) each of the 256 threads takes two.
+        for (int id = w * 32 + lane; id < VALS; id += SLICE_WARPS * 32) {
             const int reg = id >> 5, ln = id & 31;
             float v = 0.f;
 #pragma unroll
@@ -820,7 +820,7 @@ int launch_slice(const GemmParams &p, const CUtensorMap &tmap_a, const CUtensorM
                  const CUtensorMap &tmap_s, const CUtensorMap &tmap_z, const GemmConfig &cfg,
                  cudaStream_t stream)
 {
-    static int attr_done[2][64];
+    static int attr_done[3][64];
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess)
@@ -829,10 +829,11 @@ int launch_slice(const GemmParams &p, const CUtensorMap &tmap_a, const CUtensorM
     switch (p.nt_max) {
     case 8: v = 0; break;
     case 16: v = 1; break;
+    case 32: v = 2; break;
     default: return cudaErrorInvalidValue;
     }
-    void (*kernels[2])(GemmParams, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap) = {
-        w4a16_slice_kernel<1>, w4a16_slice_kernel<2>};
+    void (*kernels[3])(GemmParams, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap) = {
+        w4a16_slice_kernel<1>, w4a16_slice_kernel<2>, w4a16_slice_kernel<4>};
     auto kernel = kernels[v];
     if (dev < 64 && attr_done[v][dev] < cfg.smem_bytes) {
         err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
