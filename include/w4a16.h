@@ -146,8 +146,13 @@ size_t w4a16_workspace_size(int m, int n, int k, int group_size, unsigned flags,
  *              (transformer.rs `marlin_num_groups`; marlin.rs Marlin-MoE validation)
  *   weight_type W4A16_TYPE_U4B8 (zeros NULL) or W4A16_TYPE_U4 (zeros and W4A16_FLAG_HAS_ZP)
  *   flags      W4A16_FLAG_*; ACT_ORDER exactly when g_idx and perm are given
+ * Kernel choice (unless a W4A16_FLAG_FORCE_* flag picks one): M <= 8 -- and M <= 32 while
+ * N / 16 <= 2 x the SM count -- with group_size -1 or a multiple of 64 and N / 16 >= the SM
+ * count runs the column-slice kernel (no split-K); the rest of M <= 32 the split-K
+ * register-fragment kernel; larger M the tcgen05 kernel.  All three give results within the
+ * same tolerance of the exact product; they round differently, so their bits may differ.
  * Results are deterministic: a fixed reduction order makes repeated calls on the same device
- * bit-identical. */
+ * with the same sizes and flags bit-identical. */
 int w4a16_gemm(const void *a, int lda, const int32_t *b_packed, void *c, int ldc,
                const void *scales, const void *zeros, const int32_t *g_idx, const int32_t *perm,
                void *workspace, size_t workspace_bytes, int m, int n, int k, int group_size,
