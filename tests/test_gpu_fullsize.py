@@ -38,8 +38,8 @@ def sample_rows(m: int):
 
 
 DENSE = [
-    ("decode", "1,4096,4096"), ("decode", "16,4096,4096"), ("decode", "32,4096,12288"),
-    ("decode", "64,4096,12288"), ("prefill", "256,4096,11008"), ("prefill", "4096,4096,11008"),
+    ("decode", "1,4096,4096"), ("decode", "16,4096,4096"), ("decode", "32,4096,4096"),
+    ("decode", "8,4096,12288"), ("decode", "32,4096,12288"), ("decode", "64,4096,12288"), ("prefill", "256,4096,11008"), ("prefill", "4096,4096,11008"),
     ("prefill", "4096,11008,4096"), ("actorder", "1,8192,28672"), ("actorder", "2048,8192,28672"),
 ]
 

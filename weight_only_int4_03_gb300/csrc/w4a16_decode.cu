@@ -1,5 +1,7 @@
-// w4a16_decode.cu -- the small-M W4A16 GEMM: weights dequantised in registers straight into
-// warp-level mma.sync (m16n8k16), for decode-sized M (up to 64 rows).
+// w4a16_decode.cu -- the small-M W4A16 GEMMs: weights dequantised in registers straight into
+// warp-level mma.sync (m16n8k16), for decode-sized M (up to 64 rows).  Two kernels share the
+// per-lane fragment work described here: the split-K kernel (w4a16_decode_kernel, below) and
+// the column-slice kernel (w4a16_slice_kernel, at the end of the file; no split-K).
 //
 // Why a second kernel: at small M the job is to stream the packed weights at HBM speed, which
 // leaves a budget of roughly 20 warp instructions per 32-bit word of codes.  The tcgen05
@@ -28,8 +30,9 @@
 // 16 tokens (whose accumulators leave no registers for a second set), keep the scale in the
 // dequantisation.
 //
-// CTA: one TMA producer warp (the producer of w4a16_common.cuh) and 8 compute warps; warp w
-// owns 16 weight columns of every 64-row block (16 columns x 64 rows = 4 words per lane).
+// Split-K kernel CTA: one TMA producer warp (the producer of w4a16_common.cuh) and 8 compute
+// warps; warp w owns 16 weight columns of every 64-row block (16 columns x 64 rows = 4 words
+// per lane).
 // Two CTAs share an SM, so one CTA's segment epilogue (partials, the split counter, the
 // reduction) overlaps the other's streaming.  Work is split over CTAs with the same
 // data-parallel + stream-K schedule as the tcgen05 kernel; split tiles are reduced in a fixed
