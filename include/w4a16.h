@@ -202,8 +202,9 @@ size_t w4a16_grouped_workspace_size(int n_pairs, int n_active, int n, int k, int
  *   ex_ids        device int32 [n_active];  ex_off device int32 [n_active+1];
  *   ex_pairs      device int32 [n_pairs];   pair_tok device int32 [n_pairs]
  *   n_active      1..W4A16_MAX_SEGMENTS; n_experts bounds ex_ids
- * Act-order is not supported here (W4A16_FLAG_ACT_ORDER is rejected).  Out-of-range schedule
- * entries are skipped and reported as W4A16_DEV_SCHEDULE. */
+ * Act-order is not supported here (W4A16_FLAG_ACT_ORDER is rejected), and every call runs the
+ * tcgen05 kernel (W4A16_FLAG_FORCE_SIMT, _FORCE_MMA and _FORCE_SLICE are rejected).
+ * Out-of-range schedule entries are skipped and reported as W4A16_DEV_SCHEDULE. */
 #define W4A16_MAX_SEGMENTS 1024
 int w4a16_gemm_grouped(const void *a, int lda, const int32_t *b_packed_stack, void *y, int ldy,
                        const void *scales_stack, const void *zeros_stack, const int32_t *ex_ids,

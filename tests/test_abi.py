@@ -136,6 +136,8 @@ def test_grouped_rejects_bad_arguments(w4):
     assert call(n_active=5) == (1 << 16 | 9)            # more active experts than experts
     assert call(n_active=2000, n_experts=4000) == (1 << 16 | 9)
     assert call(flags=1 << 1) == (1 << 16 | 4)          # act-order unsupported here
+    assert call(flags=1 << 11) == (1 << 16 | 4)         # small-M kernels: dense calls only
+    assert call(flags=1 << 13) == (1 << 16 | 4)
     assert call(ids=None) == (1 << 16 | 1)
     assert call(tok=0xC0002) == (1 << 16 | 2)
     assert call(k=320) == (2 << 16 | 3)

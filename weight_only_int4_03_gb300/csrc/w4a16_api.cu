@@ -821,7 +821,8 @@ int w4a16_gemm_grouped(const void *a, int lda, const int32_t *b_packed_stack, vo
                            flags);
     if (st)
         return st;
-    if (flags & (W4A16_FLAG_ACT_ORDER | W4A16_FLAG_FORCE_SIMT | W4A16_FLAG_FORCE_MMA))
+    if (flags & (W4A16_FLAG_ACT_ORDER | W4A16_FLAG_FORCE_SIMT | W4A16_FLAG_FORCE_MMA |
+                 W4A16_FLAG_FORCE_SLICE))
         return status_of(STAGE_ARG, W4A16_ARG_FLAGS);
     if (n_active <= 0 || n_active > W4A16_MAX_SEGMENTS || n_experts <= 0 || n_pairs <= 0 ||
         n_tokens <= 0 || n_active > n_experts)
