@@ -364,10 +364,12 @@ def test_empty_m_is_a_noop(w4):
     assert float(dp.c.float().min()) == 3.0
 
 
-def test_strided_a_and_c(w4, orc):
+@pytest.mark.parametrize("m,flag", [(45, 0), (5, FLAG_FORCE_SLICE), (12, FLAG_FORCE_MMA)])
+def test_strided_a_and_c(w4, orc, m, flag):
+    """lda > K and ldc > N through each kernel; the columns of C past N stay untouched."""
     import torch
-    pb = make_problem(801, 45, 512, 256)
-    dp = DeviceProblem(w4, pb)
+    pb = make_problem(801 + m, m, 512, 256)
+    dp = DeviceProblem(w4, pb, flags_extra=flag)
     lda, ldc = 512 + 24, 256 + 40
     a_big = torch.zeros((pb.m, lda), dtype=torch.float16, device="cuda")
     a_big[:, :512] = dp.a
