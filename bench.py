@@ -616,14 +616,14 @@ def _oracle_inputs(s, rows: int):
     return synth.activations(s["seed"], rows, k, sigma=s["sigma"]), qw, synth.scales(s["seed"], g, n), z
 
 
-def oracle_sample(workload: str, budget_s: float):
+def oracle_sample(workload: str, budget_s: float, threads: int | None = None):
     """Times the oracle on a bounded sample of one step of the workload: r output rows of every
     GEMM (r sized so the sample takes about `budget_s`), then extrapolates the step time
     linearly in the rows (the oracle's cost is linear in M).
     Returns (step_seconds_estimate, units_per_step, unit, threads, sample_text)."""
     import oracle
     orc = oracle.Oracle()
-    threads = oracle.default_threads()
+    threads = threads or oracle.default_threads()
     specs = workload_specs(workload)
 
     def row_seconds(s, r):
@@ -654,11 +654,74 @@ def oracle_sample(workload: str, budget_s: float):
     return est, units, unit, threads, text
 
 
+def _dequant_fp32(qw, scales, zeros, gs, wt):
+    """[K][N] fp32 weights (q - z) * s from GPTQ words (row 8r+i at bits 4i..4i+3), for the
+    BLAS baseline; z = 8 for u4b8."""
+    k8, n = qw.shape
+    q = np.empty((k8 * 8, n), dtype=np.float32)
+    w = qw.view(np.uint32)
+    for i in range(8):
+        q[i::8] = ((w >> np.uint32(4 * i)) & np.uint32(0xF)).astype(np.float32)
+    k = k8 * 8
+    g = np.arange(k) // (gs if gs > 0 else k)
+    s = scales.astype(np.float32)[g]
+    z = zeros.astype(np.float32)[g] if wt == U4 else np.float32(8.0)
+    q -= z
+    q *= s
+    return q
+
+
+def blas_sample(workload: str, repeats: int = 3):
+    """A CPU baseline that is not the oracle: each GEMM's weights dequantised once to fp32
+    (outside the timing), then numpy's fp32 GEMM (BLAS, the host's threads) on the GEMM's full
+    M, best of `repeats`.  For a grouped GEMM one expert's weights stand for every expert and
+    the time is scaled by the experts.  Returns (step_seconds, units_per_step, unit, text)."""
+    hbm = workload == "decode"
+    est = units = 0.0
+    for s in workload_specs(workload):
+        rows = s["n_tok"] * s["top_k"] if s.get("grouped") else s["m"]
+        per = rows // s["n_exp"] if s.get("grouped") else rows
+        a, qw, sc, z = _oracle_inputs(s, per)
+        w = _dequant_fp32(qw, sc, z, s["gs"], s["wt"])
+        a32 = a.astype(np.float32)
+        best = float("inf")
+        for _ in range(repeats):
+            t0 = time.perf_counter()
+            (a32 @ w).astype(np.float16)
+            best = min(best, time.perf_counter() - t0)
+        est += best * (s["n_exp"] if s.get("grouped") else 1)
+        if s.get("grouped"):
+            wb, _, f = grouped_accounting(s)
+        else:
+            wb, f = weight_bytes(s), gemm_flops(s)
+        units += wb if hbm else f
+        del w, a32
+    unit = "GB/s (weight stream)" if hbm else "TFLOP/s"
+    text = (f"all {len(workload_specs(workload))} GEMMs of one step at full M, weights dequantised "
+            f"once to fp32 outside the timing, numpy fp32 matmul (BLAS), best of {repeats}")
+    return est, units, unit, text
+
+
 def cpu_baseline(workload: str, budget_s: float = 15.0):
+    """The oracle on the host's threads (the reported baseline), plus, labelled separately, the
+    oracle on one thread and a BLAS fp32 GEMM on weights dequantised once.  The two extras are
+    best effort: a failure is recorded in the line, it does not end the run."""
     est, units, unit, threads, text = oracle_sample(workload, budget_s)
     scale = 1e9 if unit.startswith("GB") else 1e12
-    return {"value": round(units / est / scale, 6), "unit": unit, "cores": threads, "kind": "oracle",
+    line = {"value": round(units / est / scale, 6), "unit": unit, "cores": threads, "kind": "oracle",
             "sample": text}
+    try:
+        est1, units1, _, _, text1 = oracle_sample(workload, budget_s / 3, threads=1)
+        line["single_core"] = {"value": round(units1 / est1 / scale, 6), "cores": 1, "sample": text1}
+    except Exception as e:  # noqa: BLE001 -- a baseline must not end the benchmark
+        line["single_core"] = {"error": f"{type(e).__name__}: {e}"}
+    try:
+        est2, units2, _, text2 = blas_sample(workload)
+        line["fp32_blas"] = {"value": round(units2 / est2 / scale, 6), "cores": os.cpu_count(),
+                             "kind": "numpy fp32 GEMM on dequantised weights", "sample": text2}
+    except Exception as e:  # noqa: BLE001
+        line["fp32_blas"] = {"error": f"{type(e).__name__}: {e}"}
+    return line
 
 
 def run_reference(args, rank):
