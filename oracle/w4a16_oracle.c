@@ -159,7 +159,13 @@ void orc_matmul(const double *a, long lda, const double *w, int m, int k, int n,
  * The W4A16 GEMM.  [marlin.rs] `marlin_gemm` doc: C[m, n] = A[m, k] @ dequant(B[k, n]).
  * A is fp16 [M][lda], C is returned in double [M][N].  Columns are split across threads;
  * each output is one plain k-ordered sum of A[m][k] * W[k][n], with W from its definition.
+ * W does not depend on the row of A, so a thread writes out the W entries of a band of its
+ * columns once (every entry by `orc_weight`) and then forms the sums of every row of A over
+ * that band; each sum is the same k-ordered double sum of the same products as when W is
+ * re-derived for every row.
  * ------------------------------------------------------------------------------------- */
+#define ORC_BAND 256 /* columns of W held at a time by one thread */
+
 struct orc_gemm_job {
     const uint16_t *a; long lda; int m;
     const int32_t *qweight; const uint16_t *scales; const uint16_t *zeros; const int32_t *g_idx;
@@ -171,24 +177,32 @@ struct orc_gemm_job {
 static void *orc_gemm_worker(void *arg)
 {
     struct orc_gemm_job *jb = (struct orc_gemm_job *)arg;
-    int width = jb->col_end - jb->col_begin;
-    if (width <= 0)
+    if (jb->col_end <= jb->col_begin)
         return NULL;
-    double *acc = (double *)malloc(sizeof(double) * (size_t)width);
-    for (int i = 0; i < jb->m; ++i) {
-        for (int j = 0; j < width; ++j)
-            acc[j] = 0.0;
-        for (int row = 0; row < jb->k; ++row) {
-            double av = orc_half_to_double(jb->a[(long)i * jb->lda + row]);
+    double *w = (double *)malloc(sizeof(double) * (size_t)jb->k * ORC_BAND);
+    double *acc = (double *)malloc(sizeof(double) * ORC_BAND);
+    for (int c0 = jb->col_begin; c0 < jb->col_end; c0 += ORC_BAND) {
+        int width = jb->col_end - c0 < ORC_BAND ? jb->col_end - c0 : ORC_BAND;
+        for (int row = 0; row < jb->k; ++row)
             for (int j = 0; j < width; ++j)
-                acc[j] += av * orc_weight(jb->qweight, jb->scales, jb->zeros, jb->g_idx, jb->k,
-                                          jb->n, jb->group_size, jb->weight_type, row,
-                                          jb->col_begin + j);
+                w[(long)row * width + j] = orc_weight(jb->qweight, jb->scales, jb->zeros, jb->g_idx,
+                                                      jb->k, jb->n, jb->group_size,
+                                                      jb->weight_type, row, c0 + j);
+        for (int i = 0; i < jb->m; ++i) {
+            for (int j = 0; j < width; ++j)
+                acc[j] = 0.0;
+            for (int row = 0; row < jb->k; ++row) {
+                double av = orc_half_to_double(jb->a[(long)i * jb->lda + row]);
+                const double *wr = w + (long)row * width;
+                for (int j = 0; j < width; ++j)
+                    acc[j] += av * wr[j];
+            }
+            for (int j = 0; j < width; ++j)
+                jb->c[(long)i * jb->n + c0 + j] = acc[j];
         }
-        for (int j = 0; j < width; ++j)
-            jb->c[(long)i * jb->n + jb->col_begin + j] = acc[j];
     }
     free(acc);
+    free(w);
     return NULL;
 }
 
@@ -419,14 +433,27 @@ void orc_grouped(const uint16_t *a, long lda, const int32_t *qweight_stack,
     long scales_per_expert = (long)groups * n;
     for (int i = 0; i < n_active; ++i) {
         int e = ex_ids[i];
+        int rows = ex_off[i + 1] - ex_off[i];
+        if (rows <= 0)
+            continue;
         const int32_t *qw = qweight_stack + (long)e * words_per_expert;
         const uint16_t *sc = scales_stack + (long)e * scales_per_expert;
         const uint16_t *zp = zeros_stack ? zeros_stack + (long)e * scales_per_expert : NULL;
-        for (int r = ex_off[i]; r < ex_off[i + 1]; ++r) {
-            int pair = ex_pairs[r];
-            orc_gemm(a + (long)pair_tok[pair] * lda, lda, 1, qw, sc, zp, NULL, k, n, group_size,
-                     weight_type, y + (long)pair * n, nthreads);
+        /* The segment's activation rows, in segment order, then one GEMM with this expert's
+         * weights; row r of its result is pair ex_pairs[ex_off[i] + r]. */
+        uint16_t *a_seg = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)rows * k);
+        double *y_seg = (double *)malloc(sizeof(double) * (size_t)rows * n);
+        for (int r = 0; r < rows; ++r) {
+            int pair = ex_pairs[ex_off[i] + r];
+            memcpy(a_seg + (long)r * k, a + (long)pair_tok[pair] * lda, sizeof(uint16_t) * (size_t)k);
         }
+        orc_gemm(a_seg, k, rows, qw, sc, zp, NULL, k, n, group_size, weight_type, y_seg, nthreads);
+        for (int r = 0; r < rows; ++r) {
+            int pair = ex_pairs[ex_off[i] + r];
+            memcpy(y + (long)pair * n, y_seg + (long)r * n, sizeof(double) * (size_t)n);
+        }
+        free(a_seg);
+        free(y_seg);
     }
 }
 

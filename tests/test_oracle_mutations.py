@@ -27,7 +27,8 @@ MUTATIONS = [
     ("zero point column dropped", "? 8.0 : orc_half_to_double(zeros[(long)g * n + col]);",
      "? 8.0 : orc_half_to_double(zeros[(long)g * n]);"),
     ("g_idx ignored", "    if (g_idx)\n        return g_idx[row];\n", "\n"),
-    ("dropped accumulation", "acc[j] += av * orc_weight(", "acc[j] = av * orc_weight("),
+    ("dropped accumulation", "acc[j] += av * wr[j];", "acc[j] = av * wr[j];"),
+    ("W band column shifted", "jb->weight_type, row, c0 + j);", "jb->weight_type, row, c0 + (j + 1) % width);"),
     ("A reversed along K", "double av = orc_half_to_double(jb->a[(long)i * jb->lda + row]);",
      "double av = orc_half_to_double(jb->a[(long)i * jb->lda + (jb->k - 1 - row)]);"),
     ("half exponent bias", "v = ldexp(1.0 + frac / 1024.0, expo - 15);",
