@@ -2,18 +2,26 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
 
-A step is one pass over every GEMM of the workload (default: the decode sweep, M in
-{1,4,8,16,32,64} x (K=4096, N=4096) and (K=4096, N=12288), group 128, u4b8).  Inputs are
-seeded synthetic data already resident in HBM.  The decode weights fit in L2, so each GEMM of
-a step reads its own copy of the weights from a ring whose total size is at least three times
-the L2 size: no step finds its weights in L2.  Steps are captured once in a CUDA graph and
-timed with CUDA events on the launching stream, W untimed warm-up steps first.
+A step is one pass over every GEMM of the workload.  The default workload, "all", is the whole
+metric, M = 1..4096: the decode sweep (M in {1,4,8,16,32,64} x 4096x4096 and 4096x12288, u4b8),
+prefill (M in {256,1024,4096} x 4096x11008 and 11008x4096, u4 + zeros), act-order (M in
+{1,16,2048}, 8192x28672) and the grouped MoE pair (8 experts, 512 tokens top-2); the single
+configurations remain selectable for profiling.  Inputs are seeded synthetic data already
+resident in HBM.  Each GEMM of a step reads its own copy of the weights from a ring whose total
+size is at least three times the L2 size: no step finds its weights in L2.  Steps are captured
+once in a CUDA graph and timed with CUDA events on the launching stream, W untimed warm-up
+steps first.
+
+`value` is the step's fraction of roofline: the sum over its GEMMs of each GEMM's roofline
+time max(bytes / HBM bandwidth, flops / dense fp16 tensor peak), over the measured step time.
+`detail` gives every GEMM's own time, rates, bound and fraction (timed live, a graph of calls
+per GEMM); `roofline` is the dominant kernel's (the one with the most time), from those times.
 
 `--impl reference` times the CPU oracle instead (the only other place this script runs it):
-each step is a bounded sample of the same workload, extrapolated linearly in M.
+each step is a bounded sample of the same workload, extrapolated per GEMM.
 
 For N > 1 (torchrun) every rank runs the full workload on its own GPU (weak scaling, no
-collective on the data path); value = all ranks' work / the slowest rank's time.
+collective on the data path); value = all ranks' roofline time / the slowest rank's time.
 """
 from __future__ import annotations
 
@@ -48,25 +56,35 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # Workloads (the configurations of the W4A16 GEMM; shapes, distributions and seeds)
 # ---------------------------------------------------------------------------------------------
 
+CONFIGS = ("decode", "prefill", "actorder", "moe")
+
+
 def workload_specs(name: str):
-    """List of GEMMs of one step: dicts with m, k, n, gs, wt, act_order, sigma, seed."""
+    """List of GEMMs of one step: dicts with m, k, n, gs, wt, act_order, sigma, seed (grouped
+    GEMMs: n_exp, n_tok, top_k, pair_rows instead of m), each tagged with its configuration."""
+    if name == "all":
+        return [s for c in CONFIGS for s in workload_specs(c)]
     if name == "decode":
-        return [dict(m=m, k=4096, n=n, gs=128, wt=U4B8, act_order=False, sigma=1.0, seed=1000 + m)
-                for n in (4096, 12288) for m in (1, 4, 8, 16, 32, 64)]
-    if name == "prefill":
-        return [dict(m=m, k=k, n=n, gs=128, wt=U4, act_order=False, sigma=0.5, seed=2000 + m)
-                for (k, n) in ((4096, 11008), (11008, 4096)) for m in (256, 1024, 4096)]
-    if name == "actorder":
-        return [dict(m=m, k=8192, n=28672, gs=128, wt=U4B8, act_order=True, sigma=1.0, seed=3000 + m)
-                for m in (1, 16, 2048)]
-    if name == "tiny":
-        return [dict(m=16, k=256, n=256, gs=128, wt=U4B8, act_order=False, sigma=1.0, seed=0)]
-    if name == "moe":
-        return [dict(grouped=True, n_exp=8, n_tok=512, top_k=2, k=4096, n=28672, gs=128, wt=U4B8,
-                     seed=5000, pair_rows=False),
-                dict(grouped=True, n_exp=8, n_tok=512, top_k=2, k=14336, n=4096, gs=128, wt=U4B8,
-                     seed=5001, pair_rows=True)]
-    raise SystemExit(f"unknown workload {name}")
+        specs = [dict(m=m, k=4096, n=n, gs=128, wt=U4B8, act_order=False, sigma=1.0, seed=1000 + m)
+                 for n in (4096, 12288) for m in (1, 4, 8, 16, 32, 64)]
+    elif name == "prefill":
+        specs = [dict(m=m, k=k, n=n, gs=128, wt=U4, act_order=False, sigma=0.5, seed=2000 + m)
+                 for (k, n) in ((4096, 11008), (11008, 4096)) for m in (256, 1024, 4096)]
+    elif name == "actorder":
+        specs = [dict(m=m, k=8192, n=28672, gs=128, wt=U4B8, act_order=True, sigma=1.0, seed=3000 + m)
+                 for m in (1, 16, 2048)]
+    elif name == "tiny":
+        specs = [dict(m=16, k=256, n=256, gs=128, wt=U4B8, act_order=False, sigma=1.0, seed=0)]
+    elif name == "moe":
+        specs = [dict(grouped=True, n_exp=8, n_tok=512, top_k=2, k=4096, n=28672, gs=128, wt=U4B8,
+                      seed=5000, pair_rows=False),
+                 dict(grouped=True, n_exp=8, n_tok=512, top_k=2, k=14336, n=4096, gs=128, wt=U4B8,
+                      seed=5001, pair_rows=True)]
+    else:
+        raise SystemExit(f"unknown workload {name}")
+    for s in specs:
+        s["config"] = name
+    return specs
 
 
 WORKLOAD_TEXT = {
@@ -76,6 +94,8 @@ WORKLOAD_TEXT = {
     "tiny": "tiny M=16, K=256, N=256, group 128, u4b8",
     "moe": "grouped MoE 8 experts, 512 tokens top-2, gate_up K=4096 N=28672 + down K=14336 N=4096, u4b8",
 }
+WORKLOAD_TEXT["all"] = ("M=1..4096, every configuration in one step: " +
+                        "; ".join(WORKLOAD_TEXT[c] for c in CONFIGS))
 
 
 def weight_bytes(s) -> int:
@@ -93,6 +113,31 @@ def gemm_bytes(s) -> int:
 
 def gemm_flops(s) -> int:
     return 2 * s["m"] * s["n"] * s["k"]
+
+
+def grouped_accounting(s):
+    """Bytes/flops of a grouped call: all experts' weights, gathered A, pair-major Y."""
+    g = synth.group_count(s["k"], s["gs"])
+    wb = s["n_exp"] * (s["k"] * s["n"] // 2 + g * s["n"] * 2)
+    n_pairs = s["n_tok"] * s["top_k"]
+    rows = n_pairs if s["pair_rows"] else s["n_tok"]
+    return wb, wb + rows * s["k"] * 2 + n_pairs * s["n"] * 2, 2 * n_pairs * s["n"] * s["k"]
+
+
+def accounting(s):
+    """(weight bytes, algorithmic bytes, flops) of one GEMM of a workload."""
+    if s.get("grouped"):
+        return grouped_accounting(s)
+    return weight_bytes(s), gemm_bytes(s), gemm_flops(s)
+
+
+def roofline_us(s, peaks):
+    """The GEMM's roofline time in microseconds, max(bytes / HBM, flops / tensor peak), and
+    which of the two bounds it ("hbm" or "tensor")."""
+    _, b, f = accounting(s)
+    t_hbm = b / peaks["hbm_gbs"] / 1e3
+    t_tc = f / peaks["bf16_tflops"] / 1e6
+    return (t_hbm, "hbm") if t_hbm >= t_tc else (t_tc, "tensor")
 
 
 def load_peaks():
@@ -370,15 +415,6 @@ class StepIO:
         self.bind(0)
 
 
-def grouped_accounting(s):
-    """Bytes/flops of a grouped call: all experts' weights, gathered A, pair-major Y."""
-    g = synth.group_count(s["k"], s["gs"])
-    wb = s["n_exp"] * (s["k"] * s["n"] // 2 + g * s["n"] * 2)
-    n_pairs = s["n_tok"] * s["top_k"]
-    rows = n_pairs if s["pair_rows"] else s["n_tok"]
-    return wb, wb + rows * s["k"] * 2 + n_pairs * s["n"] * 2, 2 * n_pairs * s["n"] * s["k"]
-
-
 def select_shape(specs, shape):
     """The GEMMs of `specs` whose (m, k, n) equal the "M,K,N" string `shape` (all if None)."""
     if not shape:
@@ -390,6 +426,63 @@ def select_shape(specs, shape):
     return picked
 
 
+def time_graph(stream, dev, fn, reps):
+    """Average microseconds of one fn(r) call, from a CUDA graph of `reps` calls (r = 0..reps-1)
+    timed with CUDA events on `stream` after one warm replay."""
+    import torch
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        fn(0)
+        torch.cuda.synchronize(dev)
+        with torch.cuda.graph(graph, stream=stream):
+            for r in range(reps):
+                fn(r)
+        graph.replay()
+    torch.cuda.synchronize(dev)
+    d0 = torch.cuda.Event(enable_timing=True)
+    d1 = torch.cuda.Event(enable_timing=True)
+    d0.record(stream)
+    with torch.cuda.stream(stream):
+        graph.replay()
+    d1.record(stream)
+    torch.cuda.synchronize(dev)
+    del graph
+    return d0.elapsed_time(d1) * 1e3 / reps
+
+
+def kernel_of(w4, g) -> int:
+    """The library's kernel for one GEMM of the workload (0 tcgen05, 1 split-K small-M,
+    2 column-slice small-M); grouped calls always run the tcgen05 kernel."""
+    s = g.s
+    if s.get("grouped"):
+        return 0
+    return w4.w4a16_kernel_for(s["m"], s["n"], s["k"], s["gs"], g.flags)
+
+
+def kernel_roofline(rows, peaks, peak_src, launches):
+    """Roofline of one kernel from the live per-GEMM timings of its calls: the bound its calls'
+    roofline times are mostly set by, achieved = their algorithmic flops (bytes) / their time."""
+    us = sum(r["us"] for r in rows)
+    flops = sum(r["flops"] for r in rows)
+    nbytes = sum(r["bytes"] for r in rows)
+    t_tc = sum(r["roof_us"] for r in rows if r["bound"] == "tensor")
+    t_hbm = sum(r["roof_us"] for r in rows if r["bound"] == "hbm")
+    if t_tc >= t_hbm:
+        achieved = flops / us / 1e6
+        out = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"],
+               "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
+               "peak_source": f"{peak_src} bf16_tflops (burst; the fp16 dense rate equals bf16)",
+               "flops_per_launch": round(flops / launches)}
+    else:
+        achieved = nbytes / us / 1e3
+        out = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+               "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+               "peak_source": f"{peak_src} hbm_gbs", "bytes_per_launch": round(nbytes / launches)}
+    out["launches_per_step"] = launches
+    out["us_per_step"] = round(us, 2)
+    return out
+
+
 def run_ours(args, rank, world, local):
     import torch
     import weight_only_int4_03_gb300 as w4
@@ -398,32 +491,26 @@ def run_ours(args, rank, world, local):
     torch.cuda.set_device(dev)
     props = torch.cuda.get_device_properties(dev)
     l2 = getattr(props, "L2_cache_size", 0) or 126 * 1024 * 1024
+    peaks, peak_src = load_peaks()
     specs = select_shape(workload_specs(args.workload), args.shape)
     gemms = []
     for s in specs:
-        if s.get("grouped"):
-            wb, _, _ = grouped_accounting(s)
-        else:
-            wb = weight_bytes(s)
+        wb = accounting(s)[0]
         copies = max(1, min(64, math.ceil(3 * l2 / wb)))
         gemms.append(GroupedGemm(w4, s, copies, dev) if s.get("grouped") else DenseGemm(w4, s, copies, dev))
 
-    # Per-step accounting.
+    # Per-step accounting: algorithmic bytes and flops, and the roofline time of every GEMM.
     step_wbytes = step_bytes = step_flops = 0
+    step_roof_us = 0.0
     for g in gemms:
-        if g.s.get("grouped"):
-            wb, b, f = grouped_accounting(g.s)
-        else:
-            wb, b, f = weight_bytes(g.s), gemm_bytes(g.s), gemm_flops(g.s)
+        wb, b, f = accounting(g.s)
         step_wbytes += wb
         step_bytes += b
         step_flops += f
+        step_roof_us += roofline_us(g.s, peaks)[0]
     launches_per_step = sum(g.launches for g in gemms)
-    hbm_bound = args.workload == "decode"
 
     stream = torch.cuda.Stream(device=dev)
-    total_steps = args.warmup + args.steps
-
     io = None   # the end-to-end staging, built after the device-timed run
 
     def run_step(st):
@@ -475,7 +562,6 @@ def run_ours(args, rank, world, local):
         timed_graph.replay()
     ev1.record(stream)
     torch.cuda.synchronize(dev)
-    t_wall1 = time.time()
     if distributed:
         dist.barrier()
     ms = ev0.elapsed_time(ev1)
@@ -487,6 +573,7 @@ def run_ours(args, rank, world, local):
         torch.cuda.synchronize(dev)
     clocks.stop()
     clk = clocks.summary(t_wall0 - 0.35, time.time())
+    del warm_graph, timed_graph
 
     # End to end: every step's A in from pinned host memory and C out, inside the timed
     # region.  The staging (a second set of device buffers, a copy stream) is made only now:
@@ -506,79 +593,64 @@ def run_ours(args, rank, world, local):
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1)
+    del e2e_graph
 
     for g in gemms:
         bits = w4.w4a16_status(g.ws, stream=stream)
         if bits:
             raise SystemExit(f"device status {bits} after timing")
 
-    units = step_wbytes * args.steps if hbm_bound else step_flops * args.steps
-    max_ms, all_units = aggregate_over_ranks(ms, units)
-    max_e2e, all_e2e_units = aggregate_over_ranks(e2e_ms, units)
+    # value: the step's roofline time over its measured time (summed over ranks' work).
+    roof_units = step_roof_us * 1e-3 * args.steps          # ms of roofline time
+    max_ms, all_roof = aggregate_over_ranks(ms, roof_units)
+    max_e2e, all_roof_e2e = aggregate_over_ranks(e2e_ms, roof_units)
 
-    # Per-GEMM detail (separate from the timed region): graph of R calls per GEMM.
+    # Per-GEMM detail, timed live (graphs of R calls of one GEMM over its weight ring): each
+    # GEMM's time, rates and roofline fraction, and which kernel ran it.  The roofline of the
+    # dominant kernel is computed from these times.
     detail = []
     if rank == 0 and not args.no_detail:
         for g in gemms:
-            reps = max(20, min(200, int(2e8 / max(1, weight_bytes(g.s) if not g.s.get("grouped") else grouped_accounting(g.s)[0]))))
-            graph = torch.cuda.CUDAGraph()
-            with torch.cuda.stream(stream):
-                g.run(0)
-                torch.cuda.synchronize(dev)
-                with torch.cuda.graph(graph, stream=stream):
-                    for r in range(reps):
-                        g.run(r)
-                graph.replay()
-            torch.cuda.synchronize(dev)
-            d0 = torch.cuda.Event(enable_timing=True)
-            d1 = torch.cuda.Event(enable_timing=True)
-            d0.record(stream)
-            with torch.cuda.stream(stream):
-                graph.replay()
-            d1.record(stream)
-            torch.cuda.synchronize(dev)
-            us = d0.elapsed_time(d1) * 1e3 / reps
+            wb, b, f = accounting(g.s)
+            reps = max(20, min(200, int(2e8 / max(1, wb))))
+            us = time_graph(stream, dev, g.run, reps)
+            roof, bound = roofline_us(g.s, peaks)
+            kern = kernel_of(w4, g)
+            row = {"config": g.s["config"], "m": g.s["m"], "k": g.s["k"], "n": g.s["n"],
+                   "kernel": w4.KERNEL_NAMES[kern], "us": round(us, 3),
+                   "tflops": round(f / us * 1e-6, 2), "weight_gbs": round(wb / us * 1e-3, 1),
+                   "bytes_gbs": round(b / us * 1e-3, 1), "bound": bound,
+                   "roof_us": round(roof, 3), "frac": round(roof / us, 4)}
             if g.s.get("grouped"):
-                wb, b, f = grouped_accounting(g.s)
-                k, n, m = g.s["k"], g.s["n"], g.s["m"]
-            else:
-                wb, b, f = weight_bytes(g.s), gemm_bytes(g.s), gemm_flops(g.s)
-                k, n, m = g.s["k"], g.s["n"], g.s["m"]
-            detail.append({"m": m, "k": k, "n": n, "us": round(us, 3),
-                           "tflops": round(f / us * 1e-6, 2), "weight_gbs": round(wb / us * 1e-3, 1),
-                           "bytes_gbs": round(b / us * 1e-3, 1)})
-            del graph
+                row["experts"] = g.s["n_exp"]
+            detail.append(row)
+            row["_flops"], row["_bytes"], row["_launches"], row["_kern"] = f, b, g.launches, kern
 
     if rank != 0:
         return None
-    peaks, peak_src = load_peaks()
     sec = max_ms * 1e-3
-    launches = launches_per_step * args.steps
-    if hbm_bound:
-        achieved = step_bytes * args.steps / sec / 1e9
-        peak = peaks["hbm_gbs"]
-        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "peak_source": f"{peak_src} hbm_gbs",
-                "traffic": recorded_traffic(args.workload),
-                "bytes_per_launch": round(step_bytes / launches_per_step)}
-        value = all_units / sec / 1e9
-        unit = "GB/s (weight stream)"
-        e2e_value = all_e2e_units / (max_e2e * 1e-3) / 1e9
-    else:
-        achieved = step_flops * args.steps / sec / 1e12
-        key = "bf16_tflops"
-        peak = peaks[key]
-        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
-                "frac": round(achieved / peak, 4), "peak_source": f"{peak_src} {key} (fp16 = bf16 rate)",
-                "traffic": recorded_traffic(args.workload),
-                "flops_per_launch": round(step_flops / len(gemms))}
-        value = all_units / sec / 1e12
-        unit = "TFLOP/s"
-        e2e_value = all_e2e_units / (max_e2e * 1e-3) / 1e12
-    h2d = io.h2d_bytes
-    d2h = io.d2h_bytes
+    by_kernel = {}
+    for r in detail:
+        by_kernel.setdefault(r["_kern"], []).append(
+            {"us": r["us"], "flops": r["_flops"], "bytes": r["_bytes"], "roof_us": r["roof_us"],
+             "bound": r["bound"], "launches": r["_launches"]})
+    kernels = {}
+    for kern, rows in by_kernel.items():
+        launches = sum(x["launches"] for x in rows)
+        kr = kernel_roofline(rows, peaks, peak_src, launches)
+        key = f"{args.workload}:{w4.KERNEL_NAMES[kern].split()[0]}"
+        kr["traffic"] = recorded_traffic(key) if not args.shape else None
+        kernels[w4.KERNEL_NAMES[kern]] = kr
+    dominant = max(kernels, key=lambda name: kernels[name]["us_per_step"]) if kernels else None
+    roof = dict(kernels[dominant], kernel=dominant) if dominant else None
+    for r in detail:
+        for key in ("_flops", "_bytes", "_launches", "_kern"):
+            r.pop(key)
+    value = all_roof / max_ms
+    e2e_value = all_roof_e2e / max_e2e
+    unit = "fraction of roofline (sum over the step's GEMMs of max(bytes/HBM, flops/tensor peak) / step time)"
     line = {
-        "metric": METRIC, "value": round(value, 2), "unit": unit, "n_gpus": world,
+        "metric": METRIC, "value": round(value, 4), "unit": unit, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(max_ms / args.steps, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16 x u4 -> f32 acc",
         "data": "synthetic (seeded LCG; shapes and distributions of the W4A16 configurations)",
@@ -588,11 +660,16 @@ def run_ours(args, rank, world, local):
                    "parallelism": f"replicas x{world}"},
         "tflops": round(step_flops * args.steps / sec / 1e12, 2),
         "weight_gbs": round(step_wbytes * args.steps / sec / 1e9, 1),
+        "roofline_us_per_step": round(step_roof_us, 2),
+        "peaks": {"hbm_gbs": peaks["hbm_gbs"], "tensor_tflops": peaks["bf16_tflops"],
+                  "source": peak_src},
         "roofline": roof,
+        "kernels": kernels,
         "clocks": clk,
-        "e2e": {"value": round(e2e_value, 2), "unit": unit, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "mode": "C ABI calls; every GEMM's A in from pinned host memory and C out, on a copy stream overlapping the neighbouring steps' compute (double-buffered), captured in a CUDA graph"},
-        "gpu_launches": launches,
+        "e2e": {"value": round(e2e_value, 4), "unit": unit, "h2d_bytes_per_step": io.h2d_bytes,
+                "d2h_bytes_per_step": io.d2h_bytes, "ms_per_step": round(max_e2e / args.steps, 5),
+                "mode": "C ABI calls; every GEMM's A in from pinned host memory and C out, on a copy stream overlapping the neighbouring steps' compute (double-buffered), captured in a CUDA graph"},
+        "gpu_launches": launches_per_step * args.steps,
         "detail": detail,
     }
     return line
@@ -610,48 +687,65 @@ def _oracle_inputs(s, rows: int):
     if s.get("grouped"):
         qw = synth.qweight(s["seed"] * 100, k, n)
         a = synth.activations(s["seed"], rows, k)
-        return a, qw, synth.scales(s["seed"], g, n), None
+        return a, qw, synth.scales(s["seed"], g, n), None, None
     qw = synth.qweight(s["seed"], k, n)
     z = synth.zeros(s["seed"], g, n) if s["wt"] == U4 else None
-    return synth.activations(s["seed"], rows, k, sigma=s["sigma"]), qw, synth.scales(s["seed"], g, n), z
+    g_idx = synth.act_order_gidx(synth.permutation(s["seed"], k), s["gs"]) if s.get("act_order") else None
+    return synth.activations(s["seed"], rows, k, sigma=s["sigma"]), qw, synth.scales(s["seed"], g, n), z, g_idx
+
+
+def step_totals(specs, peaks):
+    """(roofline microseconds, flops, weight bytes) of one step of these GEMMs."""
+    roof = flops = wbytes = 0.0
+    for s in specs:
+        wb, _, f = accounting(s)
+        roof += roofline_us(s, peaks)[0]
+        flops += f
+        wbytes += wb
+    return roof, flops, wbytes
 
 
 def oracle_sample(workload: str, budget_s: float, threads: int | None = None):
-    """Times the oracle on a bounded sample of one step of the workload: r output rows of every
-    GEMM (r sized so the sample takes about `budget_s`), then extrapolates the step time
-    linearly in the rows (the oracle's cost is linear in M).
-    Returns (step_seconds_estimate, units_per_step, unit, threads, sample_text)."""
+    """Times the oracle on a bounded sample of one step of the workload and estimates the time
+    of the whole step.  The oracle derives W once per call (a fixed cost) and then spends a
+    fixed time per output row, so every GEMM is timed at 1 row and at r rows (r sized from the
+    budget) and the two-point fit extrapolates to all of its rows (a grouped GEMM pays the W
+    derivation once per expert).
+    Returns (step_seconds_estimate, threads, sample_text)."""
     import oracle
     orc = oracle.Oracle()
     threads = threads or oracle.default_threads()
     specs = workload_specs(workload)
 
-    def row_seconds(s, r):
-        a, qw, sc, z = _oracle_inputs(s, r)
-        t0 = time.time()
-        orc.gemm(a, qw, sc, z, None, s["gs"], s["wt"], threads=threads)
-        return (time.time() - t0) / r
+    def seconds(s, r):
+        a, qw, sc, z, g_idx = _oracle_inputs(s, r)
+        t0 = time.perf_counter()
+        orc.gemm(a, qw, sc, z, g_idx, s["gs"], s["wt"], threads=threads)
+        return time.perf_counter() - t0
 
-    # Calibrate with one row per GEMM, then spend the budget on r rows of each.
-    calib = sum(row_seconds(s, 1) for s in specs)
-    r = max(1, int(budget_s / max(calib, 1e-9)))
-    hbm = workload == "decode"
-    est = units = 0.0
+    per_gemm = budget_s / max(1, len(specs))
+    est = 0.0
     sample_rows = 0
     for s in specs:
         rows_total = s["n_tok"] * s["top_k"] if s.get("grouped") else s["m"]
-        rr = min(r, rows_total)
-        est += row_seconds(s, rr) * rows_total
-        sample_rows += rr
-        if s.get("grouped"):
-            wb, _, f = grouped_accounting(s)
+        fixed_count = s["n_exp"] if s.get("grouped") else 1
+        t1 = seconds(s, 1)
+        sample_rows += 1
+        # A row costs roughly a twentieth of deriving W (one multiply-add per weight against
+        # the weight's full derivation); the second point then measures it.
+        r = int(min(rows_total, 4096, max(2, (per_gemm - t1) / max(t1 / 20, 1e-9))))
+        if rows_total > 1 and r >= 2:
+            tr = seconds(s, r)
+            sample_rows += r
+            per_row = max(0.0, (tr - t1) / (r - 1))
+            fixed = max(0.0, t1 - per_row)
         else:
-            wb, f = weight_bytes(s), gemm_flops(s)
-        units += wb if hbm else f
-    unit = "GB/s (weight stream)" if hbm else "TFLOP/s"
-    text = (f"{sample_rows} output rows over the {len(specs)} GEMMs of one step (at most {r} per "
-            f"GEMM), fp64 on {threads} threads, extrapolated linearly to all rows of the step")
-    return est, units, unit, threads, text
+            per_row, fixed = t1, 0.0
+        est += fixed_count * fixed + rows_total * per_row
+    text = (f"{sample_rows} output rows over the {len(specs)} GEMMs of one step (each GEMM at 1 "
+            f"row and at up to 4096 rows), fp64 on {threads} threads; the step time is the "
+            f"two-point fit (W derivation + rows x per-row time) summed over the GEMMs")
+    return est, threads, text
 
 
 def _dequant_fp32(qw, scales, zeros, gs, wt):
@@ -675,13 +769,13 @@ def blas_sample(workload: str, repeats: int = 3):
     """A CPU baseline that is not the oracle: each GEMM's weights dequantised once to fp32
     (outside the timing), then numpy's fp32 GEMM (BLAS, the host's threads) on the GEMM's full
     M, best of `repeats`.  For a grouped GEMM one expert's weights stand for every expert and
-    the time is scaled by the experts.  Returns (step_seconds, units_per_step, unit, text)."""
-    hbm = workload == "decode"
-    est = units = 0.0
-    for s in workload_specs(workload):
+    the time is scaled by the experts.  Returns (step_seconds, text)."""
+    est = 0.0
+    specs = workload_specs(workload)
+    for s in specs:
         rows = s["n_tok"] * s["top_k"] if s.get("grouped") else s["m"]
         per = rows // s["n_exp"] if s.get("grouped") else rows
-        a, qw, sc, z = _oracle_inputs(s, per)
+        a, qw, sc, z, _ = _oracle_inputs(s, per)
         w = _dequant_fp32(qw, sc, z, s["gs"], s["wt"])
         a32 = a.astype(np.float32)
         best = float("inf")
@@ -690,35 +784,38 @@ def blas_sample(workload: str, repeats: int = 3):
             (a32 @ w).astype(np.float16)
             best = min(best, time.perf_counter() - t0)
         est += best * (s["n_exp"] if s.get("grouped") else 1)
-        if s.get("grouped"):
-            wb, _, f = grouped_accounting(s)
-        else:
-            wb, f = weight_bytes(s), gemm_flops(s)
-        units += wb if hbm else f
         del w, a32
-    unit = "GB/s (weight stream)" if hbm else "TFLOP/s"
-    text = (f"all {len(workload_specs(workload))} GEMMs of one step at full M, weights dequantised "
-            f"once to fp32 outside the timing, numpy fp32 matmul (BLAS), best of {repeats}")
-    return est, units, unit, text
+    text = (f"all {len(specs)} GEMMs of one step at full M, weights dequantised once to fp32 "
+            f"outside the timing, numpy fp32 matmul (BLAS), best of {repeats}")
+    return est, text
+
+
+def cpu_line(workload: str, seconds: float, peaks):
+    """A CPU step time in the line's units: the step's roofline time on the GPU over the CPU's
+    step time (the same fraction the GPU line reports), plus TFLOP/s and weight GB/s."""
+    roof, flops, wbytes = step_totals(workload_specs(workload), peaks)
+    return {"value": round(roof * 1e-6 / seconds, 8),
+            "unit": "fraction of the GPU roofline (the step's roofline time / the CPU step time)",
+            "tflops": round(flops / seconds / 1e12, 6), "weight_gbs": round(wbytes / seconds / 1e9, 6),
+            "step_s": round(seconds, 3)}
 
 
 def cpu_baseline(workload: str, budget_s: float = 15.0):
     """The oracle on the host's threads (the reported baseline), plus, labelled separately, the
     oracle on one thread and a BLAS fp32 GEMM on weights dequantised once.  The two extras are
     best effort: a failure is recorded in the line, it does not end the run."""
-    est, units, unit, threads, text = oracle_sample(workload, budget_s)
-    scale = 1e9 if unit.startswith("GB") else 1e12
-    line = {"value": round(units / est / scale, 6), "unit": unit, "cores": threads, "kind": "oracle",
-            "sample": text}
+    peaks = load_peaks()[0]
+    est, threads, text = oracle_sample(workload, budget_s)
+    line = dict(cpu_line(workload, est, peaks), cores=threads, kind="oracle", sample=text)
     try:
-        est1, units1, _, _, text1 = oracle_sample(workload, budget_s / 3, threads=1)
-        line["single_core"] = {"value": round(units1 / est1 / scale, 6), "cores": 1, "sample": text1}
+        est1, _, text1 = oracle_sample(workload, budget_s / 3, threads=1)
+        line["single_core"] = dict(cpu_line(workload, est1, peaks), cores=1, sample=text1)
     except Exception as e:  # noqa: BLE001 -- a baseline must not end the benchmark
         line["single_core"] = {"error": f"{type(e).__name__}: {e}"}
     try:
-        est2, units2, _, text2 = blas_sample(workload)
-        line["fp32_blas"] = {"value": round(units2 / est2 / scale, 6), "cores": os.cpu_count(),
-                             "kind": "numpy fp32 GEMM on dequantised weights", "sample": text2}
+        est2, text2 = blas_sample(workload)
+        line["fp32_blas"] = dict(cpu_line(workload, est2, peaks), cores=os.cpu_count(),
+                                 kind="numpy fp32 GEMM on dequantised weights", sample=text2)
     except Exception as e:  # noqa: BLE001
         line["fp32_blas"] = {"error": f"{type(e).__name__}: {e}"}
     return line
@@ -727,31 +824,30 @@ def cpu_baseline(workload: str, budget_s: float = 15.0):
 def run_reference(args, rank):
     if rank != 0:
         return None
+    peaks, peak_src = load_peaks()
     per_step_budget = max(0.5, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
         oracle_sample(args.workload, per_step_budget)
     total_est = 0.0
-    total_units = 0.0
     wall0 = time.time()
     threads = 1
     text = ""
-    unit = ""
     for _ in range(args.steps):
-        est, units, unit, threads, text = oracle_sample(args.workload, per_step_budget)
+        est, threads, text = oracle_sample(args.workload, per_step_budget)
         total_est += est
-        total_units += units
     wall = time.time() - wall0
-    scale = 1e9 if unit.startswith("GB") else 1e12
-    value = total_units / total_est / scale
+    cl = cpu_line(args.workload, total_est / args.steps, peaks)
     return {
-        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": unit, "n_gpus": 1,
+        "impl": "reference", "metric": METRIC, "value": cl["value"], "unit": cl["unit"], "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_est / args.steps * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded LCG)", "config": {"workload": WORKLOAD_TEXT[args.workload],
                                                      "parallelism": "CPU threads"},
-        "cpu_baseline": {"value": round(value, 6), "unit": unit, "cores": threads, "kind": "oracle",
+        "tflops": cl["tflops"], "weight_gbs": cl["weight_gbs"],
+        "peaks": {"hbm_gbs": peaks["hbm_gbs"], "tensor_tflops": peaks["bf16_tflops"], "source": peak_src},
+        "cpu_baseline": {"value": cl["value"], "unit": cl["unit"], "cores": threads, "kind": "oracle",
                          "sample": text},
-        "e2e": {"value": round(value, 6), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "e2e": {"value": cl["value"], "unit": cl["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "wall_s": round(wall, 2),
     }
 
@@ -762,9 +858,10 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=list(WORKLOAD_TEXT), default="decode")
+    ap.add_argument("--workload", choices=list(WORKLOAD_TEXT), default="all")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-detail", action="store_true")
+    ap.add_argument("--no-detail", action="store_true",
+                    help="skip the per-GEMM timings (and with them the kernel rooflines): for profiling runs")
     ap.add_argument("--shape", default=None,
                     help="M,K,N: run only this GEMM of the workload (for profiling one kernel)")
     args = ap.parse_args(argv)

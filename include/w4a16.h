@@ -78,12 +78,17 @@ extern "C" {
 #define W4A16_ARG_TYPE 8        /* unknown weight type                                         */
 #define W4A16_ARG_SCHEDULE 9    /* grouped schedule sizes out of range                         */
 #define W4A16_ARG_SCRATCH 10    /* w4a16_gemm_noalloc: the call needs more scratch than it has */
+#define W4A16_ARG_QZERO 11      /* a packed GPTQ zero code of 15 (its zero point would be 16)  */
 
 /* Device-side error bits (stage 7), accumulated in the workspace status word. */
-#define W4A16_DEV_TIMEOUT 1     /* a bounded wait inside a kernel ran out                      */
+#define W4A16_DEV_TIMEOUT 1     /* a bounded wait inside a kernel ran out; the workspace's
+                                   split-tile counters may then be left non-zero, so zero-fill
+                                   the whole workspace again before its next use             */
 #define W4A16_DEV_PERM 2        /* a perm entry was outside [0, K)                             */
 #define W4A16_DEV_GIDX 4        /* g_idx[perm[i]] != i / group_size (groups not equal-sized)   */
 #define W4A16_DEV_SCHEDULE 8    /* a CSR entry was outside its range                           */
+#define W4A16_DEV_ZERO 16       /* w4a16_zero_points_check: a zero point is not an integer in
+                                   [0, 15]                                                   */
 
 /* ------------------------------------------------------------------------------------------
  * Packed tile layout (this library's own; the pages only say the kernel layout is a
@@ -126,8 +131,11 @@ int w4_unpack(const int32_t *b_packed, int32_t *qweight, int k, int n, cudaStrea
  * sizes are invalid).  The workspace holds a status word, the split-K tile counters, the
  * fp32 partial tiles and, with act-order, the gathered copy of A.  It must be zero-filled
  * once after allocation; the kernels leave it ready for the next call (counters reset
- * themselves), so no per-call memset is needed.  Calls that run concurrently need separate
- * workspaces. */
+ * themselves), so no per-call memset is needed.  The one exception: after w4a16_status has
+ * reported W4A16_DEV_TIMEOUT, a CTA that gave up may have left its tile counters part-way, and
+ * the next call would then reduce the wrong partials -- zero-fill the whole workspace again
+ * (cudaMemsetAsync over its size) before reusing it.  Calls that run concurrently need
+ * separate workspaces. */
 size_t w4a16_workspace_size(int m, int n, int k, int group_size, unsigned flags, int num_sms);
 
 /* The W4A16 GEMM.
@@ -135,11 +143,15 @@ size_t w4a16_workspace_size(int m, int n, int k, int group_size, unsigned flags,
  *   b_packed   device int32 tile layout of the [K][N] codes (from w4_repack)
  *   c          device fp16 [M][ldc], ldc >= N, ldc % 8 == 0; written
  *   scales     device fp16 [G][N], G = K / group_size (1 for group_size -1)
- *   zeros      device fp16 [G][N] integer zero points in [0, 15], or NULL (u4b8)
+ *   zeros      device fp16 [G][N] integer zero points in [0, 15], or NULL (u4b8).  The
+ *              kernels form (q - z) exactly by integer arithmetic inside fp16 and do not check
+ *              the values: a zero point that is not an integer in [0, 15] gives unspecified
+ *              results (w4a16_zero_points_check reports such values)
  *   g_idx      device int32 [K] or NULL: group of each logical row (act-order)
- *   perm       device int32 [K] or NULL: stable argsort of g_idx, the permutation that
- *              w4_repack applied.  Groups must be equal-sized (g_idx[perm[i]] == i/group_size,
- *              as GPTQ's desc_act layout is); a violation sets W4A16_DEV_GIDX.
+ *   perm       device int32 [K] or NULL: the permutation that w4_repack applied, one that
+ *              sorts g_idx (argsort; any order of the rows inside a group is accepted).
+ *              Groups must be equal-sized (g_idx[perm[i]] == i/group_size, as GPTQ's desc_act
+ *              layout is); a violation sets W4A16_DEV_GIDX.
  *   workspace  device, >= w4a16_workspace_size(...) bytes, 256-byte aligned, zero-filled once
  *   m          >= 0 (0 is a no-op);  n % 256 == 0;  k % 128 == 0
  *   group_size -1 (one group) or a positive multiple of 16 dividing K
@@ -152,11 +164,23 @@ size_t w4a16_workspace_size(int m, int n, int k, int group_size, unsigned flags,
  * register-fragment kernel; larger M the tcgen05 kernel.  All three give results within the
  * same tolerance of the exact product; they round differently, so their bits may differ.
  * Results are deterministic: a fixed reduction order makes repeated calls on the same device
- * with the same sizes and flags bit-identical. */
+ * with the same sizes and flags bit-identical.  Tuning overrides read once from the
+ * environment (W4A16_STAGE_BLOCKS, W4A16_DECODE_ROWS, W4A16_DECODE_GRID, W4A16_TILE_TOKENS,
+ * W4A16_SLICE; unset by default) change the kernel choice and tiling, and with them the
+ * rounding order: results stay within tolerance but their bits can differ between processes
+ * whose environments differ. */
 int w4a16_gemm(const void *a, int lda, const int32_t *b_packed, void *c, int ldc,
                const void *scales, const void *zeros, const int32_t *g_idx, const int32_t *perm,
                void *workspace, size_t workspace_bytes, int m, int n, int k, int group_size,
                int weight_type, unsigned flags, cudaStream_t stream);
+
+/* Which kernel w4a16_gemm runs for these sizes and flags on a device with `num_sms`
+ * multiprocessors (num_sms <= 0: the current device): 0 the tcgen05 kernel, 1 the split-K
+ * small-M kernel, 2 the column-slice small-M kernel; -1 for sizes or flags that w4a16_gemm
+ * rejects.  Host code only (with num_sms > 0 it touches no GPU).  For tests and benchmarks:
+ * the pages check the tile geometry a launch picked (marlin.rs, the profile-sink test of the
+ * vLLM Marlin-MoE path). */
+int w4a16_kernel_for(int m, int n, int k, int group_size, unsigned flags, int num_sms);
 
 /* Device scratch of w4a16_gemm_noalloc, per GPU that loads the library (held until exit). */
 #define W4A16_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
@@ -171,13 +195,17 @@ int w4a16_gemm(const void *a, int lda, const int32_t *b_packed, void *c, int ldc
  *   status_out  device int32 or NULL, 4-byte aligned: receives (stream-ordered) the call's
  *               device-side error bits (W4A16_DEV_*), 0 when all went well
  * It holds the tcgen05 kernel's token tiles to at most 192 rows (w4a16_gemm goes up to 256),
- * so that their partial-tile slots fit the array for every shape; M above 192 then runs in
- * tiles of 192 rows, a little slower than w4a16_gemm where that would pick taller tiles.  A
- * call whose scratch still exceeds the array -- an act-order call whose copy of A (M*K*2
- * bytes) does not fit beside the rest -- returns stage 2 with detail W4A16_ARG_SCRATCH and
+ * so that their partial-tile slots stay small; M above 192 then runs in tiles of 192 rows, a
+ * little slower than w4a16_gemm where that would pick taller tiles.  The scratch a call needs
+ * is the status header, one counter per output tile, two fp32 partial slots per CTA (SM count
+ * x tile rows x 128 columns each) and, with act-order, the copy of A (M*K*2 bytes); a call for
+ * which these exceed W4A16_NOALLOC_SCRATCH_BYTES (an act-order call with a large M*K, a very
+ * large M, or a part with many more SMs) returns stage 2 with detail W4A16_ARG_SCRATCH and
  * launches nothing.
- * The first call on a device looks up the array's device address (once per device); make
- * that first call before any stream capture.  Each call clears the status word and tile
+ * The first call on a device looks up the array's device address (once per device, cached
+ * for the life of the process); make that first call before any stream capture.  A
+ * cudaDeviceReset makes the cached address stale: calling this entry point after one is not
+ * supported.  Each call clears the status word and tile
  * counters it needs on `stream` before its kernels run.  All calls on one device share the
  * array: calls whose work overlaps on the GPU (other streams, other host threads) race and
  * produce wrong results, so serialise them. */
@@ -220,6 +248,37 @@ int w4a16_gemm_grouped(const void *a, int lda, const int32_t *b_packed_stack, vo
 int w4a16_csr_from_token_routes(int n_expert, int n_tokens, int experts_per_token,
                                 const int32_t *selected, int32_t *ex_ids, int32_t *ex_off,
                                 int32_t *ex_pairs, int32_t *pair_tok);
+
+/* ------------------------------------------------------------------------------------------
+ * Checkpoint loading helpers (off the GEMM's path).
+ * ---------------------------------------------------------------------------------------- */
+
+/* AutoGPTQ packed zero points -> the fp16 zero points w4a16_gemm takes (host memory, host
+ * code).  ferrum-kernels 0.8.4 vllm_marlin.rs, `repack_gptq_qzeros_to_marlin`: a checkpoint
+ * stores `zero - 1`, eight 4-bit codes per int32 word along N, column 8w + i at bits 4i..4i+3,
+ * so the runtime zero point is the stored code + 1, and a stored 15 (zero point 16, not a
+ * 4-bit value) is rejected.
+ *   qzeros  host int32 [groups][n / 8]
+ *   zeros   host uint16 [groups][n], written: IEEE binary16 bit patterns of the zero points
+ *           (integers 1..15), ready to copy to the device
+ *   n       a positive multiple of 8
+ * Returns 0, or stage 1 with W4A16_ARG_QZERO if any code is 15 (then nothing is written),
+ * W4A16_ARG_SHAPE or W4A16_ARG_NULL. */
+int w4_qzeros_to_zero_points(const int32_t *qzeros, int groups, int n, uint16_t *zeros);
+
+/* Whether a checkpoint's packed zero words say "symmetric": every 4-bit code of every word is
+ * 7 (zero point 8), so the weights can run as W4A16_TYPE_U4B8 without zero points
+ * (vllm_marlin.rs, `gptq_qzeros_are_symmetric_code7`).  Host memory; returns 1 or 0 (0 for
+ * an empty or NULL array). */
+int w4_qzeros_symmetric_code7(const int32_t *qzeros, long long count);
+
+/* Device check of fp16 zero points before they are handed to w4a16_gemm (whose kernels assume
+ * integers in [0, 15] and do not check): ORs W4A16_DEV_ZERO into *status (device int32,
+ * 4-byte aligned) if any of the `count` values is not an integer in [0, 15] or is NaN.
+ * Asynchronous on `stream`; `zeros` is device fp16, 2-byte aligned.  Returns 0, a stage-1
+ * status for bad arguments, or a stage-6 launch status. */
+int w4a16_zero_points_check(const void *zeros, long long count, int32_t *status,
+                            cudaStream_t stream);
 
 /* Reads (synchronously, on `stream`) the device-side status word of a workspace and clears
  * it.  *device_bits receives the W4A16_DEV_* bits seen since the last read.  Returns 0, or a

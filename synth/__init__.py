@@ -168,8 +168,11 @@ def group_count(k: int, group_size: int) -> int:
 def act_order_gidx(perm: np.ndarray, group_size: int) -> np.ndarray:
     """g_idx for a shuffled act-order layer whose groups each hold `group_size` rows.
 
-    Row perm[i] of the logical weight belongs to group i // group_size, so sorting g_idx
-    (stably) recovers perm.  This is a drawing recipe, not part of the GEMM.
+    Row perm[i] of the logical weight belongs to group i // group_size, so perm sorts g_idx:
+    it lists the rows of group 0 first, then those of group 1, and so on.  Inside a group its
+    order is the shuffle's, not increasing row index (a stable argsort of g_idx would differ
+    there); the GEMM accepts any order inside a group.  This is a drawing recipe, not part of
+    the GEMM.
     """
     g = np.empty(perm.shape[0], dtype=np.int32)
     g[perm] = np.arange(perm.shape[0], dtype=np.int32) // group_size

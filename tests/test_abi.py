@@ -194,3 +194,79 @@ def test_csr_builder_matches_oracle(w4, seed, n_exp, n_tok, top_k):
     for x, y in zip(got, want):
         assert np.array_equal(x, y)
     assert oracle.Oracle().csr_validate(n_exp, n_tok, *got)
+
+
+# --- checkpoint loading helpers (host code, pinned by the pages' three qzeros tests) ----------
+
+def _qzeros_golden():
+    with open(os.path.join(ROOT, "tests", "golden", "qzeros_examples.json")) as f:
+        return json.load(f)
+
+
+def test_qzeros_code7_detection_matches_page_examples(w4):
+    """vllm_marlin.rs `qzeros_code7_detects_symmetric_gptq`: all-7 words are symmetric, one
+    code 8 is not, an empty array is not."""
+    for words, want in _qzeros_golden()["code7"]:
+        assert w4.w4_qzeros_symmetric_code7(np.array(words, dtype=np.uint32).view(np.int32)) == want
+
+
+def test_qzeros_code8_converts_to_zero_point_9(w4):
+    """vllm_marlin.rs `qzeros_code8_repack_converts_to_actual_zero_point_9`."""
+    c = _qzeros_golden()["code8_to_9"]
+    groups = c["k"] // c["group_size"]
+    qz = np.full(groups * c["n"] // 8, c["qzeros_word"], dtype=np.uint32).view(np.int32)
+    zp = w4.w4_qzeros_to_zero_points(qz, groups, c["n"])
+    assert zp.dtype == np.float16 and zp.shape == (groups, c["n"])
+    assert np.all(zp == c["zero_point"])
+
+
+def test_qzeros_layout_matches_page_example(w4):
+    """vllm_marlin.rs `qzeros_repack_preserves_kernel_layout`: the stored codes of the first two
+    words give the zero points 1..8, 8..15 of the first 16 columns, and the runtime zero points
+    re-packed 4 bits per column give the page's three words."""
+    lay = _qzeros_golden()["layout"]
+    groups = lay["k"] // lay["group_size"]
+    actual = lay["actual_zero_points_first_16_columns"]
+    words = np.full(groups * lay["n"] // 8, lay["rest_of_qzeros_word"], dtype=np.uint32)
+    for pc in range(2):
+        words[pc] = sum((actual[pc * 8 + lane] - 1) << (4 * lane) for lane in range(8))
+    zp = w4.w4_qzeros_to_zero_points(words.view(np.int32), groups, lay["n"])
+    assert list(zp[0, :16].astype(int)) == actual
+    runtime = [sum(int(zp[0, pc * 8 + lane]) << (4 * lane) for lane in range(8)) for pc in range(3)]
+    assert runtime == lay["packed_runtime_words_first_three"]
+
+
+def test_qzeros_code15_rejected_and_output_untouched(w4):
+    qz = np.array([0x12345678, 0x0000F000], dtype=np.uint32).view(np.int32)
+    out = np.full((1, 16), 3.0, dtype=np.float16).view(np.uint16)
+    status = w4._lib.w4_qzeros_to_zero_points(qz.ctypes.data, 1, 16, out.ctypes.data)
+    assert status == (1 << 16) | w4.W4A16_ARG_QZERO
+    assert np.all(out.view(np.float16) == 3.0)
+    with pytest.raises(w4.W4A16Error):
+        w4.w4_qzeros_to_zero_points(qz, 1, 16)
+
+
+def test_qzeros_every_code_and_column(w4):
+    """Every stored code 0..14 in every lane position becomes code + 1 at column 8w + lane."""
+    rng = np.random.default_rng(5)
+    codes = rng.integers(0, 15, size=(3, 64), dtype=np.uint32)
+    words = np.zeros((3, 8), dtype=np.uint32)
+    for lane in range(8):
+        words |= codes[:, lane::8] << np.uint32(4 * lane)
+    zp = w4.w4_qzeros_to_zero_points(words.view(np.int32), 3, 64)
+    assert np.array_equal(zp.astype(np.int64), codes.astype(np.int64) + 1)
+
+
+@pytest.mark.parametrize("m,n,gs,flags,want", [
+    (1, 4096, 128, 0, 2), (8, 12288, 128, 0, 2),       # column-slice: M <= 8
+    (16, 4096, 128, 0, 2), (32, 4096, 128, 0, 2),      # ... and M <= 32 while N/16 <= 2 x SMs
+    (16, 12288, 128, 0, 1), (32, 12288, 128, 0, 1),    # split-K small-M above that
+    (8, 4096, 32, 0, 1),                               # groups smaller than a 64-row block
+    (8, 1024, 128, 0, 1),                              # fewer 16-column slices than SMs
+    (33, 4096, 128, 0, 0), (4096, 11008 // 256 * 256, 128, 0, 0),
+    (16, 4096, 128, 1 << 10, 0), (64, 4096, 128, 1 << 11, 1), (32, 4096, 128, 1 << 13, 2),
+    (65, 4096, 128, 1 << 11, -1), (33, 4096, 128, 1 << 13, -1), (4, 4096, 100, 0, -1),
+])
+def test_kernel_choice(w4, m, n, gs, flags, want):
+    """The documented dispatch rule, for a 152-SM part (host only)."""
+    assert w4.w4a16_kernel_for(m, n, 4096, gs, flags, 152) == want

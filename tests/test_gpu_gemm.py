@@ -442,7 +442,9 @@ def test_grouped_small(w4, orc, n_exp, n_tok, top_k, wt):
     k, n = 256, 512
     sel, a, qw, s, z = _grouped_problem(900 + n_tok, n_exp, n_tok, top_k, k, n, wt)
     y, csr = run_grouped(w4, sel, a, qw, s, z, n_exp, n_tok, top_k, k, n, wt)
-    ref = orc.grouped(a, qw.ravel(), s, z, *csr, k, n, 128, wt)
+    # The reference schedule comes from the oracle's own CSR builder.
+    csr_ref = orc.csr_from_token_routes(n_exp, n_tok, top_k, sel)
+    ref = orc.grouped(a, qw.ravel(), s, z, *csr_ref, k, n, 128, wt)
     ok, msg = within_tol(y, ref)
     assert ok, msg
 
@@ -463,3 +465,55 @@ def test_grouped_segment_equals_dense(w4):
         dp.run()
         dense = dp.result()
         assert np.all(np.abs(dense - y[pairs]) <= 1e-3 * np.abs(dense) + 1e-3)
+
+
+# --- loader helpers and workspace recovery --------------------------------------------------
+
+def test_zero_points_check(w4):
+    """Integer zero points in [0, 15] pass; a fraction, 16, a negative value or NaN anywhere
+    is reported."""
+    import torch
+    good = torch.tensor([[0, 1, 7, 15]], dtype=torch.float16, device="cuda").repeat(300, 1)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    w4.w4a16_zero_points_check(good, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    for bad in (7.5, 16.0, -1.0, float("nan"), 0.0625):
+        z = good.clone()
+        z[123, 2] = bad
+        status.zero_()
+        w4.w4a16_zero_points_check(z, status)
+        torch.cuda.synchronize()
+        assert int(status.item()) & w4.W4A16_DEV_ZERO, bad
+
+
+def test_converted_qzeros_run_as_u4(w4, orc):
+    """Packed GPTQ zero words converted by the library's loader helper (code + 1) drive a u4
+    GEMM that matches the oracle fed with the oracle's own conversion."""
+    m, k, n, gs = 9, 512, 256, 128
+    pb = make_problem(805, m, k, n, weight_type=U4)
+    groups = k // gs
+    codes = np.asarray(synth.qweight(806, 8 * groups, n)).view(np.uint32)[:groups, : n // 8]
+    codes = codes & np.uint32(0x77777777)   # stored codes 0..7: zero points 1..8
+    qz = np.ascontiguousarray(codes).view(np.int32)
+    pb.zeros = w4.w4_qzeros_to_zero_points(qz, groups, n)
+    ref_z = orc.qzeros_to_zero_points(qz, groups, n)
+    assert np.array_equal(pb.zeros.astype(np.float64), ref_z)
+    dp = DeviceProblem(w4, pb)
+    dp.run()
+    check(dp, orc)
+
+
+def test_workspace_reset_after_timeout_report(w4, orc):
+    """The recovery documented for W4A16_DEV_TIMEOUT: a workspace whose counters were left
+    part-way (simulated here by writing them on the host side) and whose status word holds the
+    bit is read back, zero-filled again, and the next call is correct."""
+    import torch
+    pb = make_problem(807, 8, 4096, 512)   # few tiles, many CTAs per tile: split tiles
+    dp = DeviceProblem(w4, pb, flags_extra=FLAG_FORCE_MMA)
+    dp.ws.fill_(3)                          # counters 0x03030303, partials garbage
+    dp.ws[:4].copy_(torch.tensor([w4.W4A16_DEV_TIMEOUT], dtype=torch.int32).view(torch.uint8))
+    assert w4.w4a16_status(dp.ws) & w4.W4A16_DEV_TIMEOUT
+    dp.ws.zero_()                           # the recovery step
+    dp.run()
+    check(dp, orc)

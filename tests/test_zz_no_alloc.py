@@ -1,14 +1,16 @@
 """w4a16_gemm_noalloc, the entry point for callers that cannot allocate device memory (code
 inside a host callback or an allocator hook, under a sealed memory pool, or in a plug-in whose
-host gives it no workspace): its scratch is a fixed array inside the library.  Checked here
-against w4a16_gemm with a caller-owned workspace, through the C ABI, on two calls in a row.
+host gives it no workspace): its scratch is a fixed array inside the library.  Checked here,
+through the C ABI and on two calls in a row, against the CPU oracle and against w4a16_gemm
+with a caller-owned workspace, both within the GEMM tolerance.
 
 Kept in a file of its own, collected after every other test file.
 """
 import numpy as np
 import pytest
 
-from helpers import FLAG_FORCE_TC, U4, DeviceProblem, make_problem, within_tol
+import oracle
+from helpers import FLAG_FORCE_TC, U4, DeviceProblem, make_problem, oracle_ref, within_tol
 
 pytestmark = pytest.mark.gpu
 
@@ -42,6 +44,7 @@ def test_noalloc_matches_workspace_entry_point(w4, case):
     extra = case.pop("flags", 0)
     m, k, n = case.pop("m"), case.pop("k"), case.pop("n")
     pb = make_problem(4000 + m, m, k, n, **case)
+    exact = oracle_ref(oracle.Oracle(), pb)
     dp = DeviceProblem(w4, pb, flags_extra=extra)
     dp.run()
     ref = dp.result()
@@ -54,8 +57,10 @@ def test_noalloc_matches_workspace_entry_point(w4, case):
                               pb.group_size, pb.weight_type, dp.flags, status_out=status)
         torch.cuda.synchronize()
         got = c.float().cpu().numpy().astype(np.float64)
+        ok, msg = within_tol(got, exact)
+        assert ok, f"vs oracle: {msg}"
         ok, msg = within_tol(got, ref)
-        assert ok, msg
+        assert ok, f"vs w4a16_gemm: {msg}"
         assert int(status.item()) == 0
 
 

@@ -32,9 +32,11 @@ W4A16_DEV_TIMEOUT = 1
 W4A16_DEV_PERM = 2
 W4A16_DEV_GIDX = 4
 W4A16_DEV_SCHEDULE = 8
+W4A16_DEV_ZERO = 16
 
 W4A16_MAX_SEGMENTS = 1024
 W4A16_ARG_SCRATCH = 10
+W4A16_ARG_QZERO = 11
 W4A16_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 
 if not os.path.exists(LIB_PATH):
@@ -62,6 +64,10 @@ _SIGNATURES = {
     "w4a16_csr_from_token_routes": (_I, [_I, _I, _I, _P, _P, _P, _P, _P]),
     "w4a16_status": (_I, [_P, _P, _P]),
     "w4a16_selftest_timeout": (_I, [_P, _LL, _P]),
+    "w4_qzeros_to_zero_points": (_I, [_P, _I, _I, _P]),
+    "w4_qzeros_symmetric_code7": (_I, [_P, _LL]),
+    "w4a16_zero_points_check": (_I, [_P, _LL, _P, _P]),
+    "w4a16_kernel_for": (_I, [_I, _I, _I, _I, _U, _I]),
 }
 for _name, (_res, _args) in _SIGNATURES.items():
     _fn = getattr(_lib, _name)
@@ -131,6 +137,14 @@ def w4_unpack(b_packed, qweight, k: int, n: int, stream=None) -> None:
 def w4a16_workspace_size(m: int, n: int, k: int, group_size: int, flags: int = 0,
                          num_sms: int = 0) -> int:
     return int(_lib.w4a16_workspace_size(m, n, k, group_size, flags, num_sms))
+
+
+KERNEL_NAMES = {0: "tcgen05", 1: "split-K small-M", 2: "column-slice small-M"}
+
+
+def w4a16_kernel_for(m: int, n: int, k: int, group_size: int, flags: int = 0, num_sms: int = 0) -> int:
+    """0 tcgen05, 1 split-K small-M, 2 column-slice small-M, -1 rejected sizes/flags."""
+    return int(_lib.w4a16_kernel_for(m, n, k, group_size, flags, num_sms))
 
 
 def w4a16_grouped_workspace_size(n_pairs: int, n_active: int, n: int, k: int, group_size: int,
@@ -216,3 +230,28 @@ def w4a16_status(workspace, stream=None) -> int:
 def w4a16_selftest_timeout(workspace, limit_ns: int, stream=None) -> None:
     _check("w4a16_selftest_timeout", _lib.w4a16_selftest_timeout(_ptr(workspace), limit_ns,
                                                                   _stream(stream)))
+
+
+def w4_qzeros_to_zero_points(qzeros, groups: int, n: int):
+    """AutoGPTQ packed `zero - 1` words [groups, n/8] (host) -> fp16 zero points [groups, n]
+    as a numpy float16 array (host); raises W4A16Error on a stored code 15."""
+    qz = np.ascontiguousarray(qzeros, dtype=np.int32)
+    if qz.size != groups * (n // 8):
+        raise W4A16Error("w4_qzeros_to_zero_points", 1 << 16 | 3)
+    out = np.empty((groups, n), dtype=np.uint16)
+    _check("w4_qzeros_to_zero_points",
+           _lib.w4_qzeros_to_zero_points(qz.ctypes.data, groups, n, out.ctypes.data))
+    return out.view(np.float16)
+
+
+def w4_qzeros_symmetric_code7(qzeros) -> bool:
+    """True when every 4-bit code of every packed zero word is 7 (a symmetric checkpoint)."""
+    qz = np.ascontiguousarray(qzeros, dtype=np.int32)
+    return bool(_lib.w4_qzeros_symmetric_code7(qz.ctypes.data if qz.size else None, qz.size))
+
+
+def w4a16_zero_points_check(zeros, status, stream=None) -> None:
+    """ORs W4A16_DEV_ZERO into the device int32 `status` if a zero point (device fp16 tensor)
+    is not an integer in [0, 15]."""
+    _check("w4a16_zero_points_check", _lib.w4a16_zero_points_check(
+        _ptr(zeros), zeros.numel(), _ptr(status), _stream(stream)))

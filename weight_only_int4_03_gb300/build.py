@@ -20,7 +20,8 @@ LIB_PATH = os.path.join(LIB_DIR, "libw4a16.so")
 INCLUDE = os.path.join(ROOT, "include")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["w4a16_gemm.cu", "w4a16_decode.cu", "w4a16_aux.cu", "w4a16_api.cu", "w4a16_noalloc.cu"]
+SOURCES = ["w4a16_gemm.cu", "w4a16_decode.cu", "w4a16_aux.cu", "w4a16_api.cu", "w4a16_noalloc.cu",
+           "w4a16_loader.cu"]
 
 
 def _nvcc() -> str:

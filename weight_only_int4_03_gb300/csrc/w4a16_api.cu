@@ -810,6 +810,18 @@ int w4a16_gemm(const void *a, int lda, const int32_t *b_packed, void *c, int ldc
                           workspace_bytes, m, n, k, group_size, weight_type, flags, stream,
                           w4::MAX_TOK);
 }
+int w4a16_kernel_for(int m, int n, int k, int group_size, unsigned flags, int num_sms)
+{
+    if (m <= 0 || n <= 0 || k <= 0 || n % 256 != 0 || k % 128 != 0 || num_groups(k, group_size) < 0)
+        return -1;
+    const int gs_resolved = group_size == -1 ? k : group_size;
+    if (check_kernel_flags(m, gs_resolved, flags) != 0)
+        return -1;
+    if (num_sms <= 0 && sm_count(&num_sms) != cudaSuccess)
+        return -1;
+    return choose_kernel(m, n, gs_resolved, flags, num_sms);
+}
+
 int w4a16_gemm_grouped(const void *a, int lda, const int32_t *b_packed_stack, void *y, int ldy,
                        const void *scales_stack, const void *zeros_stack, const int32_t *ex_ids,
                        const int32_t *ex_off, const int32_t *ex_pairs, const int32_t *pair_tok,
