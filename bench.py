@@ -75,6 +75,13 @@ def workload_specs(name: str):
                  for m in (1, 16, 2048)]
     elif name == "tiny":
         specs = [dict(m=16, k=256, n=256, gs=128, wt=U4B8, act_order=False, sigma=1.0, seed=0)]
+    elif name == "moe_swiglu":
+        # The MoE FFN as two chained grouped calls: gate_up (2I = 28672 interleaved gate/up
+        # columns) with the SwiGLU epilogue writing H [1024 pairs][14336], then down reading H.
+        specs = [dict(grouped=True, n_exp=8, n_tok=512, top_k=2, k=4096, n=28672, gs=128, wt=U4B8,
+                      seed=5000, pair_rows=False, glu=1),
+                 dict(grouped=True, n_exp=8, n_tok=512, top_k=2, k=14336, n=4096, gs=128, wt=U4B8,
+                      seed=5001, pair_rows=True, a_from=0)]
     elif name == "moe":
         specs = [dict(grouped=True, n_exp=8, n_tok=512, top_k=2, k=4096, n=28672, gs=128, wt=U4B8,
                       seed=5000, pair_rows=False),
@@ -93,6 +100,8 @@ WORKLOAD_TEXT = {
     "actorder": "act-order M in {1,16,2048}, K=8192, N=28672, group 128, u4b8, shuffled g_idx",
     "tiny": "tiny M=16, K=256, N=256, group 128, u4b8",
     "moe": "grouped MoE 8 experts, 512 tokens top-2, gate_up K=4096 N=28672 + down K=14336 N=4096, u4b8",
+    "moe_swiglu": ("grouped MoE FFN 8 experts, 512 tokens top-2: gate_up K=4096 2I=28672 with the "
+                   "fused SwiGLU epilogue -> H [1024, 14336] -> down K=14336 N=4096 reading H, u4b8"),
 }
 WORKLOAD_TEXT["all"] = ("M=1..4096, every configuration in one step: " +
                         "; ".join(WORKLOAD_TEXT[c] for c in CONFIGS))
@@ -121,7 +130,8 @@ def grouped_accounting(s):
     wb = s["n_exp"] * (s["k"] * s["n"] // 2 + g * s["n"] * 2)
     n_pairs = s["n_tok"] * s["top_k"]
     rows = n_pairs if s["pair_rows"] else s["n_tok"]
-    return wb, wb + rows * s["k"] * 2 + n_pairs * s["n"] * 2, 2 * n_pairs * s["n"] * s["k"]
+    n_out = s["n"] // 2 if s.get("glu") else s["n"]
+    return wb, wb + rows * s["k"] * 2 + n_pairs * n_out * 2, 2 * n_pairs * s["n"] * s["k"]
 
 
 def accounting(s):
@@ -322,22 +332,34 @@ class GroupedGemm:
             rows = n_pairs
             pair_tok = np.arange(n_pairs, dtype=np.int32)
         a = synth.activations(s["seed"], rows, k)
+        glu = s.get("glu", 0)   # gated FFN: planar gate|up weights, interleaved on the device
         packed = torch.empty(n_exp * k * n // 8, dtype=torch.int32, device=dev)
         per = k * n // 8
         for e in range(n_exp):
             qw = torch.from_numpy(synth.qweight(s["seed"] * 100 + e, k, n)).to(dev)
+            if glu:
+                qw_i = torch.empty_like(qw)
+                w4.w4_gate_up_interleave(qw, qw_i, k // 8, n)
+                qw = qw_i
             w4.w4_repack(qw, None, packed[e * per:(e + 1) * per], k, n)
             del qw
         scales = torch.from_numpy(synth.scales(s["seed"], n_exp * groups, n)).to(dev)
+        if glu:
+            planar = scales
+            scales = torch.empty_like(planar)
+            w4.w4_gate_up_interleave(planar, scales, n_exp * groups, n)
+            del planar
         self.b = [packed] + [packed.clone() for _ in range(copies - 1)]
         self.scales = [scales] + [scales.clone() for _ in range(copies - 1)]
         self.csr = [torch.from_numpy(x).to(dev) for x in (ex_ids, ex_off, ex_pairs, pair_tok)]
         self.n_active, self.n_pairs, self.rows = len(ex_ids), n_pairs, rows
-        self.flags = FLAG_IS_K_FULL
+        self.flags = FLAG_IS_K_FULL | (0 if not glu else w4.W4A16_FLAG_SWIGLU if glu == 1
+                                       else w4.W4A16_FLAG_GEGLU)
         self.a_host = torch.from_numpy(a).pin_memory()
         self.a = self.a_host.to(dev)
-        self.c = torch.empty((n_pairs, n), dtype=torch.float16, device=dev)
-        self.ws = torch.zeros(w4.w4a16_grouped_workspace_size(n_pairs, self.n_active, n, k, gs, 0),
+        self.c = torch.empty((n_pairs, n // 2 if glu else n), dtype=torch.float16, device=dev)
+        self.ws = torch.zeros(w4.w4a16_grouped_workspace_size(n_pairs, self.n_active, n, k, gs,
+                                                              self.flags),
                               dtype=torch.uint8, device=dev)
         self.w4 = w4
         self.launches = 2
@@ -364,21 +386,35 @@ class StepIO:
     def __init__(self, gemms, dev):
         import torch
         self.gemms = gemms
-        self.a_views = [[g.a for g in gemms], [g.a.clone() for g in gemms]]
+        # A GEMM whose A is an earlier GEMM's C (a chained FFN) reads that C in the same buffer
+        # set and copies nothing in; a C that feeds a later GEMM is not copied out.
+        self.src = [g.s.get("a_from") for g in gemms]
+        fed = {i for i in self.src if i is not None}
         self.c_views = [[g.c for g in gemms], [torch.empty_like(g.c) for g in gemms]]
+        self.a_views = [[g.a for g in gemms],
+                        [g.a.clone() if i is None else None for g, i in zip(gemms, self.src)]]
+        for b in range(2):
+            for j, i in enumerate(self.src):
+                if i is not None:
+                    self.a_views[b][j] = self.c_views[b][i]
+        self.copy_in = [i is None for i in self.src]
+        self.copy_out = [j not in fed for j in range(len(gemms))]
         self.a_host = [g.a_host for g in gemms]
-        self.c_host = [torch.empty(g.c.shape, dtype=g.c.dtype).pin_memory() for g in gemms]
-        self.h2d_bytes = sum(g.a.numel() * 2 for g in gemms)
-        self.d2h_bytes = sum(g.c.numel() * 2 for g in gemms)
+        self.c_host = [torch.empty(g.c.shape, dtype=g.c.dtype).pin_memory() if out else None
+                       for g, out in zip(gemms, self.copy_out)]
+        self.h2d_bytes = sum(g.a.numel() * 2 for g, cin in zip(gemms, self.copy_in) if cin)
+        self.d2h_bytes = sum(g.c.numel() * 2 for g, out in zip(gemms, self.copy_out) if out)
         self.copy_stream = torch.cuda.Stream(device=dev)
 
     def h2d(self, b: int):
-        for dst, src in zip(self.a_views[b], self.a_host):
-            dst.copy_(src, non_blocking=True)
+        for dst, src, cin in zip(self.a_views[b], self.a_host, self.copy_in):
+            if cin:
+                dst.copy_(src, non_blocking=True)
 
     def d2h(self, b: int):
-        for dst, src in zip(self.c_host, self.c_views[b]):
-            dst.copy_(src, non_blocking=True)
+        for dst, src, out in zip(self.c_host, self.c_views[b], self.copy_out):
+            if out:
+                dst.copy_(src, non_blocking=True)
 
     def bind(self, b: int):
         for g, a, c in zip(self.gemms, self.a_views[b], self.c_views[b]):
@@ -498,6 +534,11 @@ def run_ours(args, rank, world, local):
         wb = accounting(s)[0]
         copies = max(1, min(64, math.ceil(3 * l2 / wb)))
         gemms.append(GroupedGemm(w4, s, copies, dev) if s.get("grouped") else DenseGemm(w4, s, copies, dev))
+    for g in gemms:   # chained FFN: this GEMM's A is an earlier GEMM's output
+        if g.s.get("a_from") is not None:
+            src = gemms[g.s["a_from"]].c
+            assert src.shape == g.a.shape, (src.shape, g.a.shape)
+            g.a = src
 
     # Per-step accounting: algorithmic bytes and flops, and the roofline time of every GEMM.
     step_wbytes = step_bytes = step_flops = 0

@@ -67,6 +67,16 @@ extern "C" {
                                            -1 or a multiple of 64 is then rejected
                                            (unsupported-shape)                               */
 
+#define W4A16_FLAG_SWIGLU (1u << 14) /* gated FFN epilogue: the weight's 2I columns are gate
+                                           and up projections interleaved by
+                                           w4_gate_up_interleave, and C receives
+                                           H[M][I] = silu(A Wg) * (A Wu) (ldc >= I) instead of
+                                           the product (tcgen05 kernel only: _FORCE_SIMT,
+                                           _FORCE_MMA and _FORCE_SLICE are rejected)        */
+#define W4A16_FLAG_GEGLU (1u << 15)  /* the same with gelu_tanh(x) = x/2 (1 + tanh(sqrt(2/pi)
+                                           (x + 0.044715 x^3))) in place of silu; exclusive
+                                           with W4A16_FLAG_SWIGLU                            */
+
 /* Detail codes of stage-1/2 statuses. */
 #define W4A16_ARG_NULL 1        /* a required pointer is NULL                                  */
 #define W4A16_ARG_ALIGN 2       /* a pointer or leading dimension breaks its alignment rule    */
@@ -122,6 +132,22 @@ extern "C" {
 int w4_repack(const int32_t *qweight, const int32_t *perm, int32_t *b_packed, int32_t *status,
               int k, int n, cudaStream_t stream);
 
+/* Gate/up interleave for the gated FFN epilogue (W4A16_FLAG_SWIGLU / _GEGLU).
+ * transformer.rs, `encode_compressed_tensors_dense_swiglu` and the U4B8 GeGLU pipeline beside
+ * it: gate = A Wg and up = A Wu are two W4A16 GEMMs over the same A, then h = act(gate) * up
+ * feeds the down projection.  Here both run as one GEMM over a [K][2I] weight whose columns
+ * alternate in blocks of 16 -- destination column 32b + r is gate column 16b + r for r < 16
+ * and up column 16b + r - 16 for r >= 16 -- so each 128-column tile of the kernel holds 64
+ * features' gate and up sums side by side and its epilogue writes act(gate) * up.
+ * This permutes the columns of a row-major [rows][n2] array, n2 = 2I, from the planar order
+ * (the I gate columns, then the I up columns) into that order; apply it to the GPTQ words
+ * [K/8][2I] (elem_bytes 4) before w4_repack, and to the scales and zeros [G][2I]
+ * (elem_bytes 2).  For w4a16_gemm, I must be a multiple of 128 (so 2I % 256 == 0).
+ *   src, dst  device arrays of rows x n2 elements, not overlapping, aligned to elem_bytes
+ *   n2        a positive multiple of 32;  elem_bytes 2 or 4 */
+int w4_gate_up_interleave(const void *src, void *dst, int rows, int n2, int elem_bytes,
+                          cudaStream_t stream);
+
 /* Tile layout -> GPTQ words of the sorted rows (the inverse of w4_repack; a permutation
  * applied at repack time is not undone).  Same shape, alignment and overlap rules. */
 int w4_unpack(const int32_t *b_packed, int32_t *qweight, int k, int n, cudaStream_t stream);
@@ -157,7 +183,11 @@ size_t w4a16_workspace_size(int m, int n, int k, int group_size, unsigned flags,
  *   group_size -1 (one group) or a positive multiple of 16 dividing K
  *              (transformer.rs `marlin_num_groups`; marlin.rs Marlin-MoE validation)
  *   weight_type W4A16_TYPE_U4B8 (zeros NULL) or W4A16_TYPE_U4 (zeros and W4A16_FLAG_HAS_ZP)
- *   flags      W4A16_FLAG_*; ACT_ORDER exactly when g_idx and perm are given
+ *   flags      W4A16_FLAG_*; ACT_ORDER exactly when g_idx and perm are given.  With
+ *              W4A16_FLAG_SWIGLU or _GEGLU, N = 2I columns of interleaved gate/up weights
+ *              (w4_gate_up_interleave) and c receives H [M][ldc], ldc >= I, with
+ *              H[m][f] = act(gate[m][f]) * up[m][f] computed in fp32 from the fp32 sums and
+ *              rounded once to fp16
  * Kernel choice (unless a W4A16_FLAG_FORCE_* flag picks one): M <= 8 -- and M <= 32 while
  * N / 16 <= 2 x the SM count -- with group_size -1 or a multiple of 64 and N / 16 >= the SM
  * count runs the column-slice kernel (no split-K); the rest of M <= 32 the split-K
@@ -231,7 +261,10 @@ size_t w4a16_grouped_workspace_size(int n_pairs, int n_active, int n, int k, int
  *   ex_pairs      device int32 [n_pairs];   pair_tok device int32 [n_pairs]
  *   n_active      1..W4A16_MAX_SEGMENTS; n_experts bounds ex_ids
  * Act-order is not supported here (W4A16_FLAG_ACT_ORDER is rejected), and every call runs the
- * tcgen05 kernel (W4A16_FLAG_FORCE_SIMT, _FORCE_MMA and _FORCE_SLICE are rejected).
+ * tcgen05 kernel (W4A16_FLAG_FORCE_SIMT, _FORCE_MMA and _FORCE_SLICE are rejected).  With
+ * W4A16_FLAG_SWIGLU / _GEGLU the experts' weights are interleaved gate/up projections of
+ * N = 2I columns and y receives [n_pairs][ldy], ldy >= I, of act(gate) * up, as for
+ * w4a16_gemm.
  * Out-of-range schedule entries are skipped and reported as W4A16_DEV_SCHEDULE. */
 #define W4A16_MAX_SEGMENTS 1024
 int w4a16_gemm_grouped(const void *a, int lda, const int32_t *b_packed_stack, void *y, int ldy,

@@ -62,6 +62,9 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.orc_grouped.argtypes = [P, L, P, P, P, P, P, P, P, I, I, I, I, I, P, I]
     lib.orc_qzeros_to_zero_points.restype = I
     lib.orc_qzeros_to_zero_points.argtypes = [P, I, I, P]
+    lib.orc_act.restype = ctypes.c_double
+    lib.orc_act.argtypes = [ctypes.c_double, I]
+    lib.orc_glu.argtypes = [P, P, L, I, P]
     lib.orc_qzeros_symmetric_code7.restype = I
     lib.orc_qzeros_symmetric_code7.argtypes = [P, L]
     return lib
@@ -223,6 +226,25 @@ class Oracle:
                              _ptr(pairs), _ptr(pt), ids.size, k, n, group_size, weight_type,
                              _ptr(out), threads or default_threads())
         return out
+
+    def act(self, x: float, kind: int) -> float:
+        """silu (kind 1) or tanh-form gelu (kind 2) of one double."""
+        return float(self.lib.orc_act(float(x), kind))
+
+    def glu(self, gate, up, kind: int = 1) -> np.ndarray:
+        """h = act(gate) * up elementwise, in double (kind 1 SiLU, 2 GELU tanh form)."""
+        g, u = _c(gate, np.float64), _c(up, np.float64)
+        assert g.shape == u.shape
+        out = np.empty(g.shape, dtype=np.float64)
+        self.lib.orc_glu(_ptr(g), _ptr(u), g.size, kind, _ptr(out))
+        return out
+
+    def gemm_glu(self, a, qweight_gate, qweight_up, scales_gate, scales_up, zeros_gate=None,
+                 zeros_up=None, g_idx=None, group_size=128, weight_type=U4B8, kind: int = 1):
+        """h = act(A Wg) * (A Wu): the two GEMMs of the gated FFN, then the activation."""
+        gate = self.gemm(a, qweight_gate, scales_gate, zeros_gate, g_idx, group_size, weight_type)
+        up = self.gemm(a, qweight_up, scales_up, zeros_up, g_idx, group_size, weight_type)
+        return self.glu(gate, up, kind)
 
     def qzeros_to_zero_points(self, qzeros, groups, n):
         qz = _c(qzeros, np.int32)

@@ -25,6 +25,9 @@
  * brute force, library routines and the worked examples the pages print; none is
  * "parity unpinned".
  */
+#ifndef M_PI
+#define M_PI 3.14159265358979323846
+#endif
 #include <math.h>
 #include <pthread.h>
 #include <stdint.h>
@@ -455,6 +458,30 @@ void orc_grouped(const uint16_t *a, long lda, const int32_t *qweight_stack,
         free(a_seg);
         free(y_seg);
     }
+}
+
+/* ---------------------------------------------------------------------------------------
+ * Gated activations after the gate and up projections.  [transformer.rs]
+ * `encode_compressed_tensors_dense_swiglu`: gate = A Wg and up = A Wu are two W4A16 GEMMs,
+ * then the planar SiLU-multiply (`launch_planar_silu_mul`) gives h = silu(gate) * up, which the
+ * down projection consumes; the symmetric U4B8 GeGLU pipeline beside it uses the tanh form of
+ * GELU instead.  Textbook definitions, in double:
+ *   silu(x)      = x / (1 + exp(-x))                     (x times the logistic sigmoid)
+ *   gelu_tanh(x) = x/2 * (1 + tanh(sqrt(2/pi) * (x + 0.044715 x^3)))
+ * kind 1 = SiLU, 2 = GELU (tanh form).  h[i] = act(gate[i]) * up[i].
+ * ------------------------------------------------------------------------------------- */
+double orc_act(double x, int kind)
+{
+    if (kind == 1)
+        return x / (1.0 + exp(-x));
+    const double c = sqrt(2.0 / M_PI);
+    return 0.5 * x * (1.0 + tanh(c * (x + 0.044715 * x * x * x)));
+}
+
+void orc_glu(const double *gate, const double *up, long count, int kind, double *h)
+{
+    for (long i = 0; i < count; ++i)
+        h[i] = orc_act(gate[i], kind) * up[i];
 }
 
 /* ---------------------------------------------------------------------------------------

@@ -450,4 +450,80 @@ def pin_grouped_closed_form(orc):
     return None
 
 
+# --- gated activations (SwiGLU / GeGLU after the gate and up projections) -------------------
+
+_XS = [-30.0, -6.5, -2.0, -1.0, -0.25, 0.0, 0.125, 0.5, 1.0, 1.75, 3.0, 8.0, 30.0]
+
+
+def pin_silu_identities(orc):
+    """silu(x) = x * sigmoid(x): silu(0) = 0; silu(x) - silu(-x) = x (sigmoid(x) +
+    sigmoid(-x) = 1); the half-angle form x/2 (1 + tanh(x/2)) through another library
+    function; silu(x) -> x for large x and -> 0 for large -x."""
+    if orc.act(0.0, 1) != 0.0:
+        return "silu(0) != 0"
+    for x in _XS:
+        got = orc.act(x, 1)
+        if abs((got - orc.act(-x, 1)) - x) > 1e-12 * max(1.0, abs(x)):
+            return f"silu odd identity at {x}"
+        if abs(got - 0.5 * x * (1.0 + math.tanh(0.5 * x))) > 1e-13 * max(1.0, abs(x)):
+            return f"silu half-angle form at {x}"
+    if abs(orc.act(40.0, 1) - 40.0) > 1e-12 or abs(orc.act(-40.0, 1)) > 1e-12:
+        return "silu asymptotes"
+    return None
+
+
+def pin_gelu_tanh_identities(orc):
+    """The tanh form of GELU: gelu(0) = 0; gelu(x) - gelu(-x) = x; within 1e-3 of the exact
+    GELU x * Phi(x) (Phi through erf, another library routine) -- which also tells it from
+    SiLU (silu(1) = 0.73, gelu(1) = 0.84); gelu(x) -> x for large x."""
+    if orc.act(0.0, 2) != 0.0:
+        return "gelu(0) != 0"
+    for x in _XS:
+        got = orc.act(x, 2)
+        if abs((got - orc.act(-x, 2)) - x) > 1e-12 * max(1.0, abs(x)):
+            return f"gelu odd identity at {x}"
+        exact = x * 0.5 * (1.0 + math.erf(x / math.sqrt(2.0)))
+        if abs(got - exact) > 1e-3:
+            return f"gelu tanh form far from x Phi(x) at {x}: {got} vs {exact}"
+    if abs(orc.act(30.0, 2) - 30.0) > 1e-12:
+        return "gelu asymptote"
+    return None
+
+
+def pin_glu_gate_times_up(orc):
+    """h = act(gate) * up elementwise: up = 1 gives act(gate), up = 0 gives 0, and the gate
+    (not the up) operand goes through the activation."""
+    g = np.array([[-2.0, 0.5, 3.0], [1.0, -0.25, 6.0]])
+    u = np.array([[1.0, 1.0, 1.0], [0.0, 2.0, -3.0]])
+    for kind in (1, 2):
+        h = orc.glu(g, u, kind)
+        want = np.array([[orc.act(x, kind) * y for x, y in zip(gr, ur)] for gr, ur in zip(g, u)])
+        bad = _mismatch(f"glu kind {kind}", h, want, rtol=1e-15)
+        if bad:
+            return bad
+        if not np.allclose(h[0], [orc.act(x, kind) for x in g[0]], rtol=1e-15) or h[1, 0] != 0.0:
+            return f"glu kind {kind}: up = 1 / up = 0 rows"
+    if abs(orc.glu(np.array([3.0]), np.array([0.5]), 1)[0] - orc.act(3.0, 1) * 0.5) > 1e-15:
+        return "glu operand order"
+    return None
+
+
+def pin_gemm_glu_closed_form(orc):
+    """Codes all 9 (w = s): gate = s_g * rowsum(A), up = s_u * rowsum(A); with s_g = 1 and
+    s_u = 1/2 the gated FFN's h = act(rowsum) * rowsum / 2 for every column."""
+    m, k, n = 3, 256, 16
+    a = synth.activations(41, m, k)
+    qw = _codes_const(orc, k, n, 9)
+    s_g = np.ones((k // 128, n), dtype=np.float16)
+    s_u = np.full((k // 128, n), 0.5, dtype=np.float16)
+    rs = _rowsums(a)
+    for kind in (1, 2):
+        h = orc.gemm_glu(a, qw, qw, s_g, s_u, kind=kind)
+        want = np.array([[orc.act(r, kind) * r / 2] * n for r in rs])
+        bad = _mismatch(f"gemm_glu closed form kind {kind}", h, want, rtol=1e-12, atol=1e-12)
+        if bad:
+            return bad
+    return None
+
+
 ALL_PINS = [v for name, v in sorted(globals().items()) if name.startswith("pin_")]

@@ -97,6 +97,11 @@ def gemm_status(w4, **kw):
     (dict(flags=1 << 13, m=33), 2, 3),           # column-slice kernel: M <= 32 only
     (dict(flags=1 << 13, gs=32), 2, 3),          # ... and groups of whole 64-row blocks
     (dict(flags=1 << 11, m=65), 2, 3),           # split-K small-M kernel: M <= 64 only
+    (dict(flags=1 << 14 | 1 << 15), 1, 4),       # SWIGLU with GEGLU
+    (dict(flags=1 << 14 | 1 << 11), 1, 4),       # gated epilogue with a small-M kernel forced
+    (dict(flags=1 << 15 | 1 << 13), 1, 4),
+    (dict(flags=1 << 14 | 1 << 8), 1, 4),        # ... or the CUDA-core reference kernel
+    (dict(flags=1 << 14, ldc=120), 1, 3),        # gated output narrower than I = 128
 ])
 def test_gemm_rejects_bad_arguments_on_host(w4, kw, stage, detail):
     st = gemm_status(w4, **kw)
@@ -270,3 +275,19 @@ def test_qzeros_every_code_and_column(w4):
 def test_kernel_choice(w4, m, n, gs, flags, want):
     """The documented dispatch rule, for a 152-SM part (host only)."""
     assert w4.w4a16_kernel_for(m, n, 4096, gs, flags, 152) == want
+
+
+def test_gated_calls_run_the_tcgen05_kernel(w4):
+    for m in (1, 16, 4096):
+        assert w4.w4a16_kernel_for(m, 4096, 4096, 128, w4.W4A16_FLAG_SWIGLU, 152) == 0
+        assert w4.w4a16_kernel_for(m, 4096, 4096, 128, w4.W4A16_FLAG_GEGLU, 152) == 0
+    assert w4.w4a16_kernel_for(1, 4096, 4096, 128, w4.W4A16_FLAG_SWIGLU | w4.W4A16_FLAG_GEGLU, 152) == -1
+
+
+def test_gate_up_interleave_rejects_bad_arguments(w4):
+    f = w4._lib.w4_gate_up_interleave
+    assert f(0x1000, 0x9000, 2, 48, 4, 0) == (1 << 16 | 3)       # n2 not a multiple of 32
+    assert f(0x1000, 0x9000, 2, 64, 8, 0) == (1 << 16 | 3)       # element size
+    assert f(None, 0x9000, 2, 64, 4, 0) == (1 << 16 | 1)
+    assert f(0x1002, 0x9000, 2, 64, 4, 0) == (1 << 16 | 2)       # misaligned int32 source
+    assert f(0x1000, 0x1010, 2, 64, 4, 0) == (1 << 16 | 4)       # overlapping

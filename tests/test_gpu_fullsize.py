@@ -171,3 +171,69 @@ def test_full_oracle_every_element(w4, orc, workload):
         assert ok, f"{what}: {msg}"
         del g
         torch.cuda.empty_cache()
+
+
+def test_full_size_moe_swiglu_chain(w4, orc):
+    """The chained MoE FFN of bench.py's moe_swiglu workload: gate_up with the SwiGLU epilogue
+    writes H, the down projection reads H.  H is checked against the oracle's silu(gate) * up
+    (the gated tolerance of test_gpu_glu), and the down output against the oracle's GEMM of the
+    GPU's own H rows, on all pairs of the first and last expert and the first and last pair of
+    every other.
+
+    The down GEMM's input rows are not N(0, 1) like the configurations' A (H has an rms of about
+    8 here).  The GEMM is linear in A and every rounding in it is relative to A's scale (the
+    weights' fp16 products (q - z) s do not depend on A; the MMA products are exact), so the bar
+    1e-2 + 1e-2 |ref| that holds for rows of rms 1 holds for A / r, i.e. 1e-2 r + 1e-2 |ref|
+    for a row of rms r: that is the bar used here, with r = max(1, rms of the H row)."""
+    import torch
+    from test_gpu_glu import glu_check
+    specs = [dict(s) for s in bench.workload_specs("moe_swiglu")]
+    g0 = bench.GroupedGemm(w4, specs[0], 1, torch.device("cuda"))
+    g1 = bench.GroupedGemm(w4, specs[1], 1, torch.device("cuda"))
+    g1.a = g0.c
+    g0.run(0)
+    g1.run(0)
+    torch.cuda.synchronize()
+    assert w4.w4a16_status(g0.ws) == 0 and w4.w4a16_status(g1.ws) == 0
+    s0 = specs[0]
+    k, n2, gs, n_exp = s0["k"], s0["n"], s0["gs"], s0["n_exp"]
+    i = n2 // 2
+    groups = synth.group_count(k, gs)
+    sel = synth.routes(5000, s0["n_tok"], n_exp, s0["top_k"])
+    ids, off, pairs, tok = orc.csr_from_token_routes(n_exp, s0["n_tok"], s0["top_k"], sel)
+    a_all = synth.activations(s0["seed"], s0["n_tok"], k)
+    scales = synth.scales(s0["seed"], n_exp * groups, n2).reshape(n_exp, groups, n2)
+    h_gpu = g0.c.float().cpu().numpy().astype(np.float64)
+    picked = []
+    for j, e in enumerate(ids):
+        seg = [int(p) for p in pairs[off[j]:off[j + 1]]]
+        if j not in (0, len(ids) - 1):
+            seg = [seg[0], seg[-1]]
+        picked += seg
+        qw = synth.qweight(s0["seed"] * 100 + int(e), k, n2)
+        rows = np.ascontiguousarray(a_all[tok[seg]])
+        gate = orc.gemm(rows, np.ascontiguousarray(qw[:, :i]), np.ascontiguousarray(scales[e][:, :i]),
+                        None, None, gs, s0["wt"])
+        up = orc.gemm(rows, np.ascontiguousarray(qw[:, i:]), np.ascontiguousarray(scales[e][:, i:]),
+                      None, None, gs, s0["wt"])
+        glu_check(orc, h_gpu[seg], gate, up, 1)
+    # down: y[p] = H[p] x dequant(B_down of p's expert), with the GPU's H as the input.
+    s1 = specs[1]
+    k1, n1 = s1["k"], s1["n"]
+    groups1 = synth.group_count(k1, gs)
+    scales1 = synth.scales(s1["seed"], n_exp * groups1, n1).reshape(n_exp, groups1, n1)
+    h16 = g0.c.cpu().numpy()
+    y = g1.c.float().cpu().numpy().astype(np.float64)
+    for j, e in enumerate(ids):
+        seg = [p for p in picked if p in set(int(x) for x in pairs[off[j]:off[j + 1]])]
+        qw1 = synth.qweight(s1["seed"] * 100 + int(e), k1, n1)
+        rows = np.ascontiguousarray(h16[seg])
+        ref = orc.gemm(rows, qw1, scales1[e], None, None, gs, s1["wt"])
+        r = np.maximum(1.0, np.sqrt(np.mean(rows.astype(np.float64) ** 2, axis=1)))[:, None]
+        err = np.abs(y[seg] - ref)
+        bound = 1e-2 * r + 1e-2 * np.abs(ref)
+        assert np.all(np.isfinite(y[seg]))
+        assert np.all(err <= bound), (f"down, expert {e}: {int((err > bound).sum())} outside, "
+                                      f"max err/bound {float((err / bound).max()):.3f}")
+        print(f"down expert {e}: max err {err.max():.3e}, max err/bound {(err / bound).max():.3f}, "
+              f"row rms {float(r.min()):.2f}..{float(r.max()):.2f}")

@@ -46,6 +46,9 @@ MUTATIONS = [
      "zero_points[(long)g * n + col] = (double)raw;"),
     ("group count ignores divisibility", "group_size % 16 != 0 || k % group_size != 0",
      "group_size % 16 != 0"),
+    ("silu sign of exp", "return x / (1.0 + exp(-x));", "return x / (1.0 + exp(x));"),
+    ("gelu cubic constant", "(x + 0.044715 * x * x * x)", "(x + 0.44715 * x * x * x)"),
+    ("glu operands swapped", "h[i] = orc_act(gate[i], kind) * up[i];", "h[i] = orc_act(up[i], kind) * gate[i];"),
     ("by-groups scale dropped", "c[(long)i * n + j] += orc_half_to_double(scales[(long)g * n + j]) * t[j];",
      "c[(long)i * n + j] += t[j];"),
 ]

@@ -27,6 +27,8 @@ W4A16_FLAG_FORCE_TC = 1 << 10
 W4A16_FLAG_FORCE_MMA = 1 << 11
 W4A16_FLAG_FORCE_SLICE = 1 << 13
 W4A16_FLAG_STATIC_WEIGHTS = 1 << 12
+W4A16_FLAG_SWIGLU = 1 << 14
+W4A16_FLAG_GEGLU = 1 << 15
 
 W4A16_DEV_TIMEOUT = 1
 W4A16_DEV_PERM = 2
@@ -68,6 +70,7 @@ _SIGNATURES = {
     "w4_qzeros_symmetric_code7": (_I, [_P, _LL]),
     "w4a16_zero_points_check": (_I, [_P, _LL, _P, _P]),
     "w4a16_kernel_for": (_I, [_I, _I, _I, _I, _U, _I]),
+    "w4_gate_up_interleave": (_I, [_P, _P, _I, _I, _I, _P]),
 }
 for _name, (_res, _args) in _SIGNATURES.items():
     _fn = getattr(_lib, _name)
@@ -129,6 +132,13 @@ def w4_repack(qweight, perm, b_packed, k: int, n: int, status=None, stream=None)
                                        k, n, _stream(stream)))
 
 
+def w4_gate_up_interleave(src, dst, rows: int, n2: int, stream=None) -> None:
+    """Planar [rows, 2I] gate|up columns -> blocks of 16 gate / 16 up columns (device tensors of
+    int32 GPTQ words or fp16 scales / zeros), for W4A16_FLAG_SWIGLU / _GEGLU."""
+    _check("w4_gate_up_interleave", _lib.w4_gate_up_interleave(
+        _ptr(src), _ptr(dst), rows, n2, src.element_size(), _stream(stream)))
+
+
 def w4_unpack(b_packed, qweight, k: int, n: int, stream=None) -> None:
     """Tile layout -> GPTQ int32 [K/8, N] of the sorted rows."""
     _check("w4_unpack", _lib.w4_unpack(_ptr(b_packed), _ptr(qweight), k, n, _stream(stream)))
@@ -159,7 +169,7 @@ def w4a16_gemm(a, b_packed, c, scales, zeros, g_idx, perm, workspace, m: int, n:
     if lda is None:
         lda = k
     if ldc is None:
-        ldc = n
+        ldc = n // 2 if flags & (W4A16_FLAG_SWIGLU | W4A16_FLAG_GEGLU) else n
     if workspace_bytes is None:
         workspace_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check("w4a16_gemm", _lib.w4a16_gemm(
@@ -177,7 +187,7 @@ def w4a16_gemm_noalloc(a, b_packed, c, scales, zeros, g_idx, perm, m: int, n: in
     if lda is None:
         lda = k
     if ldc is None:
-        ldc = n
+        ldc = n // 2 if flags & (W4A16_FLAG_SWIGLU | W4A16_FLAG_GEGLU) else n
     _check("w4a16_gemm_noalloc", _lib.w4a16_gemm_noalloc(
         _ptr(a), lda, _ptr(b_packed), _ptr(c), ldc, _ptr(scales), _ptr(zeros), _ptr(g_idx),
         _ptr(perm), _ptr(status_out), m, n, k, group_size, weight_type, flags, _stream(stream)))
@@ -192,7 +202,7 @@ def w4a16_gemm_grouped(a, b_packed_stack, y, scales_stack, zeros_stack, ex_ids, 
     if lda is None:
         lda = k
     if ldy is None:
-        ldy = n
+        ldy = n // 2 if flags & (W4A16_FLAG_SWIGLU | W4A16_FLAG_GEGLU) else n
     if workspace_bytes is None:
         workspace_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check("w4a16_gemm_grouped", _lib.w4a16_gemm_grouped(

@@ -439,12 +439,25 @@ bool slice_default()
     return v != 0;
 }
 
+// Gated-activation epilogue selected by the flags: 0 none, 1 SwiGLU, 2 GeGLU (tanh form), -1
+// both (rejected).
+int glu_kind(unsigned flags)
+{
+    const bool sw = (flags & W4A16_FLAG_SWIGLU) != 0, ge = (flags & W4A16_FLAG_GEGLU) != 0;
+    return sw && ge ? -1 : sw ? 1 : ge ? 2 : 0;
+}
+
 // Kernel flags of a dense call, checked before anything touches the device: 0, or the status
 // of flags that conflict or force a small-M kernel beyond what it takes.  The column-slice
 // kernel needs M <= 32 and groups of whole 64-row blocks (`gs` resolved: K for one group); the
 // split-K small-M kernel M <= 64.
 int check_kernel_flags(int m, int gs, unsigned flags)
 {
+    // The gated epilogue lives in the tcgen05 kernel (and its split-tile reduction) only.
+    const int glu = glu_kind(flags);
+    if (glu < 0 || (glu > 0 && (flags & (W4A16_FLAG_FORCE_SIMT | W4A16_FLAG_FORCE_MMA |
+                                         W4A16_FLAG_FORCE_SLICE))))
+        return status_of(STAGE_ARG, W4A16_ARG_FLAGS);
     const unsigned other = W4A16_FLAG_FORCE_TC | W4A16_FLAG_A_SMEM | W4A16_FLAG_FORCE_SIMT;
     if (flags & W4A16_FLAG_FORCE_SLICE) {
         if (flags & (other | W4A16_FLAG_FORCE_MMA))
@@ -472,7 +485,8 @@ int choose_kernel(int m, int n, int gs, unsigned flags, int num_sms)
         return 2;
     if (flags & W4A16_FLAG_FORCE_MMA)
         return 1;
-    if (flags & (W4A16_FLAG_FORCE_TC | W4A16_FLAG_A_SMEM | W4A16_FLAG_FORCE_SIMT))
+    if (flags & (W4A16_FLAG_FORCE_TC | W4A16_FLAG_A_SMEM | W4A16_FLAG_FORCE_SIMT |
+                 W4A16_FLAG_SWIGLU | W4A16_FLAG_GEGLU))
         return 0;
     // 9..32 tokens (two or four 8-token tiles, a shallower ring) only while each CTA gets one
     // slice: at N=12288 (3 slices per CTA) the split-K kernel is faster at M=16.
@@ -635,7 +649,10 @@ int dense_gemm(const void *a, int lda, const int32_t *b_packed, void *c, int ldc
         return 0; // empty input: nothing to compute
     if (!a || !c || !workspace)
         return status_of(STAGE_ARG, W4A16_ARG_NULL);
-    if (lda < k || ldc < n)
+    const int glu = glu_kind(flags);
+    if (glu < 0)
+        return status_of(STAGE_ARG, W4A16_ARG_FLAGS);
+    if (lda < k || ldc < (glu > 0 ? n / 2 : n))
         return status_of(STAGE_ARG, W4A16_ARG_SHAPE);
     if (lda % 8 != 0 || ldc % 8 != 0 || !aligned(a, 16) || !aligned(c, 16) ||
         !aligned(workspace, 256) || (g_idx && !aligned(g_idx, 4)) || (perm && !aligned(perm, 4)))
@@ -674,6 +691,7 @@ int dense_gemm(const void *a, int lda, const int32_t *b_packed, void *c, int ldc
     p.c = static_cast<__half *>(c);
     p.ldc = ldc;
     p.static_weights = (flags & W4A16_FLAG_STATIC_WEIGHTS) ? 1 : 0;
+    p.glu = glu;
     // Tile order: walk token tiles outermost when the activations outweigh the weights and
     // would not stay in L2 while every column tile passes over them (e.g. M=4096, K=11008:
     // 90 MB of A, read 4.6 times from DRAM column-tile-major).
@@ -765,6 +783,25 @@ int w4_repack(const int32_t *qweight, const int32_t *perm, int32_t *b_packed, in
     return launch_status(launch_repack(qweight, perm, b_packed, status, k, n, stream));
 }
 
+int w4_gate_up_interleave(const void *src, void *dst, int rows, int n2, int elem_bytes,
+                          cudaStream_t stream)
+{
+    if (rows <= 0 || n2 <= 0 || n2 % 32 != 0 || (elem_bytes != 2 && elem_bytes != 4))
+        return status_of(STAGE_ARG, W4A16_ARG_SHAPE);
+    if (!src || !dst)
+        return status_of(STAGE_ARG, W4A16_ARG_NULL);
+    if (!aligned(src, elem_bytes) || !aligned(dst, elem_bytes))
+        return status_of(STAGE_ARG, W4A16_ARG_ALIGN);
+    const long long bytes = (long long)rows * n2 * elem_bytes;
+    if (bytes > (1LL << 40))
+        return status_of(STAGE_ARG, W4A16_ARG_OVERFLOW);
+    const char *sa = static_cast<const char *>(src);
+    const char *da = static_cast<const char *>(dst);
+    if (sa < da + bytes && da < sa + bytes)
+        return status_of(STAGE_ARG, W4A16_ARG_FLAGS);
+    return launch_status(launch_gate_up_interleave(src, dst, rows, n2, elem_bytes, stream));
+}
+
 int w4_unpack(const int32_t *b_packed, int32_t *qweight, int k, int n, cudaStream_t stream)
 {
     if (k <= 0 || n <= 0)
@@ -836,12 +873,15 @@ int w4a16_gemm_grouped(const void *a, int lda, const int32_t *b_packed_stack, vo
     if (flags & (W4A16_FLAG_ACT_ORDER | W4A16_FLAG_FORCE_SIMT | W4A16_FLAG_FORCE_MMA |
                  W4A16_FLAG_FORCE_SLICE))
         return status_of(STAGE_ARG, W4A16_ARG_FLAGS);
+    const int glu = glu_kind(flags);
+    if (glu < 0)
+        return status_of(STAGE_ARG, W4A16_ARG_FLAGS);
     if (n_active <= 0 || n_active > W4A16_MAX_SEGMENTS || n_experts <= 0 || n_pairs <= 0 ||
         n_tokens <= 0 || n_active > n_experts)
         return status_of(STAGE_ARG, W4A16_ARG_SCHEDULE);
     if (!a || !y || !workspace || !ex_ids || !ex_off || !ex_pairs || !pair_tok)
         return status_of(STAGE_ARG, W4A16_ARG_NULL);
-    if (lda < k || ldy < n)
+    if (lda < k || ldy < (glu > 0 ? n / 2 : n))
         return status_of(STAGE_ARG, W4A16_ARG_SHAPE);
     if (lda % 8 != 0 || ldy % 8 != 0 || !aligned(a, 16) || !aligned(y, 16) ||
         !aligned(workspace, 256) || !aligned(ex_ids, 4) || !aligned(ex_off, 4) ||
@@ -874,6 +914,7 @@ int w4a16_gemm_grouped(const void *a, int lda, const int32_t *b_packed_stack, vo
     p.zeros = static_cast<const __half *>(zeros_stack);
     p.c = static_cast<__half *>(y);
     p.ldc = ldy;
+    p.glu = glu;
     p.status = reinterpret_cast<int *>(ws);
     p.counters = reinterpret_cast<int *>(ws + pl.counters_off);
     p.partials = reinterpret_cast<float *>(ws + pl.partials_off);

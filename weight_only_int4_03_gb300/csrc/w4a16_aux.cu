@@ -137,6 +137,24 @@ __global__ void gather_rows_kernel(const __half *__restrict__ a, int lda,
         dst[i] = src[i];
 }
 
+// Gate/up interleave of a row-major [rows][2I] array: destination column j takes source
+// column 16b + r (gate) for j = 32b + r, r < 16, and I + 16b + r - 16 (up) for r >= 16.
+template <typename T>
+__global__ void gate_up_interleave_kernel(const T *__restrict__ src, T *__restrict__ dst, int rows,
+                                          int n2)
+{
+    const int half_n = n2 / 2;
+    const long long total = (long long)rows * n2;
+    for (long long o = blockIdx.x * (long long)blockDim.x + threadIdx.x; o < total;
+         o += (long long)gridDim.x * blockDim.x) {
+        const long long row = o / n2;
+        const int j = (int)(o - row * n2);
+        const int b = j >> 5, r = j & 31;
+        const int from = r < 16 ? 16 * b + r : half_n + 16 * b + r - 16;
+        dst[o] = src[row * n2 + from];
+    }
+}
+
 // CUDA-core reference GEMM: one thread per output, fp32 accumulation in k order, weights
 // dequantised with the same fp16 arithmetic as the tensor-core path ((q - z) exact, then one
 // rounding of the product with the scale).
@@ -222,6 +240,19 @@ int launch_gather_rows(const __half *a, int lda, const int32_t *ex_pairs, const 
 {
     gather_rows_kernel<<<n_pairs, 128, 0, stream>>>(a, lda, ex_pairs, pair_tok, out, n_pairs,
                                                     n_tokens, k, status);
+    return cudaGetLastError();
+}
+
+int launch_gate_up_interleave(const void *src, void *dst, int rows, int n2, int elem_bytes,
+                              cudaStream_t stream)
+{
+    const long long total = (long long)rows * n2;
+    if (elem_bytes == 4)
+        gate_up_interleave_kernel<int32_t><<<grid_for(total, 256), 256, 0, stream>>>(
+            static_cast<const int32_t *>(src), static_cast<int32_t *>(dst), rows, n2);
+    else
+        gate_up_interleave_kernel<uint16_t><<<grid_for(total, 256), 256, 0, stream>>>(
+            static_cast<const uint16_t *>(src), static_cast<uint16_t *>(dst), rows, n2);
     return cudaGetLastError();
 }
 

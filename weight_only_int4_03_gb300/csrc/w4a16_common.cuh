@@ -536,6 +536,59 @@ __device__ __forceinline__ const float4 *partial_quads(const GemmParams &p, cons
     return reinterpret_cast<const float4 *>(partial_slot(p, c, c == cb.lo ? cb.lo_slot : 0));
 }
 
+// ---------------------------------------------------------------------------------------
+// Gated activation epilogue (W4A16_FLAG_SWIGLU / _GEGLU).  The weight's columns are gate and up
+// projections interleaved in blocks of 16: packed columns 32b .. 32b+15 are gate features
+// 16b .. 16b+15 and packed columns 32b+16 .. 32b+31 the up features of the same indices, so a
+// 128-column tile holds features n0/2 .. n0/2 + 63 and writes act(gate) * up there.
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ float glu_act(float g, int kind)
+{
+    if (kind == 1)
+        return g / (1.0f + expf(-g)); // silu: g * sigmoid(g)
+    const float c = 0.7978845608028654f; // sqrt(2 / pi)
+    return 0.5f * g * (1.0f + tanhf(c * (g + 0.044715f * g * g * g)));
+}
+
+// Split tile of a gated call: items are (row, gate quad); each sums its gate quad and the up
+// quad 16 columns on over the contributors in index order, then writes 4 features.
+static __device__ void reduce_tile_glu(const GemmParams &p, const TileInfo &ti, const Contributors &cb,
+                                       int tid, int nthreads)
+{
+    constexpr int QUADS = TILE_N / 4;
+    constexpr int OUTQ = TILE_N / 8; // 16 gate quads per row
+    const int items = ti.rows * OUTQ;
+    for (int item = tid; item < items; item += nthreads) {
+        const int row = item / OUTQ, gq = item - (item / OUTQ) * OUTQ;
+        const int qg = row * QUADS + (gq >> 2) * 8 + (gq & 3);
+        float4 g = make_float4(0.f, 0.f, 0.f, 0.f), u = g;
+        for (int c0 = cb.lo; c0 <= cb.hi; c0 += 4) {
+            float4 vg[4], vu[4];
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+                const bool ok = c0 + x <= cb.hi;
+                const float4 *src = partial_quads(p, cb, ok ? c0 + x : cb.lo);
+                vg[x] = ok ? __ldcg(src + qg) : make_float4(0.f, 0.f, 0.f, 0.f);
+                vu[x] = ok ? __ldcg(src + qg + 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+                g.x += vg[x].x; g.y += vg[x].y; g.z += vg[x].z; g.w += vg[x].w;
+                u.x += vu[x].x; u.y += vu[x].y; u.z += vu[x].z; u.w += vu[x].w;
+            }
+        }
+        const int out_row = output_row(p, ti, row);
+        if (out_row < 0)
+            continue;
+        const __half2 lo = __floats2half2_rn(glu_act(g.x, p.glu) * u.x, glu_act(g.y, p.glu) * u.y);
+        const __half2 hi = __floats2half2_rn(glu_act(g.z, p.glu) * u.z, glu_act(g.w, p.glu) * u.w);
+        uint2 packed;
+        packed.x = *reinterpret_cast<const uint32_t *>(&lo);
+        packed.y = *reinterpret_cast<const uint32_t *>(&hi);
+        *reinterpret_cast<uint2 *>(p.c + (long long)out_row * p.ldc + ti.n0 / 2 + 4 * gq) = packed;
+    }
+}
+
 template <int RB = 4>
 static __device__ void reduce_tile(const GemmParams &p, const TileInfo &ti, const Contributors &cb,
                                    int tid, int nthreads)

@@ -245,7 +245,33 @@ __device__ void run_epilogue(const GemmParams &p, const SegTable &seg, Sched sch
             if (c0 + 16 < ti.ntok)
                 tmem_ld16(taddr + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
             tmem_ld_wait();
-            if (whole) {
+            if (whole && p.glu) {
+                // Lanes 0..15 hold gate features n0/2 + 16q + lane, lanes 16..31 the up values
+                // of the same features: 32 rows x 16 features through the staging buffer.
+#pragma unroll
+                for (int j = 0; j < EPI_ROWS; ++j) {
+                    const float g = __uint_as_float(v[j]);
+                    const float u = __shfl_down_sync(0xffffffffu, g, 16);
+                    if (lane < 16)
+                        stg[j * 16 + lane] = __float2half_rn(glu_act(g, p.glu) * u);
+                }
+                __syncwarp();
+#pragma unroll
+                for (int i = 0; i < EPI_ROWS / 16; ++i) {
+                    const int r = i * 16 + (lane >> 1);
+                    const int cseg = (lane & 1) * 8;
+                    const uint4 val = *reinterpret_cast<const uint4 *>(stg + r * 16 + cseg);
+                    const int row = c0 + r;
+                    if (row < ti.rows) {
+                        const int out_row = output_row(p, ti, row);
+                        if (out_row >= 0)
+                            __stcs(reinterpret_cast<uint4 *>(p.c + (long long)out_row * p.ldc +
+                                                             ti.n0 / 2 + q * 16 + cseg),
+                                   val);
+                    }
+                }
+                __syncwarp();
+            } else if (whole) {
 #pragma unroll
                 for (int j = 0; j < EPI_ROWS; ++j)
                     stg[j * 32 + lane] = __float2half_rn(__uint_as_float(v[j]));
@@ -396,7 +422,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int tile = split_tiles_sh[i];
         const TileInfo ti = tile_info(p, seg, tile);
         const Contributors cb = contributors(p, sched, (long long)tile - sched.dp_tiles);
-        reduce_tile<4>(p, ti, cb, threadIdx.x, NUM_THREADS);
+        if (p.glu)
+            reduce_tile_glu(p, ti, cb, threadIdx.x, NUM_THREADS);
+        else
+            reduce_tile<4>(p, ti, cb, threadIdx.x, NUM_THREADS);
         if (threadIdx.x == 0)
             p.counters[tile] = 0;
     }

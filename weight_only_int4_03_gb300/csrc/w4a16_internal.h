@@ -76,6 +76,8 @@ struct GemmParams {
     int split;                // > 0: tile-aligned split schedule (grid = tiles * split)
     int m_outer;              // dense: tile index runs token-tile-major
     int n_slices, slice_per;  // column-slice kernel: N / 16 slices, consecutive slices per CTA
+    int glu;                  // 0: C = the product; 1 / 2: C[., f] = silu / gelu_tanh(gate) * up
+                              // over gate/up columns interleaved in 16-column blocks
     // grouped schedule (null ex_off = dense)
     const int *ex_off;
     const int *ex_ids;
@@ -109,6 +111,8 @@ int launch_gather_rows(const __half *a, int lda, const int32_t *ex_pairs, const 
                        __half *out, int n_pairs, int n_tokens, int k, int *status,
                        cudaStream_t stream);
 int launch_selftest_timeout(int *status, unsigned long long limit_ns, cudaStream_t stream);
+int launch_gate_up_interleave(const void *src, void *dst, int rows, int n2, int elem_bytes,
+                              cudaStream_t stream);
 int gemm_smem_limit(int *bytes);
 
 // Dynamic shared memory the kernels need beyond the stages.
