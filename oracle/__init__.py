@@ -62,6 +62,10 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.orc_grouped.argtypes = [P, L, P, P, P, P, P, P, P, I, I, I, I, I, P, I]
     lib.orc_qzeros_to_zero_points.restype = I
     lib.orc_qzeros_to_zero_points.argtypes = [P, I, I, P]
+    lib.orc_moe_align_block_size.restype = I
+    lib.orc_moe_align_block_size.argtypes = [P, I, I, I, I, I, P, P]
+    lib.orc_moe_blocks.restype = I
+    lib.orc_moe_blocks.argtypes = [P, L, P, P, P, P, P, I, P, I, I, I, I, I, I, I, I, I, P, I]
     lib.orc_act.restype = ctypes.c_double
     lib.orc_act.argtypes = [ctypes.c_double, I]
     lib.orc_glu.argtypes = [P, P, L, I, P]
@@ -226,6 +230,36 @@ class Oracle:
                              _ptr(pairs), _ptr(pt), ids.size, k, n, group_size, weight_type,
                              _ptr(out), threads or default_threads())
         return out
+
+    def moe_align_block_size(self, topk_ids, m, top_k, n_experts, block_size, capacity=None):
+        """(sorted_ids, expert_ids, num_tokens_past_padded) of the vLLM routing, or None."""
+        ids = _c(topk_ids, np.int32)
+        if capacity is None:
+            capacity = m * top_k + n_experts * (block_size - 1)
+        sorted_ids = np.full(max(capacity, 1), -7, np.int32)
+        expert_ids = np.full(max(capacity // block_size, 1), -7, np.int32)
+        r = self.lib.orc_moe_align_block_size(_ptr(ids), m, top_k, n_experts, block_size, capacity,
+                                              _ptr(sorted_ids), _ptr(expert_ids))
+        if r < 0:
+            return None
+        return sorted_ids[:r].copy(), expert_ids[:r // block_size].copy(), r
+
+    def moe_blocks(self, a, qweight_stack, scales_stack, zeros_stack, sorted_ids, expert_ids,
+                   padded, topk_weights, block_size, top_k, is_ep, n_experts, k, n,
+                   group_size=128, weight_type=U4B8, threads: int | None = None):
+        """c [m*top_k][n] in double (NaN in rows no entry names), or None on bad expert ids."""
+        a = _h(a)
+        m = a.shape[0]
+        qw = _c(qweight_stack, np.int32)
+        s, z = _h(scales_stack), _h(zeros_stack)
+        sid, eid = _c(sorted_ids, np.int32), _c(expert_ids, np.int32)
+        tw = _c(topk_weights, np.float32)
+        out = np.full((m * top_k, n), np.nan)
+        r = self.lib.orc_moe_blocks(_ptr(a), a.shape[1], _ptr(qw), _ptr(s), _ptr(z), _ptr(sid),
+                                    _ptr(eid), padded, _ptr(tw), block_size, top_k, int(is_ep),
+                                    n_experts, m, k, n, group_size, weight_type, _ptr(out),
+                                    threads or default_threads())
+        return None if r != 0 else out
 
     def act(self, x: float, kind: int) -> float:
         """silu (kind 1) or tanh-form gelu (kind 2) of one double."""

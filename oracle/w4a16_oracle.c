@@ -461,6 +461,93 @@ void orc_grouped(const uint16_t *a, long lda, const int32_t *qweight_stack,
 }
 
 /* ---------------------------------------------------------------------------------------
+ * The vLLM Marlin-MoE routing.  [marlin.rs] `ferrum_vllm_marlin_moe_f16` declaration and
+ * `marlin_gemm_moe_vllm` doc: the caller first runs `moe_align_block_size`, which lists, for
+ * each expert in turn, the flattened (token, slot) ids routed to it -- id = token * top_k + slot
+ * -- padded to a multiple of moe_block_size with the sentinel prob_m * top_k; expert_ids gives
+ * the expert of every block of moe_block_size rows and num_tokens_past_padded the padded
+ * length.  The launch then computes, for every non-sentinel row r of block b,
+ *     c[id][:] = A[id / top_k][:] @ dequant(B_{expert_ids[b]})  (times topk_weights[id] when
+ *     mul_topk_weights is set),
+ * and leaves c's other rows alone; with is_ep, a block whose expert id is -1 (an expert another
+ * rank holds) is skipped.  The page test that runs it puts a batch's tokens in the prefix of
+ * one block and fills the rest with the sentinel.
+ *
+ * moe_align_block_size as read here: experts in increasing order; inside an expert its ids in
+ * increasing order; experts with no ids get no block.  Writes at most `capacity` entries;
+ * returns num_tokens_past_padded, or -1 on an expert id out of range or a too small capacity.
+ * ------------------------------------------------------------------------------------- */
+int orc_moe_align_block_size(const int32_t *topk_ids, int m, int top_k, int n_experts,
+                             int block_size, int capacity, int32_t *sorted_ids,
+                             int32_t *expert_ids)
+{
+    int n_ids = m * top_k;
+    for (int i = 0; i < n_ids; ++i)
+        if (topk_ids[i] < 0 || topk_ids[i] >= n_experts)
+            return -1;
+    int len = 0;
+    for (int e = 0; e < n_experts; ++e) {
+        int count = 0;
+        for (int i = 0; i < n_ids; ++i)
+            if (topk_ids[i] == e) {
+                if (len + count >= capacity)
+                    return -1;
+                sorted_ids[len + count] = i;
+                ++count;
+            }
+        if (count == 0)
+            continue;
+        int padded = (count + block_size - 1) / block_size * block_size;
+        if (len + padded > capacity)
+            return -1;
+        for (int r = count; r < padded; ++r)
+            sorted_ids[len + r] = n_ids; /* the sentinel */
+        for (int b = 0; b < padded / block_size; ++b)
+            expert_ids[len / block_size + b] = e;
+        len += padded;
+    }
+    return len;
+}
+
+/* The launch's result in double: c [m * top_k][n], rows that no non-sentinel entry names are
+ * not written.  Returns 0, or -1 on an expert id out of range (or -1 without is_ep). */
+int orc_moe_blocks(const uint16_t *a, long lda, const int32_t *qweight_stack,
+                   const uint16_t *scales_stack, const uint16_t *zeros_stack,
+                   const int32_t *sorted_ids, const int32_t *expert_ids, int padded,
+                   const float *topk_weights, int block_size, int top_k, int is_ep,
+                   int n_experts, int m, int k, int n, int group_size, int weight_type, double *c,
+                   int nthreads)
+{
+    int groups = orc_group_count(k, group_size);
+    long words_per_expert = (long)(k / 8) * n;
+    long scales_per_expert = (long)groups * n;
+    double *row = (double *)malloc(sizeof(double) * (size_t)n);
+    for (int b = 0; b < padded / block_size; ++b) {
+        int e = expert_ids[b];
+        if (e == -1 && is_ep)
+            continue;
+        if (e < 0 || e >= n_experts) {
+            free(row);
+            return -1;
+        }
+        for (int r = b * block_size; r < (b + 1) * block_size; ++r) {
+            int id = sorted_ids[r];
+            if (id < 0 || id >= m * top_k)
+                continue; /* sentinel (or padding beyond the ids) */
+            orc_gemm(a + (long)(id / top_k) * lda, lda, 1, qweight_stack + (long)e * words_per_expert,
+                     scales_stack + (long)e * scales_per_expert,
+                     zeros_stack ? zeros_stack + (long)e * scales_per_expert : NULL, NULL, k, n,
+                     group_size, weight_type, row, nthreads);
+            double w = topk_weights ? (double)topk_weights[id] : 1.0;
+            for (int j = 0; j < n; ++j)
+                c[(long)id * n + j] = row[j] * w;
+        }
+    }
+    free(row);
+    return 0;
+}
+
+/* ---------------------------------------------------------------------------------------
  * Gated activations after the gate and up projections.  [transformer.rs]
  * `encode_compressed_tensors_dense_swiglu`: gate = A Wg and up = A Wu are two W4A16 GEMMs,
  * then the planar SiLU-multiply (`launch_planar_silu_mul`) gives h = silu(gate) * up, which the

@@ -450,6 +450,80 @@ def pin_grouped_closed_form(orc):
     return None
 
 
+# --- vLLM Marlin-MoE routing (sorted_token_ids / expert_ids / sentinel rows) ------------------
+
+def pin_moe_align_examples(orc):
+    """The page's one-block example (batch prefix, sentinel prob_m * top_k after it) and a
+    hand-worked top-2 routing."""
+    g = _golden("moe_align_examples.json")
+    ex = g["page_example"]
+    got = orc.moe_align_block_size(np.zeros(ex["batch"], np.int32), ex["batch"], ex["top_k"],
+                                   ex["n_experts"], ex["block_size"])
+    if got is None or list(got[0]) != ex["sorted_token_ids"] or list(got[1]) != ex["expert_ids"] \
+            or got[2] != ex["num_tokens_past_padded"]:
+        return f"page example: {got}"
+    hw = g["hand_worked"]
+    got = orc.moe_align_block_size(np.array(hw["topk_ids"]), hw["m"], hw["top_k"], hw["n_experts"],
+                                   hw["block_size"])
+    if got is None or list(got[0]) != hw["sorted_token_ids"] or list(got[1]) != hw["expert_ids"] \
+            or got[2] != hw["num_tokens_past_padded"]:
+        return f"hand-worked example: {got}"
+    if orc.moe_align_block_size(np.array([0, 4]), 2, 1, 4, 8) is not None:
+        return "expert id out of range accepted"
+    return None
+
+
+def pin_moe_align_invariants(orc):
+    """On a seeded routing: every id appears once, blocks hold one expert each in increasing
+    expert order, the length is a multiple of the block, padding is the sentinel only."""
+    m, top_k, n_exp, bs = 37, 3, 6, 8
+    ids = synth.routes(51, m, n_exp, top_k)
+    sid, eid, padded = orc.moe_align_block_size(ids, m, top_k, n_exp, bs)
+    if padded % bs or len(eid) != padded // bs:
+        return "padded length"
+    real = [int(x) for x in sid if x != m * top_k]
+    if sorted(real) != list(range(m * top_k)):
+        return "ids not a permutation"
+    for b in range(len(eid)):
+        blk = [int(x) for x in sid[b * bs:(b + 1) * bs] if x != m * top_k]
+        if any(ids[x] != eid[b] for x in blk) or blk != sorted(blk):
+            return f"block {b}"
+    if list(eid) != sorted(eid):
+        return "experts not in order"
+    return None
+
+
+def pin_moe_blocks_equals_csr_grouped(orc):
+    """The block-routed launch gives each id's row of the CSR-routed grouped GEMM (same routes),
+    scaled by its top-k weight, bit for bit; sentinel rows and skipped (-1, is_ep) blocks write
+    nothing."""
+    m, top_k, n_exp, bs, k, n = 9, 2, 4, 4, 256, 32
+    sel = synth.routes(52, m, n_exp, top_k)
+    a = synth.activations(53, m, k)
+    qw = synth.qweight(54, k, n * n_exp).reshape(k // 8, n_exp, n).transpose(1, 0, 2).copy()
+    s = synth.scales(55, n_exp * 2, n).reshape(n_exp, 2, n)
+    ex_ids, ex_off, ex_pairs, pair_tok = orc.csr_from_token_routes(n_exp, m, top_k, sel)
+    y = orc.grouped(a, qw.ravel(), s, None, ex_ids, ex_off, ex_pairs, pair_tok, k, n)
+    sid, eid, padded = orc.moe_align_block_size(sel, m, top_k, n_exp, bs)
+    c = orc.moe_blocks(a, qw.ravel(), s, None, sid, eid, padded, None, bs, top_k, False, n_exp, k, n)
+    if c is None or not np.array_equal(c, y):
+        return "unweighted block routing != CSR grouped"
+    w = (np.arange(m * top_k, dtype=np.float32) + 1) / 8
+    cw = orc.moe_blocks(a, qw.ravel(), s, None, sid, eid, padded, w, bs, top_k, False, n_exp, k, n)
+    if not np.array_equal(cw, y * w.astype(np.float64)[:, None]):
+        return "top-k weights"
+    eid2 = eid.copy()
+    eid2[0] = -1
+    c2 = orc.moe_blocks(a, qw.ravel(), s, None, sid, eid2, padded, None, bs, top_k, True, n_exp, k, n)
+    skipped = [int(x) for x in sid[:bs] if x < m * top_k]
+    kept = [p for p in range(m * top_k) if p not in skipped]
+    if not np.all(np.isnan(c2[skipped])) or not np.array_equal(c2[kept], y[kept]):
+        return "is_ep skip"
+    if orc.moe_blocks(a, qw.ravel(), s, None, sid, eid2, padded, None, bs, top_k, False, n_exp, k, n) is not None:
+        return "expert -1 accepted without is_ep"
+    return None
+
+
 # --- gated activations (SwiGLU / GeGLU after the gate and up projections) -------------------
 
 _XS = [-30.0, -6.5, -2.0, -1.0, -0.25, 0.0, 0.125, 0.5, 1.0, 1.75, 3.0, 8.0, 30.0]

@@ -46,6 +46,10 @@ MUTATIONS = [
      "zero_points[(long)g * n + col] = (double)raw;"),
     ("group count ignores divisibility", "group_size % 16 != 0 || k % group_size != 0",
      "group_size % 16 != 0"),
+    ("moe sentinel off by one", "sorted_ids[len + r] = n_ids; /* the sentinel */",
+     "sorted_ids[len + r] = n_ids - 1; /* the sentinel */"),
+    ("moe top-k weight dropped", "double w = topk_weights ? (double)topk_weights[id] : 1.0;", "double w = 1.0;"),
+    ("moe A row by id", "orc_gemm(a + (long)(id / top_k) * lda, lda, 1,", "orc_gemm(a + (long)(id % m) * lda, lda, 1,"),
     ("silu sign of exp", "return x / (1.0 + exp(-x));", "return x / (1.0 + exp(x));"),
     ("gelu cubic constant", "(x + 0.044715 * x * x * x)", "(x + 0.44715 * x * x * x)"),
     ("glu operands swapped", "h[i] = orc_act(gate[i], kind) * up[i];", "h[i] = orc_act(up[i], kind) * gate[i];"),
