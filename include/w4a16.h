@@ -274,6 +274,69 @@ int w4a16_gemm_grouped(const void *a, int lda, const int32_t *b_packed_stack, vo
                        int group_size, int weight_type, unsigned flags, void *workspace,
                        size_t workspace_bytes, cudaStream_t stream);
 
+/* ------------------------------------------------------------------------------------------
+ * Block-routed MoE: the vLLM Marlin-MoE routing interface (ferrum-kernels 0.8.5 marlin.rs,
+ * `ferrum_vllm_marlin_moe_f16` and `marlin_gemm_moe_vllm`), on the same tcgen05 kernel as
+ * w4a16_gemm_grouped.  Rows are flattened (token, slot) ids, id = token * top_k + slot:
+ *   sorted_token_ids  [num_tokens_past_padded] ids listed per expert, each expert's run
+ *                     padded to a multiple of moe_block_size with the sentinel prob_m * top_k
+ *   expert_ids        [num_tokens_past_padded / moe_block_size] expert of each block; with
+ *                     is_ep, -1 marks an expert another rank holds (the block is skipped)
+ *   num_tokens_past_padded  one device int32, the padded length (read on the device, so the
+ *                     call needs no host synchronisation)
+ * and for every non-sentinel row r of block b:
+ *     c[id][:] = a[id / top_k][:] x dequant(B_{expert_ids[b]})   (x topk_weights[id] when
+ *     mul_topk_weights is 1), rounded once to fp16;
+ * rows of c that no entry names are not written.
+ * ---------------------------------------------------------------------------------------- */
+#define W4A16_MOE_MAX_BLOCKS 4096
+
+/* Host builder of the routing above (vLLM's `moe_align_block_size`, as marlin.rs's doc has the
+ * caller run it first): topk_ids [m * top_k] host int32, token-major (id t * top_k + j is token
+ * t's j-th expert).  Experts in increasing order, each expert's ids in increasing order, an
+ * expert with no ids gets no block.  sorted_token_ids needs `capacity` entries
+ * (m * top_k + n_experts * (block_size - 1) always suffices), expert_ids capacity / block_size.
+ * Returns num_tokens_past_padded, or -1 on an expert id out of range, a too small capacity or
+ * bad sizes. */
+int w4a16_moe_align_block_size(const int32_t *topk_ids, int m, int top_k, int n_experts,
+                               int block_size, int capacity, int32_t *sorted_token_ids,
+                               int32_t *expert_ids);
+
+/* Workspace bytes for w4a16_gemm_moe_blocks (same rules as w4a16_workspace_size). */
+size_t w4a16_moe_blocks_workspace_size(int max_padded, int moe_block_size, int n_experts, int n,
+                                       int k, int group_size, unsigned flags, int num_sms);
+
+/* The block-routed grouped GEMM.
+ *   a               device fp16 [prob_m][lda]
+ *   b_packed_stack, scales_stack, zeros_stack  as w4a16_gemm_grouped (expert e's tiles at word
+ *                   e*K*N/8, its [G][N] scales / zeros at element e*G*N); zeros for U4 only
+ *   c               device fp16 [prob_m * top_k][ldc] (ldc >= N, or >= N/2 with the gated flags)
+ *   sorted_token_ids, expert_ids, num_tokens_past_padded  device int32, 4-byte aligned
+ *   topk_weights    device fp32 [prob_m * top_k] (4-byte aligned), required when
+ *                   mul_topk_weights is 1
+ *   max_padded      capacity of sorted_token_ids: a multiple of moe_block_size, at most
+ *                   W4A16_MOE_MAX_BLOCKS blocks; num_tokens_past_padded must not exceed it
+ *   moe_block_size  8, 16, 32, 48 or 64;  top_k, prob_m, n_experts positive
+ *   mul_topk_weights, is_ep  0 or 1
+ *   flags           as w4a16_gemm_grouped (W4A16_FLAG_HAS_ZP, W4A16_FLAG_SWIGLU / _GEGLU, ...)
+ *   workspace       >= w4a16_moe_blocks_workspace_size(...) bytes, 256-byte aligned,
+ *                   zero-filled once (as w4a16_gemm's)
+ * Three launches on `stream`: a one-CTA routing kernel that turns the blocks into the grouped
+ * kernel's segments (runs of blocks of one expert, blocks of expert -1 dropped) in the
+ * workspace, a gather of the rows' activations, and the grouped tcgen05 GEMM.  A padded length
+ * that is negative, larger than max_padded or not a whole number of blocks, an expert id out of
+ * range (or -1 without is_ep), an id other than a valid one or the sentinel, or more runs than
+ * the schedule holds (min(blocks, 1024)) set W4A16_DEV_SCHEDULE; the affected rows are not
+ * written. */
+int w4a16_gemm_moe_blocks(const void *a, int lda, const int32_t *b_packed_stack, void *c, int ldc,
+                          const void *scales_stack, const void *zeros_stack,
+                          const int32_t *sorted_token_ids, const int32_t *expert_ids,
+                          const int32_t *num_tokens_past_padded, const float *topk_weights,
+                          int max_padded, int moe_block_size, int top_k, int mul_topk_weights,
+                          int is_ep, int n_experts, int prob_m, int n, int k, int group_size,
+                          int weight_type, unsigned flags, void *workspace, size_t workspace_bytes,
+                          cudaStream_t stream);
+
 /* Host-side schedule builder (memra-engine mmq_ffi.rs `ExpertCsr::from_token_routes`):
  * token-major routes selected[t*experts_per_token + j] -> expert-major CSR.  Host pointers;
  * ex_ids needs n_expert entries, ex_off n_expert+1, ex_pairs and pair_tok n_tokens*experts_per_token.

@@ -291,3 +291,76 @@ def test_gate_up_interleave_rejects_bad_arguments(w4):
     assert f(None, 0x9000, 2, 64, 4, 0) == (1 << 16 | 1)
     assert f(0x1002, 0x9000, 2, 64, 4, 0) == (1 << 16 | 2)       # misaligned int32 source
     assert f(0x1000, 0x1010, 2, 64, 4, 0) == (1 << 16 | 4)       # overlapping
+
+
+# --- block-routed MoE (vLLM interface): host builder and host checks --------------------------
+
+@pytest.mark.parametrize("m,top_k,n_exp,bs", [(4, 2, 4, 4), (37, 3, 6, 8), (100, 2, 8, 64),
+                                              (5, 1, 1, 16), (300, 4, 16, 16)])
+def test_moe_align_builder_matches_oracle(w4, m, top_k, n_exp, bs):
+    orc = oracle.Oracle()
+    ids = synth.routes(60 + m, m, n_exp, top_k) if n_exp > 1 else np.zeros(m * top_k, np.int32)
+    got = w4.w4a16_moe_align_block_size(ids, m, top_k, n_exp, bs)
+    want = orc.moe_align_block_size(ids, m, top_k, n_exp, bs)
+    assert np.array_equal(got[0], want[0]) and np.array_equal(got[1], want[1]) and got[2] == want[2]
+
+
+def test_moe_align_builder_page_examples(w4):
+    with open(os.path.join(ROOT, "tests", "golden", "moe_align_examples.json")) as f:
+        g = json.load(f)
+    ex = g["page_example"]
+    sid, eid, padded = w4.w4a16_moe_align_block_size(np.zeros(ex["batch"], np.int32), ex["batch"],
+                                                     ex["top_k"], ex["n_experts"], ex["block_size"])
+    assert list(sid) == ex["sorted_token_ids"] and list(eid) == ex["expert_ids"]
+    assert padded == ex["num_tokens_past_padded"]
+    hw = g["hand_worked"]
+    sid, eid, padded = w4.w4a16_moe_align_block_size(np.array(hw["topk_ids"]), hw["m"], hw["top_k"],
+                                                     hw["n_experts"], hw["block_size"])
+    assert list(sid) == hw["sorted_token_ids"] and list(eid) == hw["expert_ids"]
+    with pytest.raises(w4.W4A16Error):
+        w4.w4a16_moe_align_block_size(np.array([0, 4]), 2, 1, 4, 8)          # expert out of range
+    with pytest.raises(w4.W4A16Error):
+        w4.w4a16_moe_align_block_size(np.array(hw["topk_ids"]), 4, 2, 4, 4, capacity=15)
+
+
+def moe_status(w4, **kw):
+    args = dict(a=A, lda=256, b=B, c=C, ldc=256, s=S, z=None, sid=0x70000, eid=0x71000,
+                ntpp=0x72000, tw=None, max_padded=64, bs=16, top_k=2, mul=0, is_ep=0, n_exp=4,
+                m=8, n=256, k=256, gs=128, wt=5, flags=0, ws=WS, ws_bytes=1 << 30)
+    args.update(kw)
+    return w4._lib.w4a16_gemm_moe_blocks(
+        args["a"], args["lda"], args["b"], args["c"], args["ldc"], args["s"], args["z"], args["sid"],
+        args["eid"], args["ntpp"], args["tw"], args["max_padded"], args["bs"], args["top_k"],
+        args["mul"], args["is_ep"], args["n_exp"], args["m"], args["n"], args["k"], args["gs"],
+        args["wt"], args["flags"], args["ws"], args["ws_bytes"], 0)
+
+
+@pytest.mark.parametrize("kw,stage,detail", [
+    (dict(bs=12), 1, 9),                       # moe_block_size not in {8, 16, 32, 48, 64}
+    (dict(top_k=0), 1, 9),
+    (dict(m=0), 1, 9),
+    (dict(max_padded=40), 1, 9),               # not whole blocks
+    (dict(max_padded=16 * 4097), 2, 9),        # more blocks than one call routes
+    (dict(mul=1), 1, 4),                       # mul_topk_weights without weights
+    (dict(mul=2, tw=0x73000), 1, 4),
+    (dict(flags=1 << 14 | 1 << 15), 1, 4),
+    (dict(flags=1 << 1), 1, 4),                # act-order is not supported here
+    (dict(sid=None), 1, 1),
+    (dict(ntpp=None), 1, 1),
+    (dict(tw=0x73002, mul=1), 1, 2),           # misaligned weights
+    (dict(ldc=128), 1, 3),
+    (dict(ws_bytes=1024), 1, 6),
+])
+def test_moe_blocks_rejects_bad_arguments_on_host(w4, kw, stage, detail):
+    if kw.get("ws_bytes") == 1024:
+        # the workspace check needs the SM count; give the size query one
+        assert w4.w4a16_moe_blocks_workspace_size(64, 16, 4, 256, 256, 128, 0, 152) > 1024
+        return
+    st = moe_status(w4, **kw)
+    assert st == (stage << 16 | detail), (kw, st >> 16, st & 0xFFFF)
+
+
+def test_moe_blocks_workspace_size(w4):
+    assert w4.w4a16_moe_blocks_workspace_size(1536, 64, 8, 28672, 4096, 128, 0, 152) > 0
+    assert w4.w4a16_moe_blocks_workspace_size(100, 64, 8, 28672, 4096, 128, 0, 152) == 0
+    assert w4.w4a16_moe_blocks_workspace_size(128, 12, 8, 28672, 4096, 128, 0, 152) == 0

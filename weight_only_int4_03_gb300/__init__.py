@@ -37,6 +37,7 @@ W4A16_DEV_SCHEDULE = 8
 W4A16_DEV_ZERO = 16
 
 W4A16_MAX_SEGMENTS = 1024
+W4A16_MOE_MAX_BLOCKS = 4096
 W4A16_ARG_SCRATCH = 10
 W4A16_ARG_QZERO = 11
 W4A16_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
@@ -71,6 +72,10 @@ _SIGNATURES = {
     "w4a16_zero_points_check": (_I, [_P, _LL, _P, _P]),
     "w4a16_kernel_for": (_I, [_I, _I, _I, _I, _U, _I]),
     "w4_gate_up_interleave": (_I, [_P, _P, _I, _I, _I, _P]),
+    "w4a16_moe_align_block_size": (_I, [_P, _I, _I, _I, _I, _I, _P, _P]),
+    "w4a16_moe_blocks_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _U, _I]),
+    "w4a16_gemm_moe_blocks": (_I, [_P, _I, _P, _P, _I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I,
+                                   _I, _I, _I, _I, _I, _I, _U, _P, _SZ, _P]),
 }
 for _name, (_res, _args) in _SIGNATURES.items():
     _fn = getattr(_lib, _name)
@@ -265,3 +270,50 @@ def w4a16_zero_points_check(zeros, status, stream=None) -> None:
     is not an integer in [0, 15]."""
     _check("w4a16_zero_points_check", _lib.w4a16_zero_points_check(
         _ptr(zeros), zeros.numel(), _ptr(status), _stream(stream)))
+
+
+def w4a16_moe_align_block_size(topk_ids, m: int, top_k: int, n_experts: int, block_size: int,
+                               capacity: int | None = None):
+    """Host routing builder: (sorted_token_ids, expert_ids, num_tokens_past_padded) numpy int32
+    arrays trimmed to the padded length (vLLM's moe_align_block_size reading)."""
+    ids = np.ascontiguousarray(topk_ids, dtype=np.int32)
+    if ids.size != m * top_k:
+        raise W4A16Error("w4a16_moe_align_block_size", 1 << 16 | 9)
+    if capacity is None:
+        capacity = m * top_k + n_experts * (block_size - 1)
+    sorted_ids = np.zeros(max(capacity, 1), np.int32)
+    expert_ids = np.zeros(max(capacity // block_size, 1), np.int32)
+    r = _lib.w4a16_moe_align_block_size(ids.ctypes.data, m, top_k, n_experts, block_size, capacity,
+                                        sorted_ids.ctypes.data, expert_ids.ctypes.data)
+    if r < 0:
+        raise W4A16Error("w4a16_moe_align_block_size", 1 << 16 | 9)
+    return sorted_ids[:r].copy(), expert_ids[:r // block_size].copy(), r
+
+
+def w4a16_moe_blocks_workspace_size(max_padded: int, moe_block_size: int, n_experts: int, n: int,
+                                    k: int, group_size: int, flags: int = 0, num_sms: int = 0) -> int:
+    return int(_lib.w4a16_moe_blocks_workspace_size(max_padded, moe_block_size, n_experts, n, k,
+                                                    group_size, flags, num_sms))
+
+
+def w4a16_gemm_moe_blocks(a, b_packed_stack, c, scales_stack, zeros_stack, sorted_token_ids,
+                          expert_ids, num_tokens_past_padded, topk_weights, max_padded: int,
+                          moe_block_size: int, top_k: int, mul_topk_weights: bool, is_ep: bool,
+                          n_experts: int, prob_m: int, n: int, k: int, group_size: int,
+                          weight_type: int, flags: int, workspace, lda: int | None = None,
+                          ldc: int | None = None, workspace_bytes: int | None = None,
+                          stream=None) -> None:
+    """c[id] = a[id / top_k] x dequant(B_expert) (x topk_weights[id]) over vLLM-style block
+    routing (sorted_token_ids / expert_ids / num_tokens_past_padded on the device)."""
+    if lda is None:
+        lda = k
+    if ldc is None:
+        ldc = n // 2 if flags & (W4A16_FLAG_SWIGLU | W4A16_FLAG_GEGLU) else n
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check("w4a16_gemm_moe_blocks", _lib.w4a16_gemm_moe_blocks(
+        _ptr(a), lda, _ptr(b_packed_stack), _ptr(c), ldc, _ptr(scales_stack), _ptr(zeros_stack),
+        _ptr(sorted_token_ids), _ptr(expert_ids), _ptr(num_tokens_past_padded), _ptr(topk_weights),
+        max_padded, moe_block_size, top_k, int(bool(mul_topk_weights)), int(bool(is_ep)), n_experts,
+        prob_m, n, k, group_size, weight_type, flags, _ptr(workspace), workspace_bytes,
+        _stream(stream)))

@@ -564,6 +564,53 @@ void grouped_plan(Plan &pl, int n_pairs, int n_active, int n, int k, unsigned fl
     carve(pl, (long long)num_sms * pl.nt_max, (long long)n_pairs * k * 2);
 }
 
+// Block-routed MoE plan: the sorted activation copy has max_padded rows cut into at most
+// seg_cap segments (one per run of blocks of one expert); the token tile follows the average
+// rows per expert.  After the activation copy the workspace holds the routing the device
+// builds: ex_off [seg_cap + 1], ex_ids [seg_cap], ex_pairs [max_padded].
+struct MoePlan {
+    int seg_cap;
+    long long off_off, ids_off, pairs_off, total;
+};
+
+void moe_blocks_plan(Plan &pl, MoePlan &mp, int max_padded, int block_size, int n_experts, int n,
+                     int k, unsigned flags, int num_sms)
+{
+    const int n_blocks = max_padded / block_size;
+    mp.seg_cap = n_blocks < MAX_SEGMENTS ? n_blocks : MAX_SEGMENTS;
+    pl.mma = false;
+    pl.a_tmem = (flags & W4A16_FLAG_A_SMEM) == 0;
+    const int per = n_experts < mp.seg_cap ? n_experts : mp.seg_cap;
+    pl.nt_max = pick_nt_grouped(max_padded, per > 0 ? per : 1);
+    pl.act_rows = pl.nt_max;
+    pl.m_tiles = 0;
+    pl.tiles_bound = ((max_padded + pl.nt_max - 1) / pl.nt_max + mp.seg_cap) * (n / TILE_N);
+    pl.grid = num_sms;
+    carve(pl, (long long)num_sms * pl.nt_max, (long long)max_padded * k * 2);
+    mp.off_off = pl.total;
+    mp.ids_off = round_up(mp.off_off + 4LL * (mp.seg_cap + 1), 256);
+    mp.pairs_off = round_up(mp.ids_off + 4LL * mp.seg_cap, 256);
+    mp.total = round_up(mp.pairs_off + 4LL * max_padded, 256);
+}
+
+// Size checks of the block-routed interface (marlin.rs, `MarlinMoeRawLaunchArgs::validate`:
+// moe_block_size in {8, 16, 32, 48, 64}, positive top_k and prob_m, prob_m * top_k within
+// int32) plus this library's capacity: whole blocks, at most MOE_MAX_BLOCKS of them.
+int check_moe_sizes(int max_padded, int block_size, int top_k, int prob_m, int n_experts)
+{
+    if (!(block_size == 8 || block_size == 16 || block_size == 32 || block_size == 48 ||
+          block_size == 64))
+        return status_of(STAGE_ARG, W4A16_ARG_SCHEDULE);
+    if (top_k <= 0 || prob_m <= 0 || n_experts <= 0 || max_padded <= 0 ||
+        max_padded % block_size != 0)
+        return status_of(STAGE_ARG, W4A16_ARG_SCHEDULE);
+    if ((long long)prob_m * top_k > 0x7FFFFFFFLL)
+        return status_of(STAGE_ARG, W4A16_ARG_OVERFLOW);
+    if (max_padded / block_size > MOE_MAX_BLOCKS)
+        return status_of(STAGE_UNSUPPORTED, W4A16_ARG_SCHEDULE);
+    return 0;
+}
+
 void fill_params(GemmParams &p, const Plan &pl, int m, int n, int k, int group_size)
 {
     memset(&p, 0, sizeof(p));
@@ -924,6 +971,7 @@ int w4a16_gemm_grouped(const void *a, int lda, const int32_t *b_packed_stack, vo
     p.n_active = n_active;
     p.n_experts = n_experts;
     p.n_pairs = n_pairs;
+    p.n_rows = n_pairs;
     p.b_expert_words = (long long)k * n / 8;
     p.s_expert_elems = (long long)p.num_groups * n;
 
@@ -939,6 +987,167 @@ int w4a16_gemm_grouped(const void *a, int lda, const int32_t *b_packed_stack, vo
         return status_of(STAGE_RESOURCE, err);
     GemmConfig cfg{pl.grid, pl.smem_bytes, pl.a_tmem};
     return launch_status(launch_gemm(p, ma, ms, mz, cfg, stream));
+}
+
+size_t w4a16_moe_blocks_workspace_size(int max_padded, int moe_block_size, int n_experts, int n,
+                                       int k, int group_size, unsigned flags, int num_sms)
+{
+    if (check_moe_sizes(max_padded, moe_block_size, 1, 1, n_experts) != 0 || n <= 0 || k <= 0 ||
+        n % 256 != 0 || k % 128 != 0 || num_groups(k, group_size) < 0)
+        return 0;
+    if (num_sms <= 0 && sm_count(&num_sms) != cudaSuccess)
+        return 0;
+    Plan pl;
+    MoePlan mp;
+    moe_blocks_plan(pl, mp, max_padded, moe_block_size, n_experts, n, k, flags, num_sms);
+    return (size_t)mp.total;
+}
+
+int w4a16_gemm_moe_blocks(const void *a, int lda, const int32_t *b_packed_stack, void *c, int ldc,
+                          const void *scales_stack, const void *zeros_stack,
+                          const int32_t *sorted_token_ids, const int32_t *expert_ids,
+                          const int32_t *num_tokens_past_padded, const float *topk_weights,
+                          int max_padded, int moe_block_size, int top_k, int mul_topk_weights,
+                          int is_ep, int n_experts, int prob_m, int n, int k, int group_size,
+                          int weight_type, unsigned flags, void *workspace, size_t workspace_bytes,
+                          cudaStream_t stream)
+{
+    int st = check_weights(b_packed_stack, scales_stack, zeros_stack, n, k, group_size, weight_type,
+                           flags);
+    if (st)
+        return st;
+    if (flags & (W4A16_FLAG_ACT_ORDER | W4A16_FLAG_FORCE_SIMT | W4A16_FLAG_FORCE_MMA |
+                 W4A16_FLAG_FORCE_SLICE))
+        return status_of(STAGE_ARG, W4A16_ARG_FLAGS);
+    const int glu = glu_kind(flags);
+    if (glu < 0 || (mul_topk_weights != 0 && topk_weights == nullptr) ||
+        (mul_topk_weights != 0 && mul_topk_weights != 1) || (is_ep != 0 && is_ep != 1))
+        return status_of(STAGE_ARG, W4A16_ARG_FLAGS);
+    st = check_moe_sizes(max_padded, moe_block_size, top_k, prob_m, n_experts);
+    if (st)
+        return st;
+    if (!a || !c || !workspace || !sorted_token_ids || !expert_ids || !num_tokens_past_padded)
+        return status_of(STAGE_ARG, W4A16_ARG_NULL);
+    if (lda < k || ldc < (glu > 0 ? n / 2 : n))
+        return status_of(STAGE_ARG, W4A16_ARG_SHAPE);
+    if (lda % 8 != 0 || ldc % 8 != 0 || !aligned(a, 16) || !aligned(c, 16) ||
+        !aligned(workspace, 256) || !aligned(sorted_token_ids, 4) || !aligned(expert_ids, 4) ||
+        !aligned(num_tokens_past_padded, 4) || (topk_weights && !aligned(topk_weights, 4)))
+        return status_of(STAGE_ARG, W4A16_ARG_ALIGN);
+    const long long n_ids = (long long)prob_m * top_k;
+    if (n_ids * ldc > (1LL << 40) || (long long)prob_m * lda > (1LL << 40) ||
+        (long long)n_experts * k * n / 8 > (1LL << 40) || (long long)max_padded * k > (1LL << 40))
+        return status_of(STAGE_ARG, W4A16_ARG_OVERFLOW);
+
+    int num_sms = 0;
+    int err = sm_count(&num_sms);
+    if (err != cudaSuccess)
+        return status_of(STAGE_RESOURCE, err);
+    Plan pl;
+    MoePlan mp;
+    moe_blocks_plan(pl, mp, max_padded, moe_block_size, n_experts, n, k, flags, num_sms);
+    if (workspace_bytes < (size_t)mp.total)
+        return status_of(STAGE_ARG, W4A16_ARG_WORKSPACE);
+    const int g = num_groups(k, group_size);
+    plan_tmem(pl);
+    err = plan_smem(pl, true, zeros_stack != nullptr, group_size == -1 ? k : group_size,
+                    g * n_experts);
+    if (err != cudaSuccess)
+        return status_of(STAGE_RESOURCE, err);
+
+    char *ws = static_cast<char *>(workspace);
+    int32_t *ex_off = reinterpret_cast<int32_t *>(ws + mp.off_off);
+    int32_t *ex_ids = reinterpret_cast<int32_t *>(ws + mp.ids_off);
+    int32_t *ex_pairs = reinterpret_cast<int32_t *>(ws + mp.pairs_off);
+    GemmParams p;
+    fill_params(p, pl, max_padded, n, k, group_size);
+    p.b = b_packed_stack;
+    p.scales = static_cast<const __half *>(scales_stack);
+    p.zeros = static_cast<const __half *>(zeros_stack);
+    p.c = static_cast<__half *>(c);
+    p.ldc = ldc;
+    p.glu = glu;
+    p.status = reinterpret_cast<int *>(ws);
+    p.counters = reinterpret_cast<int *>(ws + pl.counters_off);
+    p.partials = reinterpret_cast<float *>(ws + pl.partials_off);
+    p.ex_off = ex_off;
+    p.ex_ids = ex_ids;
+    p.ex_pairs = ex_pairs;
+    p.n_active = mp.seg_cap;
+    p.n_experts = n_experts;
+    p.n_pairs = (int)n_ids;
+    p.n_rows = max_padded;
+    p.skip_sentinel = 1;
+    p.row_weight = mul_topk_weights ? topk_weights : nullptr;
+    p.b_expert_words = (long long)k * n / 8;
+    p.s_expert_elems = (long long)p.num_groups * n;
+
+    err = launch_moe_route(sorted_token_ids, expert_ids, num_tokens_past_padded, max_padded,
+                           moe_block_size, (int)n_ids, n_experts, is_ep, mp.seg_cap, ex_off, ex_ids,
+                           ex_pairs, p.status, stream);
+    if (err != cudaSuccess)
+        return status_of(STAGE_LAUNCH, err);
+    __half *a_sorted = reinterpret_cast<__half *>(ws + pl.a_off);
+    err = launch_moe_gather(static_cast<const __half *>(a), lda, ex_off + mp.seg_cap, ex_pairs, top_k,
+                            a_sorted, max_padded, k, stream);
+    if (err != cudaSuccess)
+        return status_of(STAGE_LAUNCH, err);
+    CUtensorMap ma, ms, mz;
+    err = encode_maps(pl, a_sorted, max_padded, k, k, scales_stack, zeros_stack, g * n_experts, n,
+                      &ma, &ms, &mz);
+    if (err != cudaSuccess)
+        return status_of(STAGE_RESOURCE, err);
+    GemmConfig cfg{pl.grid, pl.smem_bytes, pl.a_tmem};
+    return launch_status(launch_gemm(p, ma, ms, mz, cfg, stream));
+}
+
+int w4a16_moe_align_block_size(const int32_t *topk_ids, int m, int top_k, int n_experts,
+                               int block_size, int capacity, int32_t *sorted_token_ids,
+                               int32_t *expert_ids)
+{
+    if (m <= 0 || top_k <= 0 || n_experts <= 0 || block_size <= 0 || capacity < 0)
+        return -1;
+    const long long n_ids_ll = (long long)m * top_k;
+    if (n_ids_ll > 0x7FFFFFFF)
+        return -1;
+    const int n_ids = (int)n_ids_ll;
+    if (!topk_ids || !sorted_token_ids || !expert_ids)
+        return -1;
+    // Counting sort: ids per expert, each expert's run padded to whole blocks, experts in
+    // order, ids in increasing order inside a run; padding rows hold the sentinel n_ids.
+    long long *start = static_cast<long long *>(calloc((size_t)n_experts + 1, sizeof(long long)));
+    if (!start)
+        return -1;
+    int ret = -1;
+    for (int i = 0; i < n_ids; ++i) {
+        const int e = topk_ids[i];
+        if (e < 0 || e >= n_experts)
+            goto out;
+        start[e + 1]++;
+    }
+    for (int e = 0; e < n_experts; ++e)
+        start[e + 1] = start[e] + (start[e + 1] + block_size - 1) / block_size * block_size;
+    if (start[n_experts] > capacity)
+        goto out;
+    {
+        long long *cursor = static_cast<long long *>(malloc(sizeof(long long) * (size_t)n_experts));
+        if (!cursor)
+            goto out;
+        for (long long r = 0; r < start[n_experts]; ++r)
+            sorted_token_ids[r] = n_ids;
+        for (int e = 0; e < n_experts; ++e) {
+            cursor[e] = start[e];
+            for (long long b = start[e] / block_size; b < start[e + 1] / block_size; ++b)
+                expert_ids[b] = e;
+        }
+        for (int i = 0; i < n_ids; ++i)
+            sorted_token_ids[cursor[topk_ids[i]]++] = i;
+        free(cursor);
+        ret = (int)start[n_experts];
+    }
+out:
+    free(start);
+    return ret;
 }
 
 int w4a16_csr_from_token_routes(int n_expert, int n_tokens, int experts_per_token,

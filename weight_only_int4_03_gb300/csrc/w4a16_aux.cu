@@ -137,6 +137,164 @@ __global__ void gather_rows_kernel(const __half *__restrict__ a, int lda,
         dst[i] = src[i];
 }
 
+// ---------------------------------------------------------------------------------------
+// Block-routed MoE (the vLLM Marlin-MoE interface) -> the grouped kernel's segment schedule,
+// on the device (the padded length is a device value).  One CTA: blocks of `block_size` sorted
+// rows with a valid expert are compacted in order (blocks of expert -1 with is_ep drop out),
+// runs of consecutive blocks of one expert become segments, and every compacted row maps to
+// its output row id, or -1 for a sentinel.  Segment slots past the last hold empty segments at
+// the end offset, so the kernel can be told the slot count, not the segment count.
+// ---------------------------------------------------------------------------------------
+constexpr int ROUTE_THREADS = 1024;
+constexpr int ROUTE_PER_THREAD = MOE_MAX_BLOCKS / ROUTE_THREADS;
+
+// Exclusive scan of up to MOE_MAX_BLOCKS flags (ROUTE_PER_THREAD consecutive per thread);
+// returns the total.  `warp_sums` holds 32 ints of shared memory.
+static __device__ int block_exclusive_scan(const int (&flag)[ROUTE_PER_THREAD],
+                                           int (&pos)[ROUTE_PER_THREAD], int *warp_sums)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int local = 0;
+#pragma unroll
+    for (int i = 0; i < ROUTE_PER_THREAD; ++i)
+        local += flag[i];
+    int incl = local;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d)
+            incl += v;
+    }
+    if (lane == 31)
+        warp_sums[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int w = warp_sums[lane];
+        int wi = w;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, wi, d);
+            if (lane >= d)
+                wi += v;
+        }
+        warp_sums[lane] = wi - w; // exclusive prefix of warp sums
+        if (lane == 31)
+            warp_sums[32] = wi;   // total
+    }
+    __syncthreads();
+    int run = warp_sums[warp] + incl - local;
+#pragma unroll
+    for (int i = 0; i < ROUTE_PER_THREAD; ++i) {
+        pos[i] = run;
+        run += flag[i];
+    }
+    const int total = warp_sums[32];
+    __syncthreads();
+    return total;
+}
+
+__global__ void __launch_bounds__(ROUTE_THREADS)
+    moe_route_kernel(const int32_t *__restrict__ sorted_ids, const int32_t *__restrict__ expert_ids,
+                     const int32_t *__restrict__ ntpp, int max_padded, int block_size, int n_ids,
+                     int n_experts, int is_ep, int seg_cap, int32_t *__restrict__ ex_off,
+                     int32_t *__restrict__ ex_ids, int32_t *__restrict__ ex_pairs, int *status)
+{
+    __shared__ int cexp[MOE_MAX_BLOCKS]; // expert of compacted block c
+    __shared__ int cblk[MOE_MAX_BLOCKS]; // its block in the caller's order
+    __shared__ int warp_sums[33];
+    pdl_launch_dependents();
+    pdl_wait();
+    int padded = *ntpp;
+    if (padded < 0 || padded > max_padded || padded % block_size != 0) {
+        if (threadIdx.x == 0)
+            atomicOr(status, W4A16_DEV_SCHEDULE);
+        padded = 0;
+    }
+    const int n_blocks = padded / block_size;
+    const int b0 = threadIdx.x * ROUTE_PER_THREAD;
+    int flag[ROUTE_PER_THREAD], pos[ROUTE_PER_THREAD], exp_[ROUTE_PER_THREAD];
+    bool bad = false;
+#pragma unroll
+    for (int i = 0; i < ROUTE_PER_THREAD; ++i) {
+        const int b = b0 + i;
+        exp_[i] = b < n_blocks ? expert_ids[b] : -1;
+        flag[i] = (b < n_blocks && exp_[i] >= 0 && exp_[i] < n_experts) ? 1 : 0;
+        bad |= b < n_blocks && !flag[i] && !(is_ep && exp_[i] == -1);
+    }
+    if (bad)
+        atomicOr(status, W4A16_DEV_SCHEDULE);
+    const int n_valid = block_exclusive_scan(flag, pos, warp_sums);
+#pragma unroll
+    for (int i = 0; i < ROUTE_PER_THREAD; ++i)
+        if (flag[i]) {
+            cexp[pos[i]] = exp_[i];
+            cblk[pos[i]] = b0 + i;
+        }
+    __syncthreads();
+    // Segment starts among the compacted blocks.
+#pragma unroll
+    for (int i = 0; i < ROUTE_PER_THREAD; ++i) {
+        const int c = b0 + i;
+        flag[i] = (c < n_valid && (c == 0 || cexp[c] != cexp[c - 1])) ? 1 : 0;
+    }
+    int n_seg = block_exclusive_scan(flag, pos, warp_sums);
+    const bool overflow = n_seg > seg_cap;
+    if (overflow) {
+        if (threadIdx.x == 0)
+            atomicOr(status, W4A16_DEV_SCHEDULE);
+        n_seg = 0;
+    }
+    const int rows = overflow ? 0 : n_valid * block_size;
+    if (!overflow) {
+#pragma unroll
+        for (int i = 0; i < ROUTE_PER_THREAD; ++i)
+            if (flag[i]) {
+                ex_ids[pos[i]] = cexp[b0 + i];
+                ex_off[pos[i]] = (b0 + i) * block_size;
+            }
+    }
+    for (int sidx = n_seg + (int)threadIdx.x; sidx <= seg_cap; sidx += ROUTE_THREADS) {
+        ex_off[sidx] = rows;
+        if (sidx < seg_cap)
+            ex_ids[sidx] = 0;
+    }
+    for (int r = threadIdx.x; r < max_padded; r += ROUTE_THREADS) {
+        int id = -1;
+        if (r < rows) {
+            const int src = sorted_ids[cblk[r / block_size] * block_size + r % block_size];
+            if (src >= 0 && src < n_ids)
+                id = src;
+            else if (src != n_ids)
+                atomicOr(status, W4A16_DEV_SCHEDULE);
+        }
+        ex_pairs[r] = id;
+    }
+}
+
+// a_sorted[r] = a[ex_pairs[r] / top_k] for the rows of the routed schedule (ex_off_end holds
+// their count), a zero row for a sentinel; rows past the count are left alone.
+__global__ void moe_gather_kernel(const __half *__restrict__ a, int lda,
+                                  const int32_t *__restrict__ ex_off_end,
+                                  const int32_t *__restrict__ ex_pairs, int top_k,
+                                  __half *__restrict__ out, int k)
+{
+    pdl_launch_dependents();
+    pdl_wait();
+    const int r = blockIdx.x;
+    if (r >= *ex_off_end)
+        return;
+    const int id = ex_pairs[r];
+    uint4 *dst = reinterpret_cast<uint4 *>(out + (long long)r * k);
+    if (id < 0) {
+        for (int i = threadIdx.x; i < k / 8; i += blockDim.x)
+            dst[i] = make_uint4(0, 0, 0, 0);
+        return;
+    }
+    const uint4 *src = reinterpret_cast<const uint4 *>(a + (long long)(id / top_k) * lda);
+    for (int i = threadIdx.x; i < k / 8; i += blockDim.x)
+        dst[i] = src[i];
+}
+
 // Gate/up interleave of a row-major [rows][2I] array: destination column j takes source
 // column 16b + r (gate) for j = 32b + r, r < 16, and I + 16b + r - 16 (up) for r >= 16.
 template <typename T>
@@ -240,6 +398,24 @@ int launch_gather_rows(const __half *a, int lda, const int32_t *ex_pairs, const 
 {
     gather_rows_kernel<<<n_pairs, 128, 0, stream>>>(a, lda, ex_pairs, pair_tok, out, n_pairs,
                                                     n_tokens, k, status);
+    return cudaGetLastError();
+}
+
+int launch_moe_route(const int32_t *sorted_ids, const int32_t *expert_ids, const int32_t *ntpp,
+                     int max_padded, int block_size, int n_ids, int n_experts, int is_ep,
+                     int seg_cap, int32_t *ex_off, int32_t *ex_ids, int32_t *ex_pairs, int *status,
+                     cudaStream_t stream)
+{
+    moe_route_kernel<<<1, ROUTE_THREADS, 0, stream>>>(sorted_ids, expert_ids, ntpp, max_padded,
+                                                      block_size, n_ids, n_experts, is_ep, seg_cap,
+                                                      ex_off, ex_ids, ex_pairs, status);
+    return cudaGetLastError();
+}
+
+int launch_moe_gather(const __half *a, int lda, const int32_t *ex_off_end, const int32_t *ex_pairs,
+                      int top_k, __half *out, int max_padded, int k, cudaStream_t stream)
+{
+    moe_gather_kernel<<<max_padded, 128, 0, stream>>>(a, lda, ex_off_end, ex_pairs, top_k, out, k);
     return cudaGetLastError();
 }
 

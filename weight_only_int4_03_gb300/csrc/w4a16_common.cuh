@@ -403,7 +403,7 @@ static __device__ int build_segments(const GemmParams &p, SegTable &seg, int lan
         bool b = false;
         if (i < p.n_active) {
             const int lo = p.ex_off[i], hi = p.ex_off[i + 1], e = p.ex_ids[i];
-            b = lo < 0 || hi < lo || hi > p.n_pairs || e < 0 || e >= p.n_experts;
+            b = lo < 0 || hi < lo || hi > p.n_rows || e < 0 || e >= p.n_experts;
         }
         bad |= __any_sync(0xffffffffu, b);
     }
@@ -460,18 +460,26 @@ __device__ __forceinline__ int own_slot(const GemmParams &p, const Sched &sched,
 }
 
 // Output row of tile row `row`: dense rows are in place; grouped rows go to pair ex_pairs[.].
-// Returns -1 (and reports) for an out-of-range pair.
+// Returns -1 for a row that writes nothing: a padding row of the block-routed interface
+// (entry -1), or an out-of-range entry, which is reported.
 __device__ __forceinline__ int output_row(const GemmParams &p, const TileInfo &ti, int row)
 {
     int out_row = ti.row0 + row;
     if (p.ex_off != nullptr) {
         out_row = p.ex_pairs[out_row];
         if (out_row < 0 || out_row >= p.n_pairs) {
-            atomicOr(p.status, W4A16_DEV_SCHEDULE);
+            if (!(p.skip_sentinel && out_row == -1))
+                atomicOr(p.status, W4A16_DEV_SCHEDULE);
             return -1;
         }
     }
     return out_row;
+}
+
+// Scale of an output row (the block-routed interface's top-k weight), 1 otherwise.
+__device__ __forceinline__ float row_scale(const GemmParams &p, int out_row)
+{
+    return p.row_weight != nullptr ? p.row_weight[out_row] : 1.0f;
 }
 
 // Contributors c_lo..c_hi of stream-K tile st_tile and the slot of the first one (the others
@@ -522,8 +530,9 @@ static __device__ __forceinline__ void store_quad(const GemmParams &p, const Til
     const int out_row = output_row(p, ti, row);
     if (out_row < 0)
         return;
-    const __half2 lo = __floats2half2_rn(acc.x, acc.y);
-    const __half2 hi = __floats2half2_rn(acc.z, acc.w);
+    const float w = row_scale(p, out_row);
+    const __half2 lo = __floats2half2_rn(acc.x * w, acc.y * w);
+    const __half2 hi = __floats2half2_rn(acc.z * w, acc.w * w);
     uint2 packed;
     packed.x = *reinterpret_cast<const uint32_t *>(&lo);
     packed.y = *reinterpret_cast<const uint32_t *>(&hi);
@@ -580,8 +589,9 @@ static __device__ void reduce_tile_glu(const GemmParams &p, const TileInfo &ti, 
         const int out_row = output_row(p, ti, row);
         if (out_row < 0)
             continue;
-        const __half2 lo = __floats2half2_rn(glu_act(g.x, p.glu) * u.x, glu_act(g.y, p.glu) * u.y);
-        const __half2 hi = __floats2half2_rn(glu_act(g.z, p.glu) * u.z, glu_act(g.w, p.glu) * u.w);
+        const float w = row_scale(p, out_row);
+        const __half2 lo = __floats2half2_rn(glu_act(g.x, p.glu) * u.x * w, glu_act(g.y, p.glu) * u.y * w);
+        const __half2 hi = __floats2half2_rn(glu_act(g.z, p.glu) * u.z * w, glu_act(g.w, p.glu) * u.w * w);
         uint2 packed;
         packed.x = *reinterpret_cast<const uint32_t *>(&lo);
         packed.y = *reinterpret_cast<const uint32_t *>(&hi);

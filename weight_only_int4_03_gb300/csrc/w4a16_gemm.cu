@@ -245,6 +245,15 @@ __device__ void run_epilogue(const GemmParams &p, const SegTable &seg, Sched sch
             if (c0 + 16 < ti.ntok)
                 tmem_ld16(taddr + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
             tmem_ld_wait();
+            // Block-routed calls may scale each output row (top-k weights): lane j holds the
+            // weight of row c0 + j, handed to every lane by a shuffle.
+            const bool weighted = p.row_weight != nullptr;
+            float rw = 1.0f;
+            if (weighted && whole && c0 + lane < ti.rows) {
+                const int orow = p.ex_pairs[ti.row0 + c0 + lane];
+                if (orow >= 0 && orow < p.n_pairs)
+                    rw = p.row_weight[orow];
+            }
             if (whole && p.glu) {
                 // Lanes 0..15 hold gate features n0/2 + 16q + lane, lanes 16..31 the up values
                 // of the same features: 32 rows x 16 features through the staging buffer.
@@ -252,8 +261,9 @@ __device__ void run_epilogue(const GemmParams &p, const SegTable &seg, Sched sch
                 for (int j = 0; j < EPI_ROWS; ++j) {
                     const float g = __uint_as_float(v[j]);
                     const float u = __shfl_down_sync(0xffffffffu, g, 16);
+                    const float w = weighted ? __shfl_sync(0xffffffffu, rw, j) : 1.0f;
                     if (lane < 16)
-                        stg[j * 16 + lane] = __float2half_rn(glu_act(g, p.glu) * u);
+                        stg[j * 16 + lane] = __float2half_rn(glu_act(g, p.glu) * u * w);
                 }
                 __syncwarp();
 #pragma unroll
@@ -273,8 +283,10 @@ __device__ void run_epilogue(const GemmParams &p, const SegTable &seg, Sched sch
                 __syncwarp();
             } else if (whole) {
 #pragma unroll
-                for (int j = 0; j < EPI_ROWS; ++j)
-                    stg[j * 32 + lane] = __float2half_rn(__uint_as_float(v[j]));
+                for (int j = 0; j < EPI_ROWS; ++j) {
+                    const float w = weighted ? __shfl_sync(0xffffffffu, rw, j) : 1.0f;
+                    stg[j * 32 + lane] = __float2half_rn(__uint_as_float(v[j]) * w);
+                }
                 __syncwarp();
 #pragma unroll
                 for (int i = 0; i < EPI_ROWS / 8; ++i) {

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "w4a16.h"
+
 namespace w4 {
 
 // Packed tile geometry (see include/w4a16.h, "Packed tile layout").
@@ -83,6 +85,9 @@ struct GemmParams {
     const int *ex_ids;
     const int *ex_pairs;
     int n_active, n_experts, n_pairs;
+    int n_rows;               // grouped: rows of the sorted activation copy (segments end there)
+    int skip_sentinel;        // grouped: an ex_pairs entry of -1 is a padding row, not an error
+    const float *row_weight;  // grouped: output row o is scaled by row_weight[o] (or null)
     long long b_expert_words;
     long long s_expert_elems;
 };
@@ -111,6 +116,13 @@ int launch_gather_rows(const __half *a, int lda, const int32_t *ex_pairs, const 
                        __half *out, int n_pairs, int n_tokens, int k, int *status,
                        cudaStream_t stream);
 int launch_selftest_timeout(int *status, unsigned long long limit_ns, cudaStream_t stream);
+constexpr int MOE_MAX_BLOCKS = W4A16_MOE_MAX_BLOCKS; // blocks per block-routed MoE call
+int launch_moe_route(const int32_t *sorted_ids, const int32_t *expert_ids, const int32_t *ntpp,
+                     int max_padded, int block_size, int n_ids, int n_experts, int is_ep,
+                     int seg_cap, int32_t *ex_off, int32_t *ex_ids, int32_t *ex_pairs, int *status,
+                     cudaStream_t stream);
+int launch_moe_gather(const __half *a, int lda, const int32_t *ex_off_end, const int32_t *ex_pairs,
+                      int top_k, __half *out, int max_padded, int k, cudaStream_t stream);
 int launch_gate_up_interleave(const void *src, void *dst, int rows, int n2, int elem_bytes,
                               cudaStream_t stream);
 int gemm_smem_limit(int *bytes);
