@@ -82,6 +82,13 @@ def workload_specs(name: str):
                       seed=5000, pair_rows=False, glu=1),
                  dict(grouped=True, n_exp=8, n_tok=512, top_k=2, k=14336, n=4096, gs=128, wt=U4B8,
                       seed=5001, pair_rows=True, a_from=0)]
+    elif name == "moe_blocks":
+        # The MoE configuration through the vLLM block-routed interface (blocks of 64 rows),
+        # the down projection scaling each pair row by its top-k weight.
+        specs = [dict(grouped=True, n_exp=8, n_tok=512, top_k=2, k=4096, n=28672, gs=128, wt=U4B8,
+                      seed=5000, pair_rows=False, blocks=64),
+                 dict(grouped=True, n_exp=8, n_tok=512, top_k=2, k=14336, n=4096, gs=128, wt=U4B8,
+                      seed=5001, pair_rows=True, blocks=64, mul_topk=True)]
     elif name == "moe":
         specs = [dict(grouped=True, n_exp=8, n_tok=512, top_k=2, k=4096, n=28672, gs=128, wt=U4B8,
                       seed=5000, pair_rows=False),
@@ -100,6 +107,9 @@ WORKLOAD_TEXT = {
     "actorder": "act-order M in {1,16,2048}, K=8192, N=28672, group 128, u4b8, shuffled g_idx",
     "tiny": "tiny M=16, K=256, N=256, group 128, u4b8",
     "moe": "grouped MoE 8 experts, 512 tokens top-2, gate_up K=4096 N=28672 + down K=14336 N=4096, u4b8",
+    "moe_blocks": ("grouped MoE 8 experts, 512 tokens top-2 through the vLLM block routing (blocks of "
+                   "64 rows, sentinel padding): gate_up K=4096 N=28672 + down K=14336 N=4096 x top-k "
+                   "weights, u4b8"),
     "moe_swiglu": ("grouped MoE FFN 8 experts, 512 tokens top-2: gate_up K=4096 2I=28672 with the "
                    "fused SwiGLU epilogue -> H [1024, 14336] -> down K=14336 N=4096 reading H, u4b8"),
 }
@@ -331,6 +341,16 @@ class GroupedGemm:
         if s["pair_rows"]:   # down projection: pair-major activations, pair p reads row p
             rows = n_pairs
             pair_tok = np.arange(n_pairs, dtype=np.int32)
+        self.blocks = s.get("blocks", 0)   # the vLLM block routing instead of the CSR schedule
+        if self.blocks:
+            # Down projection over pair rows: every pair is its own "token" with top_k 1.
+            m_rows, tk = (n_tok, top_k) if not s["pair_rows"] else (n_pairs, 1)
+            sid, eid, padded = w4.w4a16_moe_align_block_size(sel, m_rows, tk, n_exp, self.blocks)
+            self.route = [torch.from_numpy(x).to(dev) for x in (sid, eid, np.array([padded], np.int32))]
+            self.route_sizes = (padded, m_rows, tk)
+            self.topk_w = (torch.from_numpy(synth.scales(s["seed"], 1, n_pairs, lo=0.05, hi=0.95)
+                                            .astype(np.float32).ravel()).to(dev)
+                           if s.get("mul_topk") else None)
         a = synth.activations(s["seed"], rows, k)
         glu = s.get("glu", 0)   # gated FFN: planar gate|up weights, interleaved on the device
         packed = torch.empty(n_exp * k * n // 8, dtype=torch.int32, device=dev)
@@ -358,11 +378,15 @@ class GroupedGemm:
         self.a_host = torch.from_numpy(a).pin_memory()
         self.a = self.a_host.to(dev)
         self.c = torch.empty((n_pairs, n // 2 if glu else n), dtype=torch.float16, device=dev)
-        self.ws = torch.zeros(w4.w4a16_grouped_workspace_size(n_pairs, self.n_active, n, k, gs,
-                                                              self.flags),
-                              dtype=torch.uint8, device=dev)
+        if self.blocks:
+            ws_bytes = w4.w4a16_moe_blocks_workspace_size(self.route_sizes[0], self.blocks, n_exp, n,
+                                                          k, gs, self.flags)
+            self.launches = 3
+        else:
+            ws_bytes = w4.w4a16_grouped_workspace_size(n_pairs, self.n_active, n, k, gs, self.flags)
+            self.launches = 2
+        self.ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
         self.w4 = w4
-        self.launches = 2
         s["m"] = n_pairs   # rows of output for the flop/byte accounting
         s["act_order"] = False
         s["sigma"] = 1.0
@@ -370,6 +394,14 @@ class GroupedGemm:
     def run(self, copy: int):
         s = self.s
         r = copy % len(self.b)
+        if self.blocks:
+            sid, eid, ntpp = self.route
+            padded, m_rows, tk = self.route_sizes
+            self.w4.w4a16_gemm_moe_blocks(self.a, self.b[r], self.c, self.scales[r], None, sid, eid,
+                                          ntpp, self.topk_w, padded, self.blocks, tk,
+                                          self.topk_w is not None, False, s["n_exp"], m_rows, s["n"],
+                                          s["k"], s["gs"], s["wt"], self.flags, self.ws)
+            return
         ids, off, pairs, tok = self.csr
         self.w4.w4a16_gemm_grouped(self.a, self.b[r], self.c, self.scales[r], None, ids, off, pairs, tok,
                                    self.n_active, s["n_exp"], self.n_pairs, self.rows, s["n"], s["k"],

@@ -196,7 +196,7 @@ size_t w4a16_workspace_size(int m, int n, int k, int group_size, unsigned flags,
  * Results are deterministic: a fixed reduction order makes repeated calls on the same device
  * with the same sizes and flags bit-identical.  Tuning overrides read once from the
  * environment (W4A16_STAGE_BLOCKS, W4A16_DECODE_ROWS, W4A16_DECODE_GRID, W4A16_TILE_TOKENS,
- * W4A16_SLICE; unset by default) change the kernel choice and tiling, and with them the
+ * W4A16_SLICE, W4A16_PAIR_HALF; unset by default) change the kernel choice and tiling, and with them the
  * rounding order: results stay within tolerance but their bits can differ between processes
  * whose environments differ. */
 int w4a16_gemm(const void *a, int lda, const int32_t *b_packed, void *c, int ldc,

@@ -143,6 +143,32 @@ def test_full_size_grouped(w4, orc, index):
     assert ok, f"moe[{index}] ({len(pick)} pairs): {msg}"
 
 
+@pytest.mark.parametrize("index", [0, 1])
+def test_full_size_moe_block_routing(w4, orc, index):
+    """The MoE configuration through the block-routed (vLLM) interface, bench.py's moe_blocks
+    workload: the same pairs as above against the oracle, the down projection's rows scaled by
+    their top-k weights."""
+    import torch
+    spec = dict(bench.workload_specs("moe_blocks")[index])
+    g = bench.GroupedGemm(w4, spec, 1, torch.device("cuda"))
+    g.run(0)
+    torch.cuda.synchronize()
+    assert w4.w4a16_status(g.ws) == 0
+    sel = synth.routes(5000, spec["n_tok"], spec["n_exp"], spec["top_k"])
+    ids, off, pairs, _ = orc.csr_from_token_routes(spec["n_exp"], spec["n_tok"], spec["top_k"], sel)
+    pick = set()
+    for i in range(len(ids)):
+        seg = [int(p) for p in pairs[off[i]:off[i + 1]]]
+        pick.update(seg if i in (0, len(ids) - 1) else (seg[0], seg[-1]))
+    pick = sorted(pick)
+    ref = grouped_reference(orc, spec, g, pick)
+    if g.topk_w is not None:
+        ref = ref * g.topk_w.cpu().numpy().astype(np.float64)[pick][:, None]
+    got = g.c[pick].float().cpu().numpy().astype(np.float64)
+    ok, msg = within_tol(got, ref)
+    assert ok, f"moe_blocks[{index}] ({len(pick)} pairs): {msg}"
+
+
 FULL = os.environ.get("W4A16_FULL_ORACLE") == "1"
 
 

@@ -56,7 +56,9 @@ struct Plan {
     int stages, stage_bytes, acc_bufs, acc_col0, tmem_cols, smem_bytes, seg_off, epi_off, a_slots;
     bool a_tmem, mma; // mma: a small-M register-fragment kernel instead of tcgen05
     bool slice = false; // ... the column-slice one (no split-K)
-    int act_rows = 0;   // rows of one activation box (slice kernel: M; others: nt_max)
+    int act_rows = 0;   // rows of one activation box (slice kernel: M; pairs: a half-tile;
+                        // others: nt_max)
+    int halves = 1, nt_half = 0; // tcgen05: token tile as a pair of half-tiles (halves 2)
     int split = 0;    // tile-aligned split factor (0: stream-K)
     int n_slices = 0, slice_per = 0;
     long long counters_off, partials_off, a_off, total;
@@ -177,6 +179,43 @@ int pick_nt(int m, int cap)
     return nt < lo ? lo : nt;
 }
 
+// The tcgen05 kernel's token tile: pick_nt's single tile, or -- for w4a16_gemm's full tile cap,
+// when it lowers the number of tiles -- a pair of half-tiles of equal height (a multiple of 16,
+// at most PAIR_HALF_TOK) whose MMAs share each dequantised weight block.  The dequantisation
+// bounds the kernel at large M, and a pair dequantises once for up to 384 tokens where a single
+// tile does for at most 256: M=4096 runs 11 pairs of 2 x 192 (19 tiles of 224 before), M=2048
+// 6 of 2 x 176, M=1024 3 of 2 x 176.
+struct TcTile {
+    int rows, halves, half;
+};
+
+int pair_half_max()
+{
+    static int v = [] {
+        const int e = env_int("W4A16_PAIR_HALF", 0, PAIR_HALF_TOK, PAIR_HALF_TOK);
+        return e % 16 == 0 ? e : PAIR_HALF_TOK;
+    }();
+    return v;
+}
+
+TcTile pick_tc_tile(int m, int cap, bool allow_pairs)
+{
+    TcTile t{pick_nt(m, cap), 1, 0};
+    t.half = t.rows;
+    const int hmax = pair_half_max();
+    if (!allow_pairs || m <= cap || cap < MAX_TOK || hmax == 0)
+        return t;
+    const int tiles = (m + t.rows - 1) / t.rows;
+    const int pairs = (m + 2 * hmax - 1) / (2 * hmax);
+    if (pairs >= tiles)
+        return t;
+    const int per_pair = (m + pairs - 1) / pairs;
+    t.half = (int)round_up((per_pair + 1) / 2, 16);
+    t.halves = 2;
+    t.rows = 2 * t.half;
+    return t;
+}
+
 // Token-tile height of the small-M kernel: the smallest of 8, 16, 32, 64 rows that holds M.
 int pick_nt_mma(int m)
 {
@@ -193,10 +232,11 @@ int pick_nt_mma(int m)
 void stage_layout(Plan &pl, int kbs, int group_size, int g_rows, bool has_zp)
 {
     pl.kbs = kbs;
-    pl.act_kb_bytes = pl.nt_max * 128;
+    const int halves = pl.halves > 1 ? pl.halves : 1;
+    pl.act_kb_bytes = (halves > 1 ? pl.nt_half : pl.nt_max) * 128; // per half-tile and block
     const int sg = (kbs * KBLK + group_size - 1) / group_size + 1;
     pl.sg_box = sg < g_rows ? sg : g_rows;
-    pl.packed_off = kbs * pl.act_kb_bytes;
+    pl.packed_off = halves * kbs * pl.act_kb_bytes; // [half][block][rows x 128 B]
     pl.scales_off = pl.packed_off + kbs * TILE_BYTES;
     pl.zeros_off = pl.scales_off + (int)round_up((long long)pl.sg_box * SG_BYTES, 128);
     const int end = has_zp ? pl.zeros_off + pl.sg_box * SG_BYTES : pl.zeros_off;
@@ -507,15 +547,18 @@ void dense_plan(Plan &pl, int m, int n, int k, unsigned flags, int num_sms, int 
     pl.slice = kernel == 2;
     pl.a_tmem = (flags & W4A16_FLAG_A_SMEM) == 0;
     const bool mma_ok = m <= decode_max_rows();
-    const int nt_tc = pick_nt(m, tile_cap);
+    const TcTile tc = pick_tc_tile(m, tile_cap, (flags & W4A16_FLAG_A_SMEM) == 0);
+    const int nt_tc = tc.rows;
     const int nt_mma = mma_ok || pl.slice ? pick_nt_mma(m) : nt_tc;
     const int nt_small = nt_tc < nt_mma ? nt_tc : nt_mma;
     pl.nt_max = mma ? nt_mma : nt_tc;
+    pl.halves = mma ? 1 : tc.halves;
+    pl.nt_half = mma ? nt_mma : tc.half;
     pl.m_tiles = (m + pl.nt_max - 1) / pl.nt_max;
     const long long units = (long long)pl.m_tiles * (n / TILE_N) * (k / KBLK);
     const int ctas = mma ? num_sms * decode_grid_per_sm() : num_sms;
     pl.grid = aligned_grid(pl.m_tiles * (n / TILE_N), k / KBLK, ctas, &pl.split);
-    pl.act_rows = pl.slice ? m : pl.nt_max;
+    pl.act_rows = pl.slice ? m : pl.halves > 1 ? pl.nt_half : pl.nt_max;
     if (pl.slice) {
         // Consecutive slices per CTA, as evenly as the CTA slots allow (N=12288: 768 slices,
         // 3 each on 256 CTAs); no split-K, so no partial slots or counters are used.
@@ -558,6 +601,8 @@ void grouped_plan(Plan &pl, int n_pairs, int n_active, int n, int k, unsigned fl
     pl.a_tmem = (flags & W4A16_FLAG_A_SMEM) == 0;
     pl.nt_max = pick_nt_grouped(n_pairs, n_active);
     pl.act_rows = pl.nt_max;
+    pl.halves = 1;
+    pl.nt_half = pl.nt_max;
     pl.m_tiles = 0;
     pl.tiles_bound = ((n_pairs + pl.nt_max - 1) / pl.nt_max + n_active) * (n / TILE_N);
     pl.grid = num_sms;
@@ -583,6 +628,8 @@ void moe_blocks_plan(Plan &pl, MoePlan &mp, int max_padded, int block_size, int 
     const int per = n_experts < mp.seg_cap ? n_experts : mp.seg_cap;
     pl.nt_max = pick_nt_grouped(max_padded, per > 0 ? per : 1);
     pl.act_rows = pl.nt_max;
+    pl.halves = 1;
+    pl.nt_half = pl.nt_max;
     pl.m_tiles = 0;
     pl.tiles_bound = ((max_padded + pl.nt_max - 1) / pl.nt_max + mp.seg_cap) * (n / TILE_N);
     pl.grid = num_sms;
@@ -633,6 +680,8 @@ void fill_params(GemmParams &p, const Plan &pl, int m, int n, int k, int group_s
     p.zeros_off = pl.zeros_off;
     p.sg_box = pl.sg_box;
     p.acc_bufs = pl.acc_bufs;
+    p.halves = pl.halves > 1 ? pl.halves : 1;
+    p.nt_half = pl.halves > 1 ? pl.nt_half : pl.nt_max;
     p.acc_col0 = pl.acc_col0;
     p.tmem_cols = pl.tmem_cols;
     p.a_slots = pl.a_slots;

@@ -281,7 +281,7 @@ static __device__ __forceinline__ void issue_stage_weights(const GemmParams &p,
 {
     const bool has_zp = p.zeros != nullptr;
     const uint32_t fixed_bytes = (uint32_t)p.sg_box * SG_BYTES * (has_zp ? 2u : 1u) +
-                                 (uint32_t)p.kbs * (uint32_t)p.act_kb_bytes;
+                                 (uint32_t)(p.halves * p.kbs) * (uint32_t)p.act_kb_bytes;
     const int32_t *bw = p.b + ti.expert * p.b_expert_words +
                         ((long long)(ti.n0 / TILE_N) * p.kblocks) * TILE_WORDS;
     mbar_arrive_expect_tx(full, fixed_bytes + nkb * (uint32_t)TILE_BYTES);
@@ -346,10 +346,13 @@ static __device__ void run_producer(const GemmParams &p, const CUtensorMap *tmap
             }
             if (dep_wait && issued == 0 && p.static_weights)
                 pdl_wait();
-            // 64 columns x nt_max rows x kbs column blocks, landing as kbs consecutive
-            // [nt_max x 128 B] tiles in the 128-byte swizzle.  Activation rows are read again
-            // for every column tile: last to leave L2.
-            tensor_load_3d_hint(st, tmap_a, 0, ti.row0, kb, full, policy_evict_last());
+            // 64 columns x (half-)tile rows x kbs column blocks, landing as kbs consecutive
+            // [rows x 128 B] tiles in the 128-byte swizzle; a paired tile loads its second
+            // half-tile's rows after the first's.  Activation rows are read again for every
+            // column tile: last to leave L2.
+            for (int h = 0; h < p.halves; ++h)
+                tensor_load_3d_hint(st + h * p.kbs * p.act_kb_bytes, tmap_a, 0,
+                                    ti.row0 + h * p.nt_half, kb, full, policy_evict_last());
             ring.advance(p.stages);
             ++issued;
         }

@@ -26,6 +26,7 @@ constexpr int MAX_STAGES = 16;
 constexpr int MAX_TOK = 256;         // activation rows per tile = tcgen05 N upper bound
 constexpr int TALL_TILE_TOK = 224;   // tallest token tile chosen for M above one tile
 constexpr int TWO_BUF_TILE_TOK = 192; // tallest token tile with two accumulator buffers
+constexpr int PAIR_HALF_TOK = 192;    // tallest half-tile of a paired token tile
 
 // Warp roles of the tcgen05 GEMM kernel.
 constexpr int NUM_THREADS = 512;
@@ -71,6 +72,9 @@ struct GemmParams {
     int packed_off, scales_off, zeros_off; // byte offsets inside a stage
     int sg_box;               // scale rows copied per stage
     int acc_bufs, acc_col0, tmem_cols;
+    int halves;               // tcgen05 kernel: 1, or 2 when a tile is a pair of token half-tiles
+                              // that share each dequantised weight block
+    int nt_half;              // rows of a half-tile (= nt_max when halves is 1)
     int a_slots;              // dequantised-weight ring slots (<= MAX_A_SLOTS)
     int seg_smem_off;         // grouped: byte offset of the schedule table in dynamic smem
     int epi_smem_off;         // tcgen05 kernel: byte offset of the epilogue's staging buffer
