@@ -62,6 +62,11 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.orc_grouped.argtypes = [P, L, P, P, P, P, P, P, P, I, I, I, I, I, P, I]
     lib.orc_qzeros_to_zero_points.restype = I
     lib.orc_qzeros_to_zero_points.argtypes = [P, I, I, P]
+    lib.orc_e4m3_to_double.restype = ctypes.c_double
+    lib.orc_e4m3_to_double.argtypes = [ctypes.c_uint8]
+    lib.orc_dequant_fp8.argtypes = [P, P, I, I, I, P]
+    lib.orc_gemm_fp8.argtypes = [P, L, I, P, P, I, I, I, P, I]
+    lib.orc_repack_fp8_tiles.argtypes = [P, I, I, P]
     lib.orc_moe_align_block_size.restype = I
     lib.orc_moe_align_block_size.argtypes = [P, I, I, I, I, I, P, P]
     lib.orc_moe_blocks.restype = I
@@ -229,6 +234,34 @@ class Oracle:
         self.lib.orc_grouped(_ptr(a), a.shape[1], _ptr(qw), _ptr(s), _ptr(z), _ptr(ids), _ptr(off),
                              _ptr(pairs), _ptr(pt), ids.size, k, n, group_size, weight_type,
                              _ptr(out), threads or default_threads())
+        return out
+
+    def e4m3(self, codes) -> np.ndarray:
+        """Doubles of E4M3 codes (uint8 array)."""
+        c = np.asarray(codes, dtype=np.uint8)
+        return np.array([self.lib.orc_e4m3_to_double(int(x)) for x in c.ravel()]).reshape(c.shape)
+
+    def dequant_fp8(self, qweight, scales, k, n, group_size=128):
+        qw, s = _c(qweight, np.int32), _h(scales)
+        out = np.empty((k, n), dtype=np.float64)
+        self.lib.orc_dequant_fp8(_ptr(qw), _ptr(s), k, n, group_size, _ptr(out))
+        return out
+
+    def gemm_fp8(self, a, qweight, scales, group_size=128, threads: int | None = None):
+        """C [M][N] in double with FP8 E4M3 weights ([K/4, N] words of 4 K-consecutive bytes)."""
+        a = _h(a)
+        m, k = a.shape
+        qw, s = _c(qweight, np.int32), _h(scales)
+        n = qw.shape[1]
+        out = np.empty((m, n), dtype=np.float64)
+        self.lib.orc_gemm_fp8(_ptr(a), k, m, _ptr(qw), _ptr(s), k, n, group_size, _ptr(out),
+                              threads or default_threads())
+        return out
+
+    def repack_fp8_tiles(self, qweight, k, n) -> np.ndarray:
+        qw = _c(qweight, np.int32)
+        out = np.empty(k * n // 4, dtype=np.int32)
+        self.lib.orc_repack_fp8_tiles(_ptr(qw), k, n, _ptr(out))
         return out
 
     def moe_align_block_size(self, topk_ids, m, top_k, n_experts, block_size, capacity=None):

@@ -461,6 +461,119 @@ void orc_grouped(const uint16_t *a, long lda, const int32_t *qweight_stack,
 }
 
 /* ---------------------------------------------------------------------------------------
+ * FP8 E4M3 weights (W8A16).  [vllm_marlin.rs] scalar id FERRUM_MARLIN_SCALAR_FE4M3FN and
+ * `vllm_fp8_marlin_repack_raw_bits`: the weights arrive as [K/4, N] 32-bit words, each holding
+ * four consecutive K-axis E4M3 bytes of one output column, little-endian (row 4r+i at byte i
+ * of word (r, n)); [marlin.rs] Marlin-MoE validation: E4M3 takes group_size -1 or 128 and no
+ * zero points.  W[k][n] = e4m3(code) * scales[g(k)][n].
+ *
+ * E4M3 ("fn" variant) from its definition: 1 sign bit, 4 exponent bits with bias 7, 3 fraction
+ * bits; exponent 0 is subnormal (fraction/8 * 2^-6); exponent 15 with fraction 7 is NaN, and
+ * there are no infinities (exponent 15 with fraction 0..6 is an ordinary value up to 448).
+ * ------------------------------------------------------------------------------------- */
+double orc_e4m3_to_double(uint8_t code)
+{
+    int sign = (code >> 7) & 1;
+    int expo = (code >> 3) & 0xF;
+    int frac = code & 0x7;
+    double v;
+    if (expo == 15 && frac == 7)
+        return NAN;
+    if (expo == 0)
+        v = ldexp((double)frac / 8.0, -6);
+    else
+        v = ldexp(1.0 + frac / 8.0, expo - 7);
+    return sign ? -v : v;
+}
+
+static int orc_fp8_code(const int32_t *qweight, int n, int row, int col)
+{
+    uint32_t word = (uint32_t)qweight[(long)(row / 4) * n + col];
+    return (int)((word >> (8 * (row % 4))) & 0xFFu);
+}
+
+/* Dequantised FP8 matrix W [K][N] in double. */
+void orc_dequant_fp8(const int32_t *qweight, const uint16_t *scales, int k, int n, int group_size,
+                     double *w)
+{
+    for (int row = 0; row < k; ++row) {
+        int g = group_size == -1 ? 0 : row / group_size;
+        for (int col = 0; col < n; ++col)
+            w[(long)row * n + col] = orc_e4m3_to_double((uint8_t)orc_fp8_code(qweight, n, row, col)) *
+                                     orc_half_to_double(scales[(long)g * n + col]);
+    }
+}
+
+/* C = A W with the FP8 weights: W derived once, then the plain k-ordered double sums (one
+ * thread per band of columns, as orc_gemm). */
+struct orc_fp8_job {
+    const uint16_t *a; long lda; int m; const double *w; int k, n; double *c; int c0, c1;
+};
+
+static void *orc_fp8_worker(void *arg)
+{
+    struct orc_fp8_job *jb = (struct orc_fp8_job *)arg;
+    for (int i = 0; i < jb->m; ++i)
+        for (int j = jb->c0; j < jb->c1; ++j) {
+            double acc = 0.0;
+            for (int row = 0; row < jb->k; ++row)
+                acc += orc_half_to_double(jb->a[(long)i * jb->lda + row]) * jb->w[(long)row * jb->n + j];
+            jb->c[(long)i * jb->n + j] = acc;
+        }
+    return NULL;
+}
+
+void orc_gemm_fp8(const uint16_t *a, long lda, int m, const int32_t *qweight, const uint16_t *scales,
+                  int k, int n, int group_size, double *c, int nthreads)
+{
+    double *w = (double *)malloc(sizeof(double) * (size_t)k * (size_t)n);
+    orc_dequant_fp8(qweight, scales, k, n, group_size, w);
+    if (nthreads < 1)
+        nthreads = 1;
+    if (nthreads > n)
+        nthreads = n;
+    if (nthreads > 256)
+        nthreads = 256;
+    pthread_t tid[256];
+    struct orc_fp8_job jobs[256];
+    for (int t = 0; t < nthreads; ++t) {
+        struct orc_fp8_job jb = {a, lda, m, w, k, n, c, (int)((long)n * t / nthreads),
+                                 (int)((long)n * (t + 1) / nthreads)};
+        jobs[t] = jb;
+    }
+    for (int t = 1; t < nthreads; ++t)
+        pthread_create(&tid[t], NULL, orc_fp8_worker, &jobs[t]);
+    orc_fp8_worker(&jobs[0]);
+    for (int t = 1; t < nthreads; ++t)
+        pthread_join(tid[t], NULL);
+    free(w);
+}
+
+/* The library's FP8 tile layout, from its definition (the pages' own FP8 Marlin tiles are
+ * another layout; this one is this project's).  Tile (nt, kb): rows kb*64 .. kb*64+63, columns
+ * nt*128 .. nt*128+127, 2048 words at word (nt * K/64 + kb) * 2048.  Word (q, c, t) at
+ * q*512 + c*4 + t, q and t in 0..3, c in 0..127, holds rows kb*64 + 16q + 4t + i of column
+ * nt*128 + c at byte i (i in 0..3). */
+void orc_repack_fp8_tiles(const int32_t *qweight, int k, int n, int32_t *out)
+{
+    int kblocks = k / 64, ntiles = n / 128;
+    for (int nt = 0; nt < ntiles; ++nt)
+        for (int kb = 0; kb < kblocks; ++kb) {
+            long base = ((long)nt * kblocks + kb) * 2048;
+            for (int q = 0; q < 4; ++q)
+                for (int c = 0; c < 128; ++c)
+                    for (int t = 0; t < 4; ++t) {
+                        uint32_t word = 0;
+                        for (int i = 0; i < 4; ++i) {
+                            int row = kb * 64 + 16 * q + 4 * t + i;
+                            word |= (uint32_t)orc_fp8_code(qweight, n, row, nt * 128 + c) << (8 * i);
+                        }
+                        out[base + q * 512 + c * 4 + t] = (int32_t)word;
+                    }
+        }
+}
+
+/* ---------------------------------------------------------------------------------------
  * The vLLM Marlin-MoE routing.  [marlin.rs] `ferrum_vllm_marlin_moe_f16` declaration and
  * `marlin_gemm_moe_vllm` doc: the caller first runs `moe_align_block_size`, which lists, for
  * each expert in turn, the flattened (token, slot) ids routed to it -- id = token * top_k + slot

@@ -123,6 +123,19 @@ def qweight(seed: int, k: int, n: int, name: str = "qweight") -> np.ndarray:
     return Stream(seed, name).words((k // 8) * n).reshape(k // 8, n)
 
 
+def fp8_weights(seed: int, k: int, n: int, name: str = "fp8") -> np.ndarray:
+    """int32 [k/4, n]: four K-consecutive E4M3 codes per word (row 4r+i at byte i), each code
+    uniform over the 254 codes that are numbers (the two NaN codes 0x7F and 0xFF are skipped)."""
+    u = Stream(seed, name).uniform(k * n)
+    idx = np.floor(u * 254).astype(np.int64)
+    codes = idx + (idx >= 0x7F) + (idx >= 0xFE)
+    codes = codes.reshape(k // 4, 4, n)          # [word row][byte][column], byte i = row 4r+i
+    words = np.zeros((k // 4, n), dtype=np.uint32)
+    for i in range(4):
+        words |= codes[:, i, :].astype(np.uint32) << np.uint32(8 * i)
+    return words.view(np.int32)
+
+
 def scales(seed: int, groups: int, n: int, lo: float = 0.001, hi: float = 0.02,
            name: str = "scales") -> np.ndarray:
     """fp16 [groups, n] ~ U[lo, hi)."""

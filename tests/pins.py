@@ -450,6 +450,92 @@ def pin_grouped_closed_form(orc):
     return None
 
 
+# --- FP8 E4M3 weights (W8A16) -----------------------------------------------------------------
+
+def _fp8_pack(codes: np.ndarray) -> np.ndarray:
+    """[K][N] uint8 codes -> [K/4][N] int32 words, row 4r+i at byte i (the pages' FP8 input ABI)."""
+    k, n = codes.shape
+    c = codes.astype(np.uint32).reshape(k // 4, 4, n)
+    w = np.zeros((k // 4, n), dtype=np.uint32)
+    for i in range(4):
+        w |= c[:, i, :] << np.uint32(8 * i)
+    return w.view(np.int32)
+
+
+def pin_e4m3_decode_all_codes(orc):
+    """Every E4M3 code decodes as torch's float8_e4m3fn does (a library routine): 0x38 = 1,
+    0x7E = 448, 0x01 = 2^-9, NaN only at 0x7F and 0xFF."""
+    import torch
+    codes = np.arange(256, dtype=np.uint8)
+    got = orc.e4m3(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    if not np.array_equal(np.isnan(got), np.isnan(ref)) or not np.array_equal(got[~np.isnan(got)], ref[~np.isnan(ref)]):
+        return "e4m3 decode differs from float8_e4m3fn"
+    if got[0x38] != 1.0 or got[0x7E] != 448.0 or got[0x01] != 2.0 ** -9 or got[0xB8] != -1.0:
+        return "e4m3 landmarks"
+    return None
+
+
+def pin_fp8_byte_order_and_groups(orc):
+    """Codes f(k, n) packed little-endian along K, power-of-two group scales 2^-g (group 128)
+    and per-column factors: W[k][n] = e4m3(f(k, n)) * 2^-(k//128) * c_n exactly."""
+    k, n = 384, 24
+    codes = ((np.arange(k)[:, None] * 7 + np.arange(n)[None, :] * 13) % 254).astype(np.uint8)
+    codes[codes >= 0x7F] += 1
+    qw = _fp8_pack(codes)
+    col = (1 + np.arange(n) % 4).astype(np.float64)
+    s = np.array([[2.0 ** -g * col[j] for j in range(n)] for g in range(k // 128)], dtype=np.float16)
+    w = orc.dequant_fp8(qw, s, k, n, 128)
+    want = orc.e4m3(codes) * (2.0 ** -(np.arange(k) // 128))[:, None] * col[None, :]
+    bad = _mismatch("fp8 dequant", w, want)
+    if bad:
+        return bad
+    s1 = np.array([col], dtype=np.float16)   # channelwise: one group
+    w1 = orc.dequant_fp8(qw, s1, k, n, -1)
+    return _mismatch("fp8 channelwise", w1, orc.e4m3(codes) * col[None, :])
+
+
+def pin_fp8_gemm_one_hot_and_library(orc):
+    """One 1.0 (0x38) per column at row pi(n), zeros elsewhere, unit scales: C[:, n] =
+    A[:, pi(n)]; and a seeded GEMM equals the library matmul of the dequantised matrix."""
+    m, k, n = 5, 256, 32
+    a = synth.activations(71, m, k)
+    pi = (np.arange(n) * 37 + 3) % k
+    codes = np.zeros((k, n), dtype=np.uint8)
+    codes[pi, np.arange(n)] = 0x38
+    c = orc.gemm_fp8(a, _fp8_pack(codes), np.ones((2, n), dtype=np.float16), 128)
+    bad = _mismatch("fp8 one-hot", c, a[:, pi].astype(np.float64))
+    if bad:
+        return bad
+    qw = synth.fp8_weights(72, k, n)
+    s = synth.scales(72, 2, n, lo=1e-4, hi=2e-4)
+    c = orc.gemm_fp8(a, qw, s, 128)
+    want = a.astype(np.float64) @ orc.dequant_fp8(qw, s, k, n, 128)
+    return _mismatch("fp8 gemm vs library matmul", c, want, rtol=1e-12, atol=1e-12)
+
+
+def pin_fp8_tile_layout(orc):
+    """Every tile word is the source word (row 4 * (kb*16 + 4q + t) / 4, column nt*128 + c) --
+    the FP8 repack moves whole words -- and every source word appears exactly once."""
+    k, n = 128, 256
+    qw = synth.fp8_weights(73, k, n)
+    tiles = orc.repack_fp8_tiles(qw, k, n)
+    want = np.empty_like(tiles)
+    for nt in range(n // 128):
+        for kb in range(k // 64):
+            base = (nt * (k // 64) + kb) * 2048
+            for q in range(4):
+                for c in range(128):
+                    for t in range(4):
+                        want[base + q * 512 + c * 4 + t] = qw[kb * 16 + 4 * q + t, nt * 128 + c]
+    bad = _mismatch("fp8 tile words", tiles, want)
+    if bad:
+        return bad
+    if sorted(tiles.view(np.uint32).tolist()) != sorted(qw.view(np.uint32).ravel().tolist()):
+        return "fp8 tiles are not a permutation of the source words"
+    return None
+
+
 # --- vLLM Marlin-MoE routing (sorted_token_ids / expert_ids / sentinel rows) ------------------
 
 def pin_moe_align_examples(orc):

@@ -46,6 +46,11 @@ MUTATIONS = [
      "zero_points[(long)g * n + col] = (double)raw;"),
     ("group count ignores divisibility", "group_size % 16 != 0 || k % group_size != 0",
      "group_size % 16 != 0"),
+    ("e4m3 exponent bias", "v = ldexp(1.0 + frac / 8.0, expo - 7);", "v = ldexp(1.0 + frac / 8.0, expo - 8);"),
+    ("e4m3 subnormal scale", "v = ldexp((double)frac / 8.0, -6);", "v = ldexp((double)frac / 8.0, -7);"),
+    ("fp8 byte order", "return (int)((word >> (8 * (row % 4))) & 0xFFu);",
+     "return (int)((word >> (8 * (3 - row % 4))) & 0xFFu);"),
+    ("fp8 tile quarter and word swapped", "int row = kb * 64 + 16 * q + 4 * t + i;", "int row = kb * 64 + 16 * t + 4 * q + i;"),
     ("moe sentinel off by one", "sorted_ids[len + r] = n_ids; /* the sentinel */",
      "sorted_ids[len + r] = n_ids - 1; /* the sentinel */"),
     ("moe top-k weight dropped", "double w = topk_weights ? (double)topk_weights[id] : 1.0;", "double w = 1.0;"),
