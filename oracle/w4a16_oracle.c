@@ -513,13 +513,25 @@ struct orc_fp8_job {
 static void *orc_fp8_worker(void *arg)
 {
     struct orc_fp8_job *jb = (struct orc_fp8_job *)arg;
-    for (int i = 0; i < jb->m; ++i)
-        for (int j = jb->c0; j < jb->c1; ++j) {
-            double acc = 0.0;
-            for (int row = 0; row < jb->k; ++row)
-                acc += orc_half_to_double(jb->a[(long)i * jb->lda + row]) * jb->w[(long)row * jb->n + j];
-            jb->c[(long)i * jb->n + j] = acc;
+    int width = jb->c1 - jb->c0;
+    if (width <= 0)
+        return NULL;
+    double *acc = (double *)malloc(sizeof(double) * (size_t)width);
+    for (int i = 0; i < jb->m; ++i) {
+        for (int j = 0; j < width; ++j)
+            acc[j] = 0.0;
+        /* Row by row of W, so that the band's entries are read in memory order; every output
+         * is still the k-ordered sum of its products. */
+        for (int row = 0; row < jb->k; ++row) {
+            double av = orc_half_to_double(jb->a[(long)i * jb->lda + row]);
+            const double *wr = jb->w + (long)row * jb->n + jb->c0;
+            for (int j = 0; j < width; ++j)
+                acc[j] += av * wr[j];
         }
+        for (int j = 0; j < width; ++j)
+            jb->c[(long)i * jb->n + jb->c0 + j] = acc[j];
+    }
+    free(acc);
     return NULL;
 }
 
