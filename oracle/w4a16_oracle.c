@@ -524,9 +524,9 @@ static void *orc_fp8_worker(void *arg)
          * is still the k-ordered sum of its products. */
         for (int row = 0; row < jb->k; ++row) {
             double av = orc_half_to_double(jb->a[(long)i * jb->lda + row]);
-            const double *wr = jb->w + (long)row * jb->n + jb->c0;
+            const double *wrow = jb->w + (long)row * jb->n + jb->c0;
             for (int j = 0; j < width; ++j)
-                acc[j] += av * wr[j];
+                acc[j] += av * wrow[j];
         }
         for (int j = 0; j < width; ++j)
             jb->c[(long)i * jb->n + jb->c0 + j] = acc[j];
