@@ -523,10 +523,10 @@ static void *orc_fp8_worker(void *arg)
         /* Row by row of W, so that the band's entries are read in memory order; every output
          * is still the k-ordered sum of its products. */
         for (int row = 0; row < jb->k; ++row) {
-            double av = orc_half_to_double(jb->a[(long)i * jb->lda + row]);
+            double a_ik = orc_half_to_double(jb->a[(long)i * jb->lda + row]);
             const double *wrow = jb->w + (long)row * jb->n + jb->c0;
             for (int j = 0; j < width; ++j)
-                acc[j] += av * wrow[j];
+                acc[j] += a_ik * wrow[j];
         }
         for (int j = 0; j < width; ++j)
             jb->c[(long)i * jb->n + jb->c0 + j] = acc[j];

@@ -46,7 +46,7 @@ MUTATIONS = [
      "zero_points[(long)g * n + col] = (double)raw;"),
     ("group count ignores divisibility", "group_size % 16 != 0 || k % group_size != 0",
      "group_size % 16 != 0"),
-    ("fp8 dropped accumulation", "acc[j] += av * wrow[j];", "acc[j] = av * wrow[j];"),
+    ("fp8 dropped accumulation", "acc[j] += a_ik * wrow[j];", "acc[j] = a_ik * wrow[j];"),
     ("e4m3 exponent bias", "v = ldexp(1.0 + frac / 8.0, expo - 7);", "v = ldexp(1.0 + frac / 8.0, expo - 8);"),
     ("e4m3 subnormal scale", "v = ldexp((double)frac / 8.0, -6);", "v = ldexp((double)frac / 8.0, -7);"),
     ("fp8 byte order", "return (int)((word >> (8 * (row % 4))) & 0xFFu);",
