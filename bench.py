@@ -45,7 +45,7 @@ if ROOT not in sys.path:
 import synth  # noqa: E402
 
 METRIC = "W4A16 GEMM TFLOP/s and weight HBM GB/s vs M=1..4096 (fraction of roofline)"
-U4, U4B8 = 4, 5
+U4, U4B8, FE4M3 = 4, 5, 8
 FLAG_ACT_ORDER, FLAG_IS_K_FULL, FLAG_HAS_ZP = 1 << 1, 1 << 2, 1 << 3
 # Inference weights are written once, long before the GEMMs that read them.
 FLAG_STATIC_WEIGHTS = 1 << 12
@@ -73,6 +73,10 @@ def workload_specs(name: str):
     elif name == "actorder":
         specs = [dict(m=m, k=8192, n=28672, gs=128, wt=U4B8, act_order=True, sigma=1.0, seed=3000 + m)
                  for m in (1, 16, 2048)]
+    elif name == "fp8":
+        # FP8 E4M3 weights (W8A16), group 128, on the prefill FFN shape across M.
+        specs = [dict(m=m, k=4096, n=11008, gs=128, wt=FE4M3, act_order=False, sigma=1.0, seed=6000 + m)
+                 for m in (1, 16, 256, 1024, 4096)]
     elif name == "tiny":
         specs = [dict(m=16, k=256, n=256, gs=128, wt=U4B8, act_order=False, sigma=1.0, seed=0)]
     elif name == "moe_swiglu":
@@ -106,6 +110,7 @@ WORKLOAD_TEXT = {
     "prefill": "prefill M in {256,1024,4096} x (K=4096,N=11008),(K=11008,N=4096), group 128, u4 + fp16 zeros",
     "actorder": "act-order M in {1,16,2048}, K=8192, N=28672, group 128, u4b8, shuffled g_idx",
     "tiny": "tiny M=16, K=256, N=256, group 128, u4b8",
+    "fp8": "FP8 E4M3 weights (W8A16) M in {1,16,256,1024,4096}, K=4096, N=11008, group 128, scales ~U[1e-4,2e-4]",
     "moe": "grouped MoE 8 experts, 512 tokens top-2, gate_up K=4096 N=28672 + down K=14336 N=4096, u4b8",
     "moe_blocks": ("grouped MoE 8 experts, 512 tokens top-2 through the vLLM block routing (blocks of "
                    "64 rows, sentinel padding): gate_up K=4096 N=28672 + down K=14336 N=4096 x top-k "
@@ -119,7 +124,8 @@ WORKLOAD_TEXT["all"] = ("M=1..4096, every configuration in one step: " +
 
 def weight_bytes(s) -> int:
     g = synth.group_count(s["k"], s["gs"])
-    return s["k"] * s["n"] // 2 + g * s["n"] * 2 * (2 if s["wt"] == U4 else 1)
+    codes = s["k"] * s["n"] if s["wt"] == FE4M3 else s["k"] * s["n"] // 2
+    return codes + g * s["n"] * 2 * (2 if s["wt"] == U4 else 1)
 
 
 def gemm_bytes(s) -> int:
@@ -294,16 +300,22 @@ class DenseGemm:
         k, n, m, gs = s["k"], s["n"], s["m"], s["gs"]
         groups = synth.group_count(k, gs)
         a = synth.activations(s["seed"], m, k, sigma=s["sigma"])
-        qw = torch.from_numpy(synth.qweight(s["seed"], k, n)).to(dev)
+        fp8 = s["wt"] == FE4M3
+        qw = torch.from_numpy(synth.fp8_weights(s["seed"], k, n) if fp8 else
+                              synth.qweight(s["seed"], k, n)).to(dev)
         perm = g_idx = None
         if s["act_order"]:
             p = synth.permutation(s["seed"], k)
             perm = torch.from_numpy(p).to(dev)
             g_idx = torch.from_numpy(synth.act_order_gidx(p, gs)).to(dev)
-        packed = torch.empty(k * n // 8, dtype=torch.int32, device=dev)
-        w4.w4_repack(qw, perm, packed, k, n)
+        if fp8:
+            packed = torch.empty(k * n // 4, dtype=torch.int32, device=dev)
+            w4.w8_repack(qw, packed, k, n)
+        else:
+            packed = torch.empty(k * n // 8, dtype=torch.int32, device=dev)
+            w4.w4_repack(qw, perm, packed, k, n)
         del qw
-        scales = torch.from_numpy(synth.scales(s["seed"], groups, n)).to(dev)
+        scales = torch.from_numpy(synth.scales(s["seed"], groups, n, *((1e-4, 2e-4) if fp8 else ()))).to(dev)
         zeros = torch.from_numpy(synth.zeros(s["seed"], groups, n)).to(dev) if s["wt"] == U4 else None
         self.b = [packed] + [packed.clone() for _ in range(copies - 1)]
         self.scales = [scales] + [scales.clone() for _ in range(copies - 1)]
@@ -522,7 +534,7 @@ def kernel_of(w4, g) -> int:
     """The library's kernel for one GEMM of the workload (0 tcgen05, 1 split-K small-M,
     2 column-slice small-M); grouped calls always run the tcgen05 kernel."""
     s = g.s
-    if s.get("grouped"):
+    if s.get("grouped") or s["wt"] == FE4M3:   # grouped and FP8 calls: always tcgen05
         return 0
     return w4.w4a16_kernel_for(s["m"], s["n"], s["k"], s["gs"], g.flags)
 
@@ -761,6 +773,9 @@ def _oracle_inputs(s, rows: int):
         qw = synth.qweight(s["seed"] * 100, k, n)
         a = synth.activations(s["seed"], rows, k)
         return a, qw, synth.scales(s["seed"], g, n), None, None
+    if s["wt"] == FE4M3:
+        return (synth.activations(s["seed"], rows, k, sigma=s["sigma"]), synth.fp8_weights(s["seed"], k, n),
+                synth.scales(s["seed"], g, n, 1e-4, 2e-4), None, None)
     qw = synth.qweight(s["seed"], k, n)
     z = synth.zeros(s["seed"], g, n) if s["wt"] == U4 else None
     g_idx = synth.act_order_gidx(synth.permutation(s["seed"], k), s["gs"]) if s.get("act_order") else None
@@ -793,7 +808,10 @@ def oracle_sample(workload: str, budget_s: float, threads: int | None = None):
     def seconds(s, r):
         a, qw, sc, z, g_idx = _oracle_inputs(s, r)
         t0 = time.perf_counter()
-        orc.gemm(a, qw, sc, z, g_idx, s["gs"], s["wt"], threads=threads)
+        if s["wt"] == FE4M3:
+            orc.gemm_fp8(a, qw, sc, s["gs"], threads=threads)
+        else:
+            orc.gemm(a, qw, sc, z, g_idx, s["gs"], s["wt"], threads=threads)
         return time.perf_counter() - t0
 
     per_gemm = budget_s / max(1, len(specs))
@@ -819,6 +837,18 @@ def oracle_sample(workload: str, budget_s: float, threads: int | None = None):
             f"row and at up to 4096 rows), fp64 on {threads} threads; the step time is the "
             f"two-point fit (W derivation + rows x per-row time) summed over the GEMMs")
     return est, threads, text
+
+
+def _dequant_fp8_fp32(qw, scales, gs):
+    """[K][N] fp32 weights e4m3(code) * s from [K/4][N] words of four K-consecutive codes (row
+    4r+i at byte i), decoded by torch's float8_e4m3fn, for the BLAS baseline."""
+    import torch
+    k4, n = qw.shape
+    codes = qw.view(np.uint8).reshape(k4, n, 4).transpose(0, 2, 1).reshape(k4 * 4, n)
+    w = torch.from_numpy(np.ascontiguousarray(codes)).view(torch.float8_e4m3fn).float().numpy()
+    k = k4 * 4
+    g = np.arange(k) // (gs if gs > 0 else k)
+    return w * scales.astype(np.float32)[g]
 
 
 def _dequant_fp32(qw, scales, zeros, gs, wt):
@@ -849,7 +879,7 @@ def blas_sample(workload: str, repeats: int = 3):
         rows = s["n_tok"] * s["top_k"] if s.get("grouped") else s["m"]
         per = rows // s["n_exp"] if s.get("grouped") else rows
         a, qw, sc, z, _ = _oracle_inputs(s, per)
-        w = _dequant_fp32(qw, sc, z, s["gs"], s["wt"])
+        w = _dequant_fp8_fp32(qw, sc, s["gs"]) if s["wt"] == FE4M3 else _dequant_fp32(qw, sc, z, s["gs"], s["wt"])
         a32 = a.astype(np.float32)
         best = float("inf")
         for _ in range(repeats):

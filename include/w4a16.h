@@ -42,6 +42,8 @@ extern "C" {
 /* Weight types: the scalar ids of ferrum-kernels 0.8.4 vllm_marlin.rs (FERRUM_MARLIN_SCALAR_*). */
 #define W4A16_TYPE_U4 4   /* codes with an explicit fp16 zero point per (group, column) */
 #define W4A16_TYPE_U4B8 5 /* symmetric codes, zero point 8                              */
+#define W4A16_TYPE_FE4M3 8 /* 8-bit FP8 E4M3 ("fn") weights, W8A16: w = e4m3(code) * s,
+                              no zero points (scalar FERRUM_MARLIN_SCALAR_FE4M3FN)      */
 
 /* Flags.  Bits 1..3 keep the positions of the page's FERRUM_MARLIN_HAS_ACT_ORDER,
  * FERRUM_MARLIN_IS_K_FULL and FERRUM_MARLIN_HAS_ZERO_POINTS (vllm_marlin.rs). */
@@ -148,6 +150,24 @@ int w4_repack(const int32_t *qweight, const int32_t *perm, int32_t *b_packed, in
 int w4_gate_up_interleave(const void *src, void *dst, int rows, int n2, int elem_bytes,
                           cudaStream_t stream);
 
+/* FP8 E4M3 weights (W8A16).  Input: int32 [K/4][N], each word holding four K-consecutive E4M3
+ * codes of one column, row 4r+i at byte i (little-endian) -- the input ABI of vllm_marlin.rs
+ * `vllm_fp8_marlin_repack_raw_bits`; a checkpoint's row-major [N][K] bytes are transposed into
+ * it.  Output (this library's FP8 tile layout, K*N/4 words): tile (nt, kb) covers rows
+ * kb*64 .. kb*64+63 and columns nt*128 .. nt*128+127 at word (nt * K/64 + kb) * 2048; word
+ * q*512 + c*4 + t (q, t in 0..3, c in 0..127) is the input word of rows kb*64 + 16q + 4t .. +3
+ * of column nt*128 + c, so each thread of the kernel reads its column's 64 rows as four 16-byte
+ * loads.  K % 128 == 0, N % 256 == 0; 16-byte aligned; the buffers must not overlap.
+ * W4A16_TYPE_FE4M3 GEMMs (w4a16_gemm, _grouped, _moe_blocks) take these tiles, fp16 scales
+ * [G][N] with group_size -1 or a positive multiple of 64 dividing K (the pages' FP8 Marlin
+ * takes -1 or 128), no zero points, no act-order, and always run the tcgen05 kernel (the
+ * small-M and CUDA-core kernels are 4-bit only: forcing them is rejected).  Each code becomes
+ * its exact fp16 value (cvt.rn.f16x2.e4m3x2); the product with the scale is rounded once. */
+int w8_repack(const int32_t *qweight, int32_t *b_packed, int k, int n, cudaStream_t stream);
+
+/* FP8 tiles -> the [K/4][N] input words (the inverse of w8_repack). */
+int w8_unpack(const int32_t *b_packed, int32_t *qweight, int k, int n, cudaStream_t stream);
+
 /* Tile layout -> GPTQ words of the sorted rows (the inverse of w4_repack; a permutation
  * applied at repack time is not undone).  Same shape, alignment and overlap rules. */
 int w4_unpack(const int32_t *b_packed, int32_t *qweight, int k, int n, cudaStream_t stream);
@@ -182,7 +202,8 @@ size_t w4a16_workspace_size(int m, int n, int k, int group_size, unsigned flags,
  *   m          >= 0 (0 is a no-op);  n % 256 == 0;  k % 128 == 0
  *   group_size -1 (one group) or a positive multiple of 16 dividing K
  *              (transformer.rs `marlin_num_groups`; marlin.rs Marlin-MoE validation)
- *   weight_type W4A16_TYPE_U4B8 (zeros NULL) or W4A16_TYPE_U4 (zeros and W4A16_FLAG_HAS_ZP)
+ *   weight_type W4A16_TYPE_U4B8 (zeros NULL), W4A16_TYPE_U4 (zeros and W4A16_FLAG_HAS_ZP) or
+ *              W4A16_TYPE_FE4M3 (FP8 tiles from w8_repack; zeros NULL, see there)
  *   flags      W4A16_FLAG_*; ACT_ORDER exactly when g_idx and perm are given.  With
  *              W4A16_FLAG_SWIGLU or _GEGLU, N = 2I columns of interleaved gate/up weights
  *              (w4_gate_up_interleave) and c receives H [M][ldc], ldc >= I, with

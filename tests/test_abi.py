@@ -27,7 +27,7 @@ def w4():
 def header_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(w4(?:a16)?_\w+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(w[48](?:a16)?_\w+)\s*\(", text)))
 
 
 def test_header_symbols_exported(w4):
@@ -164,15 +164,17 @@ def test_workspace_size_host_only(w4):
 def test_token_tile_height_from_workspace(w4):
     """The tcgen05 kernel's token-tile height, read back from the workspace size on a 152-SM
     device (the partial slots are 2 x nt x 128 fp32 per CTA): one tile up to 256 rows; above
-    that ceil(M / 224) equal tiles rounded up to 16 rows, never below 192."""
+    that ceil(M / 224) equal tiles rounded up to 16 rows, never below 192 -- unless a pair of
+    half-tiles (each at most 192 rows) needs fewer tiles: then ceil(M / 384) pairs of two equal
+    halves rounded up to 16 rows (M=449: 2 pairs of 2 x 128 instead of 3 tiles of 192)."""
     def nt_of(m, n=256):
         total = w4.w4a16_workspace_size(m, n, 128, 128, 0, 152)
         slots = 152 * 2 * 128 * 4
         head = total % slots
         assert head % 256 == 0
         return total // slots
-    expect = {100: 112, 256: 256, 257: 192, 448: 224, 449: 192, 512: 192, 600: 208, 672: 224,
-              1024: 208, 2048: 208, 4096: 224, 8192: 224}
+    expect = {100: 112, 256: 256, 257: 288, 448: 224, 449: 256, 512: 256, 600: 320, 672: 352,
+              1024: 352, 2048: 352, 4096: 384, 8192: 384}
     assert {m: nt_of(m) for m in expect} == expect
 
 

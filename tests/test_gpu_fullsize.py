@@ -79,7 +79,7 @@ def run_dense(w4, spec):
 
 
 DENSE = [(wl, f"{s['m']},{s['k']},{s['n']}")
-         for wl in ("decode", "prefill", "actorder") for s in bench.workload_specs(wl)]
+         for wl in ("decode", "prefill", "actorder", "fp8") for s in bench.workload_specs(wl)]
 
 
 @pytest.mark.parametrize("workload,shape", DENSE)
@@ -87,6 +87,15 @@ def test_full_size_dense(w4, orc, workload, shape):
     spec = dict(bench.select_shape(bench.workload_specs(workload), shape)[0])
     g = run_dense(w4, spec)
     rows = sample_rows(spec["m"])
+    if spec["wt"] == bench.FE4M3:
+        a = synth.activations(spec["seed"], spec["m"], spec["k"], sigma=spec["sigma"])[rows]
+        qw = synth.fp8_weights(spec["seed"], spec["k"], spec["n"])
+        s = synth.scales(spec["seed"], synth.group_count(spec["k"], spec["gs"]), spec["n"], 1e-4, 2e-4)
+        ref = orc.gemm_fp8(np.ascontiguousarray(a), qw, s, spec["gs"])
+        got = g.c[rows].float().cpu().numpy().astype(np.float64)
+        ok, msg = within_tol(got, ref)
+        assert ok, f"{workload} {shape} ({len(rows)} rows): {msg}"
+        return
     a, qw, scales, zeros, g_idx = dense_inputs(spec, rows)
     ref = orc.gemm(a, qw, scales, zeros, g_idx, spec["gs"], spec["wt"])
     got = g.c[rows].float().cpu().numpy().astype(np.float64)

@@ -17,6 +17,7 @@ from .build import LIB_PATH
 
 W4A16_TYPE_U4 = 4
 W4A16_TYPE_U4B8 = 5
+W4A16_TYPE_FE4M3 = 8
 
 W4A16_FLAG_ACT_ORDER = 1 << 1
 W4A16_FLAG_IS_K_FULL = 1 << 2
@@ -72,6 +73,8 @@ _SIGNATURES = {
     "w4a16_zero_points_check": (_I, [_P, _LL, _P, _P]),
     "w4a16_kernel_for": (_I, [_I, _I, _I, _I, _U, _I]),
     "w4_gate_up_interleave": (_I, [_P, _P, _I, _I, _I, _P]),
+    "w8_repack": (_I, [_P, _P, _I, _I, _P]),
+    "w8_unpack": (_I, [_P, _P, _I, _I, _P]),
     "w4a16_moe_align_block_size": (_I, [_P, _I, _I, _I, _I, _I, _P, _P]),
     "w4a16_moe_blocks_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I, _U, _I]),
     "w4a16_gemm_moe_blocks": (_I, [_P, _I, _P, _P, _I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I,
@@ -142,6 +145,16 @@ def w4_gate_up_interleave(src, dst, rows: int, n2: int, stream=None) -> None:
     int32 GPTQ words or fp16 scales / zeros), for W4A16_FLAG_SWIGLU / _GEGLU."""
     _check("w4_gate_up_interleave", _lib.w4_gate_up_interleave(
         _ptr(src), _ptr(dst), rows, n2, src.element_size(), _stream(stream)))
+
+
+def w8_repack(qweight, b_packed, k: int, n: int, stream=None) -> None:
+    """FP8 E4M3 [K/4, N] words (four K-consecutive codes each) -> FP8 tile layout."""
+    _check("w8_repack", _lib.w8_repack(_ptr(qweight), _ptr(b_packed), k, n, _stream(stream)))
+
+
+def w8_unpack(b_packed, qweight, k: int, n: int, stream=None) -> None:
+    """FP8 tile layout -> [K/4, N] words."""
+    _check("w8_unpack", _lib.w8_unpack(_ptr(b_packed), _ptr(qweight), k, n, _stream(stream)))
 
 
 def w4_unpack(b_packed, qweight, k: int, n: int, stream=None) -> None:

@@ -59,6 +59,7 @@ struct Plan {
     int act_rows = 0;   // rows of one activation box (slice kernel: M; pairs: a half-tile;
                         // others: nt_max)
     int halves = 1, nt_half = 0; // tcgen05: token tile as a pair of half-tiles (halves 2)
+    int tile_bytes = TILE_BYTES; // one packed 64 x 128 tile (FP8: twice as large)
     int split = 0;    // tile-aligned split factor (0: stream-K)
     int n_slices = 0, slice_per = 0;
     long long counters_off, partials_off, a_off, total;
@@ -237,7 +238,7 @@ void stage_layout(Plan &pl, int kbs, int group_size, int g_rows, bool has_zp)
     const int sg = (kbs * KBLK + group_size - 1) / group_size + 1;
     pl.sg_box = sg < g_rows ? sg : g_rows;
     pl.packed_off = halves * kbs * pl.act_kb_bytes; // [half][block][rows x 128 B]
-    pl.scales_off = pl.packed_off + kbs * TILE_BYTES;
+    pl.scales_off = pl.packed_off + kbs * pl.tile_bytes;
     pl.zeros_off = pl.scales_off + (int)round_up((long long)pl.sg_box * SG_BYTES, 128);
     const int end = has_zp ? pl.zeros_off + pl.sg_box * SG_BYTES : pl.zeros_off;
     pl.stage_bytes = (int)round_up(end, 1024);
@@ -423,7 +424,8 @@ int encode_slice_weight_map(CUtensorMap *map, const void *base, int n, int k, in
 int check_weights(const void *b, const void *scales, const void *zeros, int n, int k, int group_size,
                   int weight_type, unsigned flags)
 {
-    if (weight_type != W4A16_TYPE_U4 && weight_type != W4A16_TYPE_U4B8)
+    if (weight_type != W4A16_TYPE_U4 && weight_type != W4A16_TYPE_U4B8 &&
+        weight_type != W4A16_TYPE_FE4M3)
         return status_of(STAGE_ARG, W4A16_ARG_TYPE);
     if (n <= 0 || k <= 0)
         return status_of(STAGE_ARG, W4A16_ARG_SHAPE);
@@ -435,14 +437,43 @@ int check_weights(const void *b, const void *scales, const void *zeros, int n, i
         return status_of(STAGE_UNSUPPORTED, W4A16_ARG_SHAPE);
     if (num_groups(k, group_size) < 0)
         return status_of(STAGE_ARG, W4A16_ARG_GROUP);
+    // FP8 weights: groups of whole 64-row blocks (the pages' Marlin-MoE rule is -1 or 128).
+    if (weight_type == W4A16_TYPE_FE4M3 && group_size != -1 && group_size % KBLK != 0)
+        return status_of(STAGE_ARG, W4A16_ARG_GROUP);
     const bool has_zp_flag = (flags & W4A16_FLAG_HAS_ZP) != 0;
     if (has_zp_flag != (zeros != nullptr))
         return status_of(STAGE_ARG, W4A16_ARG_FLAGS);
     if ((weight_type == W4A16_TYPE_U4) != (zeros != nullptr))
         return status_of(STAGE_ARG, W4A16_ARG_FLAGS);
-    if ((long long)k * n / 8 > (1LL << 40))
+    if ((long long)k * n / 4 > (1LL << 40))
         return status_of(STAGE_ARG, W4A16_ARG_OVERFLOW);
     return 0;
+}
+
+// FP8 weights run on the tcgen05 kernel only, without act-order (the pages' FP8 Marlin has
+// neither zero points nor act-order).
+int check_fp8_flags(int weight_type, unsigned flags)
+{
+    if (weight_type != W4A16_TYPE_FE4M3)
+        return 0;
+    if (flags & (W4A16_FLAG_ACT_ORDER | W4A16_FLAG_FORCE_SIMT | W4A16_FLAG_FORCE_MMA |
+                 W4A16_FLAG_FORCE_SLICE))
+        return status_of(STAGE_ARG, W4A16_ARG_FLAGS);
+    return 0;
+}
+
+int tile_bytes_of(int weight_type)
+{
+    return weight_type == W4A16_TYPE_FE4M3 ? TILE_BYTES_FP8 : TILE_BYTES;
+}
+
+// The packed-tile geometry of a call's weight type, after fill_params.
+void set_weight_type(GemmParams &p, int weight_type)
+{
+    const bool w8 = weight_type == W4A16_TYPE_FE4M3;
+    p.w8 = w8 ? 1 : 0;
+    p.tile_words = w8 ? TILE_WORDS_FP8 : TILE_WORDS;
+    p.tile_bytes = w8 ? TILE_BYTES_FP8 : TILE_BYTES;
 }
 
 int launch_status(int err)
@@ -691,6 +722,8 @@ void fill_params(GemmParams &p, const Plan &pl, int m, int n, int k, int group_s
     p.split = pl.split;
     p.n_slices = pl.n_slices;
     p.slice_per = pl.slice_per;
+    p.tile_words = TILE_WORDS;
+    p.tile_bytes = TILE_BYTES;
 }
 
 // Tensor maps of one launch: activations (3-D, swizzled) and the scale / zero rows.  With no
@@ -762,18 +795,22 @@ int dense_gemm(const void *a, int lda, const int32_t *b_packed, void *c, int ldc
     st = check_kernel_flags(m, gs_resolved, flags);
     if (st)
         return st;
+    st = check_fp8_flags(weight_type, flags);
+    if (st)
+        return st;
 
     int num_sms = 0;
     int err = sm_count(&num_sms);
     if (err != cudaSuccess)
         return status_of(STAGE_RESOURCE, err);
-    const int kernel = choose_kernel(m, n, gs_resolved, flags, num_sms);
+    const int kernel = weight_type == W4A16_TYPE_FE4M3 ? 0 : choose_kernel(m, n, gs_resolved, flags, num_sms);
     Plan pl;
     dense_plan(pl, m, n, k, flags, num_sms, kernel, tile_cap);
     if (workspace_bytes < (size_t)pl.total)
         return status_of(STAGE_ARG, W4A16_ARG_WORKSPACE);
     const int g = num_groups(k, group_size);
     plan_tmem(pl);
+    pl.tile_bytes = tile_bytes_of(weight_type);
     err = plan_smem(pl, false, zeros != nullptr, group_size == -1 ? k : group_size, g);
     if (err != cudaSuccess)
         return status_of(STAGE_RESOURCE, err);
@@ -781,6 +818,7 @@ int dense_gemm(const void *a, int lda, const int32_t *b_packed, void *c, int ldc
     char *ws = static_cast<char *>(workspace);
     GemmParams p;
     fill_params(p, pl, m, n, k, group_size);
+    set_weight_type(p, weight_type);
     p.b = b_packed;
     p.scales = static_cast<const __half *>(scales);
     p.zeros = static_cast<const __half *>(zeros);
@@ -879,6 +917,42 @@ int w4_repack(const int32_t *qweight, const int32_t *perm, int32_t *b_packed, in
     return launch_status(launch_repack(qweight, perm, b_packed, status, k, n, stream));
 }
 
+int w8_repack(const int32_t *qweight, int32_t *b_packed, int k, int n, cudaStream_t stream)
+{
+    if (k <= 0 || n <= 0)
+        return status_of(STAGE_ARG, W4A16_ARG_SHAPE);
+    if (!qweight || !b_packed)
+        return status_of(STAGE_ARG, W4A16_ARG_NULL);
+    if (!aligned(qweight, 16) || !aligned(b_packed, 16))
+        return status_of(STAGE_ARG, W4A16_ARG_ALIGN);
+    if (k % 128 != 0 || n % 256 != 0)
+        return status_of(STAGE_UNSUPPORTED, W4A16_ARG_SHAPE);
+    const long long bytes = (long long)k * n;
+    const char *qa = reinterpret_cast<const char *>(qweight);
+    const char *ob = reinterpret_cast<const char *>(b_packed);
+    if (qa < ob + bytes && ob < qa + bytes)
+        return status_of(STAGE_ARG, W4A16_ARG_FLAGS);
+    return launch_status(launch_repack_fp8(qweight, b_packed, k, n, stream));
+}
+
+int w8_unpack(const int32_t *b_packed, int32_t *qweight, int k, int n, cudaStream_t stream)
+{
+    if (k <= 0 || n <= 0)
+        return status_of(STAGE_ARG, W4A16_ARG_SHAPE);
+    if (!qweight || !b_packed)
+        return status_of(STAGE_ARG, W4A16_ARG_NULL);
+    if (!aligned(qweight, 16) || !aligned(b_packed, 16))
+        return status_of(STAGE_ARG, W4A16_ARG_ALIGN);
+    if (k % 128 != 0 || n % 256 != 0)
+        return status_of(STAGE_UNSUPPORTED, W4A16_ARG_SHAPE);
+    const long long bytes = (long long)k * n;
+    const char *qa = reinterpret_cast<const char *>(qweight);
+    const char *ob = reinterpret_cast<const char *>(b_packed);
+    if (qa < ob + bytes && ob < qa + bytes)
+        return status_of(STAGE_ARG, W4A16_ARG_FLAGS);
+    return launch_status(launch_unpack_fp8(b_packed, qweight, k, n, stream));
+}
+
 int w4_gate_up_interleave(const void *src, void *dst, int rows, int n2, int elem_bytes,
                           cudaStream_t stream)
 {
@@ -972,6 +1046,9 @@ int w4a16_gemm_grouped(const void *a, int lda, const int32_t *b_packed_stack, vo
     const int glu = glu_kind(flags);
     if (glu < 0)
         return status_of(STAGE_ARG, W4A16_ARG_FLAGS);
+    st = check_fp8_flags(weight_type, flags);
+    if (st)
+        return st;
     if (n_active <= 0 || n_active > W4A16_MAX_SEGMENTS || n_experts <= 0 || n_pairs <= 0 ||
         n_tokens <= 0 || n_active > n_experts)
         return status_of(STAGE_ARG, W4A16_ARG_SCHEDULE);
@@ -997,6 +1074,7 @@ int w4a16_gemm_grouped(const void *a, int lda, const int32_t *b_packed_stack, vo
         return status_of(STAGE_ARG, W4A16_ARG_WORKSPACE);
     const int g = num_groups(k, group_size);
     plan_tmem(pl);
+    pl.tile_bytes = tile_bytes_of(weight_type);
     err = plan_smem(pl, true, zeros_stack != nullptr, group_size == -1 ? k : group_size,
                     g * n_experts);
     if (err != cudaSuccess)
@@ -1005,6 +1083,7 @@ int w4a16_gemm_grouped(const void *a, int lda, const int32_t *b_packed_stack, vo
     char *ws = static_cast<char *>(workspace);
     GemmParams p;
     fill_params(p, pl, n_pairs, n, k, group_size);
+    set_weight_type(p, weight_type);
     p.b = b_packed_stack;
     p.scales = static_cast<const __half *>(scales_stack);
     p.zeros = static_cast<const __half *>(zeros_stack);
@@ -1021,7 +1100,7 @@ int w4a16_gemm_grouped(const void *a, int lda, const int32_t *b_packed_stack, vo
     p.n_experts = n_experts;
     p.n_pairs = n_pairs;
     p.n_rows = n_pairs;
-    p.b_expert_words = (long long)k * n / 8;
+    p.b_expert_words = (long long)k * n / (p.w8 ? 4 : 8);
     p.s_expert_elems = (long long)p.num_groups * n;
 
     __half *a_sorted = reinterpret_cast<__half *>(ws + pl.a_off);
@@ -1072,6 +1151,9 @@ int w4a16_gemm_moe_blocks(const void *a, int lda, const int32_t *b_packed_stack,
     if (glu < 0 || (mul_topk_weights != 0 && topk_weights == nullptr) ||
         (mul_topk_weights != 0 && mul_topk_weights != 1) || (is_ep != 0 && is_ep != 1))
         return status_of(STAGE_ARG, W4A16_ARG_FLAGS);
+    st = check_fp8_flags(weight_type, flags);
+    if (st)
+        return st;
     st = check_moe_sizes(max_padded, moe_block_size, top_k, prob_m, n_experts);
     if (st)
         return st;
@@ -1099,6 +1181,7 @@ int w4a16_gemm_moe_blocks(const void *a, int lda, const int32_t *b_packed_stack,
         return status_of(STAGE_ARG, W4A16_ARG_WORKSPACE);
     const int g = num_groups(k, group_size);
     plan_tmem(pl);
+    pl.tile_bytes = tile_bytes_of(weight_type);
     err = plan_smem(pl, true, zeros_stack != nullptr, group_size == -1 ? k : group_size,
                     g * n_experts);
     if (err != cudaSuccess)
@@ -1110,6 +1193,7 @@ int w4a16_gemm_moe_blocks(const void *a, int lda, const int32_t *b_packed_stack,
     int32_t *ex_pairs = reinterpret_cast<int32_t *>(ws + mp.pairs_off);
     GemmParams p;
     fill_params(p, pl, max_padded, n, k, group_size);
+    set_weight_type(p, weight_type);
     p.b = b_packed_stack;
     p.scales = static_cast<const __half *>(scales_stack);
     p.zeros = static_cast<const __half *>(zeros_stack);
@@ -1128,7 +1212,7 @@ int w4a16_gemm_moe_blocks(const void *a, int lda, const int32_t *b_packed_stack,
     p.n_rows = max_padded;
     p.skip_sentinel = 1;
     p.row_weight = mul_topk_weights ? topk_weights : nullptr;
-    p.b_expert_words = (long long)k * n / 8;
+    p.b_expert_words = (long long)k * n / (p.w8 ? 4 : 8);
     p.s_expert_elems = (long long)p.num_groups * n;
 
     err = launch_moe_route(sorted_token_ids, expert_ids, num_tokens_past_padded, max_padded,

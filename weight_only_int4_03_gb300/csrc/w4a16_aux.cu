@@ -88,6 +88,40 @@ __global__ void unpack_kernel(const int32_t *__restrict__ tiles, int32_t *__rest
     }
 }
 
+// FP8 tiles: tile (nt, kb) holds 2048 words; word (q, c, t) at q*512 + c*4 + t is the source
+// word of rows kb*64 + 16q + 4t .. +3 of column nt*128 + c (four K-consecutive E4M3 codes,
+// already in the source's byte order), so the repack only moves whole words.
+__global__ void repack_fp8_kernel(const int32_t *__restrict__ qweight, int32_t *__restrict__ out,
+                                  int k, int n)
+{
+    const long long total = (long long)k * n / 4;
+    const int kblocks = k / KBLK;
+    for (long long o = blockIdx.x * (long long)blockDim.x + threadIdx.x; o < total;
+         o += (long long)gridDim.x * blockDim.x) {
+        const long long tile = o / TILE_WORDS_FP8;
+        const int w = (int)(o - tile * TILE_WORDS_FP8);
+        const int nt = (int)(tile / kblocks);
+        const int kb = (int)(tile - (long long)nt * kblocks);
+        const int q = w >> 9, c = (w >> 2) & 127, t = w & 3;
+        out[o] = qweight[(long long)(kb * 16 + 4 * q + t) * n + nt * TILE_N + c];
+    }
+}
+
+__global__ void unpack_fp8_kernel(const int32_t *__restrict__ tiles, int32_t *__restrict__ qweight,
+                                  int k, int n)
+{
+    const long long total = (long long)k * n / 4;
+    const int kblocks = k / KBLK;
+    for (long long o = blockIdx.x * (long long)blockDim.x + threadIdx.x; o < total;
+         o += (long long)gridDim.x * blockDim.x) {
+        const int r = (int)(o / n);              // source word row: rows 4r .. 4r+3
+        const int col = (int)(o - (long long)r * n);
+        const int kb = r / 16, q = (r % 16) / 4, t = r % 4;
+        const int nt = col / TILE_N, c = col % TILE_N;
+        qweight[o] = tiles[((long long)nt * kblocks + kb) * TILE_WORDS_FP8 + q * 512 + c * 4 + t];
+    }
+}
+
 // a_perm[m][i] = a[m][perm[i]].  Row 0's threads also check the equal-group property
 // g_idx[perm[i]] == i / group_size that the GEMM relies on.
 __global__ void gather_cols_kernel(const __half *__restrict__ a, int lda,
@@ -380,6 +414,20 @@ int launch_unpack(const int32_t *tiles, int32_t *qweight, int k, int n, cudaStre
 {
     const long long total = (long long)k * n / 8;
     unpack_kernel<<<grid_for(total, 256), 256, 0, stream>>>(tiles, qweight, k, n);
+    return cudaGetLastError();
+}
+
+int launch_repack_fp8(const int32_t *qweight, int32_t *out, int k, int n, cudaStream_t stream)
+{
+    const long long total = (long long)k * n / 4;
+    repack_fp8_kernel<<<grid_for(total, 256), 256, 0, stream>>>(qweight, out, k, n);
+    return cudaGetLastError();
+}
+
+int launch_unpack_fp8(const int32_t *tiles, int32_t *qweight, int k, int n, cudaStream_t stream)
+{
+    const long long total = (long long)k * n / 4;
+    unpack_fp8_kernel<<<grid_for(total, 256), 256, 0, stream>>>(tiles, qweight, k, n);
     return cudaGetLastError();
 }
 

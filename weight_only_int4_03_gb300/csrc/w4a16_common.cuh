@@ -283,11 +283,11 @@ static __device__ __forceinline__ void issue_stage_weights(const GemmParams &p,
     const uint32_t fixed_bytes = (uint32_t)p.sg_box * SG_BYTES * (has_zp ? 2u : 1u) +
                                  (uint32_t)(p.halves * p.kbs) * (uint32_t)p.act_kb_bytes;
     const int32_t *bw = p.b + ti.expert * p.b_expert_words +
-                        ((long long)(ti.n0 / TILE_N) * p.kblocks) * TILE_WORDS;
-    mbar_arrive_expect_tx(full, fixed_bytes + nkb * (uint32_t)TILE_BYTES);
+                        ((long long)(ti.n0 / TILE_N) * p.kblocks) * p.tile_words;
+    mbar_arrive_expect_tx(full, fixed_bytes + nkb * (uint32_t)p.tile_bytes);
     // The codes are read once per call: first to leave L2, so that what is re-read (the
     // activations, scales, split partials, the kernel's own instructions) stays.
-    bulk_load_hint(st + p.packed_off, bw + (long long)kb * TILE_WORDS, nkb * TILE_BYTES, full,
+    bulk_load_hint(st + p.packed_off, bw + (long long)kb * p.tile_words, nkb * p.tile_bytes, full,
                    policy_evict_first());
     const int g_first = ti.expert * p.num_groups + (kb * KBLK) / p.group_size;
     tensor_load_2d(st + p.scales_off, tmap_s, ti.n0, g_first, full);

@@ -13,6 +13,8 @@
 // Work is split "data-parallel + stream-K"; tiles cut by a range boundary are summed from
 // fp32 partials in a fixed order by the last contributor to finish (a self-resetting atomic
 // counter), so results are deterministic and no CTA ever waits for another.
+#include <cuda_fp8.h>
+
 #include "w4a16_common.cuh"
 
 namespace w4 {
@@ -170,7 +172,49 @@ __device__ __forceinline__ void dequant_block(const GemmParams &p, const uint8_t
     }
 }
 
+// FP8 E4M3: the thread's column holds its block's 64 rows as 16 words of four K-consecutive
+// codes (word (q, t) = rows 16q + 4t .. 16q + 4t + 3, at q*512 + c*4 + t); each 16-bit half
+// converts exactly to an fp16 pair (rows 2p, 2p+1 -> tensor-memory column p), and one multiply
+// by the group's scale rounds it.  The block lies in one group (group_size -1 or a multiple of
+// 64 for FP8).
 template <bool A_TMEM>
+__device__ __forceinline__ void dequant_block_fp8(const uint8_t *packed, const __half *ssm, int grp_rel,
+                                                  int nl, uint32_t dst_tmem, uint8_t *dst_smem)
+{
+    const __half2 s = __half2half2(ssm[grp_rel * TILE_N + nl]);
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+        uint32_t out[16];
+#pragma unroll
+        for (int qq = 0; qq < 2; ++qq) {
+            const int q = hh * 2 + qq;
+            const uint4 wv = *reinterpret_cast<const uint4 *>(packed + (q * 512 + nl * 4) * 4);
+            const uint32_t words[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2(
+                    (__nv_fp8x2_storage_t)(words[t] & 0xFFFFu), __NV_E4M3);
+                const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2(
+                    (__nv_fp8x2_storage_t)(words[t] >> 16), __NV_E4M3);
+                out[qq * 8 + 2 * t] = h2_as_u32(__hmul2(__half2(lo), s));
+                out[qq * 8 + 2 * t + 1] = h2_as_u32(__hmul2(__half2(hi), s));
+            }
+        }
+        if (A_TMEM) {
+            tmem_st16(dst_tmem + hh * 16, out);
+        } else {
+            uint8_t *rowp = dst_smem + nl * 128;
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                const int chunk = hh * 4 + q4;
+                *reinterpret_cast<uint4 *>(rowp + ((chunk ^ (nl & 7)) << 4)) =
+                    make_uint4(out[q4 * 4], out[q4 * 4 + 1], out[q4 * 4 + 2], out[q4 * 4 + 3]);
+            }
+        }
+    }
+}
+
+template <bool A_TMEM, bool W8>
 __device__ void run_dequant(const GemmParams &p, Sched sched, uint8_t *smem, uint8_t *aring,
                             Bars &bars, uint32_t tmem_base, const WaitCtl &ctl, int warp, int lane)
 {
@@ -208,10 +252,16 @@ __device__ void run_dequant(const GemmParams &p, Sched sched, uint8_t *smem, uin
                     const int grp_rel = gs_kb == 0   ? -1
                                         : gs_sh >= 0 ? (kbj >> gs_sh) - g_first
                                                      : kbj / gs_kb - g_first;
-                    dequant_block<A_TMEM>(p, st + p.packed_off + j * TILE_BYTES, ssm, zsm, kbj,
-                                          g_first, grp_rel, nl, has_zp,
-                                          tmem_base + lane_base + a.idx * A_SLOT_COLS,
-                                          aring + a.idx * A_SLOT_BYTES);
+                    if (W8)
+                        dequant_block_fp8<A_TMEM>(st + p.packed_off + j * TILE_BYTES_FP8, ssm,
+                                                  grp_rel, nl,
+                                                  tmem_base + lane_base + a.idx * A_SLOT_COLS,
+                                                  aring + a.idx * A_SLOT_BYTES);
+                    else
+                        dequant_block<A_TMEM>(p, st + p.packed_off + j * TILE_BYTES, ssm, zsm, kbj,
+                                              g_first, grp_rel, nl, has_zp,
+                                              tmem_base + lane_base + a.idx * A_SLOT_COLS,
+                                              aring + a.idx * A_SLOT_BYTES);
                     mine |= 1u << j;
                 }
                 a.advance(p.a_slots);
@@ -352,7 +402,7 @@ __device__ void run_epilogue(const GemmParams &p, const SegTable &seg, Sched sch
     }
 }
 
-template <bool A_TMEM>
+template <bool A_TMEM, bool W8>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     w4a16_gemm_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap tmap_a,
                       const __grid_constant__ CUtensorMap tmap_s, const __grid_constant__ CUtensorMap tmap_z)
@@ -434,7 +484,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         run_epilogue(p, seg, sched, bars, tmem_base, smem, ctl, warp, lane, split_tiles_sh,
                      &n_split_sh);
     } else if (warp >= DQ_WARP0) {
-        run_dequant<A_TMEM>(p, sched, smem, aring, bars, tmem_base, ctl, warp, lane);
+        run_dequant<A_TMEM, W8>(p, sched, smem, aring, bars, tmem_base, ctl, warp, lane);
     }
     __syncwarp();
 
@@ -502,13 +552,16 @@ static int launch_pdl(const void *kernel_fn, int grid, int threads, int smem, cu
 int launch_gemm(const GemmParams &p, const CUtensorMap &tmap_a, const CUtensorMap &tmap_s,
                 const CUtensorMap &tmap_z, const GemmConfig &cfg, cudaStream_t stream)
 {
-    static int attr_done[2][64];
+    static int attr_done[4][64];
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess)
         return err;
-    const int variant = cfg.a_tmem ? 1 : 0;
-    auto kernel = cfg.a_tmem ? w4a16_gemm_kernel<true> : w4a16_gemm_kernel<false>;
+    const int variant = (cfg.a_tmem ? 1 : 0) + (p.w8 ? 2 : 0);
+    void (*kernels[4])(GemmParams, CUtensorMap, CUtensorMap, CUtensorMap) = {
+        w4a16_gemm_kernel<false, false>, w4a16_gemm_kernel<true, false>,
+        w4a16_gemm_kernel<false, true>, w4a16_gemm_kernel<true, true>};
+    auto kernel = kernels[variant];
     if (dev < 64 && attr_done[variant][dev] < cfg.smem_bytes) {
         err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    cfg.smem_bytes);
@@ -534,7 +587,7 @@ int gemm_smem_limit(int *bytes)
     if (err != cudaSuccess)
         return err;
     cudaFuncAttributes fa;
-    err = cudaFuncGetAttributes(&fa, w4a16_gemm_kernel<true>);
+    err = cudaFuncGetAttributes(&fa, w4a16_gemm_kernel<true, false>);
     if (err != cudaSuccess)
         return err;
     *bytes = optin - (int)fa.sharedSizeBytes - 256;

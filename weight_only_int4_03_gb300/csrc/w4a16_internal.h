@@ -15,6 +15,8 @@ constexpr int TILE_N = 128;      // weight columns per tile = tcgen05 M (weights
 constexpr int KBLK = 64;         // K rows per tile
 constexpr int TILE_WORDS = 1024; // 32-bit words per tile
 constexpr int TILE_BYTES = 4096;
+constexpr int TILE_WORDS_FP8 = 2048; // the same tile of FP8 E4M3 codes
+constexpr int TILE_BYTES_FP8 = 8192;
 
 // Pipeline geometry.
 constexpr int SG_BYTES = TILE_N * 2; // one scale (or zero) row of a column tile
@@ -72,6 +74,8 @@ struct GemmParams {
     int packed_off, scales_off, zeros_off; // byte offsets inside a stage
     int sg_box;               // scale rows copied per stage
     int acc_bufs, acc_col0, tmem_cols;
+    int w8;                   // FP8 E4M3 weights (tcgen05 kernel only)
+    int tile_words, tile_bytes; // one packed 64 x 128 tile: 1024 words (4-bit) or 2048 (FP8)
     int halves;               // tcgen05 kernel: 1, or 2 when a tile is a pair of token half-tiles
                               // that share each dequantised weight block
     int nt_half;              // rows of a half-tile (= nt_max when halves is 1)
@@ -114,6 +118,8 @@ int launch_gemm_simt(const GemmParams &p, const __half *a, int lda, cudaStream_t
 int launch_repack(const int32_t *qweight, const int32_t *perm, int32_t *out, int32_t *status, int k,
                   int n, cudaStream_t stream);
 int launch_unpack(const int32_t *tiles, int32_t *qweight, int k, int n, cudaStream_t stream);
+int launch_repack_fp8(const int32_t *qweight, int32_t *out, int k, int n, cudaStream_t stream);
+int launch_unpack_fp8(const int32_t *tiles, int32_t *qweight, int k, int n, cudaStream_t stream);
 int launch_gather_cols(const __half *a, int lda, const int32_t *perm, const int32_t *g_idx,
                        int group_size, __half *out, int m, int k, int *status, cudaStream_t stream);
 int launch_gather_rows(const __half *a, int lda, const int32_t *ex_pairs, const int32_t *pair_tok,
