@@ -50,6 +50,9 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.orc_dequant.argtypes = [P, P, P, P, I, I, I, I, P]
     lib.orc_matmul.argtypes = [P, L, P, I, I, I, P]
     lib.orc_gemm.argtypes = [P, L, I, P, P, P, P, I, I, I, I, P, I]
+    lib.orc_gemm_bf16.argtypes = [P, L, I, P, P, P, P, I, I, I, I, P, I]
+    lib.orc_bf16_to_double.restype = ctypes.c_double
+    lib.orc_bf16_to_double.argtypes = [ctypes.c_uint16]
     lib.orc_gemm_by_groups.argtypes = [P, L, I, P, P, P, P, I, I, I, I, I, P]
     lib.orc_repack_tiles.argtypes = [P, P, I, I, P]
     lib.orc_unpack_tiles.argtypes = [P, I, I, P]
@@ -162,6 +165,26 @@ class Oracle:
         out = np.empty((m, n), dtype=np.float64)
         self.lib.orc_gemm(_ptr(a), k, m, _ptr(qw), _ptr(s), _ptr(z), _ptr(g), k, n, group_size,
                           weight_type, _ptr(out), threads or default_threads())
+        return out
+
+    def bf16_to_double(self, bits) -> np.ndarray:
+        """Doubles of bfloat16 bit patterns (uint16 array)."""
+        b = np.asarray(bits, dtype=np.uint16)
+        return np.array([self.lib.orc_bf16_to_double(int(x)) for x in b.ravel()]).reshape(b.shape)
+
+    def gemm_bf16(self, a_bits, qweight, scale_bits, zero_bits=None, g_idx=None, group_size=128,
+                  weight_type=U4B8, threads: int | None = None) -> np.ndarray:
+        """C [M][N] in double with bfloat16 activations, scales and zeros, given as their uint16
+        bit patterns."""
+        a = np.ascontiguousarray(a_bits, dtype=np.uint16)
+        m, k = a.shape
+        qw, g = _c(qweight, np.int32), _c(g_idx, np.int32)
+        s = np.ascontiguousarray(scale_bits, dtype=np.uint16)
+        z = None if zero_bits is None else np.ascontiguousarray(zero_bits, dtype=np.uint16)
+        n = qw.shape[1]
+        out = np.empty((m, n), dtype=np.float64)
+        self.lib.orc_gemm_bf16(_ptr(a), k, m, _ptr(qw), _ptr(s), _ptr(z), _ptr(g), k, n, group_size,
+                               weight_type, _ptr(out), threads or default_threads())
         return out
 
     def gemm_by_groups(self, a, qweight, scales, zeros=None, g_idx=None, group_size=128,

@@ -56,6 +56,30 @@ double orc_half_to_double(uint16_t h)
     return sign ? -v : v;
 }
 
+/* bfloat16 -> double, from the format's definition: the top half of an IEEE binary32 (1 sign
+ * bit, 8 exponent bits with bias 127, 7 fraction bits; exponent 0 = subnormal, 255 = inf/NaN).
+ * The BF16-activation GEMM reads its activations, scales and zeros this way. */
+double orc_bf16_to_double(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int expo = (h >> 7) & 0xFF;
+    int frac = h & 0x7F;
+    double v;
+    if (expo == 0)
+        v = ldexp((double)frac, -133);                /* 0.frac * 2^-126 */
+    else if (expo == 255)
+        v = frac ? NAN : INFINITY;
+    else
+        v = ldexp(1.0 + frac / 128.0, expo - 127);
+    return sign ? -v : v;
+}
+
+/* A 16-bit input value: binary16, or bfloat16 when `bf16` is set. */
+static double orc_h16(uint16_t h, int bf16)
+{
+    return bf16 ? orc_bf16_to_double(h) : orc_half_to_double(h);
+}
+
 void orc_halves_to_doubles(const uint16_t *h, long count, double *out)
 {
     for (long i = 0; i < count; ++i)
@@ -127,11 +151,11 @@ static int orc_group_of(int row, int k, int group_size, const int32_t *g_idx)
  * double as both factors have at most 11 significant bits. */
 static double orc_weight(const int32_t *qweight, const uint16_t *scales, const uint16_t *zeros,
                          const int32_t *g_idx, int k, int n, int group_size, int weight_type,
-                         int row, int col)
+                         int row, int col, int bf16)
 {
     int g = orc_group_of(row, k, group_size, g_idx);
-    double s = orc_half_to_double(scales[(long)g * n + col]);
-    double zp = (weight_type == ORC_U4B8) ? 8.0 : orc_half_to_double(zeros[(long)g * n + col]);
+    double s = orc_h16(scales[(long)g * n + col], bf16);
+    double zp = (weight_type == ORC_U4B8) ? 8.0 : orc_h16(zeros[(long)g * n + col], bf16);
     double q = (double)orc_code(qweight, n, row, col);
     return (q - zp) * s;
 }
@@ -143,7 +167,7 @@ void orc_dequant(const int32_t *qweight, const uint16_t *scales, const uint16_t 
     for (int row = 0; row < k; ++row)
         for (int col = 0; col < n; ++col)
             w[(long)row * n + col] = orc_weight(qweight, scales, zeros, g_idx, k, n, group_size,
-                                                weight_type, row, col);
+                                                weight_type, row, col, 0);
 }
 
 /* Plain triple loop C = A * W over double matrices (A [M][K] with row stride lda). */
@@ -175,6 +199,7 @@ struct orc_gemm_job {
     int k, n, group_size, weight_type;
     double *c;
     int col_begin, col_end;
+    int bf16; /* A, scales and zeros are bfloat16 (else binary16) */
 };
 
 static void *orc_gemm_worker(void *arg)
@@ -190,12 +215,12 @@ static void *orc_gemm_worker(void *arg)
             for (int j = 0; j < width; ++j)
                 w[(long)row * width + j] = orc_weight(jb->qweight, jb->scales, jb->zeros, jb->g_idx,
                                                       jb->k, jb->n, jb->group_size,
-                                                      jb->weight_type, row, c0 + j);
+                                                      jb->weight_type, row, c0 + j, jb->bf16);
         for (int i = 0; i < jb->m; ++i) {
             for (int j = 0; j < width; ++j)
                 acc[j] = 0.0;
             for (int row = 0; row < jb->k; ++row) {
-                double av = orc_half_to_double(jb->a[(long)i * jb->lda + row]);
+                double av = orc_h16(jb->a[(long)i * jb->lda + row], jb->bf16);
                 const double *wr = w + (long)row * width;
                 for (int j = 0; j < width; ++j)
                     acc[j] += av * wr[j];
@@ -209,9 +234,30 @@ static void *orc_gemm_worker(void *arg)
     return NULL;
 }
 
+static void orc_gemm_fmt(const uint16_t *a, long lda, int m, const int32_t *qweight,
+                         const uint16_t *scales, const uint16_t *zeros, const int32_t *g_idx, int k,
+                         int n, int group_size, int weight_type, double *c, int nthreads, int bf16);
+
 void orc_gemm(const uint16_t *a, long lda, int m, const int32_t *qweight, const uint16_t *scales,
               const uint16_t *zeros, const int32_t *g_idx, int k, int n, int group_size,
               int weight_type, double *c, int nthreads)
+{
+    orc_gemm_fmt(a, lda, m, qweight, scales, zeros, g_idx, k, n, group_size, weight_type, c,
+                 nthreads, 0);
+}
+
+/* The same GEMM with bfloat16 activations, scales and zeros (BF16 activations). */
+void orc_gemm_bf16(const uint16_t *a, long lda, int m, const int32_t *qweight,
+                   const uint16_t *scales, const uint16_t *zeros, const int32_t *g_idx, int k,
+                   int n, int group_size, int weight_type, double *c, int nthreads)
+{
+    orc_gemm_fmt(a, lda, m, qweight, scales, zeros, g_idx, k, n, group_size, weight_type, c,
+                 nthreads, 1);
+}
+
+static void orc_gemm_fmt(const uint16_t *a, long lda, int m, const int32_t *qweight,
+                         const uint16_t *scales, const uint16_t *zeros, const int32_t *g_idx, int k,
+                         int n, int group_size, int weight_type, double *c, int nthreads, int bf16)
 {
     if (nthreads < 1)
         nthreads = 1;
@@ -224,7 +270,7 @@ void orc_gemm(const uint16_t *a, long lda, int m, const int32_t *qweight, const 
     for (int t = 0; t < nthreads; ++t) {
         struct orc_gemm_job jb = {a, lda, m, qweight, scales, zeros, g_idx, k, n, group_size,
                                   weight_type, c, (int)((long)n * t / nthreads),
-                                  (int)((long)n * (t + 1) / nthreads)};
+                                  (int)((long)n * (t + 1) / nthreads), bf16};
         jobs[t] = jb;
     }
     for (int t = 1; t < nthreads; ++t)

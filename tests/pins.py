@@ -450,6 +450,48 @@ def pin_grouped_closed_form(orc):
     return None
 
 
+# --- BF16 activations ----------------------------------------------------------------------------
+
+def _bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Bit patterns of values exactly representable in bfloat16 (the top half of binary32)."""
+    f = np.asarray(x, dtype=np.float32)
+    bits = f.view(np.uint32)
+    assert np.all((bits & 0xFFFF) == 0), "value not exact in bfloat16"
+    return (bits >> np.uint32(16)).astype(np.uint16)
+
+
+def pin_bf16_decode_all_patterns(orc):
+    """Every bfloat16 bit pattern decodes as torch's bfloat16 does (a library routine)."""
+    import torch
+    b = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    got = np.array([orc.lib.orc_bf16_to_double(int(x)) for x in b])
+    ref = torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).double().numpy()
+    if not np.array_equal(np.isnan(got), np.isnan(ref)) or not np.array_equal(got[~np.isnan(got)], ref[~np.isnan(ref)]):
+        return "bfloat16 decode differs from torch.bfloat16"
+    return None
+
+
+def pin_bf16_gemm_equals_fp16_gemm_on_shared_values(orc):
+    """Activations k/32 in [-2, 2), scales 2^-j and integer zero points are exact in both
+    binary16 and bfloat16: the BF16-activation GEMM of their bf16 patterns equals the fp16 GEMM
+    of their fp16 patterns exactly (u4b8 and u4)."""
+    m, k, n = 5, 256, 48
+    rng = np.random.default_rng(81)
+    a = (rng.integers(-64, 64, size=(m, k)) / 32.0)
+    s = 2.0 ** -rng.integers(4, 9, size=(2, n)).astype(np.float64)
+    z = rng.integers(5, 11, size=(2, n)).astype(np.float64)
+    qw = synth.qweight(82, k, n)
+    for wt, zz in ((U4B8, None), (U4, z)):
+        ref = orc.gemm(a.astype(np.float16), qw, s.astype(np.float16),
+                       None if zz is None else zz.astype(np.float16), None, 128, wt)
+        got = orc.gemm_bf16(_bf16_bits(a), qw, _bf16_bits(s), None if zz is None else _bf16_bits(zz),
+                            None, 128, wt)
+        bad = _mismatch(f"bf16 vs fp16 gemm (type {wt})", got, ref)
+        if bad:
+            return bad
+    return None
+
+
 # --- FP8 E4M3 weights (W8A16) -----------------------------------------------------------------
 
 def _fp8_pack(codes: np.ndarray) -> np.ndarray:

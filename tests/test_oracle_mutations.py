@@ -16,21 +16,26 @@ SRC = os.path.join(os.path.dirname(oracle.__file__), "w4a16_oracle.c")
 
 MUTATIONS = [
     ("sign of q - zp", "return (q - zp) * s;", "return (zp - q) * s;"),
-    ("u4b8 bias 7", "? 8.0 : orc_half_to_double(zeros[(long)g * n + col]);",
-     "? 7.0 : orc_half_to_double(zeros[(long)g * n + col]);"),
+    ("u4b8 bias 7", "? 8.0 : orc_h16(zeros[(long)g * n + col], bf16);",
+     "? 7.0 : orc_h16(zeros[(long)g * n + col], bf16);"),
     ("nibble order high first", "return (int)((word >> (4 * (row % 8))) & 0xFu);",
      "return (int)((word >> (4 * (7 - row % 8))) & 0xFu);"),
     ("group off by one row", "    return row / group_size;\n}",
      "    return (row > 0 ? row - 1 : 0) / group_size;\n}"),
-    ("scale column reversed", "double s = orc_half_to_double(scales[(long)g * n + col]);",
-     "double s = orc_half_to_double(scales[(long)g * n + (n - 1 - col)]);"),
-    ("zero point column dropped", "? 8.0 : orc_half_to_double(zeros[(long)g * n + col]);",
-     "? 8.0 : orc_half_to_double(zeros[(long)g * n]);"),
+    ("scale column reversed", "double s = orc_h16(scales[(long)g * n + col], bf16);",
+     "double s = orc_h16(scales[(long)g * n + (n - 1 - col)], bf16);"),
+    ("zero point column dropped", "? 8.0 : orc_h16(zeros[(long)g * n + col], bf16);",
+     "? 8.0 : orc_h16(zeros[(long)g * n], bf16);"),
     ("g_idx ignored", "    if (g_idx)\n        return g_idx[row];\n", "\n"),
     ("dropped accumulation", "acc[j] += av * wr[j];", "acc[j] = av * wr[j];"),
-    ("W band column shifted", "jb->weight_type, row, c0 + j);", "jb->weight_type, row, c0 + (j + 1) % width);"),
-    ("A reversed along K", "double av = orc_half_to_double(jb->a[(long)i * jb->lda + row]);",
-     "double av = orc_half_to_double(jb->a[(long)i * jb->lda + (jb->k - 1 - row)]);"),
+    ("W band column shifted", "jb->weight_type, row, c0 + j, jb->bf16);",
+     "jb->weight_type, row, c0 + (j + 1) % width, jb->bf16);"),
+    ("A reversed along K", "double av = orc_h16(jb->a[(long)i * jb->lda + row], jb->bf16);",
+     "double av = orc_h16(jb->a[(long)i * jb->lda + (jb->k - 1 - row)], jb->bf16);"),
+    ("bf16 activations read as fp16", "double av = orc_h16(jb->a[(long)i * jb->lda + row], jb->bf16);",
+     "double av = orc_h16(jb->a[(long)i * jb->lda + row], 0);"),
+    ("bf16 exponent bias", "v = ldexp(1.0 + frac / 128.0, expo - 127);", "v = ldexp(1.0 + frac / 128.0, expo - 126);"),
+    ("bf16 fraction width", "v = ldexp(1.0 + frac / 128.0, expo - 127);", "v = ldexp(1.0 + frac / 64.0, expo - 127);"),
     ("half exponent bias", "v = ldexp(1.0 + frac / 1024.0, expo - 15);",
      "v = ldexp(1.0 + frac / 1024.0, expo - 14);"),
     ("half subnormal scale", "v = ldexp((double)frac, -24);", "v = ldexp((double)frac, -23);"),
