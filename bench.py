@@ -49,6 +49,7 @@ U4, U4B8, FE4M3 = 4, 5, 8
 FLAG_ACT_ORDER, FLAG_IS_K_FULL, FLAG_HAS_ZP = 1 << 1, 1 << 2, 1 << 3
 # Inference weights are written once, long before the GEMMs that read them.
 FLAG_STATIC_WEIGHTS = 1 << 12
+W4A16_FLAG_BF16 = 1 << 16
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -77,6 +78,10 @@ def workload_specs(name: str):
         # FP8 E4M3 weights (W8A16), group 128, on the prefill FFN shape across M.
         specs = [dict(m=m, k=4096, n=11008, gs=128, wt=FE4M3, act_order=False, sigma=1.0, seed=6000 + m)
                  for m in (1, 16, 256, 1024, 4096)]
+    elif name == "bf16":
+        # BF16 activations, scales, zeros and output on the prefill FFN shape across M.
+        specs = [dict(m=m, k=4096, n=11008, gs=128, wt=U4, act_order=False, sigma=0.5, seed=7000 + m,
+                      bf16=True) for m in (1, 16, 256, 1024, 4096)]
     elif name == "tiny":
         specs = [dict(m=16, k=256, n=256, gs=128, wt=U4B8, act_order=False, sigma=1.0, seed=0)]
     elif name == "moe_swiglu":
@@ -110,6 +115,8 @@ WORKLOAD_TEXT = {
     "prefill": "prefill M in {256,1024,4096} x (K=4096,N=11008),(K=11008,N=4096), group 128, u4 + fp16 zeros",
     "actorder": "act-order M in {1,16,2048}, K=8192, N=28672, group 128, u4b8, shuffled g_idx",
     "tiny": "tiny M=16, K=256, N=256, group 128, u4b8",
+    "bf16": ("BF16 activations/scales/zeros/output M in {1,16,256,1024,4096}, K=4096, N=11008, "
+             "group 128, u4 + bf16 zeros"),
     "fp8": "FP8 E4M3 weights (W8A16) M in {1,16,256,1024,4096}, K=4096, N=11008, group 128, scales ~U[1e-4,2e-4]",
     "moe": "grouped MoE 8 experts, 512 tokens top-2, gate_up K=4096 N=28672 + down K=14336 N=4096, u4b8",
     "moe_blocks": ("grouped MoE 8 experts, 512 tokens top-2 through the vLLM block routing (blocks of "
@@ -301,6 +308,7 @@ class DenseGemm:
         groups = synth.group_count(k, gs)
         a = synth.activations(s["seed"], m, k, sigma=s["sigma"])
         fp8 = s["wt"] == FE4M3
+        bf16 = bool(s.get("bf16"))
         qw = torch.from_numpy(synth.fp8_weights(s["seed"], k, n) if fp8 else
                               synth.qweight(s["seed"], k, n)).to(dev)
         perm = g_idx = None
@@ -315,17 +323,22 @@ class DenseGemm:
             packed = torch.empty(k * n // 8, dtype=torch.int32, device=dev)
             w4.w4_repack(qw, perm, packed, k, n)
         del qw
-        scales = torch.from_numpy(synth.scales(s["seed"], groups, n, *((1e-4, 2e-4) if fp8 else ()))).to(dev)
-        zeros = torch.from_numpy(synth.zeros(s["seed"], groups, n)).to(dev) if s["wt"] == U4 else None
+        sc = synth.scales(s["seed"], groups, n, *((1e-4, 2e-4) if fp8 else ()))
+        zr = synth.zeros(s["seed"], groups, n) if s["wt"] == U4 else None
+        if bf16:   # the same values rounded to bfloat16, passed as raw 16-bit words
+            a, sc = _bf16_words(a), _bf16_words(sc)
+            zr = None if zr is None else _bf16_words(zr)
+        scales = torch.from_numpy(sc).to(dev)
+        zeros = torch.from_numpy(zr).to(dev) if zr is not None else None
         self.b = [packed] + [packed.clone() for _ in range(copies - 1)]
         self.scales = [scales] + [scales.clone() for _ in range(copies - 1)]
         self.zeros = None if zeros is None else [zeros] + [zeros.clone() for _ in range(copies - 1)]
         self.perm, self.g_idx = perm, g_idx
         self.flags = FLAG_IS_K_FULL | FLAG_STATIC_WEIGHTS | (FLAG_HAS_ZP if zeros is not None else 0) | (
-            FLAG_ACT_ORDER if perm is not None else 0)
+            FLAG_ACT_ORDER if perm is not None else 0) | (W4A16_FLAG_BF16 if bf16 else 0)
         self.a_host = torch.from_numpy(a).pin_memory()
         self.a = self.a_host.to(dev)
-        self.c = torch.empty((m, n), dtype=torch.float16, device=dev)
+        self.c = torch.empty((m, n), dtype=torch.int16 if bf16 else torch.float16, device=dev)
         self.ws = torch.zeros(w4.w4a16_workspace_size(m, n, k, gs, self.flags), dtype=torch.uint8,
                               device=dev)
         self.w4 = w4
@@ -737,7 +750,7 @@ def run_ours(args, rank, world, local):
     line = {
         "metric": METRIC, "value": round(value, 4), "unit": unit, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(max_ms / args.steps, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16 x u4 -> f32 acc",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": _dtype_text(specs),
         "data": "synthetic (seeded LCG; shapes and distributions of the W4A16 configurations)",
         "config": {"workload": WORKLOAD_TEXT[args.workload] + (f" (only {args.shape})" if args.shape else ""),
                    "gemms_per_step": len(gemms),
@@ -764,6 +777,21 @@ def run_ours(args, rank, world, local):
 # The oracle (CPU) as a reported baseline and as the reference arm
 # ---------------------------------------------------------------------------------------------
 
+def _dtype_text(specs) -> str:
+    acts = "bf16" if any(s.get("bf16") for s in specs) else "f16"
+    codes = "/".join(sorted({"e4m3" if s["wt"] == FE4M3 else "u4" for s in specs}))
+    return f"{acts} x {codes} -> f32 acc"
+
+
+def _bf16_words(x):
+    """int16 words of the bfloat16 roundings of an array's values."""
+    return synth.bf16_bits(np.asarray(x, dtype=np.float64)).view(np.int16)
+
+
+def _bf16_values(words):
+    return (np.asarray(words).view(np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
 def _oracle_inputs(s, rows: int):
     """Oracle inputs of one GEMM of the workload with `rows` activation rows (for a grouped
     GEMM: one expert's weights, rows standing for (token, expert) pairs)."""
@@ -779,7 +807,11 @@ def _oracle_inputs(s, rows: int):
     qw = synth.qweight(s["seed"], k, n)
     z = synth.zeros(s["seed"], g, n) if s["wt"] == U4 else None
     g_idx = synth.act_order_gidx(synth.permutation(s["seed"], k), s["gs"]) if s.get("act_order") else None
-    return synth.activations(s["seed"], rows, k, sigma=s["sigma"]), qw, synth.scales(s["seed"], g, n), z, g_idx
+    a, sc = synth.activations(s["seed"], rows, k, sigma=s["sigma"]), synth.scales(s["seed"], g, n)
+    if s.get("bf16"):
+        a, sc = _bf16_words(a), _bf16_words(sc)
+        z = None if z is None else _bf16_words(z)
+    return a, qw, sc, z, g_idx
 
 
 def step_totals(specs, peaks):
@@ -810,6 +842,9 @@ def oracle_sample(workload: str, budget_s: float, threads: int | None = None):
         t0 = time.perf_counter()
         if s["wt"] == FE4M3:
             orc.gemm_fp8(a, qw, sc, s["gs"], threads=threads)
+        elif s.get("bf16"):
+            orc.gemm_bf16(a.view(np.uint16), qw, sc.view(np.uint16),
+                          None if z is None else z.view(np.uint16), g_idx, s["gs"], s["wt"], threads=threads)
         else:
             orc.gemm(a, qw, sc, z, g_idx, s["gs"], s["wt"], threads=threads)
         return time.perf_counter() - t0
@@ -879,6 +914,9 @@ def blas_sample(workload: str, repeats: int = 3):
         rows = s["n_tok"] * s["top_k"] if s.get("grouped") else s["m"]
         per = rows // s["n_exp"] if s.get("grouped") else rows
         a, qw, sc, z, _ = _oracle_inputs(s, per)
+        if s.get("bf16"):
+            a, sc = _bf16_values(a), _bf16_values(sc)
+            z = None if z is None else _bf16_values(z)
         w = _dequant_fp8_fp32(qw, sc, s["gs"]) if s["wt"] == FE4M3 else _dequant_fp32(qw, sc, z, s["gs"], s["wt"])
         a32 = a.astype(np.float32)
         best = float("inf")

@@ -78,6 +78,16 @@ extern "C" {
 #define W4A16_FLAG_GEGLU (1u << 15)  /* the same with gelu_tanh(x) = x/2 (1 + tanh(sqrt(2/pi)
                                            (x + 0.044715 x^3))) in place of silu; exclusive
                                            with W4A16_FLAG_SWIGLU                            */
+#define W4A16_FLAG_BF16 (1u << 16)   /* a, scales, zeros and c are bfloat16 instead of fp16
+                                           (marlin.rs declares bf16 A and C for its
+                                           `ferrum_vllm_marlin_moe_mxfp4_bf16` entry point;
+                                           here with the 4-bit codes).  4-bit weight types
+                                           only (not W4A16_TYPE_FE4M3); tcgen05 kernel only
+                                           (_FORCE_SIMT, _FORCE_MMA and _FORCE_SLICE are
+                                           rejected).  (q - z) is exact in bf16 for integer
+                                           zero points, the product with the scale is rounded
+                                           once to bf16 (8 significant bits), products sum in
+                                           fp32 and C is rounded once to bf16               */
 
 /* Detail codes of stage-1/2 statuses. */
 #define W4A16_ARG_NULL 1        /* a required pointer is NULL                                  */

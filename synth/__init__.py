@@ -113,6 +113,14 @@ def fp16(values: np.ndarray) -> np.ndarray:
     return np.asarray(values, dtype=np.float64).astype(np.float16)
 
 
+def bf16_bits(values: np.ndarray) -> np.ndarray:
+    """uint16 bit patterns of doubles rounded to bfloat16 (through binary32, each step to nearest
+    even); finite inputs only."""
+    u = np.asarray(values, dtype=np.float64).astype(np.float32).view(np.uint32).astype(np.uint64)
+    r = (u + 0x7FFF + ((u >> np.uint64(16)) & np.uint64(1))) >> np.uint64(16)
+    return r.astype(np.uint16)
+
+
 def activations(seed: int, m: int, k: int, sigma: float = 1.0, name: str = "A") -> np.ndarray:
     """fp16 [m, k] ~ N(0, sigma)."""
     return fp16(Stream(seed, name).normal(m * k, sigma)).reshape(m, k)

@@ -30,6 +30,7 @@ W4A16_FLAG_FORCE_SLICE = 1 << 13
 W4A16_FLAG_STATIC_WEIGHTS = 1 << 12
 W4A16_FLAG_SWIGLU = 1 << 14
 W4A16_FLAG_GEGLU = 1 << 15
+W4A16_FLAG_BF16 = 1 << 16
 
 W4A16_DEV_TIMEOUT = 1
 W4A16_DEV_PERM = 2
@@ -183,7 +184,7 @@ def w4a16_grouped_workspace_size(n_pairs: int, n_active: int, n: int, k: int, gr
 def w4a16_gemm(a, b_packed, c, scales, zeros, g_idx, perm, workspace, m: int, n: int, k: int,
                group_size: int, weight_type: int, flags: int = 0, lda: int | None = None,
                ldc: int | None = None, workspace_bytes: int | None = None, stream=None) -> None:
-    """C[M, N] (fp16) = A[M, K] (fp16) x dequant(B) -- see include/w4a16.h."""
+    """C[M, N] = A[M, K] x dequant(B), fp16 (bf16 with W4A16_FLAG_BF16) -- see include/w4a16.h."""
     if lda is None:
         lda = k
     if ldc is None:

@@ -277,6 +277,12 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(int m, int n)
     return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
+// The same with bf16 A and B (format 1 at bits 7-9 and 10-12).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n)
+{
+    return idesc_f16_f32(m, n) | (1u << 7) | (1u << 10);
+}
+
 // D[tmem] (+)= A[smem desc] * B[smem desc]
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                        uint32_t idesc, uint32_t accumulate)

@@ -451,13 +451,13 @@ int check_weights(const void *b, const void *scales, const void *zeros, int n, i
 }
 
 // FP8 weights run on the tcgen05 kernel only, without act-order (the pages' FP8 Marlin has
-// neither zero points nor act-order).
+// neither zero points nor act-order), and with fp16 activations.
 int check_fp8_flags(int weight_type, unsigned flags)
 {
     if (weight_type != W4A16_TYPE_FE4M3)
         return 0;
     if (flags & (W4A16_FLAG_ACT_ORDER | W4A16_FLAG_FORCE_SIMT | W4A16_FLAG_FORCE_MMA |
-                 W4A16_FLAG_FORCE_SLICE))
+                 W4A16_FLAG_FORCE_SLICE | W4A16_FLAG_BF16))
         return status_of(STAGE_ARG, W4A16_ARG_FLAGS);
     return 0;
 }
@@ -468,10 +468,11 @@ int tile_bytes_of(int weight_type)
 }
 
 // The packed-tile geometry of a call's weight type, after fill_params.
-void set_weight_type(GemmParams &p, int weight_type)
+void set_weight_type(GemmParams &p, int weight_type, unsigned flags)
 {
     const bool w8 = weight_type == W4A16_TYPE_FE4M3;
     p.w8 = w8 ? 1 : 0;
+    p.bf16 = (flags & W4A16_FLAG_BF16) ? 1 : 0;
     p.tile_words = w8 ? TILE_WORDS_FP8 : TILE_WORDS;
     p.tile_bytes = w8 ? TILE_BYTES_FP8 : TILE_BYTES;
 }
@@ -525,8 +526,10 @@ int glu_kind(unsigned flags)
 int check_kernel_flags(int m, int gs, unsigned flags)
 {
     // The gated epilogue lives in the tcgen05 kernel (and its split-tile reduction) only.
+    // So do the bfloat16 operand formats.
     const int glu = glu_kind(flags);
-    if (glu < 0 || (glu > 0 && (flags & (W4A16_FLAG_FORCE_SIMT | W4A16_FLAG_FORCE_MMA |
+    const bool tc_only = glu > 0 || (flags & W4A16_FLAG_BF16);
+    if (glu < 0 || (tc_only && (flags & (W4A16_FLAG_FORCE_SIMT | W4A16_FLAG_FORCE_MMA |
                                          W4A16_FLAG_FORCE_SLICE))))
         return status_of(STAGE_ARG, W4A16_ARG_FLAGS);
     const unsigned other = W4A16_FLAG_FORCE_TC | W4A16_FLAG_A_SMEM | W4A16_FLAG_FORCE_SIMT;
@@ -557,7 +560,7 @@ int choose_kernel(int m, int n, int gs, unsigned flags, int num_sms)
     if (flags & W4A16_FLAG_FORCE_MMA)
         return 1;
     if (flags & (W4A16_FLAG_FORCE_TC | W4A16_FLAG_A_SMEM | W4A16_FLAG_FORCE_SIMT |
-                 W4A16_FLAG_SWIGLU | W4A16_FLAG_GEGLU))
+                 W4A16_FLAG_SWIGLU | W4A16_FLAG_GEGLU | W4A16_FLAG_BF16))
         return 0;
     // 9..32 tokens (two or four 8-token tiles, a shallower ring) only while each CTA gets one
     // slice: at N=12288 (3 slices per CTA) the split-K kernel is faster at M=16.
@@ -818,7 +821,7 @@ int dense_gemm(const void *a, int lda, const int32_t *b_packed, void *c, int ldc
     char *ws = static_cast<char *>(workspace);
     GemmParams p;
     fill_params(p, pl, m, n, k, group_size);
-    set_weight_type(p, weight_type);
+    set_weight_type(p, weight_type, flags);
     p.b = b_packed;
     p.scales = static_cast<const __half *>(scales);
     p.zeros = static_cast<const __half *>(zeros);
@@ -1083,7 +1086,7 @@ int w4a16_gemm_grouped(const void *a, int lda, const int32_t *b_packed_stack, vo
     char *ws = static_cast<char *>(workspace);
     GemmParams p;
     fill_params(p, pl, n_pairs, n, k, group_size);
-    set_weight_type(p, weight_type);
+    set_weight_type(p, weight_type, flags);
     p.b = b_packed_stack;
     p.scales = static_cast<const __half *>(scales_stack);
     p.zeros = static_cast<const __half *>(zeros_stack);
@@ -1193,7 +1196,7 @@ int w4a16_gemm_moe_blocks(const void *a, int lda, const int32_t *b_packed_stack,
     int32_t *ex_pairs = reinterpret_cast<int32_t *>(ws + mp.pairs_off);
     GemmParams p;
     fill_params(p, pl, max_padded, n, k, group_size);
-    set_weight_type(p, weight_type);
+    set_weight_type(p, weight_type, flags);
     p.b = b_packed_stack;
     p.scales = static_cast<const __half *>(scales_stack);
     p.zeros = static_cast<const __half *>(zeros_stack);

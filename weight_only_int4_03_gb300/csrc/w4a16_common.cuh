@@ -3,6 +3,8 @@
 // producer and the fixed-order split-K reduction.
 #pragma once
 
+#include <cuda_bf16.h>
+
 #include "ptx.cuh"
 #include "w4a16_internal.h"
 #include "w4a16.h"
@@ -91,6 +93,22 @@ __device__ __forceinline__ void load_scales_row(const __half *ssm, const __half 
         zlo[pp] = lo;
         zhi[pp] = hi;
     }
+}
+
+// Two fp32 results rounded to the output's 16-bit format (fp16, or bf16), packed low-first.
+__device__ __forceinline__ uint32_t pack_out2(float lo, float hi, bool bf16)
+{
+    if (bf16) {
+        const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<const uint32_t *>(&v);
+    }
+    const __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&v);
+}
+
+__device__ __forceinline__ uint16_t to_out16(float x, bool bf16)
+{
+    return bf16 ? __bfloat16_as_ushort(__float2bfloat16_rn(x)) : __half_as_ushort(__float2half_rn(x));
 }
 
 // log2 of the blocks per group when that is a power of two, else -1.
@@ -534,11 +552,9 @@ static __device__ __forceinline__ void store_quad(const GemmParams &p, const Til
     if (out_row < 0)
         return;
     const float w = row_scale(p, out_row);
-    const __half2 lo = __floats2half2_rn(acc.x * w, acc.y * w);
-    const __half2 hi = __floats2half2_rn(acc.z * w, acc.w * w);
     uint2 packed;
-    packed.x = *reinterpret_cast<const uint32_t *>(&lo);
-    packed.y = *reinterpret_cast<const uint32_t *>(&hi);
+    packed.x = pack_out2(acc.x * w, acc.y * w, p.bf16);
+    packed.y = pack_out2(acc.z * w, acc.w * w, p.bf16);
     *reinterpret_cast<uint2 *>(p.c + (long long)out_row * p.ldc + ti.n0 + 4 * cq) = packed;
 }
 
@@ -593,11 +609,9 @@ static __device__ void reduce_tile_glu(const GemmParams &p, const TileInfo &ti, 
         if (out_row < 0)
             continue;
         const float w = row_scale(p, out_row);
-        const __half2 lo = __floats2half2_rn(glu_act(g.x, p.glu) * u.x * w, glu_act(g.y, p.glu) * u.y * w);
-        const __half2 hi = __floats2half2_rn(glu_act(g.z, p.glu) * u.z * w, glu_act(g.w, p.glu) * u.w * w);
         uint2 packed;
-        packed.x = *reinterpret_cast<const uint32_t *>(&lo);
-        packed.y = *reinterpret_cast<const uint32_t *>(&hi);
+        packed.x = pack_out2(glu_act(g.x, p.glu) * u.x * w, glu_act(g.y, p.glu) * u.y * w, p.bf16);
+        packed.y = pack_out2(glu_act(g.z, p.glu) * u.z * w, glu_act(g.w, p.glu) * u.w * w, p.bf16);
         *reinterpret_cast<uint2 *>(p.c + (long long)out_row * p.ldc + ti.n0 / 2 + 4 * gq) = packed;
     }
 }

@@ -69,8 +69,9 @@ __device__ void run_mma(const GemmParams &p, const SegTable &seg, Sched sched, u
         // operand, into adjacent accumulator columns (half 1 starts nt_half columns on).
         const int n_first = ti.ntok < p.nt_half ? ti.ntok : p.nt_half;
         const int n_second = ti.ntok - n_first;
-        const uint32_t idesc = idesc_f16_f32(TILE_N, n_first);
-        const uint32_t idesc2 = idesc_f16_f32(TILE_N, n_second > 0 ? n_second : 16);
+        const uint32_t idesc = p.bf16 ? idesc_bf16_f32(TILE_N, n_first) : idesc_f16_f32(TILE_N, n_first);
+        const int n2 = n_second > 0 ? n_second : 16;
+        const uint32_t idesc2 = p.bf16 ? idesc_bf16_f32(TILE_N, n2) : idesc_f16_f32(TILE_N, n2);
         const uint32_t half_bytes = (uint32_t)(p.kbs * p.act_kb_bytes);
         const int abuf = seg_i % p.acc_bufs;
         const uint32_t acc_ph = (seg_i / p.acc_bufs) & 1u;
@@ -214,7 +215,101 @@ __device__ __forceinline__ void dequant_block_fp8(const uint8_t *packed, const _
     }
 }
 
-template <bool A_TMEM, bool W8>
+// bfloat16 operands (7 fraction bits).
+__device__ __forceinline__ __nv_bfloat162 u32_as_bf2(uint32_t v)
+{
+    return *reinterpret_cast<__nv_bfloat162 *>(&v);
+}
+
+__device__ __forceinline__ uint32_t bf2_as_u32(__nv_bfloat162 v)
+{
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// Scale and -(128 + zero) of one (group, column), as bf16 pairs.
+__device__ __forceinline__ void bf16_scale_zero(const uint16_t *ssm, const uint16_t *zsm, bool has_zp,
+                                                int idx, __nv_bfloat162 &s2, __nv_bfloat162 &z2)
+{
+    s2 = __bfloat162bfloat162(__ushort_as_bfloat16(ssm[idx]));
+    __nv_bfloat16 zb = __ushort_as_bfloat16((uint16_t)0xC308); // -136 = -(128 + 8)
+    if (has_zp)
+        zb = __hneg(__hadd(__ushort_as_bfloat16((uint16_t)0x4300), __ushort_as_bfloat16(zsm[idx])));
+    z2 = __bfloat162bfloat162(zb);
+}
+
+// One word's four row pairs (bits 4p, 16 + 4p) as bf16 pairs (q - z) * s.  The fraction of a
+// bf16 has 7 bits (bit 7 is the exponent's lowest), so each nibble is first moved to bits 0-3
+// (shifts as high halves of products, on the FMA pipe) and OR-ed into 128.0 (0x4300, spacing
+// 1): 128 + q exactly.  Adding -(128 + z) is exact for integer zero points; the product with
+// the scale rounds once.
+__device__ __forceinline__ void dequant_word_bf16(uint32_t x, const __nv_bfloat162 (&z2)[4],
+                                                  const __nv_bfloat162 (&s2)[4], uint32_t (&out)[4])
+{
+    const uint32_t xs[4] = {x, __umulhi(x, 1u << 28), __umulhi(x, 1u << 24), __umulhi(x, 1u << 20)};
+#pragma unroll
+    for (int pp = 0; pp < 4; ++pp) {
+        const uint32_t t = (xs[pp] & 0x000F000Fu) | 0x43004300u;
+        out[pp] = bf2_as_u32(__hmul2(__hadd2(u32_as_bf2(t), z2[pp]), s2[pp]));
+    }
+}
+
+// grp_rel >= 0: the block lies in one group, row grp_rel of the stage's scales; otherwise
+// each 8-row pair looks up its own group.
+template <bool A_TMEM>
+__device__ __forceinline__ void dequant_block_bf16(const GemmParams &p, const uint8_t *packed,
+                                                   const uint16_t *ssm, const uint16_t *zsm, int kb,
+                                                   int g_first, int grp_rel, int nl, bool has_zp,
+                                                   uint32_t dst_tmem, uint8_t *dst_smem)
+{
+    __nv_bfloat162 s2[4], z2[4];
+    if (grp_rel >= 0) {
+        bf16_scale_zero(ssm, zsm, has_zp, grp_rel * TILE_N + nl, s2[0], z2[0]);
+#pragma unroll
+        for (int pp = 1; pp < 4; ++pp) {
+            s2[pp] = s2[0];
+            z2[pp] = z2[0];
+        }
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        if (grp_rel < 0) {
+#pragma unroll
+            for (int pp = 0; pp < 4; ++pp) {
+                const int gl = (kb * KBLK + h * 32 + pp * 8) / p.group_size - g_first;
+                bf16_scale_zero(ssm, zsm, has_zp, gl * TILE_N + nl, s2[pp], z2[pp]);
+            }
+        }
+        const uint4 wv = *reinterpret_cast<const uint4 *>(packed + (h * 512 + nl * 4) * 4);
+        const uint32_t words[4] = {wv.x, wv.y, wv.z, wv.w};
+        uint32_t out[16];
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            // word jj holds rows 2jj + 8pp + {0,1} at bits (4pp, 16 + 4pp): column jj + 4pp
+            uint32_t o4[4];
+            dequant_word_bf16(words[jj], z2, s2, o4);
+#pragma unroll
+            for (int pp = 0; pp < 4; ++pp)
+                out[jj + 4 * pp] = o4[pp];
+        }
+        if (A_TMEM) {
+            tmem_st16(dst_tmem + h * 16, out);
+        } else {
+            uint8_t *rowp = dst_smem + nl * 128;
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                const int chunk = h * 4 + q4;
+                *reinterpret_cast<uint4 *>(rowp + ((chunk ^ (nl & 7)) << 4)) =
+                    make_uint4(out[q4 * 4], out[q4 * 4 + 1], out[q4 * 4 + 2], out[q4 * 4 + 3]);
+            }
+        }
+    }
+}
+
+// Weight kinds of the tcgen05 kernel: 4-bit codes with fp16 operands, FP8 E4M3 codes with
+// fp16 operands, 4-bit codes with bf16 operands.
+constexpr int WK_U4_F16 = 0, WK_FP8_F16 = 1, WK_U4_BF16 = 2;
+
+template <bool A_TMEM, int WK>
 __device__ void run_dequant(const GemmParams &p, Sched sched, uint8_t *smem, uint8_t *aring,
                             Bars &bars, uint32_t tmem_base, const WaitCtl &ctl, int warp, int lane)
 {
@@ -252,11 +347,18 @@ __device__ void run_dequant(const GemmParams &p, Sched sched, uint8_t *smem, uin
                     const int grp_rel = gs_kb == 0   ? -1
                                         : gs_sh >= 0 ? (kbj >> gs_sh) - g_first
                                                      : kbj / gs_kb - g_first;
-                    if (W8)
+                    if (WK == WK_FP8_F16)
                         dequant_block_fp8<A_TMEM>(st + p.packed_off + j * TILE_BYTES_FP8, ssm,
                                                   grp_rel, nl,
                                                   tmem_base + lane_base + a.idx * A_SLOT_COLS,
                                                   aring + a.idx * A_SLOT_BYTES);
+                    else if (WK == WK_U4_BF16)
+                        dequant_block_bf16<A_TMEM>(p, st + p.packed_off + j * TILE_BYTES,
+                                                   reinterpret_cast<const uint16_t *>(ssm),
+                                                   reinterpret_cast<const uint16_t *>(zsm), kbj,
+                                                   g_first, grp_rel, nl, has_zp,
+                                                   tmem_base + lane_base + a.idx * A_SLOT_COLS,
+                                                   aring + a.idx * A_SLOT_BYTES);
                     else
                         dequant_block<A_TMEM>(p, st + p.packed_off + j * TILE_BYTES, ssm, zsm, kbj,
                                               g_first, grp_rel, nl, has_zp,
@@ -301,6 +403,7 @@ __device__ void run_epilogue(const GemmParams &p, const SegTable &seg, Sched sch
 {
     const int q = warp & 3;
     __half *stg = reinterpret_cast<__half *>(smem + p.epi_smem_off) + q * EPI_ROWS * 32;
+    uint16_t *stg16 = reinterpret_cast<uint16_t *>(stg); // fp16 or bf16 bits
     const int nl = q * 32 + lane;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     uint32_t seg_i = 0;
@@ -343,7 +446,7 @@ __device__ void run_epilogue(const GemmParams &p, const SegTable &seg, Sched sch
                     const float u = __shfl_down_sync(0xffffffffu, g, 16);
                     const float w = weighted ? __shfl_sync(0xffffffffu, rw, j) : 1.0f;
                     if (lane < 16)
-                        stg[j * 16 + lane] = __float2half_rn(glu_act(g, p.glu) * u * w);
+                        stg16[j * 16 + lane] = to_out16(glu_act(g, p.glu) * u * w, p.bf16);
                 }
                 __syncwarp();
 #pragma unroll
@@ -365,7 +468,7 @@ __device__ void run_epilogue(const GemmParams &p, const SegTable &seg, Sched sch
 #pragma unroll
                 for (int j = 0; j < EPI_ROWS; ++j) {
                     const float w = weighted ? __shfl_sync(0xffffffffu, rw, j) : 1.0f;
-                    stg[j * 32 + lane] = __float2half_rn(__uint_as_float(v[j]) * w);
+                    stg16[j * 32 + lane] = to_out16(__uint_as_float(v[j]) * w, p.bf16);
                 }
                 __syncwarp();
 #pragma unroll
@@ -402,7 +505,7 @@ __device__ void run_epilogue(const GemmParams &p, const SegTable &seg, Sched sch
     }
 }
 
-template <bool A_TMEM, bool W8>
+template <bool A_TMEM, int WK>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     w4a16_gemm_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap tmap_a,
                       const __grid_constant__ CUtensorMap tmap_s, const __grid_constant__ CUtensorMap tmap_z)
@@ -484,7 +587,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         run_epilogue(p, seg, sched, bars, tmem_base, smem, ctl, warp, lane, split_tiles_sh,
                      &n_split_sh);
     } else if (warp >= DQ_WARP0) {
-        run_dequant<A_TMEM, W8>(p, sched, smem, aring, bars, tmem_base, ctl, warp, lane);
+        run_dequant<A_TMEM, WK>(p, sched, smem, aring, bars, tmem_base, ctl, warp, lane);
     }
     __syncwarp();
 
@@ -552,15 +655,17 @@ static int launch_pdl(const void *kernel_fn, int grid, int threads, int smem, cu
 int launch_gemm(const GemmParams &p, const CUtensorMap &tmap_a, const CUtensorMap &tmap_s,
                 const CUtensorMap &tmap_z, const GemmConfig &cfg, cudaStream_t stream)
 {
-    static int attr_done[4][64];
+    static int attr_done[6][64];
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess)
         return err;
-    const int variant = (cfg.a_tmem ? 1 : 0) + (p.w8 ? 2 : 0);
-    void (*kernels[4])(GemmParams, CUtensorMap, CUtensorMap, CUtensorMap) = {
-        w4a16_gemm_kernel<false, false>, w4a16_gemm_kernel<true, false>,
-        w4a16_gemm_kernel<false, true>, w4a16_gemm_kernel<true, true>};
+    const int wk = p.w8 ? WK_FP8_F16 : p.bf16 ? WK_U4_BF16 : WK_U4_F16;
+    const int variant = (cfg.a_tmem ? 1 : 0) + 2 * wk;
+    void (*kernels[6])(GemmParams, CUtensorMap, CUtensorMap, CUtensorMap) = {
+        w4a16_gemm_kernel<false, WK_U4_F16>,  w4a16_gemm_kernel<true, WK_U4_F16>,
+        w4a16_gemm_kernel<false, WK_FP8_F16>, w4a16_gemm_kernel<true, WK_FP8_F16>,
+        w4a16_gemm_kernel<false, WK_U4_BF16>, w4a16_gemm_kernel<true, WK_U4_BF16>};
     auto kernel = kernels[variant];
     if (dev < 64 && attr_done[variant][dev] < cfg.smem_bytes) {
         err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -587,7 +692,7 @@ int gemm_smem_limit(int *bytes)
     if (err != cudaSuccess)
         return err;
     cudaFuncAttributes fa;
-    err = cudaFuncGetAttributes(&fa, w4a16_gemm_kernel<true, false>);
+    err = cudaFuncGetAttributes(&fa, w4a16_gemm_kernel<true, WK_U4_F16>);
     if (err != cudaSuccess)
         return err;
     *bytes = optin - (int)fa.sharedSizeBytes - 256;

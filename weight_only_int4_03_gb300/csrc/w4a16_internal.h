@@ -75,6 +75,7 @@ struct GemmParams {
     int sg_box;               // scale rows copied per stage
     int acc_bufs, acc_col0, tmem_cols;
     int w8;                   // FP8 E4M3 weights (tcgen05 kernel only)
+    int bf16;                 // bfloat16 activations, scales, zeros and output (tcgen05 only)
     int tile_words, tile_bytes; // one packed 64 x 128 tile: 1024 words (4-bit) or 2048 (FP8)
     int halves;               // tcgen05 kernel: 1, or 2 when a tile is a pair of token half-tiles
                               // that share each dequantised weight block
