@@ -283,6 +283,14 @@ struct Ring {
     }
 };
 
+// The position `steps` entries after r in a ring of `size`.
+__device__ __forceinline__ Ring ring_after(Ring r, int steps, int size)
+{
+    for (int i = 0; i < steps; ++i)
+        r.advance(size);
+    return r;
+}
+
 // ---------------------------------------------------------------------------------------
 // TMA producer (one thread).  A stage holds up to p.kbs consecutive 64-row blocks of one
 // segment: their packed codes (one contiguous bulk copy -- copies have a large fixed cost, so

@@ -81,10 +81,8 @@ __device__ void run_mma(const GemmParams &p, const SegTable &seg, Sched sched, u
         const uint32_t d_tmem = tmem_base + p.acc_col0 + abuf * p.nt_max;
         for (int kb = kb0; ok && kb < kb1; kb += p.kbs) {
             const int nkb = min(p.kbs, kb1 - kb);
-            if (!mbar_wait(&bars.full[ring.idx], ring.phase, ctl, W4A16_DEV_TIMEOUT)) {
-                ok = false;
-                break;
-            }
+            // No wait for the stage itself: a block's dequant-done barrier completes only after
+            // its dequant set has waited for the stage, so the activation rows have landed.
             const uint32_t st = smem_u32(smem + (size_t)ring.idx * p.stage_bytes);
             for (int j = 0; j < nkb; ++j) {
                 const int aslot = apos.idx;
@@ -327,8 +325,16 @@ __device__ void run_dequant(const GemmParams &p, Sched sched, uint8_t *smem, uin
     while (sched.next(tile, kb0, kb1)) {
         for (int kb = kb0; kb < kb1; kb += p.kbs) {
             const int nkb = min(p.kbs, kb1 - kb);
-            // Every warp waits for the stage (even with no block of its own in it) so that it
-            // can never run a whole ring ahead of the barrier it arrives on.
+            // A stage without a block of this set is skipped: the set neither waits for it nor
+            // signals it (the stage is released by the MMA warp's commit alone, issued after
+            // every block's dequant-done barrier, so after this set's last read of the stage).
+            const int j0 = set >= owner_set ? set - owner_set : set - owner_set + DQ_SETS;
+            if (j0 >= nkb) {
+                apos = ring_after(apos, nkb, p.a_slots);
+                owner_set = (owner_set + nkb) % DQ_SETS;
+                ring.advance(p.stages);
+                continue;
+            }
             if (!mbar_wait(&bars.full[ring.idx], ring.phase, ctl, W4A16_DEV_TIMEOUT))
                 return;
             const uint8_t *st = smem + (size_t)ring.idx * p.stage_bytes;
@@ -369,13 +375,11 @@ __device__ void run_dequant(const GemmParams &p, Sched sched, uint8_t *smem, uin
                 a.advance(p.a_slots);
                 os = (os + 1 == DQ_SETS) ? 0 : os + 1;
             }
-            if (mine) {
-                if (A_TMEM) {
-                    tmem_st_wait();
-                    tc_fence_before();
-                } else {
-                    fence_proxy_async_smem();
-                }
+            if (A_TMEM) {
+                tmem_st_wait();
+                tc_fence_before();
+            } else {
+                fence_proxy_async_smem();
             }
             // One arrival per warp: every lane's writes are complete and fenced first.
             __syncwarp();
@@ -386,7 +390,6 @@ __device__ void run_dequant(const GemmParams &p, Sched sched, uint8_t *smem, uin
                         mbar_arrive(&bars.afull[b.idx]);
                     b.advance(p.a_slots);
                 }
-                mbar_arrive(&bars.empty[ring.idx]);
             }
             apos = a;
             owner_set = os;
@@ -533,7 +536,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.stages; ++s) {
             mbar_init(&bars.full[s], 1);
-            mbar_init(&bars.empty[s], DQ_WARPS + 1);
+            mbar_init(&bars.empty[s], 1); // the MMA warp's commit
         }
         for (int s = 0; s < p.a_slots; ++s) {
             mbar_init(&bars.afull[s], 4); // the four warps of one dequant set
