@@ -38,14 +38,16 @@ __device__ __forceinline__ void issue_block_mmas(uint32_t d_tmem, int nt_half, u
                                                  uint32_t half_bytes, uint32_t idesc,
                                                  uint32_t idesc2, bool accumulate)
 {
+    // The k steps advance the B descriptors' start address by 32 bytes (2 in its 16-byte
+    // units); shared-memory addresses stay below 2^18, so the 14-bit field never carries.
+    const uint64_t b0 = desc_sw128(act), b1 = desc_sw128(act + half_bytes);
 #pragma unroll
     for (int kk = 0; kk < KBLK / 16; ++kk) {
         const uint32_t acc = (accumulate || kk > 0) ? 1u : 0u;
         if (A_TMEM) {
-            mma_ts(d_tmem, a_tmem + kk * 8, desc_sw128(act + kk * 32), idesc, acc);
+            mma_ts(d_tmem, a_tmem + kk * 8, b0 + (uint64_t)(kk * 2), idesc, acc);
             if (PAIR)
-                mma_ts(d_tmem + nt_half, a_tmem + kk * 8, desc_sw128(act + half_bytes + kk * 32),
-                       idesc2, acc);
+                mma_ts(d_tmem + nt_half, a_tmem + kk * 8, b1 + (uint64_t)(kk * 2), idesc2, acc);
         } else {
             const uint64_t adesc = desc_sw128(smem_u32(a_smem) + kk * 32);
             mma_ss(d_tmem, adesc, desc_sw128(act + kk * 32), idesc, acc);
