@@ -435,10 +435,11 @@ class GroupedGemm:
 class StepIO:
     """A step's activations in and results out for the end-to-end run: every GEMM's A and C
     in two device buffers (the step's parity picks one) and one pinned host buffer each, copied
-    on a copy stream: step s+1's inputs go up while step s computes, and step s's results come
-    down behind it.  (Each GEMM keeps tensors of its own: packing all of a step's A and C into
-    one buffer changed nothing measurable; what cost 4 % on prefill was building this staging
-    before the device-timed run, so bench builds it after.)"""
+    on two copy streams, one per direction: step s+1's inputs go up while step s computes, and
+    step s's results come down behind it, while the next inputs go up.  (Each GEMM keeps
+    tensors of its own: packing all of a step's A and C into one buffer changed nothing
+    measurable; what cost 4 % on prefill was building this staging before the device-timed
+    run, so bench builds it after.)"""
 
     def __init__(self, gemms, dev):
         import torch
@@ -461,7 +462,8 @@ class StepIO:
                        for g, out in zip(gemms, self.copy_out)]
         self.h2d_bytes = sum(g.a.numel() * 2 for g, cin in zip(gemms, self.copy_in) if cin)
         self.d2h_bytes = sum(g.c.numel() * 2 for g, out in zip(gemms, self.copy_out) if out)
-        self.copy_stream = torch.cuda.Stream(device=dev)
+        self.in_stream = torch.cuda.Stream(device=dev)
+        self.out_stream = torch.cuda.Stream(device=dev)
 
     def h2d(self, b: int):
         for dst, src, cin in zip(self.a_views[b], self.a_host, self.copy_in):
@@ -480,31 +482,37 @@ class StepIO:
     def enqueue_steps(self, stream, step0, nsteps, run_step):
         """Steps step0.. with their copies: h2d(s+1) overlaps step s, d2h(s) follows it."""
         import torch
-        cs = self.copy_stream
+        cin, cout = self.in_stream, self.out_stream
         ev_in = [torch.cuda.Event(), torch.cuda.Event()]
         ev_done = [torch.cuda.Event(), torch.cuda.Event()]
-        cs.wait_stream(stream)
-        with torch.cuda.stream(cs):
+        ev_out = [torch.cuda.Event(), torch.cuda.Event()]
+        cin.wait_stream(stream)
+        cout.wait_stream(stream)
+        with torch.cuda.stream(cin):
             self.h2d(0)
-            ev_in[0].record(cs)
+            ev_in[0].record(cin)
         for i in range(nsteps):
             b = i & 1
             if i + 1 < nsteps:
                 nb = (i + 1) & 1
-                with torch.cuda.stream(cs):
+                with torch.cuda.stream(cin):
                     if i >= 1:
-                        cs.wait_event(ev_done[nb])   # step i-1 is done with buffer nb
+                        cin.wait_event(ev_done[nb])   # step i-1 is done with buffer nb
                     self.h2d(nb)
-                    ev_in[nb].record(cs)
+                    ev_in[nb].record(cin)
             stream.wait_event(ev_in[b])
+            if i >= 2:
+                stream.wait_event(ev_out[b])         # step i-2's results have left buffer b
             self.bind(b)
             with torch.cuda.stream(stream):
                 run_step(step0 + i)
             ev_done[b].record(stream)
-            with torch.cuda.stream(cs):
-                cs.wait_event(ev_done[b])
+            with torch.cuda.stream(cout):
+                cout.wait_event(ev_done[b])
                 self.d2h(b)
-        stream.wait_stream(cs)
+                ev_out[b].record(cout)
+        stream.wait_stream(cin)
+        stream.wait_stream(cout)
         self.bind(0)
 
 
@@ -766,7 +774,7 @@ def run_ours(args, rank, world, local):
         "clocks": clk,
         "e2e": {"value": round(e2e_value, 4), "unit": unit, "h2d_bytes_per_step": io.h2d_bytes,
                 "d2h_bytes_per_step": io.d2h_bytes, "ms_per_step": round(max_e2e / args.steps, 5),
-                "mode": "C ABI calls; every GEMM's A in from pinned host memory and C out, on a copy stream overlapping the neighbouring steps' compute (double-buffered), captured in a CUDA graph"},
+                "mode": "C ABI calls; every GEMM's A in from pinned host memory and C out, on two copy streams (one per direction) overlapping the neighbouring steps' compute (double-buffered), captured in a CUDA graph"},
         "gpu_launches": launches_per_step * args.steps,
         "detail": detail,
     }

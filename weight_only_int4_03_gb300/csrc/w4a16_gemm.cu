@@ -523,6 +523,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     __shared__ int split_tiles_sh[2];
     __shared__ int n_split_sh;
     __shared__ int total_tiles_sh;
+    __shared__ int pre_sh;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -557,6 +558,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         prefetch_tensormap(&tmap_s);
         if (p.zeros != nullptr)
             prefetch_tensormap(&tmap_z);
+        // Static weights of a dense call: the codes and scales of the first stages go out
+        // before the dependency wait, overlapping the preceding kernel's tail (the schedule of
+        // a dense call reads nothing from memory; a grouped one needs its segment table).
+        pre_sh = 0;
+        if (p.static_weights && p.ex_off == nullptr) {
+            Sched first;
+            first.init(p.m_tiles * p.n_tiles, p.kblocks, p.split);
+            pre_sh = issue_static_weights(p, &tmap_s, &tmap_z, seg, first, smem, bars.full);
+        }
     }
     if (warp == MMA_WARP) {
         tmem_alloc(&tmem_base_sh, p.tmem_cols);
@@ -584,7 +594,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     if (warp == PRODUCER_WARP) {
         if (lane == 0)
-            run_producer(p, &tmap_a, &tmap_s, &tmap_z, seg, sched, smem, bars.full, bars.empty, ctl);
+            run_producer(p, &tmap_a, &tmap_s, &tmap_z, seg, sched, smem, bars.full, bars.empty, ctl,
+                         pre_sh);
     } else if (warp == MMA_WARP) {
         if (lane == 0)
             run_mma<A_TMEM>(p, seg, sched, smem, aring, bars, tmem_base, ctl);
