@@ -97,7 +97,7 @@ def test_zero_points_u4(w4, orc, m):
     check(dp, orc)
 
 
-@pytest.mark.parametrize("m,gs", [(1, 128), (16, 128), (200, 64), (33, 32), (1000, 128)])
+@pytest.mark.parametrize("m,gs", [(1, 128), (16, 128), (200, 64), (33, 32), (1000, 128), (64, 128)])
 def test_act_order(w4, orc, m, gs):
     dp = DeviceProblem(w4, make_problem(400 + m, m, 1024, 512, group_size=gs, act_order=True))
     dp.run()
@@ -343,8 +343,9 @@ def test_repeated_runs_bit_identical(w4, m):
         assert np.array_equal(dp.c.cpu().numpy().view(np.uint16), first.view(np.uint16))
 
 
-def test_unequal_groups_reported(w4):
-    pb = make_problem(706, 8, 256, 256, act_order=True)
+@pytest.mark.parametrize("m", [8, 300])   # element-wise and row-staged gathers
+def test_unequal_groups_reported(w4, m):
+    pb = make_problem(706, m, 256, 256, act_order=True)
     pb.g_idx = pb.g_idx.copy()
     pb.g_idx[pb.perm[0]] = 1   # sorted row 0 claims group 1
     dp = DeviceProblem(w4, pb)

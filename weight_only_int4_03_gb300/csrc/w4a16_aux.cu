@@ -122,6 +122,50 @@ __global__ void unpack_fp8_kernel(const int32_t *__restrict__ tiles, int32_t *__
     }
 }
 
+// The same gather for tall A: one row at a time is staged whole in shared memory with 16-byte
+// loads, then each thread forms eight consecutive outputs from it and writes them as one
+// 16-byte store (K % 8 == 0, lda % 8 == 0, both checked by the caller).  A row costs one read
+// and one write of its bytes instead of a scattered 2-byte load per element.
+__global__ void gather_cols_staged_kernel(const __half *__restrict__ a, int lda,
+                                          const int32_t *__restrict__ perm,
+                                          const int32_t *__restrict__ g_idx, int group_size,
+                                          __half *__restrict__ out, int m, int k, int *status)
+{
+    extern __shared__ __align__(16) uint16_t rowbuf[];
+    pdl_launch_dependents();
+    pdl_wait();
+    const int chunks = k / 8;
+    for (int row = blockIdx.x; row < m; row += gridDim.x) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(a + (long long)row * lda);
+        for (int i = threadIdx.x; i < chunks; i += blockDim.x)
+            reinterpret_cast<uint4 *>(rowbuf)[i] = src[i];
+        __syncthreads();
+        uint4 *dst = reinterpret_cast<uint4 *>(out + (long long)row * k);
+        for (int i = threadIdx.x; i < chunks; i += blockDim.x) {
+            uint32_t w[4];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int col = 8 * i + j;
+                const int sc = perm[col];
+                uint32_t v = 0;
+                if (sc >= 0 && sc < k) {
+                    v = rowbuf[sc];
+                    if (row == 0 && g_idx != nullptr && g_idx[sc] != col / group_size)
+                        atomicOr(status, W4A16_DEV_GIDX);
+                } else if (row == 0) {
+                    atomicOr(status, W4A16_DEV_PERM);
+                }
+                if (j & 1)
+                    w[j >> 1] |= v << 16;
+                else
+                    w[j >> 1] = v;
+            }
+            dst[i] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        __syncthreads();
+    }
+}
+
 // a_perm[m][i] = a[m][perm[i]].  Row 0's threads also check the equal-group property
 // g_idx[perm[i]] == i / group_size that the GEMM relies on.
 __global__ void gather_cols_kernel(const __half *__restrict__ a, int lda,
@@ -434,6 +478,15 @@ int launch_unpack_fp8(const int32_t *tiles, int32_t *qweight, int k, int n, cuda
 int launch_gather_cols(const __half *a, int lda, const int32_t *perm, const int32_t *g_idx,
                        int group_size, __half *out, int m, int k, int *status, cudaStream_t stream)
 {
+    // Tall A with rows that fit the default shared-memory window: staged rows, one CTA per row
+    // (up to 4096 CTAs, each looping).  Short A keeps the element-wise kernel, whose grid also
+    // spreads each row over CTAs.
+    if (m >= 64 && k * 2 <= 48 * 1024 && k % 8 == 0 && lda % 8 == 0) {
+        const int grid = m < 4096 ? m : 4096;
+        gather_cols_staged_kernel<<<grid, 256, k * 2, stream>>>(a, lda, perm, g_idx, group_size,
+                                                                out, m, k, status);
+        return cudaGetLastError();
+    }
     const int bx = (k + 255) / 256;
     dim3 grid(bx, m < 65535 ? m : 65535);
     gather_cols_kernel<<<grid, 256, 0, stream>>>(a, lda, perm, g_idx, group_size, out, m, k, status);
