@@ -304,19 +304,42 @@ int plan_smem(Plan &pl, bool grouped, bool has_zp, int group_size, int g_rows)
         pl.smem_bytes = pl.stages * pl.stage_bytes + red + extra;
         return cudaSuccess;
     }
-    int kbs = stage_blocks_default();
-    if (!pl.mma && kbs > pl.a_slots)
-        kbs = pl.a_slots;
-    for (;; kbs = kbs > 1 ? kbs / 2 : 0) {
-        if (kbs == 0)
+    if (pl.mma) {
+        int kbs = stage_blocks_default();
+        for (;; kbs = kbs > 1 ? kbs / 2 : 0) {
+            if (kbs == 0)
+                return cudaErrorInvalidConfiguration;
+            stage_layout(pl, kbs, group_size, g_rows, has_zp);
+            pl.stages = (limit - extra) / pl.stage_bytes;
+            if (pl.stages >= 3 || (kbs == 1 && pl.stages >= 2))
+                break;
+        }
+        if (pl.stages > MAX_STAGES)
+            pl.stages = MAX_STAGES;
+    } else {
+        // The tcgen05 kernel gives each stage its own kbs weight slots, so stages x kbs <=
+        // a_slots.  The largest stage (from the default block count down) that leaves three
+        // stages in flight, else the one with the most stages (two at the least).
+        int best_kbs = 0, best_stages = 0;
+        for (int kbs = stage_blocks_default(); kbs >= 1; kbs /= 2) {
+            stage_layout(pl, kbs, group_size, g_rows, has_zp);
+            int st = (limit - extra) / pl.stage_bytes;
+            if (st > MAX_STAGES)
+                st = MAX_STAGES;
+            if (st * kbs > pl.a_slots)
+                st = pl.a_slots / kbs;
+            if (st > best_stages) {
+                best_kbs = kbs;
+                best_stages = st;
+            }
+            if (st >= 3)
+                break;
+        }
+        if (best_stages < 2)
             return cudaErrorInvalidConfiguration;
-        stage_layout(pl, kbs, group_size, g_rows, has_zp);
-        pl.stages = (limit - extra) / pl.stage_bytes;
-        if (pl.stages >= 3 || (kbs == 1 && pl.stages >= 2))
-            break;
+        stage_layout(pl, best_kbs, group_size, g_rows, has_zp);
+        pl.stages = best_stages;
     }
-    if (pl.stages > MAX_STAGES)
-        pl.stages = MAX_STAGES;
     pl.epi_off = pl.stages * pl.stage_bytes + (!pl.mma && !pl.a_tmem ? SMEM_A_SLOTS * A_SLOT_BYTES : 0);
     pl.seg_off = pl.epi_off + (pl.mma ? 0 : EPI_STAGE_BYTES);
     pl.smem_bytes = pl.stages * pl.stage_bytes + extra;

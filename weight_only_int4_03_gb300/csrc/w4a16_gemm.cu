@@ -22,8 +22,7 @@ namespace w4 {
 struct Bars {
     uint64_t full[MAX_STAGES];
     uint64_t empty[MAX_STAGES];
-    uint64_t afull[MAX_A_SLOTS];
-    uint64_t aempty[MAX_A_SLOTS];
+    uint64_t afull[MAX_STAGES]; // a stage's weight slots dequantised (its dequant set)
     uint64_t accfull[2];
     uint64_t accempty[2];
     uint64_t drain;
@@ -61,7 +60,7 @@ template <bool A_TMEM>
 __device__ void run_mma(const GemmParams &p, const SegTable &seg, Sched sched, uint8_t *smem,
                         uint8_t *aring, Bars &bars, uint32_t tmem_base, const WaitCtl &ctl)
 {
-    Ring ring, apos;
+    Ring ring;
     uint32_t seg_i = 0;
     int tile, kb0, kb1;
     bool ok = true;
@@ -83,16 +82,17 @@ __device__ void run_mma(const GemmParams &p, const SegTable &seg, Sched sched, u
         const uint32_t d_tmem = tmem_base + p.acc_col0 + abuf * p.nt_max;
         for (int kb = kb0; ok && kb < kb1; kb += p.kbs) {
             const int nkb = min(p.kbs, kb1 - kb);
-            // No wait for the stage itself: a block's dequant-done barrier completes only after
-            // its dequant set has waited for the stage, so the activation rows have landed.
+            // One wait per stage: the stage's dequant set signals all of its blocks at once,
+            // after waiting for the stage itself, so the activation rows have landed too.
+            if (!mbar_wait(&bars.afull[ring.idx], ring.phase, ctl, W4A16_DEV_TIMEOUT)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
             const uint32_t st = smem_u32(smem + (size_t)ring.idx * p.stage_bytes);
+            const int slot0 = ring.idx * p.kbs;
             for (int j = 0; j < nkb; ++j) {
-                const int aslot = apos.idx;
-                if (!mbar_wait(&bars.afull[aslot], apos.phase, ctl, W4A16_DEV_TIMEOUT)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
+                const int aslot = slot0 + j;
                 const uint32_t act = st + j * p.act_kb_bytes;
                 // The single / paired choice is made per block, outside the k steps: a branch
                 // between the MMAs of a block, even one never taken, slowed the kernel by 40 %.
@@ -104,11 +104,9 @@ __device__ void run_mma(const GemmParams &p, const SegTable &seg, Sched sched, u
                     issue_block_mmas<A_TMEM, false>(d_tmem, p.nt_half, tmem_base + aslot * A_SLOT_COLS,
                                                     aring + aslot * A_SLOT_BYTES, act, half_bytes,
                                                     idesc, idesc2, kb + j > kb0);
-                mma_commit(&bars.aempty[aslot]);
-                apos.advance(p.a_slots);
             }
-            if (!ok)
-                break;
+            // One commit releases the stage: its shared memory to the producer and its weight
+            // slots to the dequant set that next fills the stage.
             mma_commit(&bars.empty[ring.idx]);
             ring.advance(p.stages);
         }
@@ -126,10 +124,10 @@ __device__ void run_mma(const GemmParams &p, const SegTable &seg, Sched sched, u
 }
 
 // Dequant: two sets of four warps (one warp per tensor-memory lane quarter).  Consecutive
-// 64-row blocks alternate between the sets; inside a stage a set converts all of its blocks,
-// issues their tensor-memory stores and waits for them once.  Each thread owns one weight
-// column (lane) and turns the 8 words of its column in a block into 64 fp16 values: 32
-// tensor-memory columns.
+// stages alternate between the sets; a set converts all of its stage's blocks into the stage's
+// own weight slots (slot stage * kbs + j), issues their tensor-memory stores and waits for them
+// once.  Each thread owns one weight column (lane) and turns the 8 words of its column in a
+// block into 64 fp16 values: 32 tensor-memory columns.
 constexpr int DQ_SETS = DQ_WARPS / 4;
 
 // grp_rel >= 0: the block lies in one group, row grp_rel of the stage's scales; otherwise
@@ -321,61 +319,73 @@ __device__ void run_dequant(const GemmParams &p, Sched sched, uint8_t *smem, uin
     const int gs = p.group_size;
     const int gs_kb = (gs % KBLK == 0) ? gs / KBLK : 0; // 64-row blocks per group, or 0
     const int gs_sh = group_shift(gs_kb);
-    Ring ring, apos;
-    int owner_set = 0; // dequant set of the next 64-row block
+    Ring ring;
+    // Stages of several blocks are shared: set s converts blocks s, s + DQ_SETS, ... of every
+    // stage, and both sets arrive on the stage's barrier (count 8), whether they had a block in
+    // it or not.  Stages of one block (the tall paired tiles) go to the sets in turn (count 4).
+    // With an even stage count a ring slot then always belongs to the same set, which so sees
+    // every phase of that slot's barrier in order and skips the other set's stages altogether;
+    // with an odd count ownership of a slot alternates, and a set that skipped could wait on a
+    // phase two ahead of the barrier, which a parity test cannot tell from the one before, so
+    // both sets then wait for every stage.
+    const bool shared = p.kbs > 1;
+    const bool lockstep = shared || (p.stages % DQ_SETS) != 0;
+    int owner_set = 0; // dequant set of the next one-block stage
     int tile, kb0, kb1;
     while (sched.next(tile, kb0, kb1)) {
         for (int kb = kb0; kb < kb1; kb += p.kbs) {
             const int nkb = min(p.kbs, kb1 - kb);
-            // A stage without a block of this set is skipped: the set neither waits for it nor
-            // signals it (the stage is released by the MMA warp's commit alone, issued after
-            // every block's dequant-done barrier, so after this set's last read of the stage).
-            const int j0 = set >= owner_set ? set - owner_set : set - owner_set + DQ_SETS;
-            if (j0 >= nkb) {
-                apos = ring_after(apos, nkb, p.a_slots);
-                owner_set = (owner_set + nkb) % DQ_SETS;
+            // A stage's weight slots are free once the stage has landed: the producer refilled
+            // it only after the MMAs that last read those slots completed.
+            bool mine = set < nkb;
+            if (!shared) {
+                mine = owner_set == set;
+                owner_set = (owner_set + 1 == DQ_SETS) ? 0 : owner_set + 1;
+            }
+            if (!mine && !lockstep) {
                 ring.advance(p.stages);
                 continue;
             }
             if (!mbar_wait(&bars.full[ring.idx], ring.phase, ctl, W4A16_DEV_TIMEOUT))
                 return;
+            if (!mine) {
+                if (shared) {
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(&bars.afull[ring.idx]);
+                }
+                ring.advance(p.stages);
+                continue;
+            }
+            tc_fence_after();
             const uint8_t *st = smem + (size_t)ring.idx * p.stage_bytes;
             const __half *ssm = reinterpret_cast<const __half *>(st + p.scales_off);
             const __half *zsm = reinterpret_cast<const __half *>(st + p.zeros_off);
             const int g_first = (kb * KBLK) / gs;
-            uint32_t mine = 0; // bit j: block j of this stage is converted by this warp
-            Ring a = apos;
-            int os = owner_set;
-            for (int j = 0; j < nkb; ++j) {
-                if (os == set) {
-                    if (!mbar_wait(&bars.aempty[a.idx], a.phase ^ 1u, ctl, W4A16_DEV_TIMEOUT))
-                        return;
-                    tc_fence_after();
-                    const int kbj = kb + j;
-                    const int grp_rel = gs_kb == 0   ? -1
-                                        : gs_sh >= 0 ? (kbj >> gs_sh) - g_first
-                                                     : kbj / gs_kb - g_first;
-                    if (WK == WK_FP8_F16)
-                        dequant_block_fp8<A_TMEM>(st + p.packed_off + j * TILE_BYTES_FP8, ssm,
-                                                  grp_rel, nl,
-                                                  tmem_base + lane_base + a.idx * A_SLOT_COLS,
-                                                  aring + a.idx * A_SLOT_BYTES);
-                    else if (WK == WK_U4_BF16)
-                        dequant_block_bf16<A_TMEM>(p, st + p.packed_off + j * TILE_BYTES,
-                                                   reinterpret_cast<const uint16_t *>(ssm),
-                                                   reinterpret_cast<const uint16_t *>(zsm), kbj,
-                                                   g_first, grp_rel, nl, has_zp,
-                                                   tmem_base + lane_base + a.idx * A_SLOT_COLS,
-                                                   aring + a.idx * A_SLOT_BYTES);
-                    else
-                        dequant_block<A_TMEM>(p, st + p.packed_off + j * TILE_BYTES, ssm, zsm, kbj,
-                                              g_first, grp_rel, nl, has_zp,
-                                              tmem_base + lane_base + a.idx * A_SLOT_COLS,
-                                              aring + a.idx * A_SLOT_BYTES);
-                    mine |= 1u << j;
-                }
-                a.advance(p.a_slots);
-                os = (os + 1 == DQ_SETS) ? 0 : os + 1;
+            const int slot0 = ring.idx * p.kbs;
+            const int jstep = shared ? DQ_SETS : 1;
+            for (int j = shared ? set : 0; j < nkb; j += jstep) {
+                const int slot = slot0 + j;
+                const int kbj = kb + j;
+                const int grp_rel = gs_kb == 0   ? -1
+                                    : gs_sh >= 0 ? (kbj >> gs_sh) - g_first
+                                                 : kbj / gs_kb - g_first;
+                if (WK == WK_FP8_F16)
+                    dequant_block_fp8<A_TMEM>(st + p.packed_off + j * TILE_BYTES_FP8, ssm, grp_rel,
+                                              nl, tmem_base + lane_base + slot * A_SLOT_COLS,
+                                              aring + slot * A_SLOT_BYTES);
+                else if (WK == WK_U4_BF16)
+                    dequant_block_bf16<A_TMEM>(p, st + p.packed_off + j * TILE_BYTES,
+                                               reinterpret_cast<const uint16_t *>(ssm),
+                                               reinterpret_cast<const uint16_t *>(zsm), kbj,
+                                               g_first, grp_rel, nl, has_zp,
+                                               tmem_base + lane_base + slot * A_SLOT_COLS,
+                                               aring + slot * A_SLOT_BYTES);
+                else
+                    dequant_block<A_TMEM>(p, st + p.packed_off + j * TILE_BYTES, ssm, zsm, kbj,
+                                          g_first, grp_rel, nl, has_zp,
+                                          tmem_base + lane_base + slot * A_SLOT_COLS,
+                                          aring + slot * A_SLOT_BYTES);
             }
             if (A_TMEM) {
                 tmem_st_wait();
@@ -383,18 +393,10 @@ __device__ void run_dequant(const GemmParams &p, Sched sched, uint8_t *smem, uin
             } else {
                 fence_proxy_async_smem();
             }
-            // One arrival per warp: every lane's writes are complete and fenced first.
+            // One arrival per warp and stage: every lane's writes are complete and fenced first.
             __syncwarp();
-            if (lane == 0) {
-                Ring b = apos;
-                for (int j = 0; j < nkb; ++j) {
-                    if (mine & (1u << j))
-                        mbar_arrive(&bars.afull[b.idx]);
-                    b.advance(p.a_slots);
-                }
-            }
-            apos = a;
-            owner_set = os;
+            if (lane == 0)
+                mbar_arrive(&bars.afull[ring.idx]);
             ring.advance(p.stages);
         }
     }
@@ -541,10 +543,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(&bars.full[s], 1);
             mbar_init(&bars.empty[s], 1); // the MMA warp's commit
         }
-        for (int s = 0; s < p.a_slots; ++s) {
-            mbar_init(&bars.afull[s], 4); // the four warps of one dequant set
-            mbar_init(&bars.aempty[s], 1);
-        }
+        for (int s = 0; s < p.stages; ++s)   // the warps of the sets converting the stage
+            mbar_init(&bars.afull[s], p.kbs > 1 ? 4 * DQ_SETS : 4);
         for (int s = 0; s < 2; ++s) {
             mbar_init(&bars.accfull[s], 1);
             mbar_init(&bars.accempty[s], EPI_THREADS / 32);
