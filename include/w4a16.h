@@ -82,9 +82,12 @@ extern "C" {
                                            (marlin.rs declares bf16 A and C for its
                                            `ferrum_vllm_marlin_moe_mxfp4_bf16` entry point;
                                            here with the 4-bit codes).  4-bit weight types
-                                           only (not W4A16_TYPE_FE4M3); tcgen05 kernel only
-                                           (_FORCE_SIMT, _FORCE_MMA and _FORCE_SLICE are
-                                           rejected).  (q - z) is exact in bf16 for integer
+                                           only (not W4A16_TYPE_FE4M3); the tcgen05 kernel and,
+                                           for group_size -1 or a multiple of 64, the small-M
+                                           kernels (_FORCE_SIMT is rejected, _FORCE_MMA with
+                                           other groups is unsupported-shape; the default choice
+                                           sends those groups to the tcgen05 kernel).  (q - z)
+                                           is exact in bf16 for integer
                                            zero points, the product with the scale is rounded
                                            once to bf16 (8 significant bits), products sum in
                                            fp32 and C is rounded once to bf16               */

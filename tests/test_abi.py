@@ -102,9 +102,8 @@ def gemm_status(w4, **kw):
     (dict(flags=1 << 15 | 1 << 13), 1, 4),
     (dict(flags=1 << 14 | 1 << 8), 1, 4),        # ... or the CUDA-core reference kernel
     (dict(flags=1 << 14, ldc=120), 1, 3),        # gated output narrower than I = 128
-    (dict(flags=1 << 16 | 1 << 11), 1, 4),       # bf16 operands with a small-M kernel forced
-    (dict(flags=1 << 16 | 1 << 13), 1, 4),
-    (dict(flags=1 << 16 | 1 << 8), 1, 4),        # ... or the CUDA-core reference kernel
+    (dict(flags=1 << 16 | 1 << 11, gs=32), 2, 3),  # bf16 small-M kernels: whole-block groups
+    (dict(flags=1 << 16 | 1 << 8), 1, 4),        # bf16 with the CUDA-core reference kernel
     (dict(flags=1 << 16 | 1 << 2, wt=8), 1, 4),  # bf16 operands with FP8 weights
 ])
 def test_gemm_rejects_bad_arguments_on_host(w4, kw, stage, detail):
@@ -290,10 +289,17 @@ def test_gated_calls_run_the_tcgen05_kernel(w4):
     assert w4.w4a16_kernel_for(1, 4096, 4096, 128, w4.W4A16_FLAG_SWIGLU | w4.W4A16_FLAG_GEGLU, 152) == -1
 
 
-def test_bf16_calls_run_the_tcgen05_kernel(w4):
-    for m in (1, 16, 64, 4096):
-        assert w4.w4a16_kernel_for(m, 4096, 4096, 128, w4.W4A16_FLAG_BF16, 152) == 0
-    assert w4.w4a16_kernel_for(1, 4096, 4096, 128, w4.W4A16_FLAG_BF16 | (1 << 11), 152) == -1
+def test_bf16_kernel_choice(w4):
+    """bf16 calls follow the fp16 dispatch rule for groups of whole blocks; smaller groups go
+    to the tcgen05 kernel (the small-M kernels' bf16 variants need whole-block groups)."""
+    bf = w4.W4A16_FLAG_BF16
+    for m, n, gs in ((1, 4096, 128), (16, 12288, 128), (64, 4096, 128), (4096, 4096, 128), (8, 4096, -1)):
+        assert w4.w4a16_kernel_for(m, n, 4096, gs, bf, 152) == w4.w4a16_kernel_for(m, n, 4096, gs, 0, 152)
+    for m in (1, 16, 32):
+        assert w4.w4a16_kernel_for(m, 4096, 4096, 32, bf, 152) == 0
+    assert w4.w4a16_kernel_for(1, 4096, 4096, 128, bf | (1 << 11), 152) == 1
+    assert w4.w4a16_kernel_for(1, 4096, 4096, 128, bf | (1 << 13), 152) == 2
+    assert w4.w4a16_kernel_for(1, 4096, 4096, 32, bf | (1 << 11), 152) == -1
 
 
 def test_gate_up_interleave_rejects_bad_arguments(w4):

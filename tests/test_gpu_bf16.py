@@ -174,3 +174,43 @@ def test_bf16_grouped_matches_oracle(w4, orc):
         ref[seg] = orc.gemm_bf16(np.ascontiguousarray(a[tok[seg]]), qws[e], ss[e], None, None, gs, U4B8)
     ok, msg = within_tol(got, ref, RTOL, ATOL)
     assert ok, msg
+
+
+FORCE_MMA, FORCE_SLICE = 1 << 11, 1 << 13
+
+
+@pytest.mark.parametrize("m,k,n,gs,wt,force", [
+    (1, 1024, 512, 128, U4B8, FORCE_SLICE),
+    (5, 4224, 768, 192, U4, FORCE_SLICE),       # groups straddle stages; partial last stage
+    (16, 2048, 4096, -1, U4B8, FORCE_SLICE),
+    (32, 1024, 512, 128, U4, FORCE_SLICE),      # four 8-token tiles
+    (1, 2048, 512, 128, U4B8, FORCE_MMA),       # split-K, deferred group scales
+    (16, 1024, 768, 256, U4, FORCE_MMA),
+    (40, 2048, 512, 128, U4B8, FORCE_MMA),      # scales in the dequantisation, ragged tile
+    (64, 1024, 1024, 64, U4, FORCE_MMA),
+])
+def test_bf16_small_m_kernels_match_oracle(w4, orc, m, k, n, gs, wt, force):
+    seed = 9400 + m + k
+    a, qw, s, z, g_idx, perm = make(seed, m, k, n, gs, wt, sigma=0.5 if wt == U4 else 1.0)
+    got = run_bf16(w4, a, qw, s, z, g_idx, perm, k, n, gs, wt, extra=force)
+    ref = orc.gemm_bf16(a, qw, s, z, g_idx, gs, wt)
+    ok, msg = within_tol(got, ref, RTOL, ATOL)
+    assert ok, msg
+
+
+@pytest.mark.parametrize("force", [0, FORCE_MMA, FORCE_SLICE])
+def test_bf16_one_hot_bit_exact_on_every_kernel(w4, force):
+    """Code 9 at row pi(n), code 8 elsewhere, unit scales: C[:, n] = A[:, pi(n)] exactly,
+    whichever kernel runs (default choice at M=4: the column-slice kernel)."""
+    m, k, n = 4, 512, 256
+    a = synth.bf16_bits(synth.Stream(9500, "A").normal(m * k, 1.0)).reshape(m, k)
+    pi = (np.arange(n) * 29 + 3) % k
+    codes = np.full((k, n), 8, dtype=np.uint32)
+    codes[pi, np.arange(n)] = 9
+    qw = np.zeros((k // 8, n), dtype=np.uint32)
+    for i in range(8):
+        qw |= codes[i::8, :] << np.uint32(4 * i)
+    s = synth.bf16_bits(np.ones((k // 128, n)))
+    got = run_bf16(w4, a, qw.view(np.int32), s, None, None, None, k, n, 128, U4B8, extra=force)
+    want = (a[:, pi].astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+    assert np.array_equal(got, want)

@@ -548,13 +548,18 @@ int glu_kind(unsigned flags)
 // split-K small-M kernel M <= 64.
 int check_kernel_flags(int m, int gs, unsigned flags)
 {
-    // The gated epilogue lives in the tcgen05 kernel (and its split-tile reduction) only.
-    // So do the bfloat16 operand formats.
+    // The gated epilogue lives in the tcgen05 kernel (and its split-tile reduction) only; the
+    // bfloat16 operand formats in the tcgen05 kernel and, for groups of whole 64-row blocks,
+    // the small-M kernels (not the CUDA-core reference kernel).
     const int glu = glu_kind(flags);
-    const bool tc_only = glu > 0 || (flags & W4A16_FLAG_BF16);
-    if (glu < 0 || (tc_only && (flags & (W4A16_FLAG_FORCE_SIMT | W4A16_FLAG_FORCE_MMA |
+    const bool bf16 = (flags & W4A16_FLAG_BF16) != 0;
+    if (glu < 0 || (glu > 0 && (flags & (W4A16_FLAG_FORCE_SIMT | W4A16_FLAG_FORCE_MMA |
                                          W4A16_FLAG_FORCE_SLICE))))
         return status_of(STAGE_ARG, W4A16_ARG_FLAGS);
+    if (bf16 && (flags & W4A16_FLAG_FORCE_SIMT))
+        return status_of(STAGE_ARG, W4A16_ARG_FLAGS);
+    if (bf16 && (flags & W4A16_FLAG_FORCE_MMA) && gs % KBLK != 0)
+        return status_of(STAGE_UNSUPPORTED, W4A16_ARG_SHAPE);
     const unsigned other = W4A16_FLAG_FORCE_TC | W4A16_FLAG_A_SMEM | W4A16_FLAG_FORCE_SIMT;
     if (flags & W4A16_FLAG_FORCE_SLICE) {
         if (flags & (other | W4A16_FLAG_FORCE_MMA))
@@ -583,7 +588,10 @@ int choose_kernel(int m, int n, int gs, unsigned flags, int num_sms)
     if (flags & W4A16_FLAG_FORCE_MMA)
         return 1;
     if (flags & (W4A16_FLAG_FORCE_TC | W4A16_FLAG_A_SMEM | W4A16_FLAG_FORCE_SIMT |
-                 W4A16_FLAG_SWIGLU | W4A16_FLAG_GEGLU | W4A16_FLAG_BF16))
+                 W4A16_FLAG_SWIGLU | W4A16_FLAG_GEGLU))
+        return 0;
+    // bf16 small-M kernels take groups of whole 64-row blocks only.
+    if ((flags & W4A16_FLAG_BF16) && gs % KBLK != 0)
         return 0;
     // 9..32 tokens (two or four 8-token tiles, a shallower ring) only while each CTA gets one
     // slice: at N=12288 (3 slices per CTA) the split-K kernel is faster at M=16.

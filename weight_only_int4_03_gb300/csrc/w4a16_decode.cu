@@ -68,63 +68,107 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr)
     return *reinterpret_cast<const uint32_t *>(smem_raw + (addr - base));
 }
 
-// D (f32 16x8) += A (f16 16x16, row) * B (f16 16x8, col).  Registers only, so the compiler
-// may schedule it freely.
+// D (f32 16x8) += A (16x16, row) * B (16x8, col), fp16 or (BF) bf16 operands.  Registers
+// only, so the compiler may schedule it freely.
+template <bool BF>
 __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                           uint32_t a3, uint32_t b0, uint32_t b1)
 {
-    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
-                 "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    if (BF)
+        asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+            "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    else
+        asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+            "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Codes -> fp16 pairs (q - z) for one column (one zero for all 8 codes), exact: pair p of
-// word x sits at bits (4p, 16 + 4p).
-__device__ __forceinline__ void dequant_word_int(uint32_t x, __half2 zlo, __half2 zhi,
+__device__ __forceinline__ __nv_bfloat162 u32_as_bf2(uint32_t v)
+{
+    return *reinterpret_cast<__nv_bfloat162 *>(&v);
+}
+
+__device__ __forceinline__ uint32_t bf2_as_u32(__nv_bfloat162 v)
+{
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// Codes -> pairs (q - z) for one column (one zero for all 8 codes), exact: pair p of word x
+// sits at bits (4p, 16 + 4p).  fp16: the nibbles at bits 0-3 go into 1024.0 (spacing 1) and
+// those at bits 4-7 into 1024.0 at spacing 16 (undone by an fma with 1/16); zlo = 1024 + z,
+// zhi = -(64 + z).  bf16 (7 fraction bits): every nibble is first shifted to bits 0-3 and
+// OR-ed into 128.0; zlo = -(128 + z).
+template <bool BF>
+__device__ __forceinline__ void dequant_word_int(uint32_t x, uint32_t zlo, uint32_t zhi,
                                                  uint32_t (&out)[4])
 {
+    if (BF) {
+        const uint32_t xs[4] = {x, __umulhi(x, 1u << 28), __umulhi(x, 1u << 24), __umulhi(x, 1u << 20)};
+#pragma unroll
+        for (int pp = 0; pp < 4; ++pp)
+            out[pp] = bf2_as_u32(__hadd2(u32_as_bf2((xs[pp] & 0x000F000Fu) | 0x43004300u),
+                                         u32_as_bf2(zlo)));
+        return;
+    }
     const uint32_t magic = 0x64006400u;
     const __half2 sixteenth = __halves2half2(__ushort_as_half(0x2C00), __ushort_as_half(0x2C00));
     const uint32_t x8 = __umulhi(x, 1u << 24); // x >> 8, on the FMA pipe (the integer pipe is the busy one)
-    out[0] = h2_as_u32(__hsub2(u32_as_h2((x & 0x000F000Fu) | magic), zlo));
-    out[1] = h2_as_u32(__hfma2(u32_as_h2((x & 0x00F000F0u) | magic), sixteenth, zhi));
-    out[2] = h2_as_u32(__hsub2(u32_as_h2((x8 & 0x000F000Fu) | magic), zlo));
-    out[3] = h2_as_u32(__hfma2(u32_as_h2((x8 & 0x00F000F0u) | magic), sixteenth, zhi));
+    out[0] = h2_as_u32(__hsub2(u32_as_h2((x & 0x000F000Fu) | magic), u32_as_h2(zlo)));
+    out[1] = h2_as_u32(__hfma2(u32_as_h2((x & 0x00F000F0u) | magic), sixteenth, u32_as_h2(zhi)));
+    out[2] = h2_as_u32(__hsub2(u32_as_h2((x8 & 0x000F000Fu) | magic), u32_as_h2(zlo)));
+    out[3] = h2_as_u32(__hfma2(u32_as_h2((x8 & 0x00F000F0u) | magic), sixteenth, u32_as_h2(zhi)));
 }
 
-// Codes -> fp16 pairs (q - z) * s for one column (one scale and zero for all 8 codes): pair p
-// of word x sits at bits (4p, 16 + 4p).  (q - z) is exact; the product is rounded once.
-__device__ __forceinline__ void dequant_word_col(uint32_t x, __half2 zlo, __half2 zhi, __half2 s,
+// The same pairs times the column's scale s: (q - z) is exact; the product is rounded once.
+template <bool BF>
+__device__ __forceinline__ void dequant_word_col(uint32_t x, uint32_t zlo, uint32_t zhi, uint32_t s,
                                                  uint32_t (&out)[4])
 {
-    const uint32_t magic = 0x64006400u;
-    const __half2 sixteenth = __halves2half2(__ushort_as_half(0x2C00), __ushort_as_half(0x2C00));
-    const uint32_t x8 = __umulhi(x, 1u << 24); // x >> 8, on the FMA pipe (the integer pipe is the busy one)
-    out[0] = h2_as_u32(__hmul2(__hsub2(u32_as_h2((x & 0x000F000Fu) | magic), zlo), s));
-    out[1] = h2_as_u32(__hmul2(__hfma2(u32_as_h2((x & 0x00F000F0u) | magic), sixteenth, zhi), s));
-    out[2] = h2_as_u32(__hmul2(__hsub2(u32_as_h2((x8 & 0x000F000Fu) | magic), zlo), s));
-    out[3] = h2_as_u32(__hmul2(__hfma2(u32_as_h2((x8 & 0x00F000F0u) | magic), sixteenth, zhi), s));
+    uint32_t v[4];
+    dequant_word_int<BF>(x, zlo, zhi, v);
+#pragma unroll
+    for (int pp = 0; pp < 4; ++pp)
+        out[pp] = BF ? bf2_as_u32(__hmul2(u32_as_bf2(v[pp]), u32_as_bf2(s)))
+                     : h2_as_u32(__hmul2(u32_as_h2(v[pp]), u32_as_h2(s)));
 }
 
-// Scale (as a broadcast pair) and (1024 + z), -(64 + z) of column `col` in group row `grp` of
-// a stage; the zero offsets are constants for u4b8 (z = 8).
+// Scale (as a broadcast pair of 16-bit values, and as a float) and the zero offsets of column
+// `col` in group row `grp` of a stage (dequant_word_int); constants for u4b8 (z = 8).
 struct ColGroup {
-    __half2 s, zlo, zhi;
+    uint32_t s, zlo, zhi;
+    float sf;
 };
 
+template <bool BF>
 __device__ __forceinline__ ColGroup col_group(bool has_zp, const __half *ssm, const __half *zsm,
                                               int idx)
 {
     ColGroup cgp;
-    cgp.s = __half2half2(ssm[idx]);
+    if (BF) {
+        const uint16_t sb = reinterpret_cast<const uint16_t *>(ssm)[idx];
+        cgp.s = (uint32_t)sb * 0x10001u;
+        cgp.sf = __bfloat162float(__ushort_as_bfloat16(sb));
+        __nv_bfloat16 zn = __ushort_as_bfloat16((uint16_t)0xC308); // -136 = -(128 + 8)
+        if (has_zp)
+            zn = __hneg(__hadd(__ushort_as_bfloat16((uint16_t)0x4300),
+                               __ushort_as_bfloat16(reinterpret_cast<const uint16_t *>(zsm)[idx])));
+        cgp.zlo = (uint32_t)__bfloat16_as_ushort(zn) * 0x10001u;
+        cgp.zhi = 0;
+        return cgp;
+    }
+    const __half sh = ssm[idx];
+    cgp.s = (uint32_t)__half_as_ushort(sh) * 0x10001u;
+    cgp.sf = __half2float(sh);
     if (has_zp) {
         const __half z = zsm[idx];
-        cgp.zlo = __half2half2(__hadd(__ushort_as_half(0x6400), z));         // 1024 + z
-        cgp.zhi = __half2half2(__hneg(__hadd(__ushort_as_half(0x5400), z))); // -(64 + z)
+        cgp.zlo = (uint32_t)__half_as_ushort(__hadd(__ushort_as_half(0x6400), z)) * 0x10001u;          // 1024 + z
+        cgp.zhi = (uint32_t)__half_as_ushort(__hneg(__hadd(__ushort_as_half(0x5400), z))) * 0x10001u; // -(64 + z)
     } else {
-        cgp.zlo = __half2half2(__ushort_as_half(0x6408)); // 1032
-        cgp.zhi = __half2half2(__ushort_as_half(0xD480)); // -72
+        cgp.zlo = 0x64086408u; // 1032
+        cgp.zhi = 0xD480D480u; // -72
     }
     return cgp;
 }
@@ -137,32 +181,32 @@ __device__ __forceinline__ ColGroup col_group(bool has_zp, const __half *ssm, co
 // acc1 (two independent MMA chains when they differ).
 // HALF: bytes from a block's first 32-row half to its second (2048 in a 128-column tile, 256
 // in a 16-column slice); column col + 8 is always 128 bytes on.
-template <int NT, bool SCALED, int HALF = 2048>
+template <int NT, bool SCALED, int HALF = 2048, bool BF = false>
 __device__ __forceinline__ void block_mma(uint32_t w_addr, uint32_t act0, uint32_t act1,
                                           const ColGroup &c0, const ColGroup &c1,
                                           float (&acc0)[NT][4], float (&acc1)[NT][4])
 {
     uint32_t a0[4], a1[4], a2[4], a3[4];
     if (SCALED) {
-        dequant_word_col(lds32(w_addr), c0.zlo, c0.zhi, c0.s, a0);
-        dequant_word_col(lds32(w_addr + 128), c1.zlo, c1.zhi, c1.s, a1);
-        dequant_word_col(lds32(w_addr + HALF), c0.zlo, c0.zhi, c0.s, a2);
-        dequant_word_col(lds32(w_addr + HALF + 128), c1.zlo, c1.zhi, c1.s, a3);
+        dequant_word_col<BF>(lds32(w_addr), c0.zlo, c0.zhi, c0.s, a0);
+        dequant_word_col<BF>(lds32(w_addr + 128), c1.zlo, c1.zhi, c1.s, a1);
+        dequant_word_col<BF>(lds32(w_addr + HALF), c0.zlo, c0.zhi, c0.s, a2);
+        dequant_word_col<BF>(lds32(w_addr + HALF + 128), c1.zlo, c1.zhi, c1.s, a3);
     } else {
-        dequant_word_int(lds32(w_addr), c0.zlo, c0.zhi, a0);
-        dequant_word_int(lds32(w_addr + 128), c1.zlo, c1.zhi, a1);
-        dequant_word_int(lds32(w_addr + HALF), c0.zlo, c0.zhi, a2);
-        dequant_word_int(lds32(w_addr + HALF + 128), c1.zlo, c1.zhi, a3);
+        dequant_word_int<BF>(lds32(w_addr), c0.zlo, c0.zhi, a0);
+        dequant_word_int<BF>(lds32(w_addr + 128), c1.zlo, c1.zhi, a1);
+        dequant_word_int<BF>(lds32(w_addr + HALF), c0.zlo, c0.zhi, a2);
+        dequant_word_int<BF>(lds32(w_addr + HALF + 128), c1.zlo, c1.zhi, a3);
     }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
         uint32_t b[4], e[4];
         ldmatrix_x4(act0 + nt * 1024, b);
         ldmatrix_x4(act1 + nt * 1024, e);
-        mma_16816(acc0[nt], a0[0], a1[0], a0[1], a1[1], b[0], b[1]);
-        mma_16816(acc1[nt], a2[0], a3[0], a2[1], a3[1], e[0], e[1]);
-        mma_16816(acc0[nt], a0[2], a1[2], a0[3], a1[3], b[2], b[3]);
-        mma_16816(acc1[nt], a2[2], a3[2], a2[3], a3[3], e[2], e[3]);
+        mma_16816<BF>(acc0[nt], a0[0], a1[0], a0[1], a1[1], b[0], b[1]);
+        mma_16816<BF>(acc1[nt], a2[0], a3[0], a2[1], a3[1], e[0], e[1]);
+        mma_16816<BF>(acc0[nt], a0[2], a1[2], a0[3], a1[3], b[2], b[3]);
+        mma_16816<BF>(acc1[nt], a2[2], a3[2], a2[3], a3[3], e[2], e[3]);
     }
 }
 
@@ -188,7 +232,7 @@ constexpr int DEC_UNROLL = 4; // stages of exactly this many blocks take the unr
 // NT: 8-token tiles per CTA tile (nt_max = 8 * NT).  BLOCK_GROUPS: group_size is a multiple
 // of 64, so a group covers whole blocks and one scale serves all of a lane's codes in a
 // block; otherwise each 8-row pair looks up its own group (slow, general path).
-template <int NT, bool BLOCK_GROUPS>
+template <int NT, bool BLOCK_GROUPS, bool BF>
 __device__ void run_compute(const GemmParams &p, Sched sched, uint8_t *smem, DecBars &bars,
                             const WaitCtl &ctl, int w, int lane, volatile int *last_flag)
 {
@@ -264,24 +308,24 @@ __device__ void run_compute(const GemmParams &p, Sched sched, uint8_t *smem, Dec
                 if (in_grp >= gs_kb)
                     in_grp = gs_pow2 ? (in_grp & (gs_kb - 1)) : in_grp % gs_kb;
                 int gidx = col0; // scale index of the current group (relative to the stage's)
-                ColGroup c0 = col_group(has_zp, ssm, zsm, gidx);
-                ColGroup c1 = col_group(has_zp, ssm, zsm, gidx + 8);
-                s0 = __low2float(c0.s);
-                s1 = __low2float(c1.s);
+                ColGroup c0 = col_group<BF>(has_zp, ssm, zsm, gidx);
+                ColGroup c1 = col_group<BF>(has_zp, ssm, zsm, gidx + 8);
+                s0 = c0.sf;
+                s1 = c1.sf;
                 auto next_group = [&]() {
                     gidx += TILE_N;
-                    c0 = col_group(has_zp, ssm, zsm, gidx);
-                    c1 = col_group(has_zp, ssm, zsm, gidx + 8);
-                    s0 = __low2float(c0.s);
-                    s1 = __low2float(c1.s);
+                    c0 = col_group<BF>(has_zp, ssm, zsm, gidx);
+                    c1 = col_group<BF>(has_zp, ssm, zsm, gidx + 8);
+                    s0 = c0.sf;
+                    s1 = c1.sf;
                 };
                 if (nkb == DEC_UNROLL) {
                     // Taller tiles keep more accumulators live: unroll less there.
                     constexpr int UNROLL = NT <= 2 ? DEC_UNROLL : 2;
 #pragma unroll UNROLL
                     for (int j = 0; j < DEC_UNROLL; ++j) {
-                        block_mma<NT, !DEFER>(w_addr + j * TILE_BYTES, act0 + j * p.act_kb_bytes,
-                                              act1 + j * p.act_kb_bytes, c0, c1, g0, g1);
+                        block_mma<NT, !DEFER, 2048, BF>(w_addr + j * TILE_BYTES, act0 + j * p.act_kb_bytes,
+                                                        act1 + j * p.act_kb_bytes, c0, c1, g0, g1);
                         if (gend & (1u << j)) {
                             if (DEFER)
                                 flush_group<NT>(acc, g0, g1, s0, s1);
@@ -291,8 +335,8 @@ __device__ void run_compute(const GemmParams &p, Sched sched, uint8_t *smem, Dec
                     }
                 } else {
                     for (int j = 0; j < nkb; ++j) {
-                        block_mma<NT, !DEFER>(w_addr + j * TILE_BYTES, act0 + j * p.act_kb_bytes,
-                                              act1 + j * p.act_kb_bytes, c0, c1, g0, g1);
+                        block_mma<NT, !DEFER, 2048, BF>(w_addr + j * TILE_BYTES, act0 + j * p.act_kb_bytes,
+                                                        act1 + j * p.act_kb_bytes, c0, c1, g0, g1);
                         if (gend & (1u << j)) {
                             if (DEFER)
                                 flush_group<NT>(acc, g0, g1, s0, s1);
@@ -318,8 +362,8 @@ __device__ void run_compute(const GemmParams &p, Sched sched, uint8_t *smem, Dec
                         for (int nt = 0; nt < NT; ++nt) {
                             uint32_t b[4];
                             ldmatrix_x4(actj + nt * 1024, b);
-                            mma_16816(acc[nt], a0[0], a1[0], a0[1], a1[1], b[0], b[1]);
-                            mma_16816(acc[nt], a0[2], a1[2], a0[3], a1[3], b[2], b[3]);
+                            mma_16816<BF>(acc[nt], a0[0], a1[0], a0[1], a1[1], b[0], b[1]);
+                            mma_16816<BF>(acc[nt], a0[2], a1[2], a0[3], a1[3], b[2], b[3]);
                         }
                     }
                     pw += TILE_WORDS;
@@ -351,7 +395,8 @@ __device__ void run_compute(const GemmParams &p, Sched sched, uint8_t *smem, Dec
                 if (row >= ti.rows)
                     continue;
                 if (whole)
-                    p.c[(long long)(ti.row0 + row) * p.ldc + ti.n0 + col] = __float2half_rn(v);
+                    reinterpret_cast<uint16_t *>(p.c)[(long long)(ti.row0 + row) * p.ldc + ti.n0 + col] =
+                        to_out16(v, BF);
                 else
                     __stcg(part + row * TILE_N + col, v);
             }
@@ -375,7 +420,7 @@ __device__ void run_compute(const GemmParams &p, Sched sched, uint8_t *smem, Dec
     }
 }
 
-template <int NT, bool BLOCK_GROUPS>
+template <int NT, bool BLOCK_GROUPS, bool BF = false>
 __global__ void __launch_bounds__(DEC_THREADS, DEC_CTAS_PER_SM)
     w4a16_decode_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap tmap_a,
                         const __grid_constant__ CUtensorMap tmap_s, const __grid_constant__ CUtensorMap tmap_z)
@@ -428,7 +473,7 @@ __global__ void __launch_bounds__(DEC_THREADS, DEC_CTAS_PER_SM)
             run_producer(p, &tmap_a, &tmap_s, &tmap_z, no_seg, sched, smem, bars.full, bars.empty,
                          ctl, pre, true);
     } else {
-        run_compute<NT, BLOCK_GROUPS>(p, sched, smem, bars, ctl, warp - 1, lane, &last_sh);
+        run_compute<NT, BLOCK_GROUPS, BF>(p, sched, smem, bars, ctl, warp - 1, lane, &last_sh);
     }
     __syncwarp();
     __syncthreads();
@@ -520,7 +565,7 @@ static __device__ void slice_producer(const GemmParams &p, const CUtensorMap *tm
 // One 64-row block of the lane's two slice columns (c and c + 8) against NT 8-token tiles:
 // `w_addr` is the lane's first code word, act0[nt] / act1[nt] its ldmatrix row addresses for
 // the block's two 32-row halves.
-template <int NT>
+template <int NT, bool BF>
 __device__ __forceinline__ void slice_block_mma(uint32_t w_addr, const uint32_t (&act0)[NT],
                                                 const uint32_t (&act1)[NT], const ColGroup &c0,
                                                 const ColGroup &c1, float (&acc0)[NT][4],
@@ -528,19 +573,19 @@ __device__ __forceinline__ void slice_block_mma(uint32_t w_addr, const uint32_t 
 {
     constexpr uint32_t HALF = SLICE_N * 4 * 4; // 256 bytes: one 32-row half of the slice
     uint32_t a0[4], a1[4], a2[4], a3[4];
-    dequant_word_col(lds32(w_addr), c0.zlo, c0.zhi, c0.s, a0);
-    dequant_word_col(lds32(w_addr + 128), c1.zlo, c1.zhi, c1.s, a1);
-    dequant_word_col(lds32(w_addr + HALF), c0.zlo, c0.zhi, c0.s, a2);
-    dequant_word_col(lds32(w_addr + HALF + 128), c1.zlo, c1.zhi, c1.s, a3);
+    dequant_word_col<BF>(lds32(w_addr), c0.zlo, c0.zhi, c0.s, a0);
+    dequant_word_col<BF>(lds32(w_addr + 128), c1.zlo, c1.zhi, c1.s, a1);
+    dequant_word_col<BF>(lds32(w_addr + HALF), c0.zlo, c0.zhi, c0.s, a2);
+    dequant_word_col<BF>(lds32(w_addr + HALF + 128), c1.zlo, c1.zhi, c1.s, a3);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
         uint32_t b[4], e[4];
         ldmatrix_x4(act0[nt], b);
         ldmatrix_x4(act1[nt], e);
-        mma_16816(acc0[nt], a0[0], a1[0], a0[1], a1[1], b[0], b[1]);
-        mma_16816(acc1[nt], a2[0], a3[0], a2[1], a3[1], e[0], e[1]);
-        mma_16816(acc0[nt], a0[2], a1[2], a0[3], a1[3], b[2], b[3]);
-        mma_16816(acc1[nt], a2[2], a3[2], a2[3], a3[3], e[2], e[3]);
+        mma_16816<BF>(acc0[nt], a0[0], a1[0], a0[1], a1[1], b[0], b[1]);
+        mma_16816<BF>(acc1[nt], a2[0], a3[0], a2[1], a3[1], e[0], e[1]);
+        mma_16816<BF>(acc0[nt], a0[2], a1[2], a0[3], a1[3], b[2], b[3]);
+        mma_16816<BF>(acc1[nt], a2[2], a3[2], a2[3], a3[3], e[2], e[3]);
     }
 }
 
@@ -548,7 +593,7 @@ __device__ __forceinline__ void slice_block_mma(uint32_t w_addr, const uint32_t 
 // A stage's activations are kbs blocks x M rows of 128 bytes in the 128-byte swizzle (16-byte
 // chunk c of row j at j*128 + ((c ^ (j & 7)) << 4) from the 1024-aligned stage start); the
 // lanes of a token row at or past M point ldmatrix at the zero row instead.
-template <int NT>
+template <int NT, bool BF>
 __device__ void slice_compute(const GemmParams &p, uint8_t *smem, DecBars &bars,
                               const WaitCtl &ctl, int w, int lane, int s_begin, int s_end,
                               int n_st)
@@ -611,8 +656,8 @@ __device__ void slice_compute(const GemmParams &p, uint8_t *smem, DecBars &bars,
                 const int bl = w * BPW + j;
                 const int kb = kb0 + bl;
                 const int g = (gsh >= 0 ? kb >> gsh : kb / gs_kb) - g_stage;
-                const ColGroup c0 = col_group(has_zp, ssm, zsm, g * SLICE_N + c);
-                const ColGroup c1 = col_group(has_zp, ssm, zsm, g * SLICE_N + c + 8);
+                const ColGroup c0 = col_group<BF>(has_zp, ssm, zsm, g * SLICE_N + c);
+                const ColGroup c1 = col_group<BF>(has_zp, ssm, zsm, g * SLICE_N + c + 8);
                 uint32_t act0[NT], act1[NT];
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
@@ -620,7 +665,7 @@ __device__ void slice_compute(const GemmParams &p, uint8_t *smem, DecBars &bars,
                     act0[nt] = ok ? act_base + act_off0[j][nt] : zero_row;
                     act1[nt] = ok ? act_base + act_off1[j][nt] : zero_row;
                 }
-                slice_block_mma<NT>(w_base + (uint32_t)(bl * 2 * SLICE_N * 4 * 4), act0, act1, c0,
+                slice_block_mma<NT, BF>(w_base + (uint32_t)(bl * 2 * SLICE_N * 4 * 4), act0, act1, c0,
                                     c1, acc0, acc1);
             };
             if (kb0 + KBS <= p.kblocks) {
@@ -671,12 +716,12 @@ __device__ void slice_compute(const GemmParams &p, uint8_t *smem, DecBars &bars,
             const int row = nt * 8 + 2 * (ln & 3) + (i & 1);
             const int col = sl * SLICE_N + (ln >> 2) + 8 * (i >> 1);
             if (row < m)
-                p.c[(long long)row * p.ldc + col] = __float2half_rn(v);
+                reinterpret_cast<uint16_t *>(p.c)[(long long)row * p.ldc + col] = to_out16(v, BF);
         }
     }
 }
 
-template <int NT>
+template <int NT, bool BF = false>
 __global__ void __launch_bounds__(DEC_THREADS, DEC_CTAS_PER_SM)
     w4a16_slice_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap tmap_a,
                        const __grid_constant__ CUtensorMap tmap_w,
@@ -731,7 +776,7 @@ __global__ void __launch_bounds__(DEC_THREADS, DEC_CTAS_PER_SM)
             slice_producer(p, &tmap_a, &tmap_w, &tmap_s, &tmap_z, s_begin, s_end, n_st, smem, bars,
                            ctl, pre);
     } else {
-        slice_compute<NT>(p, smem, bars, ctl, warp - 1, lane, s_begin, s_end, n_st);
+        slice_compute<NT, BF>(p, smem, bars, ctl, warp - 1, lane, s_begin, s_end, n_st);
     }
     __syncwarp();
     __syncthreads();
@@ -780,7 +825,7 @@ int decode_smem_limit(int *bytes)
 int launch_decode(const GemmParams &p, const CUtensorMap &tmap_a, const CUtensorMap &tmap_s,
                   const CUtensorMap &tmap_z, const GemmConfig &cfg, cudaStream_t stream)
 {
-    static int attr_done[8][64];
+    static int attr_done[12][64];
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess)
@@ -793,11 +838,17 @@ int launch_decode(const GemmParams &p, const CUtensorMap &tmap_a, const CUtensor
     case 64: v = 3; break;
     default: return cudaErrorInvalidValue;
     }
-    void (*kernels[8])(GemmParams, CUtensorMap, CUtensorMap, CUtensorMap) = {
+    // bf16 operands: whole-block groups only (the host sends smaller groups to the tcgen05
+    // kernel).
+    if (p.bf16 && p.group_size % KBLK != 0)
+        return cudaErrorInvalidValue;
+    void (*kernels[12])(GemmParams, CUtensorMap, CUtensorMap, CUtensorMap) = {
         w4a16_decode_kernel<1, true>,  w4a16_decode_kernel<2, true>,  w4a16_decode_kernel<4, true>,
         w4a16_decode_kernel<8, true>,  w4a16_decode_kernel<1, false>, w4a16_decode_kernel<2, false>,
-        w4a16_decode_kernel<4, false>, w4a16_decode_kernel<8, false>};
-    const int variant = v + (p.group_size % KBLK == 0 ? 0 : 4);
+        w4a16_decode_kernel<4, false>, w4a16_decode_kernel<8, false>,
+        w4a16_decode_kernel<1, true, true>, w4a16_decode_kernel<2, true, true>,
+        w4a16_decode_kernel<4, true, true>, w4a16_decode_kernel<8, true, true>};
+    const int variant = p.bf16 ? 8 + v : v + (p.group_size % KBLK == 0 ? 0 : 4);
     auto kernel = kernels[variant];
     if (dev < 64 && attr_done[variant][dev] < cfg.smem_bytes) {
         err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -823,7 +874,7 @@ int launch_slice(const GemmParams &p, const CUtensorMap &tmap_a, const CUtensorM
                  const CUtensorMap &tmap_s, const CUtensorMap &tmap_z, const GemmConfig &cfg,
                  cudaStream_t stream)
 {
-    static int attr_done[3][64];
+    static int attr_done[6][64];
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess)
@@ -835,8 +886,11 @@ int launch_slice(const GemmParams &p, const CUtensorMap &tmap_a, const CUtensorM
     case 32: v = 2; break;
     default: return cudaErrorInvalidValue;
     }
-    void (*kernels[3])(GemmParams, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap) = {
-        w4a16_slice_kernel<1>, w4a16_slice_kernel<2>, w4a16_slice_kernel<4>};
+    if (p.bf16)
+        v += 3;
+    void (*kernels[6])(GemmParams, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap) = {
+        w4a16_slice_kernel<1>,       w4a16_slice_kernel<2>,       w4a16_slice_kernel<4>,
+        w4a16_slice_kernel<1, true>, w4a16_slice_kernel<2, true>, w4a16_slice_kernel<4, true>};
     auto kernel = kernels[v];
     if (dev < 64 && attr_done[v][dev] < cfg.smem_bytes) {
         err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
