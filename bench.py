@@ -555,9 +555,12 @@ def kernel_of(w4, g) -> int:
     """The library's kernel for one GEMM of the workload (0 tcgen05, 1 split-K small-M,
     2 column-slice small-M); grouped calls always run the tcgen05 kernel."""
     s = g.s
-    if s.get("grouped") or s["wt"] == FE4M3:   # grouped and FP8 calls: always tcgen05
+    if s.get("grouped"):   # grouped calls: always tcgen05
         return 0
-    return w4.w4a16_kernel_for(s["m"], s["n"], s["k"], s["gs"], g.flags)
+    kern = w4.w4a16_kernel_for(s["m"], s["n"], s["k"], s["gs"], g.flags)
+    if s["wt"] == FE4M3 and kern == 1:   # FP8: the split-K small-M kernel is 4-bit only
+        return 0
+    return kern
 
 
 def kernel_roofline(rows, peaks, peak_src, launches):

@@ -173,9 +173,12 @@ int w4_gate_up_interleave(const void *src, void *dst, int rows, int n2, int elem
  * loads.  K % 128 == 0, N % 256 == 0; 16-byte aligned; the buffers must not overlap.
  * W4A16_TYPE_FE4M3 GEMMs (w4a16_gemm, _grouped, _moe_blocks) take these tiles, fp16 scales
  * [G][N] with group_size -1 or a positive multiple of 64 dividing K (the pages' FP8 Marlin
- * takes -1 or 128), no zero points, no act-order, and always run the tcgen05 kernel (the
- * small-M and CUDA-core kernels are 4-bit only: forcing them is rejected).  Each code becomes
- * its exact fp16 value (cvt.rn.f16x2.e4m3x2); the product with the scale is rounded once. */
+ * takes -1 or 128), no zero points, no act-order, fp16 activations.  They run on the
+ * column-slice kernel where the 4-bit rule picks it and M <= 16 (W4A16_FLAG_FORCE_SLICE forces it;
+ * M above 16 is then unsupported-shape)
+ * and otherwise on the tcgen05 kernel; forcing the split-K small-M or the CUDA-core kernel is
+ * rejected (those are 4-bit only).  Each code becomes its exact fp16 value
+ * (cvt.rn.f16x2.e4m3x2); the product with the scale is rounded once. */
 int w8_repack(const int32_t *qweight, int32_t *b_packed, int k, int n, cudaStream_t stream);
 
 /* FP8 tiles -> the [K/4][N] input words (the inverse of w8_repack). */

@@ -10,7 +10,8 @@ import pytest
 
 import oracle
 import synth
-from helpers import FLAG_ACT_ORDER, FLAG_FORCE_MMA, FLAG_HAS_ZP, FLAG_IS_K_FULL, torch_dev, within_tol
+from helpers import (FLAG_ACT_ORDER, FLAG_FORCE_MMA, FLAG_FORCE_SLICE, FLAG_HAS_ZP, FLAG_IS_K_FULL,
+                     torch_dev, within_tol)
 
 pytestmark = pytest.mark.gpu
 FE4M3 = 8
@@ -81,16 +82,42 @@ def test_fp8_gemm_matches_oracle(w4, orc, m, k, n, gs):
     assert ok, msg
 
 
-def test_fp8_one_hot_is_bit_exact(w4):
+@pytest.mark.parametrize("m,flags", [(40, FLAG_IS_K_FULL), (5, FLAG_IS_K_FULL | FLAG_FORCE_SLICE)])
+def test_fp8_one_hot_is_bit_exact(w4, m, flags):
     """One 1.0 (0x38) per column at row pi(n), zeros elsewhere, unit scales: C[:, n] = A[:, pi(n)]
-    exactly (one nonzero product, exact in fp32 and fp16)."""
-    m, k, n = 40, 512, 256
-    a = synth.activations(8100, m, k)
+    exactly (one nonzero product, exact in fp32 and fp16); tcgen05 and column-slice kernels."""
+    k, n = 512, 256
+    a = synth.activations(8100 + m, m, k)
     pi = (np.arange(n) * 37 + 11) % k
     codes = np.zeros((k, n), dtype=np.uint8)
     codes[pi, np.arange(n)] = 0x38
-    got = run_fp8(w4, a, pack(codes), np.ones((k // 128, n), dtype=np.float16), k, n, 128)
+    got = run_fp8(w4, a, pack(codes), np.ones((k // 128, n), dtype=np.float16), k, n, 128, flags)
     assert np.array_equal(got.astype(np.float16).view(np.uint16), a[:, pi].view(np.uint16))
+
+
+@pytest.mark.parametrize("m,k,n,gs", [(1, 1024, 512, 128), (3, 4224, 768, 64), (8, 2048, 4096, -1),
+                                      (16, 1024, 512, 256), (16, 4096, 4096, 128), (12, 4224, 768, 192)])
+def test_fp8_column_slice_kernel_matches_oracle(w4, orc, m, k, n, gs):
+    """FP8 tiles read through the column-slice view (four 256-byte rows per block)."""
+    seed = 8600 + m + k
+    a = synth.activations(seed, m, k)
+    qw = synth.fp8_weights(seed, k, n)
+    s = synth.scales(seed, synth.group_count(k, gs), n, lo=1e-4, hi=2e-4)
+    got = run_fp8(w4, a, qw, s, k, n, gs, FLAG_IS_K_FULL | FLAG_FORCE_SLICE)
+    ok, msg = within_tol(got, orc.gemm_fp8(a, qw, s, gs))
+    assert ok, msg
+
+
+def test_fp8_decode_shape_defaults_to_column_slice(w4):
+    """M=4 at N=4096 (256 slices): the default choice is the column-slice kernel, the same bits
+    as forcing it."""
+    m, k, n = 4, 2048, 4096
+    a = synth.activations(8700, m, k)
+    qw = synth.fp8_weights(8700, k, n)
+    s = synth.scales(8700, k // 128, n, lo=1e-4, hi=2e-4)
+    d = run_fp8(w4, a, qw, s, k, n, 128)
+    f = run_fp8(w4, a, qw, s, k, n, 128, FLAG_IS_K_FULL | FLAG_FORCE_SLICE)
+    assert np.array_equal(d.astype(np.float16).view(np.uint16), f.astype(np.float16).view(np.uint16))
 
 
 def test_fp8_nan_code_propagates(w4):
@@ -153,6 +180,12 @@ def test_fp8_unsupported_combinations_rejected(w4):
         dict(flags=FLAG_FORCE_MMA, detail=4),                       # tcgen05 kernel only
         dict(gs=32, detail=7),                                      # groups of whole 64-row blocks
     ]
+    big = torch.zeros((32, k), dtype=torch.float16, device="cuda")
+    cbig = torch.zeros((32, n), dtype=torch.float16, device="cuda")
+    with pytest.raises(w4.W4A16Error) as e:                          # FP8 slices: M <= 16
+        w4.w4a16_gemm(big, b, cbig, s, None, None, None, ws, 32, n, k, 128, FE4M3,
+                      FLAG_IS_K_FULL | FLAG_FORCE_SLICE)
+    assert e.value.stage == 2 and e.value.detail == 3
     for cs in cases:
         with pytest.raises(w4.W4A16Error) as e:
             w4.w4a16_gemm(a, b, c, s, cs.get("zeros"), cs.get("g_idx"), cs.get("perm"), ws, m, n, k,

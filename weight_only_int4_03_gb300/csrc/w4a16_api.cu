@@ -283,13 +283,14 @@ int plan_smem(Plan &pl, bool grouped, bool has_zp, int group_size, int g_rows)
         // activation box is exactly M rows (the token rows an 8-token MMA tile has beyond M read
         // a zero row instead).  After the stages: two buffers for the cross-warp sum of a slice
         // (8 warps x nt_max/8 x 4 x 32 fp32 each), then the 128-byte zero row.
-        const int kbs = SLICE_WARPS * slice_bpw(pl.nt_max);
+        const int kbs = SLICE_WARPS * slice_bpw(pl.nt_max, pl.tile_bytes == TILE_BYTES_FP8);
         pl.kbs = kbs;
         pl.act_kb_bytes = pl.act_rows * 128;
         const int sg = (kbs * KBLK + group_size - 1) / group_size + 1;
         pl.sg_box = sg < g_rows ? sg : g_rows;
         pl.packed_off = (int)round_up((long long)kbs * pl.act_kb_bytes, 1024);
-        pl.scales_off = pl.packed_off + kbs * SLICE_BLOCK_BYTES;
+        const int block_bytes = pl.tile_bytes == TILE_BYTES_FP8 ? 2 * SLICE_BLOCK_BYTES : SLICE_BLOCK_BYTES;
+        pl.scales_off = pl.packed_off + kbs * block_bytes;
         pl.zeros_off = pl.scales_off + (int)round_up((long long)pl.sg_box * SLICE_N * 2, 128);
         const int end = has_zp ? pl.zeros_off + pl.sg_box * SLICE_N * 2 : pl.zeros_off;
         pl.stage_bytes = (int)round_up(end, 1024);
@@ -427,15 +428,18 @@ int encode_group_map(CUtensorMap *map, const void *base, int g_rows, int n, int 
 // Packed tiles viewed as [tiles x K/64 x 2][512] int32 rows (a row is one 32-row half of a
 // 64-row block of a 128-column tile: 128 columns x 4 words): a box of 64 words x 2*kbs rows
 // brings the codes of one 16-column slice for kbs consecutive blocks, 256 bytes per row.
-int encode_slice_weight_map(CUtensorMap *map, const void *base, int n, int k, int kbs)
+int encode_slice_weight_map(CUtensorMap *map, const void *base, int n, int k, int kbs, bool w8)
 {
     auto fn = encode_fn();
     if (!fn)
         return cudaErrorNotSupported;
+    // Rows of 512 words: the two 32-row halves of a 4-bit tile, or the four 16-row quarters of
+    // an FP8 tile; a slice's block is 64 words of 2 (or 4) consecutive rows.
+    const int rows_per_block = w8 ? 4 : 2;
     cuuint64_t dims[2] = {(cuuint64_t)(TILE_WORDS / 2),
-                          (cuuint64_t)(n / TILE_N) * (cuuint64_t)(k / KBLK) * 2};
+                          (cuuint64_t)(n / TILE_N) * (cuuint64_t)(k / KBLK) * rows_per_block};
     cuuint64_t strides[1] = {(cuuint64_t)TILE_BYTES / 2};
-    cuuint32_t box[2] = {(cuuint32_t)(SLICE_N * 4), (cuuint32_t)(2 * kbs)};
+    cuuint32_t box[2] = {(cuuint32_t)(SLICE_N * 4), (cuuint32_t)(rows_per_block * kbs)};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_INT32, 2, const_cast<void *>(base), dims, strides,
                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -480,7 +484,7 @@ int check_fp8_flags(int weight_type, unsigned flags)
     if (weight_type != W4A16_TYPE_FE4M3)
         return 0;
     if (flags & (W4A16_FLAG_ACT_ORDER | W4A16_FLAG_FORCE_SIMT | W4A16_FLAG_FORCE_MMA |
-                 W4A16_FLAG_FORCE_SLICE | W4A16_FLAG_BF16))
+                 W4A16_FLAG_BF16))
         return status_of(STAGE_ARG, W4A16_ARG_FLAGS);
     return 0;
 }
@@ -837,7 +841,16 @@ int dense_gemm(const void *a, int lda, const int32_t *b_packed, void *c, int ldc
     int err = sm_count(&num_sms);
     if (err != cudaSuccess)
         return status_of(STAGE_RESOURCE, err);
-    const int kernel = weight_type == W4A16_TYPE_FE4M3 ? 0 : choose_kernel(m, n, gs_resolved, flags, num_sms);
+    // FP8 weights: the column-slice kernel where the 4-bit rule picks it, else the tcgen05
+    // kernel (the split-K small-M kernel is 4-bit only).
+    int kernel = choose_kernel(m, n, gs_resolved, flags, num_sms);
+    if (weight_type == W4A16_TYPE_FE4M3) {
+        // FP8 column slices: two stages of their doubled code bytes fit up to 16 tokens.
+        if (m > 16 && (flags & W4A16_FLAG_FORCE_SLICE))
+            return status_of(STAGE_UNSUPPORTED, W4A16_ARG_SHAPE);
+        if (kernel == 1 || (kernel == 2 && m > 16))
+            kernel = 0;
+    }
     Plan pl;
     dense_plan(pl, m, n, k, flags, num_sms, kernel, tile_cap);
     if (workspace_bytes < (size_t)pl.total)
@@ -892,7 +905,7 @@ int dense_gemm(const void *a, int lda, const int32_t *b_packed, void *c, int ldc
     GemmConfig cfg{pl.grid, pl.smem_bytes, pl.a_tmem};
     if (pl.slice) {
         CUtensorMap mw;
-        err = encode_slice_weight_map(&mw, b_packed, n, k, pl.kbs);
+        err = encode_slice_weight_map(&mw, b_packed, n, k, pl.kbs, p.w8 != 0);
         if (err != cudaSuccess)
             return status_of(STAGE_RESOURCE, err);
         return launch_status(launch_slice(p, ma, mw, ms, mz, cfg, stream));

@@ -37,6 +37,8 @@
 // reduction) overlaps the other's streaming.  Work is split over CTAs with the same
 // data-parallel + stream-K schedule as the tcgen05 kernel; split tiles are reduced in a fixed
 // order by the last contributor.
+#include <cuda_fp8.h>
+
 #include "w4a16_common.cuh"
 
 namespace w4 {
@@ -66,6 +68,13 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr)
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base = (uint32_t)__cvta_generic_to_shared(smem_raw);
     return *reinterpret_cast<const uint32_t *>(smem_raw + (addr - base));
+}
+
+__device__ __forceinline__ uint16_t lds16(uint32_t addr)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t base = (uint32_t)__cvta_generic_to_shared(smem_raw);
+    return *reinterpret_cast<const uint16_t *>(smem_raw + (addr - base));
 }
 
 // D (f32 16x8) += A (16x16, row) * B (16x8, col), fp16 or (BF) bf16 operands.  Registers
@@ -503,13 +512,15 @@ static __device__ __forceinline__ void slice_issue_weights(const GemmParams &p,
 {
     const bool has_zp = p.zeros != nullptr;
     const uint32_t sg_bytes = (uint32_t)p.sg_box * SLICE_N * 2;
+    // A block of a slice is 2 rows of the weight view (4-bit) or 4 (FP8), 256 bytes each.
+    const int rows_per_block = p.w8 ? 4 : 2;
     mbar_arrive_expect_tx(full, (uint32_t)p.kbs * (uint32_t)p.act_kb_bytes +
-                                    (uint32_t)p.kbs * SLICE_BLOCK_BYTES +
+                                    (uint32_t)(p.kbs * rows_per_block) * 256u +
                                     sg_bytes * (has_zp ? 2u : 1u));
     constexpr int SLICES_PER_TILE = TILE_N / SLICE_N;
     const int tile = slice / SLICES_PER_TILE;
-    const int x = (slice % SLICES_PER_TILE) * SLICE_N * 4; // word offset inside a half row
-    const int row = (tile * p.kblocks + kb0) * 2;
+    const int x = (slice % SLICES_PER_TILE) * SLICE_N * 4; // word offset inside a view row
+    const int row = (tile * p.kblocks + kb0) * rows_per_block;
     tensor_load_2d_hint(st + p.packed_off, tmap_w, x, row, full, policy_evict_first());
     const int g0 = (kb0 * KBLK) / p.group_size;
     tensor_load_2d(st + p.scales_off, tmap_s, slice * SLICE_N, g0, full);
@@ -589,22 +600,60 @@ __device__ __forceinline__ void slice_block_mma(uint32_t w_addr, const uint32_t 
     }
 }
 
+// FP8 E4M3 codes: one 64-row block of the lane's two slice columns.  In shared memory the block
+// is four 256-byte rows, one per 16-row quarter q (= k step), each holding the slice's 16
+// columns x 4 words of four K-consecutive codes.  For k step q the lane's A fragment needs rows
+// 2t, 2t+1 and 2t+8, 2t+9 of columns c and c+8: the 16-bit halves at `w_addr` + q*256 (+ 8 for
+// the rows 8 on, + 128 for column c + 8), each converting exactly to an fp16 pair; the product
+// with the column's scale is rounded once.
+template <int NT>
+__device__ __forceinline__ void slice_block_mma_fp8(uint32_t w_addr, const uint32_t (&act0)[NT],
+                                                    const uint32_t (&act1)[NT], uint32_t s0,
+                                                    uint32_t s1, float (&acc0)[NT][4],
+                                                    float (&acc1)[NT][4])
+{
+    uint32_t a[4][4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const uint32_t base = w_addr + q * 256;
+        const uint16_t h[4] = {lds16(base), lds16(base + 128), lds16(base + 8), lds16(base + 136)};
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const __half2_raw v = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)h[r], __NV_E4M3);
+            a[q][r] = h2_as_u32(__hmul2(__half2(v), u32_as_h2((r & 1) ? s1 : s0)));
+        }
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        uint32_t b[4], e[4];
+        ldmatrix_x4(act0[nt], b);
+        ldmatrix_x4(act1[nt], e);
+        mma_16816<false>(acc0[nt], a[0][0], a[0][1], a[0][2], a[0][3], b[0], b[1]);
+        mma_16816<false>(acc0[nt], a[1][0], a[1][1], a[1][2], a[1][3], b[2], b[3]);
+        mma_16816<false>(acc1[nt], a[2][0], a[2][1], a[2][2], a[2][3], e[0], e[1]);
+        mma_16816<false>(acc1[nt], a[3][0], a[3][1], a[3][2], a[3][3], e[2], e[3]);
+    }
+}
+
 // Compute warp w of the column-slice kernel: blocks w*BPW .. w*BPW + BPW - 1 of every stage.
 // A stage's activations are kbs blocks x M rows of 128 bytes in the 128-byte swizzle (16-byte
 // chunk c of row j at j*128 + ((c ^ (j & 7)) << 4) from the 1024-aligned stage start); the
 // lanes of a token row at or past M point ldmatrix at the zero row instead.
-template <int NT, bool BF>
+template <int NT, bool BF, bool W8>
 __device__ void slice_compute(const GemmParams &p, uint8_t *smem, DecBars &bars,
                               const WaitCtl &ctl, int w, int lane, int s_begin, int s_end,
                               int n_st)
 {
-    constexpr int BPW = slice_bpw(8 * NT);
+    constexpr int BPW = slice_bpw(8 * NT, W8);
     constexpr int KBS = SLICE_WARPS * BPW;
     const bool has_zp = p.zeros != nullptr;
     const int t = lane & 3;
     const int c = lane >> 2; // this lane's slice columns: c and c + 8
-    // Word of column c, half 0, of block bl: row 2*bl of 16 columns x 4 words.
-    const uint32_t w_lane = (uint32_t)((c * 4 + t) * 4);
+    // 4-bit: word t of column c, half 0, of block bl (row 2*bl of 16 columns x 4 words).
+    // FP8: the 16-bit half (t & 1) of word t >> 1 of column c, quarter 0 (row 4*bl).
+    const uint32_t w_lane = W8 ? (uint32_t)(c * 16 + (t >> 1) * 4 + (t & 1) * 2)
+                               : (uint32_t)((c * 4 + t) * 4);
+    constexpr uint32_t BLOCK_STRIDE = W8 ? 1024u : 2u * SLICE_N * 4 * 4;
     constexpr int VALS = NT * 4 * 32; // one warp's accumulators
     float *red = reinterpret_cast<float *>(smem + p.epi_smem_off);
     const uint32_t zero_row = smem_u32(smem + p.epi_smem_off + 2 * SLICE_WARPS * VALS * 4);
@@ -665,8 +714,12 @@ __device__ void slice_compute(const GemmParams &p, uint8_t *smem, DecBars &bars,
                     act0[nt] = ok ? act_base + act_off0[j][nt] : zero_row;
                     act1[nt] = ok ? act_base + act_off1[j][nt] : zero_row;
                 }
-                slice_block_mma<NT, BF>(w_base + (uint32_t)(bl * 2 * SLICE_N * 4 * 4), act0, act1, c0,
-                                    c1, acc0, acc1);
+                if (W8)
+                    slice_block_mma_fp8<NT>(w_base + (uint32_t)bl * BLOCK_STRIDE, act0, act1, c0.s,
+                                            c1.s, acc0, acc1);
+                else
+                    slice_block_mma<NT, BF>(w_base + (uint32_t)bl * BLOCK_STRIDE, act0, act1, c0,
+                                            c1, acc0, acc1);
             };
             if (kb0 + KBS <= p.kblocks) {
                 // A full stage: no per-block bound in the unrolled loop.
@@ -721,7 +774,7 @@ __device__ void slice_compute(const GemmParams &p, uint8_t *smem, DecBars &bars,
     }
 }
 
-template <int NT, bool BF = false>
+template <int NT, bool BF = false, bool W8 = false>
 __global__ void __launch_bounds__(DEC_THREADS, DEC_CTAS_PER_SM)
     w4a16_slice_kernel(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap tmap_a,
                        const __grid_constant__ CUtensorMap tmap_w,
@@ -776,7 +829,7 @@ __global__ void __launch_bounds__(DEC_THREADS, DEC_CTAS_PER_SM)
             slice_producer(p, &tmap_a, &tmap_w, &tmap_s, &tmap_z, s_begin, s_end, n_st, smem, bars,
                            ctl, pre);
     } else {
-        slice_compute<NT, BF>(p, smem, bars, ctl, warp - 1, lane, s_begin, s_end, n_st);
+        slice_compute<NT, BF, W8>(p, smem, bars, ctl, warp - 1, lane, s_begin, s_end, n_st);
     }
     __syncwarp();
     __syncthreads();
@@ -874,7 +927,7 @@ int launch_slice(const GemmParams &p, const CUtensorMap &tmap_a, const CUtensorM
                  const CUtensorMap &tmap_s, const CUtensorMap &tmap_z, const GemmConfig &cfg,
                  cudaStream_t stream)
 {
-    static int attr_done[6][64];
+    static int attr_done[9][64];
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess)
@@ -888,9 +941,13 @@ int launch_slice(const GemmParams &p, const CUtensorMap &tmap_a, const CUtensorM
     }
     if (p.bf16)
         v += 3;
-    void (*kernels[6])(GemmParams, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap) = {
+    else if (p.w8)
+        v += 6;
+    void (*kernels[9])(GemmParams, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap) = {
         w4a16_slice_kernel<1>,       w4a16_slice_kernel<2>,       w4a16_slice_kernel<4>,
-        w4a16_slice_kernel<1, true>, w4a16_slice_kernel<2, true>, w4a16_slice_kernel<4, true>};
+        w4a16_slice_kernel<1, true>, w4a16_slice_kernel<2, true>, w4a16_slice_kernel<4, true>,
+        w4a16_slice_kernel<1, false, true>, w4a16_slice_kernel<2, false, true>,
+        w4a16_slice_kernel<4, false, true>};
     auto kernel = kernels[v];
     if (dev < 64 && attr_done[v][dev] < cfg.smem_bytes) {
         err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -47,7 +47,11 @@ constexpr int MAX_SEGMENTS = 1024;
 // Column-slice small-M kernel: 16 weight columns over all of K per work item; a pipeline
 // stage holds slice_bpw consecutive blocks for each of the 8 compute warps.
 constexpr int SLICE_N = 16;
-__host__ __device__ constexpr int slice_bpw(int nt_max) { return nt_max <= 8 ? 4 : nt_max <= 16 ? 2 : 1; }
+__host__ __device__ constexpr int slice_bpw(int nt_max, bool w8 = false)
+{
+    // FP8 blocks carry twice the code bytes: half as many per warp (at least one).
+    return (nt_max <= 8 ? 4 : nt_max <= 16 ? 2 : 1) / (w8 && nt_max <= 16 ? 2 : 1);
+}
 constexpr int SLICE_BLOCK_BYTES = SLICE_N * KBLK / 2; // codes of one block of a slice
 constexpr int SLICE_MAX_ROWS = 32;
 constexpr int SLICE_WARPS = 8; // compute warps of the small-M kernels
