@@ -557,10 +557,11 @@ def kernel_of(w4, g) -> int:
     s = g.s
     if s.get("grouped"):   # grouped calls: always tcgen05
         return 0
-    kern = w4.w4a16_kernel_for(s["m"], s["n"], s["k"], s["gs"], g.flags)
-    if s["wt"] == FE4M3 and kern == 1:   # FP8: the split-K small-M kernel is 4-bit only
-        return 0
-    return kern
+    if s["wt"] == FE4M3:   # FP8: the column-slice kernel up to 16 tokens, else tcgen05
+        import torch
+        sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+        return 2 if s["m"] <= 16 and s["n"] // 16 >= sms else 0
+    return w4.w4a16_kernel_for(s["m"], s["n"], s["k"], s["gs"], g.flags)
 
 
 def kernel_roofline(rows, peaks, peak_src, launches):

@@ -174,7 +174,7 @@ int w4_gate_up_interleave(const void *src, void *dst, int rows, int n2, int elem
  * W4A16_TYPE_FE4M3 GEMMs (w4a16_gemm, _grouped, _moe_blocks) take these tiles, fp16 scales
  * [G][N] with group_size -1 or a positive multiple of 64 dividing K (the pages' FP8 Marlin
  * takes -1 or 128), no zero points, no act-order, fp16 activations.  They run on the
- * column-slice kernel where the 4-bit rule picks it and M <= 16 (W4A16_FLAG_FORCE_SLICE forces it;
+ * column-slice kernel for M <= 16 with N / 16 >= the SM count (W4A16_FLAG_FORCE_SLICE forces it;
  * M above 16 is then unsupported-shape)
  * and otherwise on the tcgen05 kernel; forcing the split-K small-M or the CUDA-core kernel is
  * rejected (those are 4-bit only).  Each code becomes its exact fp16 value

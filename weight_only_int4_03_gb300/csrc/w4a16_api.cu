@@ -845,11 +845,16 @@ int dense_gemm(const void *a, int lda, const int32_t *b_packed, void *c, int ldc
     // kernel (the split-K small-M kernel is 4-bit only).
     int kernel = choose_kernel(m, n, gs_resolved, flags, num_sms);
     if (weight_type == W4A16_TYPE_FE4M3) {
-        // FP8 column slices: two stages of their doubled code bytes fit up to 16 tokens.
+        // FP8 column slices: two stages of their doubled code bytes fit up to 16 tokens.  By
+        // default they take M <= 16 with at least one slice per SM (measured at N = 4096 …
+        // 12288: 4.8-14.6 us against 11.1-22.0 us on the tcgen05 kernel), else the tcgen05
+        // kernel (the split-K small-M kernel is 4-bit only).
         if (m > 16 && (flags & W4A16_FLAG_FORCE_SLICE))
             return status_of(STAGE_UNSUPPORTED, W4A16_ARG_SHAPE);
-        if (kernel == 1 || (kernel == 2 && m > 16))
-            kernel = 0;
+        const unsigned tc_flags = W4A16_FLAG_FORCE_TC | W4A16_FLAG_A_SMEM | W4A16_FLAG_SWIGLU |
+                                  W4A16_FLAG_GEGLU;
+        if (!(flags & W4A16_FLAG_FORCE_SLICE))
+            kernel = (!(flags & tc_flags) && m <= 16 && n / SLICE_N >= num_sms && slice_default()) ? 2 : 0;
     }
     Plan pl;
     dense_plan(pl, m, n, k, flags, num_sms, kernel, tile_cap);
