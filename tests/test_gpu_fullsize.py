@@ -79,7 +79,34 @@ def run_dense(w4, spec):
 
 
 DENSE = [(wl, f"{s['m']},{s['k']},{s['n']}")
-         for wl in ("decode", "prefill", "actorder", "fp8") for s in bench.workload_specs(wl)]
+         for wl in ("decode", "prefill", "actorder", "fp8", "bf16") for s in bench.workload_specs(wl)]
+
+
+def dense_reference(orc, spec, rows):
+    """The oracle's rows `rows` (None: all) of one dense GEMM of bench.py's workloads, with the
+    elementwise bar (atol = rtol) that applies: 1e-2, or 8e-2 for bf16 operands (R25)."""
+    if spec["wt"] == bench.FE4M3:
+        a = synth.activations(spec["seed"], spec["m"], spec["k"], sigma=spec["sigma"])
+        if rows is not None:
+            a = a[rows]
+        qw = synth.fp8_weights(spec["seed"], spec["k"], spec["n"])
+        s = synth.scales(spec["seed"], synth.group_count(spec["k"], spec["gs"]), spec["n"], 1e-4, 2e-4)
+        return orc.gemm_fp8(np.ascontiguousarray(a), qw, s, spec["gs"]), 1e-2
+    a, qw, scales, zeros, g_idx = dense_inputs(spec, rows)
+    if spec.get("bf16"):
+        # bench.py's bf16 operands: the same draws rounded to bfloat16
+        bits = lambda x: synth.bf16_bits(np.asarray(x, dtype=np.float64))
+        return orc.gemm_bf16(bits(a), qw, bits(scales), None if zeros is None else bits(zeros),
+                             g_idx, spec["gs"], spec["wt"]), 8e-2
+    return orc.gemm(a, qw, scales, zeros, g_idx, spec["gs"], spec["wt"]), 1e-2
+
+
+def dense_output(g, spec, rows):
+    c = g.c if rows is None else g.c[rows]
+    if spec.get("bf16"):
+        u = c.cpu().numpy().view(np.uint16).astype(np.uint32) << np.uint32(16)
+        return u.view(np.float32).astype(np.float64)
+    return c.float().cpu().numpy().astype(np.float64)
 
 
 @pytest.mark.parametrize("workload,shape", DENSE)
@@ -87,19 +114,9 @@ def test_full_size_dense(w4, orc, workload, shape):
     spec = dict(bench.select_shape(bench.workload_specs(workload), shape)[0])
     g = run_dense(w4, spec)
     rows = sample_rows(spec["m"])
-    if spec["wt"] == bench.FE4M3:
-        a = synth.activations(spec["seed"], spec["m"], spec["k"], sigma=spec["sigma"])[rows]
-        qw = synth.fp8_weights(spec["seed"], spec["k"], spec["n"])
-        s = synth.scales(spec["seed"], synth.group_count(spec["k"], spec["gs"]), spec["n"], 1e-4, 2e-4)
-        ref = orc.gemm_fp8(np.ascontiguousarray(a), qw, s, spec["gs"])
-        got = g.c[rows].float().cpu().numpy().astype(np.float64)
-        ok, msg = within_tol(got, ref)
-        assert ok, f"{workload} {shape} ({len(rows)} rows): {msg}"
-        return
-    a, qw, scales, zeros, g_idx = dense_inputs(spec, rows)
-    ref = orc.gemm(a, qw, scales, zeros, g_idx, spec["gs"], spec["wt"])
-    got = g.c[rows].float().cpu().numpy().astype(np.float64)
-    ok, msg = within_tol(got, ref)
+    ref, tol = dense_reference(orc, spec, rows)
+    got = dense_output(g, spec, rows)
+    ok, msg = within_tol(got, ref, tol, tol)
     assert ok, f"{workload} {shape} ({len(rows)} rows): {msg}"
 
 
@@ -182,7 +199,7 @@ FULL = os.environ.get("W4A16_FULL_ORACLE") == "1"
 
 
 @pytest.mark.skipif(not FULL, reason="set W4A16_FULL_ORACLE=1 to compare every element")
-@pytest.mark.parametrize("workload", ["tiny", "decode", "prefill", "actorder", "moe"])
+@pytest.mark.parametrize("workload", ["tiny", "decode", "prefill", "actorder", "moe", "fp8", "bf16"])
 def test_full_oracle_every_element(w4, orc, workload):
     import torch
     for spec in bench.workload_specs(workload):
@@ -198,10 +215,10 @@ def test_full_oracle_every_element(w4, orc, workload):
             what = f"moe k={spec['k']} n={spec['n']}"
         else:
             g = run_dense(w4, spec)
-            ref = orc.gemm(*dense_inputs(spec), spec["gs"], spec["wt"])
-            got = g.c.float().cpu().numpy().astype(np.float64)
+            ref, tol = dense_reference(orc, spec, None)
+            got = dense_output(g, spec, None)
             what = f"{workload} m={spec['m']} k={spec['k']} n={spec['n']}"
-        ok, msg = within_tol(got, ref)
+        ok, msg = within_tol(got, ref, tol, tol) if not spec.get("grouped") else within_tol(got, ref)
         print(f"full oracle {what}: {got.size} elements, {msg}")
         assert ok, f"{what}: {msg}"
         del g
