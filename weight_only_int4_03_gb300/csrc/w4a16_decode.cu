@@ -38,6 +38,7 @@
 // data-parallel + stream-K schedule as the tcgen05 kernel; split tiles are reduced in a fixed
 // order by the last contributor.
 #include <cuda_fp8.h>
+#include <type_traits>
 
 #include "w4a16_common.cuh"
 
@@ -95,6 +96,16 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
             : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// D (f32 16x8) = A * B with no accumulator input (fp16 operands).
+__device__ __forceinline__ void mma_16816_z(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                            uint32_t a3, uint32_t b0, uint32_t b1)
+{
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%10, %10, %10, %10};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
+}
+
 __device__ __forceinline__ __nv_bfloat162 u32_as_bf2(uint32_t v)
 {
     return *reinterpret_cast<__nv_bfloat162 *>(&v);
@@ -150,6 +161,34 @@ struct ColGroup {
     uint32_t s, zlo, zhi;
     float sf;
 };
+
+// The same from shared addresses of the scale and zero elements (explicit shared loads).
+template <bool BF>
+__device__ __forceinline__ ColGroup col_group_sh(bool has_zp, uint32_t s_addr, uint32_t z_addr)
+{
+    ColGroup cgp;
+    const uint16_t sb = lds16(s_addr);
+    cgp.s = (uint32_t)sb * 0x10001u;
+    if (BF) {
+        cgp.sf = __bfloat162float(__ushort_as_bfloat16(sb));
+        __nv_bfloat16 zn = __ushort_as_bfloat16((uint16_t)0xC308); // -136 = -(128 + 8)
+        if (has_zp)
+            zn = __hneg(__hadd(__ushort_as_bfloat16((uint16_t)0x4300), __ushort_as_bfloat16(lds16(z_addr))));
+        cgp.zlo = (uint32_t)__bfloat16_as_ushort(zn) * 0x10001u;
+        cgp.zhi = 0;
+        return cgp;
+    }
+    cgp.sf = __half2float(__ushort_as_half(sb));
+    if (has_zp) {
+        const __half z = __ushort_as_half(lds16(z_addr));
+        cgp.zlo = (uint32_t)__half_as_ushort(__hadd(__ushort_as_half(0x6400), z)) * 0x10001u;          // 1024 + z
+        cgp.zhi = (uint32_t)__half_as_ushort(__hneg(__hadd(__ushort_as_half(0x5400), z))) * 0x10001u; // -(64 + z)
+    } else {
+        cgp.zlo = 0x64086408u; // 1032
+        cgp.zhi = 0xD480D480u; // -72
+    }
+    return cgp;
+}
 
 template <bool BF>
 __device__ __forceinline__ ColGroup col_group(bool has_zp, const __half *ssm, const __half *zsm,
@@ -600,6 +639,41 @@ __device__ __forceinline__ void slice_block_mma(uint32_t w_addr, const uint32_t 
     }
 }
 
+// The same block, fp16, with the scale applied in fp32 per block: the MMAs take the exact
+// (q - z) (9 instructions per 8 codes instead of 13), start from zero, and the block's sums are
+// multiplied by the column's s into the output accumulators -- (q - z) s is never rounded to
+// fp16 (for a one-hot row of A the result is the exact product, rounded once on output).
+template <int NT>
+__device__ __forceinline__ void slice_block_mma_bs(uint32_t w_addr, const uint32_t (&act0)[NT],
+                                                   const uint32_t (&act1)[NT], const ColGroup &c0,
+                                                   const ColGroup &c1, float (&acc0)[NT][4],
+                                                   float (&acc1)[NT][4])
+{
+    constexpr uint32_t HALF = SLICE_N * 4 * 4;
+    uint32_t a0[4], a1[4], a2[4], a3[4];
+    dequant_word_int<false>(lds32(w_addr), c0.zlo, c0.zhi, a0);
+    dequant_word_int<false>(lds32(w_addr + 128), c1.zlo, c1.zhi, a1);
+    dequant_word_int<false>(lds32(w_addr + HALF), c0.zlo, c0.zhi, a2);
+    dequant_word_int<false>(lds32(w_addr + HALF + 128), c1.zlo, c1.zhi, a3);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        uint32_t b[4], e[4];
+        ldmatrix_x4(act0[nt], b);
+        ldmatrix_x4(act1[nt], e);
+        float d0[4], d1[4];
+        mma_16816_z(d0, a0[0], a1[0], a0[1], a1[1], b[0], b[1]);
+        mma_16816_z(d1, a2[0], a3[0], a2[1], a3[1], e[0], e[1]);
+        mma_16816<false>(d0, a0[2], a1[2], a0[3], a1[3], b[2], b[3]);
+        mma_16816<false>(d1, a2[2], a3[2], a2[3], a3[3], e[2], e[3]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float sc = i < 2 ? c0.sf : c1.sf;
+            acc0[nt][i] = fmaf(d0[i], sc, acc0[nt][i]);
+            acc1[nt][i] = fmaf(d1[i], sc, acc1[nt][i]);
+        }
+    }
+}
+
 // FP8 E4M3 codes: one 64-row block of the lane's two slice columns.  In shared memory the block
 // is four 256-byte rows, one per 16-row quarter q (= k step), each holding the slice's 16
 // columns x 4 words of four K-consecutive codes.  For k step q the lane's A fragment needs rows
@@ -640,7 +714,7 @@ __device__ __forceinline__ void slice_block_mma_fp8(uint32_t w_addr, const uint3
 // chunk c of row j at j*128 + ((c ^ (j & 7)) << 4) from the 1024-aligned stage start); the
 // lanes of a token row at or past M point ldmatrix at the zero row instead.
 template <int NT, bool BF, bool W8>
-__device__ void slice_compute(const GemmParams &p, uint8_t *smem, DecBars &bars,
+__device__ __forceinline__ void slice_compute(const GemmParams &p, uint8_t *smem, DecBars &bars,
                               const WaitCtl &ctl, int w, int lane, int s_begin, int s_end,
                               int n_st)
 {
@@ -697,16 +771,33 @@ __device__ void slice_compute(const GemmParams &p, uint8_t *smem, DecBars &bars,
             const uint8_t *stp = smem + (size_t)ring.idx * p.stage_bytes;
             const uint32_t act_base = smem_u32(stp);
             const uint32_t w_base = smem_u32(stp + p.packed_off) + w_lane;
-            const __half *ssm = reinterpret_cast<const __half *>(stp + p.scales_off);
-            const __half *zsm = reinterpret_cast<const __half *>(stp + p.zeros_off);
+            const uint32_t s_sh = act_base + (uint32_t)p.scales_off;
+            const uint32_t z_sh = act_base + (uint32_t)p.zeros_off;
             const int kb0 = st * KBS;
-            const int g_stage = gsh >= 0 ? kb0 >> gsh : kb0 / gs_kb;
-            auto block = [&](int j) {
+            // Group of each of the warp's blocks relative to the stage's first group (the
+            // stage's scale rows start there), stepped along the blocks: no division per block.
+            int gj[BPW];
+            {
+                const int kbw = kb0 + w * BPW;
+                const int gw = gsh >= 0 ? kbw >> gsh : kbw / gs_kb;
+                const int g_stage = gsh >= 0 ? kb0 >> gsh : kb0 / gs_kb;
+                int g = gw - g_stage, r = kbw - gw * gs_kb;
+#pragma unroll
+                for (int j = 0; j < BPW; ++j) {
+                    gj[j] = g;
+                    if (++r == gs_kb) {
+                        r = 0;
+                        ++g;
+                    }
+                }
+            }
+            // ZP: the zero-point branch resolved at compile time, outside the unrolled blocks.
+            auto block = [&](int j, auto zp_c) {
+                constexpr bool ZP = decltype(zp_c)::value;
                 const int bl = w * BPW + j;
-                const int kb = kb0 + bl;
-                const int g = (gsh >= 0 ? kb >> gsh : kb / gs_kb) - g_stage;
-                const ColGroup c0 = col_group<BF>(has_zp, ssm, zsm, g * SLICE_N + c);
-                const ColGroup c1 = col_group<BF>(has_zp, ssm, zsm, g * SLICE_N + c + 8);
+                const uint32_t so = (uint32_t)(gj[j] * SLICE_N + c) * 2u;
+                const ColGroup c0 = col_group_sh<BF>(ZP, s_sh + so, z_sh + so);
+                const ColGroup c1 = col_group_sh<BF>(ZP, s_sh + so + 16, z_sh + so + 16);
                 uint32_t act0[NT], act1[NT];
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
@@ -717,23 +808,32 @@ __device__ void slice_compute(const GemmParams &p, uint8_t *smem, DecBars &bars,
                 if (W8)
                     slice_block_mma_fp8<NT>(w_base + (uint32_t)bl * BLOCK_STRIDE, act0, act1, c0.s,
                                             c1.s, acc0, acc1);
+                else if (!BF && NT <= 2)
+                    slice_block_mma_bs<NT>(w_base + (uint32_t)bl * BLOCK_STRIDE, act0, act1, c0,
+                                           c1, acc0, acc1);
                 else
                     slice_block_mma<NT, BF>(w_base + (uint32_t)bl * BLOCK_STRIDE, act0, act1, c0,
                                             c1, acc0, acc1);
             };
-            if (kb0 + KBS <= p.kblocks) {
-                // A full stage: no per-block bound in the unrolled loop.
+            auto blocks = [&](auto zp_c) {
+                if (kb0 + KBS <= p.kblocks) {
+                    // A full stage: no per-block bound in the unrolled loop.
 #pragma unroll
-                for (int j = 0; j < BPW; ++j)
-                    block(j);
-            } else {
-                // The last, partial stage of a slice: blocks past K are skipped (their scale
-                // rows were never loaded).
+                    for (int j = 0; j < BPW; ++j)
+                        block(j, zp_c);
+                } else {
+                    // The last, partial stage of a slice: blocks past K are skipped (their
+                    // scale rows were never loaded).
 #pragma unroll
-                for (int j = 0; j < BPW; ++j)
-                    if (kb0 + w * BPW + j < p.kblocks)
-                        block(j);
-            }
+                    for (int j = 0; j < BPW; ++j)
+                        if (kb0 + w * BPW + j < p.kblocks)
+                            block(j, zp_c);
+                }
+            };
+            if (!W8 && has_zp)
+                blocks(std::true_type{});
+            else
+                blocks(std::false_type{});
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&bars.empty[ring.idx]);
