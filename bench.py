@@ -479,20 +479,29 @@ class StepIO:
         for g, a, c in zip(self.gemms, self.a_views[b], self.c_views[b]):
             g.a, g.c = a, c
 
-    def enqueue_steps(self, stream, step0, nsteps, run_step):
-        """Steps step0.. with their copies: h2d(s+1) overlaps step s, d2h(s) follows it."""
+    def enqueue_steps(self, stream, step0, nsteps, run_gemm):
+        """Steps step0.. with their copies: h2d(s+1) overlaps step s, d2h(s) follows it.  The
+        first step's GEMMs each wait only for their own inputs, and the last step's results
+        each leave as soon as their GEMM is done (the pipeline's fill and drain are one GEMM's
+        copy, not a whole step's).  run_gemm(st, j) runs GEMM j of step st."""
         import torch
+        n = len(self.gemms)
         cin, cout = self.in_stream, self.out_stream
         ev_in = [torch.cuda.Event(), torch.cuda.Event()]
         ev_done = [torch.cuda.Event(), torch.cuda.Event()]
         ev_out = [torch.cuda.Event(), torch.cuda.Event()]
+        ev_in0 = [torch.cuda.Event() for _ in range(n)]
+        ev_c = [torch.cuda.Event() for _ in range(n)]
         cin.wait_stream(stream)
         cout.wait_stream(stream)
         with torch.cuda.stream(cin):
-            self.h2d(0)
-            ev_in[0].record(cin)
+            for j in range(n):
+                if self.copy_in[j]:
+                    self.a_views[0][j].copy_(self.a_host[j], non_blocking=True)
+                    ev_in0[j].record(cin)
         for i in range(nsteps):
             b = i & 1
+            last = i == nsteps - 1
             if i + 1 < nsteps:
                 nb = (i + 1) & 1
                 with torch.cuda.stream(cin):
@@ -500,17 +509,27 @@ class StepIO:
                         cin.wait_event(ev_done[nb])   # step i-1 is done with buffer nb
                     self.h2d(nb)
                     ev_in[nb].record(cin)
-            stream.wait_event(ev_in[b])
+            if i > 0:
+                stream.wait_event(ev_in[b])
             if i >= 2:
                 stream.wait_event(ev_out[b])         # step i-2's results have left buffer b
             self.bind(b)
             with torch.cuda.stream(stream):
-                run_step(step0 + i)
+                for j in range(n):
+                    if i == 0 and self.copy_in[j]:
+                        stream.wait_event(ev_in0[j])
+                    run_gemm(step0 + i, j)
+                    if last and self.copy_out[j]:
+                        ev_c[j].record(stream)
+                        with torch.cuda.stream(cout):
+                            cout.wait_event(ev_c[j])
+                            self.c_host[j].copy_(self.c_views[b][j], non_blocking=True)
             ev_done[b].record(stream)
-            with torch.cuda.stream(cout):
-                cout.wait_event(ev_done[b])
-                self.d2h(b)
-                ev_out[b].record(cout)
+            if not last:
+                with torch.cuda.stream(cout):
+                    cout.wait_event(ev_done[b])
+                    self.d2h(b)
+                    ev_out[b].record(cout)
         stream.wait_stream(cin)
         stream.wait_stream(cout)
         self.bind(0)
@@ -623,13 +642,16 @@ def run_ours(args, rank, world, local):
     stream = torch.cuda.Stream(device=dev)
     io = None   # the end-to-end staging, built after the device-timed run
 
+    def run_gemm(st, gi):
+        gemms[gi].run(st * len(gemms) + gi)
+
     def run_step(st):
-        for gi, g in enumerate(gemms):
-            g.run(st * len(gemms) + gi)
+        for gi in range(len(gemms)):
+            run_gemm(st, gi)
 
     def enqueue(step0, nsteps, e2e=False):
         if e2e:
-            io.enqueue_steps(stream, step0, nsteps, run_step)
+            io.enqueue_steps(stream, step0, nsteps, run_gemm)
             return
         for st in range(step0, step0 + nsteps):
             run_step(st)
