@@ -96,14 +96,21 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
             : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// D (f32 16x8) = A * B with no accumulator input (fp16 operands).
+// D (f32 16x8) = A * B with no accumulator input, fp16 or (BF) bf16 operands.
+template <bool BF>
 __device__ __forceinline__ void mma_16816_z(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                             uint32_t a3, uint32_t b0, uint32_t b1)
 {
-    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
-        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%10, %10, %10, %10};"
-        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
+    if (BF)
+        asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+            "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%10, %10, %10, %10};"
+            : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
+    else
+        asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+            "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%10, %10, %10, %10};"
+            : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
 }
 
 __device__ __forceinline__ __nv_bfloat162 u32_as_bf2(uint32_t v)
@@ -639,11 +646,12 @@ __device__ __forceinline__ void slice_block_mma(uint32_t w_addr, const uint32_t 
     }
 }
 
-// The same block, fp16, with the scale applied in fp32 per block: the MMAs take the exact
-// (q - z) (9 instructions per 8 codes instead of 13), start from zero, and the block's sums are
-// multiplied by the column's s into the output accumulators -- (q - z) s is never rounded to
-// fp16 (for a one-hot row of A the result is the exact product, rounded once on output).
-template <int NT>
+// The same block with the scale applied in fp32 per block: the MMAs take the exact (q - z)
+// (fp16: 9 instructions per 8 codes instead of 13; bf16: 12 instead of 16), start from zero,
+// and the block's sums are multiplied by the column's s into the output accumulators --
+// (q - z) s is never rounded to 16 bits (for a one-hot row of A the result is the exact
+// product, rounded once on output).
+template <int NT, bool BF>
 __device__ __forceinline__ void slice_block_mma_bs(uint32_t w_addr, const uint32_t (&act0)[NT],
                                                    const uint32_t (&act1)[NT], const ColGroup &c0,
                                                    const ColGroup &c1, float (&acc0)[NT][4],
@@ -651,20 +659,20 @@ __device__ __forceinline__ void slice_block_mma_bs(uint32_t w_addr, const uint32
 {
     constexpr uint32_t HALF = SLICE_N * 4 * 4;
     uint32_t a0[4], a1[4], a2[4], a3[4];
-    dequant_word_int<false>(lds32(w_addr), c0.zlo, c0.zhi, a0);
-    dequant_word_int<false>(lds32(w_addr + 128), c1.zlo, c1.zhi, a1);
-    dequant_word_int<false>(lds32(w_addr + HALF), c0.zlo, c0.zhi, a2);
-    dequant_word_int<false>(lds32(w_addr + HALF + 128), c1.zlo, c1.zhi, a3);
+    dequant_word_int<BF>(lds32(w_addr), c0.zlo, c0.zhi, a0);
+    dequant_word_int<BF>(lds32(w_addr + 128), c1.zlo, c1.zhi, a1);
+    dequant_word_int<BF>(lds32(w_addr + HALF), c0.zlo, c0.zhi, a2);
+    dequant_word_int<BF>(lds32(w_addr + HALF + 128), c1.zlo, c1.zhi, a3);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
         uint32_t b[4], e[4];
         ldmatrix_x4(act0[nt], b);
         ldmatrix_x4(act1[nt], e);
         float d0[4], d1[4];
-        mma_16816_z(d0, a0[0], a1[0], a0[1], a1[1], b[0], b[1]);
-        mma_16816_z(d1, a2[0], a3[0], a2[1], a3[1], e[0], e[1]);
-        mma_16816<false>(d0, a0[2], a1[2], a0[3], a1[3], b[2], b[3]);
-        mma_16816<false>(d1, a2[2], a3[2], a2[3], a3[3], e[2], e[3]);
+        mma_16816_z<BF>(d0, a0[0], a1[0], a0[1], a1[1], b[0], b[1]);
+        mma_16816_z<BF>(d1, a2[0], a3[0], a2[1], a3[1], e[0], e[1]);
+        mma_16816<BF>(d0, a0[2], a1[2], a0[3], a1[3], b[2], b[3]);
+        mma_16816<BF>(d1, a2[2], a3[2], a2[3], a3[3], e[2], e[3]);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const float sc = i < 2 ? c0.sf : c1.sf;
@@ -706,6 +714,43 @@ __device__ __forceinline__ void slice_block_mma_fp8(uint32_t w_addr, const uint3
         mma_16816<false>(acc0[nt], a[1][0], a[1][1], a[1][2], a[1][3], b[2], b[3]);
         mma_16816<false>(acc1[nt], a[2][0], a[2][1], a[2][2], a[2][3], e[0], e[1]);
         mma_16816<false>(acc1[nt], a[3][0], a[3][1], a[3][2], a[3][3], e[2], e[3]);
+    }
+}
+
+// FP8 with the scale applied in fp32 per block: each code converts exactly to fp16, the MMAs
+// start from zero, and the block's sums times the column's s go into the output accumulators.
+template <int NT>
+__device__ __forceinline__ void slice_block_mma_fp8_bs(uint32_t w_addr, const uint32_t (&act0)[NT],
+                                                       const uint32_t (&act1)[NT], float s0, float s1,
+                                                       float (&acc0)[NT][4], float (&acc1)[NT][4])
+{
+    uint32_t a[4][4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const uint32_t base = w_addr + q * 256;
+        const uint16_t h[4] = {lds16(base), lds16(base + 128), lds16(base + 8), lds16(base + 136)};
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const __half2_raw v = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)h[r], __NV_E4M3);
+            a[q][r] = h2_as_u32(__half2(v));
+        }
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        uint32_t b[4], e[4];
+        ldmatrix_x4(act0[nt], b);
+        ldmatrix_x4(act1[nt], e);
+        float d0[4], d1[4];
+        mma_16816_z<false>(d0, a[0][0], a[0][1], a[0][2], a[0][3], b[0], b[1]);
+        mma_16816_z<false>(d1, a[2][0], a[2][1], a[2][2], a[2][3], e[0], e[1]);
+        mma_16816<false>(d0, a[1][0], a[1][1], a[1][2], a[1][3], b[2], b[3]);
+        mma_16816<false>(d1, a[3][0], a[3][1], a[3][2], a[3][3], e[2], e[3]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float sc = i < 2 ? s0 : s1;
+            acc0[nt][i] = fmaf(d0[i], sc, acc0[nt][i]);
+            acc1[nt][i] = fmaf(d1[i], sc, acc1[nt][i]);
+        }
     }
 }
 
@@ -805,12 +850,15 @@ __device__ __forceinline__ void slice_compute(const GemmParams &p, uint8_t *smem
                     act0[nt] = ok ? act_base + act_off0[j][nt] : zero_row;
                     act1[nt] = ok ? act_base + act_off1[j][nt] : zero_row;
                 }
-                if (W8)
+                if (W8 && NT <= 2)
+                    slice_block_mma_fp8_bs<NT>(w_base + (uint32_t)bl * BLOCK_STRIDE, act0, act1,
+                                               c0.sf, c1.sf, acc0, acc1);
+                else if (W8)
                     slice_block_mma_fp8<NT>(w_base + (uint32_t)bl * BLOCK_STRIDE, act0, act1, c0.s,
                                             c1.s, acc0, acc1);
-                else if (!BF && NT <= 2)
-                    slice_block_mma_bs<NT>(w_base + (uint32_t)bl * BLOCK_STRIDE, act0, act1, c0,
-                                           c1, acc0, acc1);
+                else if (NT <= 2)
+                    slice_block_mma_bs<NT, BF>(w_base + (uint32_t)bl * BLOCK_STRIDE, act0, act1, c0,
+                                               c1, acc0, acc1);
                 else
                     slice_block_mma<NT, BF>(w_base + (uint32_t)bl * BLOCK_STRIDE, act0, act1, c0,
                                             c1, acc0, acc1);
