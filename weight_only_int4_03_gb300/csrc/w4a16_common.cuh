@@ -624,7 +624,7 @@ static __device__ void reduce_tile_glu(const GemmParams &p, const TileInfo &ti, 
     }
 }
 
-template <int RB = 4>
+template <int RB = 4, int CB = 4>
 static __device__ void reduce_tile(const GemmParams &p, const TileInfo &ti, const Contributors &cb,
                                    int tid, int nthreads)
 {
@@ -668,7 +668,8 @@ static __device__ void reduce_tile(const GemmParams &p, const TileInfo &ti, cons
             store_quad(p, ti, item / QUADS, item % QUADS, acc);
         return;
     }
-    constexpr int CB = 4; // RB items per round x CB contributors per batch in flight
+    // RB items per round x CB contributors per batch: RB * CB independent 16-byte loads in
+    // flight per thread (the reduction is bound by their latency).
     for (int base = tid; base < items; base += nthreads * RB) {
         float4 acc[RB];
 #pragma unroll

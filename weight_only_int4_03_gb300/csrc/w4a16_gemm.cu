@@ -635,8 +635,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const Contributors cb = contributors(p, sched, (long long)tile - sched.dp_tiles);
         if (p.glu)
             reduce_tile_glu(p, ti, cb, threadIdx.x, NUM_THREADS);
+        else if (ti.rows * (TILE_N / 4) <= 4 * NUM_THREADS)
+            // A short tile (up to 64 rows, typically 4+ contributors): one round of 4 items per
+            // thread covers it, with 4 contributors' loads in flight.
+            reduce_tile<4, 4>(p, ti, cb, threadIdx.x, NUM_THREADS);
         else
-            reduce_tile<4>(p, ti, cb, threadIdx.x, NUM_THREADS);
+            // Taller tiles (2-3 contributors): 8 items x 2 contributors in flight per thread.
+            reduce_tile<8, 2>(p, ti, cb, threadIdx.x, NUM_THREADS);
         if (threadIdx.x == 0)
             p.counters[tile] = 0;
     }
