@@ -26,6 +26,7 @@ struct Bars {
     uint64_t accfull[2];
     uint64_t accempty[2];
     uint64_t drain;
+    uint64_t split_done[2]; // the epilogue warps' partial stores of the CTA's split tiles
 };
 
 // The four k steps of one 64-row block: MMAs on the dequantised weight slot (tensor memory at
@@ -402,18 +403,21 @@ __device__ void run_dequant(const GemmParams &p, Sched sched, uint8_t *smem, uin
     }
 }
 
-// Split tiles get only their fp32 partial here; the counter and the reduction wait until the
-// whole CTA is done (see the kernel's end), when all of its threads can share the reduction.
+// Split tiles get only their fp32 partial here.  The segment that starts a stream-K range
+// arrives on its tile's counter as soon as the four epilogue warps have stored it, long before
+// the contributor whose range ends in that tile, which so is the tile's last arriver and a CTA
+// is last for at most one tile; the other split segments arrive, and every reduction runs,
+// once the whole CTA is done (see the kernel's end), when all of its threads can share it.
 __device__ void run_epilogue(const GemmParams &p, const SegTable &seg, Sched sched, Bars &bars,
                              uint32_t tmem_base, uint8_t *smem, const WaitCtl &ctl, int warp,
-                             int lane, int *split_tiles, int *n_split)
+                             int lane, int *split_tiles, volatile int *split_last, int *n_split)
 {
     const int q = warp & 3;
     __half *stg = reinterpret_cast<__half *>(smem + p.epi_smem_off) + q * EPI_ROWS * 32;
     uint16_t *stg16 = reinterpret_cast<uint16_t *>(stg); // fp16 or bf16 bits
     const int nl = q * 32 + lane;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-    uint32_t seg_i = 0;
+    uint32_t seg_i = 0, n_seen = 0; // n_seen: split segments so far
     int tile, kb0, kb1;
     while (sched.next(tile, kb0, kb1)) {
         const TileInfo ti = tile_info(p, seg, tile);
@@ -507,8 +511,31 @@ __device__ void run_epilogue(const GemmParams &p, const SegTable &seg, Sched sch
         if (lane == 0)
             mbar_arrive(&bars.accempty[abuf]);
         ++seg_i;
-        if (!whole && warp == EPI_WARP0 && lane == 0)
-            split_tiles[(*n_split)++] = tile;
+        if (!whole && kb1 == p.kblocks && sched.split == 0 && n_seen < 2) {
+            // A stream-K segment that ends at its tile's end: the start of this CTA's range,
+            // done long before the range's end.  Arrive now: every lane's partial stores are
+            // made visible at GPU scope, each warp arrives on this split tile's rendezvous (a
+            // barrier of its own, used once), and one thread, once all four have (a bounded
+            // wait: no thread waits on a warp that gave up), makes the acquire-release arrival.
+            __threadfence();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&bars.split_done[n_seen]);
+            if (warp == EPI_WARP0 && lane == 0) {
+                if (!mbar_wait(&bars.split_done[n_seen], 0, ctl, W4A16_DEV_TIMEOUT))
+                    return;
+                const Contributors cb = contributors(p, sched, st_tile);
+                const int old = split_counter_arrive(&p.counters[tile]);
+                split_tiles[*n_split] = tile;
+                split_last[*n_split] = old == (cb.hi - cb.lo);
+                ++*n_split;
+            }
+            ++n_seen;
+        } else if (!whole && warp == EPI_WARP0 && lane == 0) {
+            split_tiles[*n_split] = tile; // arrives at the CTA's end
+            split_last[*n_split] = -1;
+            ++*n_split;
+        }
     }
 }
 
@@ -550,6 +577,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(&bars.accempty[s], EPI_THREADS / 32);
         }
         mbar_init(&bars.drain, 1);
+        mbar_init(&bars.split_done[0], EPI_THREADS / 32);
+        mbar_init(&bars.split_done[1], EPI_THREADS / 32);
         fence_mbar_init();
         abort_sh = 0;
         last_sh[0] = last_sh[1] = 0;
@@ -601,7 +630,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             run_mma<A_TMEM>(p, seg, sched, smem, aring, bars, tmem_base, ctl);
     } else if (warp >= EPI_WARP0 && warp < EPI_WARP0 + 4) {
         run_epilogue(p, seg, sched, bars, tmem_base, smem, ctl, warp, lane, split_tiles_sh,
-                     &n_split_sh);
+                     last_sh, &n_split_sh);
     } else if (warp >= DQ_WARP0) {
         run_dequant<A_TMEM, WK>(p, sched, smem, aring, bars, tmem_base, ctl, warp, lane);
     }
@@ -614,13 +643,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tmem_dealloc(tmem_base, p.tmem_cols);
     }
 
-    // Split tiles of this CTA (at most two: where its range starts and ends).  The barrier
-    // above orders the partial stores before the counter atomics (release is cumulative); the
-    // last contributor of a tile sums the partials with all of the CTA's threads.
+    // Split tiles of this CTA (at most two: where its range starts and ends).  The one that
+    // starts the range was counted in by the epilogue; the others arrive here (the barrier
+    // above orders the partial stores before the atomics; release is cumulative).  The last
+    // contributor of a tile sums the partials with all of the CTA's threads (the acquire half
+    // of its arrival, and a barrier, make the other contributors' partials visible to all).
     const int n_split = n_split_sh;
     if (n_split == 0 || abort_sh)
         return;
-    if (threadIdx.x < n_split) {
+    if (threadIdx.x < n_split && last_sh[threadIdx.x] < 0) {
         const int tile = split_tiles_sh[threadIdx.x];
         const Contributors cb = contributors(p, sched, (long long)tile - sched.dp_tiles);
         const int old = split_counter_arrive(&p.counters[tile]);
