@@ -578,12 +578,19 @@ __device__ __forceinline__ const float4 *partial_quads(const GemmParams &p, cons
 // 16b .. 16b+15 and packed columns 32b+16 .. 32b+31 the up features of the same indices, so a
 // 128-column tile holds features n0/2 .. n0/2 + 63 and writes act(gate) * up there.
 // ---------------------------------------------------------------------------------------
+// Both are g * sigmoid(x): silu with x = g; gelu_tanh, 0.5 g (1 + tanh t) with
+// t = sqrt(2/pi) (g + 0.044715 g^3), since 1 + tanh t = 2 sigmoid(2t).  One fast exponential and
+// one reciprocal per element: the epilogue warps share their SM sub-partitions with the MMA-
+// issuing thread, and accurate expf / division / tanhf there slowed the gated MoE GEMM by 5 %.
+// (x -> -inf: the exponential is inf, its reciprocal 0; x -> +inf: the result is g.)
 __device__ __forceinline__ float glu_act(float g, int kind)
 {
-    if (kind == 1)
-        return g / (1.0f + expf(-g)); // silu: g * sigmoid(g)
-    const float c = 0.7978845608028654f; // sqrt(2 / pi)
-    return 0.5f * g * (1.0f + tanhf(c * (g + 0.044715f * g * g * g)));
+    float x = g;
+    if (kind != 1) {
+        const float c = 0.7978845608028654f; // sqrt(2 / pi)
+        x = 2.0f * c * (g + 0.044715f * g * g * g);
+    }
+    return g * __frcp_rn(1.0f + __expf(-x));
 }
 
 // Split tile of a gated call: items are (row, gate quad); each sums its gate quad and the up
