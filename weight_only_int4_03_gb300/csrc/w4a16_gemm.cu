@@ -432,12 +432,18 @@ __device__ void run_epilogue(const GemmParams &p, const SegTable &seg, Sched sch
         float *part = whole ? nullptr : partial_slot(p, sched.cta, own_slot(p, sched, st_tile));
         // Batches of 32 token rows: two tensor-memory loads per wait.  A whole tile goes out
         // through this warp's staging buffer (its 32 columns x 32 rows as fp16), so that each
-        // lane writes 16-byte runs of a C row instead of single halves.
-        for (int c0 = 0; c0 < ti.ntok; c0 += EPI_ROWS) {
-            uint32_t v[32];
+        // lane writes 16-byte runs of a C row instead of single halves.  The next batch's loads
+        // are issued as soon as this batch's registers are consumed (staged, or stored as a
+        // partial), so that their latency overlaps the stores.
+        uint32_t v[32];
+        auto load_batch = [&](int c0) {
             tmem_ld16(taddr + c0, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
             if (c0 + 16 < ti.ntok)
                 tmem_ld16(taddr + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
+        };
+        load_batch(0);
+        for (int c0 = 0; c0 < ti.ntok; c0 += EPI_ROWS) {
+            const bool more = c0 + EPI_ROWS < ti.ntok;
             tmem_ld_wait();
             // Block-routed calls may scale each output row (top-k weights): lane j holds the
             // weight of row c0 + j, handed to every lane by a shuffle.
@@ -460,6 +466,8 @@ __device__ void run_epilogue(const GemmParams &p, const SegTable &seg, Sched sch
                         stg16[j * 16 + lane] = to_out16(glu_act(g, p.glu) * u * w, p.bf16);
                 }
                 __syncwarp();
+                if (more)
+                    load_batch(c0 + EPI_ROWS);
 #pragma unroll
                 for (int i = 0; i < EPI_ROWS / 16; ++i) {
                     const int r = i * 16 + (lane >> 1);
@@ -482,6 +490,8 @@ __device__ void run_epilogue(const GemmParams &p, const SegTable &seg, Sched sch
                     stg16[j * 32 + lane] = to_out16(__uint_as_float(v[j]) * w, p.bf16);
                 }
                 __syncwarp();
+                if (more)
+                    load_batch(c0 + EPI_ROWS);
 #pragma unroll
                 for (int i = 0; i < EPI_ROWS / 8; ++i) {
                     const int r = i * 8 + (lane >> 2);
@@ -504,6 +514,8 @@ __device__ void run_epilogue(const GemmParams &p, const SegTable &seg, Sched sch
                     if (row < ti.rows)
                         __stcg(part + row * TILE_N + nl, __uint_as_float(v[j]));
                 }
+                if (more)
+                    load_batch(c0 + EPI_ROWS);
             }
         }
         tc_fence_before();
