@@ -183,3 +183,25 @@ def test_grouped_gated_matches_oracle(w4, orc, kind):
         u[seg] = orc.gemm(rows, np.ascontiguousarray(qw[e][:, i:]), np.ascontiguousarray(s[e][:, i:]),
                           None, None, gs, U4B8)
     glu_check(orc, got, g, u, kind)
+
+
+@pytest.mark.parametrize("kind", [1, 2])
+def test_gated_activation_at_extreme_gates(w4, orc, kind):
+    """One-hot rows of A pick weight rows whose gate values run from -100 to 87.5 (codes 0..15
+    at scale 12.5) and whose up values are 1, so the output is act(gate) itself: it must match
+    the oracle and stay finite at both ends (for large negative gates the exponential in the
+    sigmoid overflows to infinity, and the product must come out 0, not NaN)."""
+    m, k, n2, gs = 16, 128, 512, 128
+    i = n2 // 2
+    codes = np.full((k, n2), 9, dtype=np.int64)             # up: (9 - 8) * 1 = 1
+    for r in range(m):
+        codes[r, :i] = (r + np.arange(i)) % 16              # every code in every row's columns
+    qw = orc.pack_gptq(codes)
+    s = np.ones((1, n2), dtype=np.float16)
+    s[0, :i] = 12.5
+    a = np.zeros((m, k), dtype=np.float16)
+    a[np.arange(m), np.arange(m)] = 1.0
+    got, _ = run_glu(w4, a, qw, s, None, k, n2, gs, U4B8, kind)
+    g = (codes[:m, :i] - 8).astype(np.float64) * 12.5
+    assert g.min() == -100.0 and g.max() == 87.5
+    glu_check(orc, got, g, np.ones_like(g), kind)
