@@ -518,3 +518,25 @@ def test_workspace_reset_after_timeout_report(w4, orc):
     dp.ws.zero_()                           # the recovery step
     dp.run()
     check(dp, orc)
+
+
+@pytest.mark.parametrize("m,flag", [(1, FLAG_FORCE_SLICE), (8, FLAG_FORCE_SLICE), (16, FLAG_FORCE_SLICE),
+                                    (8, FLAG_FORCE_MMA), (16, FLAG_FORCE_MMA), (8, FLAG_FORCE_TC)])
+@pytest.mark.parametrize("wt", [U4B8, U4])
+def test_one_hot_rows_give_rounded_weights_on_every_kernel(w4, orc, m, flag, wt):
+    """Row r of A is 1 at column k_r and 0 elsewhere, so row r of C is row k_r of the
+    dequantised weight, (q - z) s, rounded once to fp16: bit for bit on every kernel, whether it
+    rounds (q - z) s to fp16 before the MMA or applies s to fp32 sums afterwards."""
+    k, n = 256, 4096  # N / 16 >= the SM count: the column-slice kernel takes these shapes
+    pb = make_problem(7100 + m + (wt == U4), m, k, n, weight_type=wt)
+    rows = (np.arange(m) * 37 + 5) % k
+    a = np.zeros((m, k), dtype=np.float16)
+    a[np.arange(m), rows] = 1.0
+    pb.a = a
+    dp = DeviceProblem(w4, pb, flags_extra=flag)
+    dp.run()
+    got = dp.result()
+    w = orc.dequant(pb.qweight, pb.scales, pb.zeros, None, k, n, pb.group_size, wt)
+    want = w[rows].astype(np.float16)
+    assert dp.status() == 0
+    assert np.array_equal(got.astype(np.float16).view(np.uint16), want.view(np.uint16))
