@@ -77,7 +77,11 @@ extern "C" {
                                            _FORCE_MMA and _FORCE_SLICE are rejected)        */
 #define W4A16_FLAG_GEGLU (1u << 15)  /* the same with gelu_tanh(x) = x/2 (1 + tanh(sqrt(2/pi)
                                            (x + 0.044715 x^3))) in place of silu; exclusive
-                                           with W4A16_FLAG_SWIGLU                            */
+                                           with W4A16_FLAG_SWIGLU.  Both activations are
+                                           evaluated in fp32 as x sigmoid(y) (y = x for silu,
+                                           2 sqrt(2/pi) (x + 0.044715 x^3) for gelu_tanh)
+                                           with a fast exponential: within the gated
+                                           tolerance, not correctly rounded               */
 #define W4A16_FLAG_BF16 (1u << 16)   /* a, scales, zeros and c are bfloat16 instead of fp16
                                            (marlin.rs declares bf16 A and C for its
                                            `ferrum_vllm_marlin_moe_mxfp4_bf16` entry point;
