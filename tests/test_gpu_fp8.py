@@ -191,3 +191,25 @@ def test_fp8_unsupported_combinations_rejected(w4):
             w4.w4a16_gemm(a, b, c, s, cs.get("zeros"), cs.get("g_idx"), cs.get("perm"), ws, m, n, k,
                           cs.get("gs", 128), FE4M3, cs.get("flags", 0))
         assert e.value.stage == 1 and e.value.detail == cs["detail"], cs
+
+
+@pytest.mark.parametrize("m,flags", [(1, FLAG_IS_K_FULL | FLAG_FORCE_SLICE), (8, FLAG_IS_K_FULL | FLAG_FORCE_SLICE),
+                                     (16, FLAG_IS_K_FULL | FLAG_FORCE_SLICE), (40, FLAG_IS_K_FULL)])
+def test_fp8_one_hot_rows_give_rounded_weights(w4, orc, m, flags):
+    """Row r of A is 1 at column k_r, so row r of C is row k_r of e4m3(code) s rounded once to
+    fp16, bit for bit: the column-slice kernel applies s to fp32 sums of exact codes, the tcgen05
+    kernel rounds the product before its MMA; both round the same exact value.  (A zero weight,
+    code 0x80 being -0, meets the other rows' +0 products in the sum: zeros are compared by
+    value, everything else by bits.)"""
+    k, n, gs = 256, 4096, 128
+    qw = synth.fp8_weights(8200 + m, k, n)
+    s = synth.scales(8200 + m, k // gs, n)
+    rows = (np.arange(m) * 37 + 5) % k
+    a = np.zeros((m, k), dtype=np.float16)
+    a[np.arange(m), rows] = 1.0
+    got = run_fp8(w4, a, qw, s, k, n, gs, flags)
+    want = orc.dequant_fp8(qw, s, k, n, gs)[rows].astype(np.float16)
+    got16 = got.astype(np.float16)
+    nz = want != 0
+    assert np.all(got16[~nz] == 0)
+    assert np.array_equal(got16[nz].view(np.uint16), want[nz].view(np.uint16))
