@@ -214,3 +214,27 @@ def test_bf16_one_hot_bit_exact_on_every_kernel(w4, force):
     got = run_bf16(w4, a, qw.view(np.int32), s, None, None, None, k, n, 128, U4B8, extra=force)
     want = (a[:, pi].astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
     assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("m,force", [(1, FORCE_SLICE), (8, FORCE_SLICE), (16, FORCE_SLICE),
+                                     (8, FORCE_MMA), (16, FORCE_MMA), (8, 1 << 10)])
+@pytest.mark.parametrize("wt", [U4B8, U4])
+def test_bf16_one_hot_rows_give_rounded_weights_on_every_kernel(w4, orc, m, force, wt):
+    """Row r of A is 1 at column k_r, so row r of C is row k_r of (q - z) s rounded once to
+    bf16, bit for bit, with random codes, scales and zero points: the small-M kernels apply s to
+    fp32 sums of the exact (q - z), the tcgen05 kernel rounds the product before its MMA.
+    (q - z) s has at most 4 + 8 significant bits, so it is exact in float32 and synth.bf16_bits
+    rounds it once.)"""
+    k, n, gs = 256, 4096, 128
+    _, qw, s, z, _, _ = make(9600 + m + (wt == U4), m, k, n, gs, wt)
+    rows = (np.arange(m) * 37 + 5) % k
+    a = np.zeros((m, k), dtype=np.uint16)
+    a[np.arange(m), rows] = 0x3F80  # bf16 1.0
+    got = run_bf16(w4, a, qw, s, z, None, None, k, n, gs, wt, extra=force)
+    q = orc.unpack_gptq(qw, k, n).astype(np.float64)
+    sd = orc.bf16_to_double(s)
+    zd = orc.bf16_to_double(z) if z is not None else np.full_like(sd, 8.0)
+    g = np.arange(k) // gs
+    w = (q - zd[g]) * sd[g]
+    want = (synth.bf16_bits(w[rows]).astype(np.uint32) << np.uint32(16)).view(np.float32)
+    assert np.array_equal(got, want.astype(np.float64))
