@@ -441,6 +441,16 @@ __device__ void run_epilogue(const GemmParams &p, const SegTable &seg, Sched sch
         // long per batch in place.
         const bool weighted = p.row_weight != nullptr;
         const bool dense = p.ex_off == nullptr;
+        // The accumulator is released as soon as the last batch has been read from tensor
+        // memory, before that batch is written out.
+        bool released = false;
+        auto release = [&]() {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&bars.accempty[abuf]);
+            released = true;
+        };
         if (whole && p.glu) {
             // Gated tiles keep the next batch's loads issued as soon as this batch is staged:
             // measured faster for them (MoE gate_up with SwiGLU 397 -> 344 us).
@@ -455,6 +465,8 @@ __device__ void run_epilogue(const GemmParams &p, const SegTable &seg, Sched sch
                 const bool more = c0 + EPI_ROWS < ti.ntok;
                 const int nr = ti.rows - c0;
                 tmem_ld_wait();
+                if (!more)
+                    release();
                 float rw = 1.0f;
                 if (weighted && lane < nr) {
                     const int orow = p.ex_pairs[ti.row0 + c0 + lane];
@@ -496,6 +508,8 @@ __device__ void run_epilogue(const GemmParams &p, const SegTable &seg, Sched sch
                 if (c0 + 16 < ti.ntok)
                     tmem_ld16(taddr + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
                 tmem_ld_wait();
+                if (c0 + EPI_ROWS >= ti.ntok)
+                    release();
                 const int nr = ti.rows - c0; // rows of this batch that exist (all 32 when >= 32)
                 if (!whole) {
                     float *dst = part + c0 * TILE_N + nl;
@@ -561,10 +575,8 @@ __device__ void run_epilogue(const GemmParams &p, const SegTable &seg, Sched sch
                 __syncwarp();
             }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0)
-            mbar_arrive(&bars.accempty[abuf]);
+        if (!released)
+            release();
         ++seg_i;
         if (!whole && kb1 == p.kblocks && sched.split == 0 && n_seen < 2) {
             // A stream-K segment that ends at its tile's end: the start of this CTA's range,
